@@ -1,0 +1,91 @@
+"""Planted mistakes in the oracle must be caught by its pins (CPU only).
+
+Each case patches one plausible error into an oracle function (a dropped
+term, a wrong sign, a wrong constant, a wrong tie rule, a dropped rule) and
+checks that at least one pin test then fails.
+"""
+import numpy as np
+import pytest
+
+from oracle import formats, hadamard, policy, quant, stats
+
+import tests.test_oracle_formats as tf
+import tests.test_oracle_hadamard as th
+import tests.test_oracle_quant as tq
+import tests.test_oracle_stats_policy as ts
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except AssertionError:
+        return True
+    return False
+
+
+def _bad_fwht_sign(x, b):
+    x = np.asarray(x, np.float32)
+    m, k = x.shape
+    v = x.reshape(m, k // b, b).copy()
+    h = 1
+    while h < b:
+        w = v.reshape(m, k // b, b // (2 * h), 2, h)
+        v = np.stack([w[:, :, :, 0] + w[:, :, :, 1], w[:, :, :, 1] - w[:, :, :, 0]], axis=3).reshape(m, k // b, b)
+        h *= 2
+    return (v * hadamard.inv_sqrt_b(b)).reshape(m, k)
+
+
+def _bad_fwht_no_norm(x, b):
+    return hadamard.fwht_blocks(x, b) / hadamard.inv_sqrt_b(b)
+
+
+def test_fwht_mutations_are_caught(monkeypatch):
+    monkeypatch.setattr(hadamard, "fwht_blocks", _bad_fwht_sign)
+    assert _fails(th.test_fwht_of_unit_vectors_is_normalised_hadamard, 16)
+    monkeypatch.undo()
+    orig = hadamard.fwht_blocks
+    monkeypatch.setattr(hadamard, "fwht_blocks", lambda x, b: orig(x, b) / hadamard.inv_sqrt_b(b))
+    assert _fails(th.test_fwht_is_an_involution_on_small_integers, 64)
+
+
+def test_format_tie_rule_mutation_is_caught(monkeypatch):
+    def away(a, fmt):   # ties away from zero instead of to even
+        ebits, mbits, bias, fmax = fmt
+        a = np.asarray(a, np.float64)
+        out = np.zeros_like(a)
+        nz = a > 0
+        _, ex = np.frexp(a[nz])
+        q = np.ldexp(1.0, np.maximum(ex - 1, 1 - bias) - mbits)
+        out[nz] = np.minimum(np.floor(a[nz] / q + 0.5) * q, fmax)
+        return out
+    monkeypatch.setattr(formats, "_round_to_format", away)
+    assert _fails(tf.test_hand_worked_encodings, "e2m1_pins.txt", formats.e2m1_encode, formats.e2m1_decode)
+    assert _fails(tf.test_e4m3_encode_matches_torch_in_range)
+
+
+def test_quantizer_constant_mutations_are_caught(monkeypatch):
+    monkeypatch.setattr(quant, "tensor_scale", lambda amax: np.float32(amax) / np.float32(448.0))
+    assert _fails(tq.test_nvfp4_hand_worked_blocks)
+    monkeypatch.undo()
+    orig = quant.int8_quantize
+    def int8_128(y):
+        y = np.asarray(y, np.float32)
+        s = (np.max(np.abs(y), axis=1) / np.float32(128.0)).astype(np.float32)
+        q = np.clip(np.rint(y / np.where(s == 0, 1, s)[:, None]), -127, 127).astype(np.int8)
+        return dict(q=q, s=s)
+    monkeypatch.setattr(quant, "int8_quantize", int8_128)
+    assert _fails(tq.test_int8_hand_worked_rows)
+
+
+def test_policy_rule_mutation_is_caught(monkeypatch):
+    orig = policy.decide
+    def no_post_skip(st, ratio, cfg):
+        st.skipped_last = False
+        return orig(st, ratio, cfg)
+    monkeypatch.setattr(policy, "decide", no_post_skip)
+    assert _fails(ts.test_policy_hand_traces, "B")
+
+
+def test_cosine_mutation_is_caught(monkeypatch):
+    monkeypatch.setattr(stats, "cosine", lambda a, b, c: a / b if b else 0.0)
+    assert _fails(ts.test_cosine_special_cases)
