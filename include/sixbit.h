@@ -1,0 +1,279 @@
+/*
+ * libsixbit -- C ABI of the dynamically quantized linear layer of a video
+ * diffusion transformer ("6Bit-Diffusion: Inference-Time Mixed-Precision
+ * Quantization for Video Diffusion Models"), for one NVIDIA GB300 (sm_103a).
+ *
+ * Conventions for every call:
+ *  - Tensor pointers are DEVICE pointers, allocated and owned by the caller.
+ *    The library never allocates or frees device memory.
+ *  - bf16 tensors are passed as uint16_t bit patterns, row-major, densely
+ *    packed (row stride = number of columns).
+ *  - Every call enqueues its kernels on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and returns without waiting for them.
+ *  - Argument errors are detected on the host before anything is enqueued
+ *    and returned as a sixbit_status; nothing is launched in that case.
+ *  - Device-side errors (a bounded wait that ran out, an out-of-range
+ *    index caught by a check) are recorded in the caller-supplied device word
+ *    `err_dev` (may be NULL to ignore them) as a SIXBIT_E* code; the first
+ *    error wins.  sixbit_check() synchronizes the stream and decodes it.
+ *  - "mode" arguments: when `mode_dev` is non-NULL the device word it points
+ *    to (written by sixbit_policy_step) selects the mode at run time and a
+ *    kernel whose mode does not match returns at once; when it is NULL the
+ *    host value `mode` is used.
+ */
+#ifndef SIXBIT_H
+#define SIXBIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int sixbit_status;
+enum {
+  SIXBIT_OK = 0,
+  SIXBIT_EINVAL = 1,       /* NULL pointer or bad enum value */
+  SIXBIT_ESHAPE = 2,       /* a size violates the documented constraints */
+  SIXBIT_EALIGN = 3,       /* a pointer is not 16-byte aligned */
+  SIXBIT_EUNSUPPORTED = 4, /* no GPU of compute capability 10.3 */
+  SIXBIT_ECUDA = 5,        /* a CUDA runtime call failed */
+  SIXBIT_ETIMEOUT = 6,     /* a device-side bounded wait ran out */
+  SIXBIT_EDEVICE = 7       /* a device-side check failed */
+};
+
+/* Per-block precision decision (low byte of the mode word) and flags. */
+enum {
+  SIXBIT_MODE_NVFP4 = 1, /* stable block: NVFP4 activations, W4A4 GEMM */
+  SIXBIT_MODE_INT8 = 2,  /* volatile block: INT8 activations, W4A8 GEMM */
+  SIXBIT_MODE_BF16 = 3,  /* PDR: full-precision recompute */
+  SIXBIT_MODE_SKIP = 4   /* TDC: output = input + cached delta */
+};
+#define SIXBIT_MODE_OF(w) ((w)&0xFF)
+enum {
+  SIXBIT_FLAG_REFRESH = 1 << 8,   /* error accumulator forced a compute */
+  SIXBIT_FLAG_PDR = 1 << 9,       /* outlier ratio forced BF16 */
+  SIXBIT_FLAG_POSTSKIP = 1 << 10, /* INT8 because the previous step skipped */
+  SIXBIT_FLAG_NEAR = 1 << 11      /* a deciding statistic was within near_rel of its threshold */
+};
+
+enum { SIXBIT_EPI_NONE = 0, SIXBIT_EPI_GELU = 1, SIXBIT_EPI_RESIDUAL = 2 };
+
+/*
+ * Quantized activations (output of sixbit_hadamard_quant, A operand of
+ * sixbit_qgemm).  M tokens x K channels.  Fields of the mode not produced may
+ * be NULL.
+ *
+ * NVFP4 (technical summary section 2.A; popular summary section 1):
+ *   fp4_codes    [M, K/2] bytes, two E2M1 codes per byte, even k in the low nibble
+ *   fp4_scales   E4M3 block scales, one per 16 elements, in the tiled layout
+ *                of sixbit_fp4_scale_offset(); sixbit_fp4_scale_bytes(M, K) bytes
+ *   tensor_amax  [1] float: max |y| of the rotated tensor (written by the call
+ *                unless an amax is supplied)
+ *   tensor_scale [1] float: s_t = amax / 2688 (1 when amax == 0)
+ * INT8 (technical summary section 2.A):
+ *   i8_codes     [M, K] int8, symmetric, per token, in [-127, 127]
+ *   row_scale    [M] float: s_m = row amax / 127
+ *   i8_operand   [M, K] bf16 bit patterns of the same integers (the form the
+ *                W4A8 GEMM reads); required by sixbit_qgemm in INT8 mode
+ * Debug:
+ *   rotated      [M, K] float, the rotated FP32 activations (optional)
+ */
+typedef struct {
+  uint8_t* fp4_codes;
+  uint8_t* fp4_scales;
+  float* tensor_amax;
+  float* tensor_scale;
+  int8_t* i8_codes;
+  float* row_scale;
+  uint16_t* i8_operand;
+  float* rotated;
+} sixbit_qact;
+
+/*
+ * Packed weights of one linear layer, W [N, K] (output channels x input
+ * channels), produced by sixbit_pack_weights.  The 4-bit forms are of the
+ * rotated weight W' = W . blockdiag(H_b / sqrt(b)); the bf16 form is unrotated.
+ *   fp4_codes        [N, K/2], fp4_scales (tiled, sixbit_fp4_scale_bytes(N, K)),
+ *   fp4_amax [1], fp4_tensor_scale [1]           -- NVFP4, static tensor scale
+ *   i4_codes         [N, K/2] two's-complement nibbles in [-7, 7], even k low
+ *   i4_scales        [K/128, N] float (group-major): s[g][n] = amax / 7
+ *   i4_operand       [N, K] bf16 bit patterns of the INT4 integers (GEMM operand)
+ *   bf16_w           [N, K] bf16(W)
+ */
+typedef struct {
+  uint8_t* fp4_codes;
+  uint8_t* fp4_scales;
+  float* fp4_amax;
+  float* fp4_tensor_scale;
+  uint8_t* i4_codes;
+  float* i4_scales;
+  uint16_t* i4_operand;
+  uint16_t* bf16_w;
+} sixbit_weights;
+
+/*
+ * Statistics of one computed block step (sixbit_block_stats) -- float64 sums
+ * over the whole [T, H] block tensor, Delta = bf16(x_out - x_in):
+ * sum_d2 = sum Delta^2, sum_xin2 = sum x_in^2, sum_ddp = sum Delta*Delta_prev,
+ * sum_dp2 = sum Delta_prev^2, then the block OUTPUT's max |x|, sum |x| and
+ * element count, which are the next block's input statistics.  The three
+ * output fields are laid out like sixbit_tensor_stats' first three, so
+ * &stats->max_abs_out can be passed as a policy `in_stats`.
+ */
+typedef struct {
+  double sum_d2;
+  double sum_xin2;
+  double sum_ddp;
+  double sum_dp2;
+  double max_abs_out;
+  double sum_abs_out;
+  double count;
+  double reserved;
+} sixbit_stats;
+
+/* Policy thresholds (technical summary sections 2.A-2.C; popular summary sections 1-3). */
+typedef struct {
+  double gamma_thr;   /* Gamma >= gamma_thr -> INT8, else NVFP4 */
+  double cos_thr;     /* cos(Delta_{t-1}, Delta_{t-2}) >= cos_thr may skip */
+  double err_cap;     /* accumulated 1 - cos above err_cap forces a refresh */
+  double pdr_ratio;   /* input max/mean above pdr_ratio forces BF16 */
+  double near_rel;    /* relative band around thresholds reported as "near" */
+  int32_t refresh_bf16; /* 1: every forced refresh runs BF16 */
+  int32_t reserved;
+} sixbit_policy_cfg;
+
+/* Per-block policy state; zero-initialise before the first step. */
+typedef struct {
+  int32_t n_computed;
+  int32_t skipped_last;
+  int32_t have_gamma;
+  int32_t pending;      /* the last decision computed; fold its stats next step */
+  double gamma;
+  double cos;
+  double acc;
+  int32_t last_word;
+  int32_t steps;
+  int32_t n_skip, n_refresh, n_pdr, n_near, n_nvfp4, n_int8, n_bf16, reserved;
+} sixbit_policy_state;
+
+/* ---- sizes and layouts ------------------------------------------------- */
+
+/* Bytes of a tiled E4M3 scale array for `rows` x K elements (K % 64 == 0):
+ * rows rounded up to 128, times K/16. */
+size_t sixbit_fp4_scale_bytes(int rows, int K);
+/* Byte offset of the scale of row r, 16-element block kb in the tiled layout:
+ * (r/128)*(128*K/16) + (kb/4)*512 + (r%32)*16 + ((r/32)%4)*4 + kb%4.  Each
+ * 512-byte chunk holds 128 rows x 4 blocks, the unit the GEMM's scale copy
+ * into tensor memory consumes. */
+size_t sixbit_fp4_scale_offset(int r, int kb, int K);
+/* Scratch bytes sixbit_tensor_stats / sixbit_block_stats / sixbit_skip_apply
+ * need for `n` elements (per-CTA partial sums and a completion counter). */
+size_t sixbit_stats_scratch_bytes(int64_t n);
+
+/* ---- the hot path ------------------------------------------------------ */
+
+/*
+ * Offline weight preparation (technical summary section 4: 4-bit weights,
+ * W4A6/W4A8).  W: [N, K] float32.  had_block b in {16, 64, 256}, K % 128 == 0,
+ * K % b == 0.  Rotates W with the same FP32 butterfly as the activations, then
+ * quantizes W' to NVFP4 (two-level, static tensor scale) and to INT4
+ * (symmetric, groups of 128 along K), and rounds W to bf16.  Every field of
+ * `out` must be non-NULL.
+ */
+sixbit_status sixbit_pack_weights(const float* W, int N, int K, int had_block,
+                                  const sixbit_weights* out, int32_t* err_dev, void* stream);
+
+/*
+ * Online block-Hadamard rotation fused with dynamic quantization (technical
+ * summary section 2.A; popular summary section 1): y = x . blockdiag(H_b/sqrt b)
+ * by a fixed-order FP32 butterfly, then NVFP4 (mode 1) or INT8 (mode 2).
+ * X: [M, K] bf16; K % 128 == 0; b in {16, 64, 256}.  In NVFP4 mode the tensor
+ * amax is taken from `tamax_in` (a device float, e.g. from the producer of X)
+ * or, when it is NULL, computed by a first pass into out->tensor_amax.  Other
+ * modes (BF16, SKIP) enqueue nothing when mode_dev is NULL and return at once
+ * on the device otherwise.
+ */
+sixbit_status sixbit_hadamard_quant(const uint16_t* X, int M, int K, int had_block, int mode,
+                                    const int32_t* mode_dev, const float* tamax_in,
+                                    const sixbit_qact* out, int32_t* err_dev, void* stream);
+
+/*
+ * Quantized GEMM with fused epilogue (technical summary sections 2.A, 2.C, 4):
+ *   NVFP4: Y = s_tx * s_tw * sum_k (E2M1*E4M3)_x (E2M1*E4M3)_w   (A = qact, W fp4)
+ *   INT8 : Y = s_m * sum_g s_w[g] * acc_g, acc_g exact integer sums over
+ *          128-wide K groups (A = qact i8_operand, W i4_operand / i4_scales)
+ *   BF16 : Y = X_bf16 . bf16(W)^T  (A = X_bf16 unrotated, W bf16_w)
+ * then epilogue NONE, GELU (exact erf) or RESIDUAL (+ residual [M, N] bf16),
+ * rounded to bf16 into Y [M, N] -- or, when Y_f32 is non-NULL, written as
+ * float32 without the bf16 rounding (Y may then be NULL).  Accumulation is on
+ * the tensor cores in FP32 (tcgen05, accumulators in tensor memory).
+ * Constraints: K % 128 == 0, N % 16 == 0, M >= 1.  acc_dbg (INT8 only,
+ * optional): receives the exact group accumulators as int32 [K/128][M][N].
+ */
+sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W,
+                           int M, int N, int K, int mode, const int32_t* mode_dev, int epilogue,
+                           const uint16_t* residual, uint16_t* Y, float* Y_f32, int32_t* acc_dbg,
+                           int32_t* err_dev, void* stream);
+
+/*
+ * Block statistics and delta cache update for a computed block step
+ * (technical summary sections 2.A-2.C; popular summary sections 1-3):
+ * Delta = bf16(f32(x_out) - f32(x_in)) overwrites delta_cache (which holds
+ * Delta_prev on entry; zero it before the first step), and stats_dev receives
+ * the sums of sixbit_stats.  n = T*H elements, n % 8 == 0.  With mode_dev
+ * non-NULL and the mode SKIP, nothing is done.  scratch: device memory of
+ * sixbit_stats_scratch_bytes(n) bytes whose completion counter is zero on
+ * entry (zero it once; every call leaves it zero again).
+ */
+sixbit_status sixbit_block_stats(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta_cache,
+                                 int64_t n, const int32_t* mode_dev, sixbit_stats* stats_dev,
+                                 void* scratch, int32_t* err_dev, void* stream);
+
+/*
+ * Per-block decision for this step (technical summary sections 2.A-2.C;
+ * popular summary sections 1-3), one device thread.  If the previous decision
+ * computed, its statistics (last_stats_dev) are folded first: Gamma =
+ * sqrt(sum_d2)/sqrt(sum_xin2), cos = sum_ddp/sqrt(sum_d2*sum_dp2).  Then:
+ * skip if at least two computes happened, cos >= cos_thr and
+ * acc + (1 - cos) <= err_cap (acc += 1 - cos); else compute in BF16 if the
+ * input ratio max/mean > pdr_ratio, INT8 after a skip or before any Gamma,
+ * else INT8 if Gamma >= gamma_thr, else NVFP4.  in_stats_dev points to
+ * {max |x_in|, sum |x_in|, count} (float64).  The decision word goes to
+ * mode_dev[0].  cfg is a HOST pointer.
+ */
+sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_state* state_dev,
+                                 const sixbit_stats* last_stats_dev, const double* in_stats_dev,
+                                 int32_t* mode_dev, int32_t* err_dev, void* stream);
+
+/* ---- companions of the hot path ---------------------------------------- */
+
+/* Input statistics of a bf16 tensor (the first block's input): out_dev[0..3] =
+ * {max |x|, sum |x|, count, sum x^2} in float64.  n % 8 == 0.  scratch as for
+ * sixbit_block_stats. */
+sixbit_status sixbit_tensor_stats(const uint16_t* x, int64_t n, double* out_dev, void* scratch,
+                                  int32_t* err_dev, void* stream);
+
+/* TDC skip (technical summary section 2.B): x_out = bf16(f32(x_in) + f32(Delta)),
+ * and the output statistics into stats_dev->{max_abs_out, sum_abs_out, count}
+ * (other fields untouched).  With mode_dev non-NULL, runs only when the mode
+ * is SKIP.  n % 8 == 0.  scratch as for sixbit_block_stats. */
+sixbit_status sixbit_skip_apply(const uint16_t* x_in, const uint16_t* delta_cache, uint16_t* x_out,
+                                int64_t n, const int32_t* mode_dev, sixbit_stats* stats_dev,
+                                void* scratch, int32_t* err_dev, void* stream);
+
+/* Synchronize `stream` and return the status recorded in err_dev (and clear it). */
+sixbit_status sixbit_check(int32_t* err_dev, void* stream);
+
+/* Human-readable name of a status code. */
+const char* sixbit_status_str(sixbit_status s);
+
+/* Number of kernels the library has launched since it was loaded. */
+uint64_t sixbit_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SIXBIT_H */

@@ -1,0 +1,82 @@
+"""The C-ABI library loads and exports every call include/sixbit.h declares (CPU only).
+
+No compute is launched here: only host-side functions and argument checks
+that fail before any kernel would be enqueued.
+"""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+from tests._layouts import scale_offsets
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from video_dit_mixed_gb300 import abi
+    return abi.lib(build_if_missing=True)
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "sixbit.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sixbit_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+    from video_dit_mixed_gb300 import abi
+    assert set(names) == set(abi.EXPORTS)
+
+
+def test_scale_layout_host_functions(lib):
+    rows, k = 300, 384
+    off = scale_offsets(rows, k)
+    for r in (0, 1, 31, 32, 127, 128, 255, 299):
+        for kb in (0, 1, 3, 4, 7, 23):
+            assert lib.sixbit_fp4_scale_offset(r, kb, k) == off[r, kb]
+    assert lib.sixbit_fp4_scale_bytes(rows, k) == 384 * (k // 16)
+    # a bijection onto the buffer for full tiles
+    full = scale_offsets(256, k)
+    assert np.array_equal(np.sort(full.ravel()), np.arange(256 * k // 16))
+
+
+def test_argument_errors_return_status_without_launching(lib):
+    from video_dit_mixed_gb300 import abi
+    before = lib.sixbit_launch_count()
+    qa = abi.QAct()
+    w = abi.Weights()
+    # NULL input
+    assert lib.sixbit_hadamard_quant(None, 16, 128, 16, abi.MODE_NVFP4, None, None, C.byref(qa), None, None) == 1
+    # K not a multiple of 128
+    buf = C.create_string_buffer(64)
+    p = C.cast(buf, C.c_void_p)
+    assert lib.sixbit_hadamard_quant(p, 16, 96, 16, abi.MODE_INT8, None, None, C.byref(qa), None, None) == 2
+    # unsupported Hadamard block
+    assert lib.sixbit_hadamard_quant(p, 16, 128, 32, abi.MODE_INT8, None, None, C.byref(qa), None, None) == 2
+    # GEMM: missing output, bad epilogue, bad N
+    assert lib.sixbit_qgemm(C.byref(qa), None, C.byref(w), 16, 128, 128, 1, None, 0, None, None, None, None,
+                            None, None) == 1
+    assert lib.sixbit_qgemm(C.byref(qa), None, C.byref(w), 16, 120, 128, 1, None, 0, None, p, None, None,
+                            None, None) == 2
+    assert lib.sixbit_qgemm(C.byref(qa), None, C.byref(w), 16, 128, 128, 1, None, 7, None, p, None, None,
+                            None, None) == 1
+    # stats: n not a multiple of 8
+    assert lib.sixbit_block_stats(p, p, p, 12, None, p, p, None, None) == 2
+    assert lib.sixbit_policy_step(None, p, p, p, p, None, None) == 1
+    assert lib.sixbit_launch_count() == before
+    assert lib.sixbit_status_str(6) == b"device-side wait timed out"
+
+
+def test_struct_sizes_match_header():
+    from video_dit_mixed_gb300 import abi
+    assert C.sizeof(abi.QAct) == 64 and C.sizeof(abi.Weights) == 64
+    assert C.sizeof(abi.Stats) == 64 and C.sizeof(abi.PolicyCfg) == 48
+    assert C.sizeof(abi.PolicyState) == 80

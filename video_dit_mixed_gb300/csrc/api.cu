@@ -1,0 +1,299 @@
+// extern "C" entry points of libsixbit: argument validation, tensor-map
+// construction for the GEMM's TMA loads, and kernel dispatch.  The library
+// allocates no device memory.
+#include <atomic>
+#include <cstdint>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace sixbit {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static bool valid_block(int b) { return b == 16 || b == 64 || b == 256; }
+
+// Checks that the current device is a compute capability 10.3 GPU (once per device).
+static sixbit_status check_device() {
+  static int ok_dev = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SIXBIT_EUNSUPPORTED;
+  if (dev == ok_dev) return SIXBIT_OK;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return SIXBIT_EUNSUPPORTED;
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return SIXBIT_EUNSUPPORTED;
+  ok_dev = dev;
+  return SIXBIT_OK;
+}
+
+static sixbit_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SIXBIT_OK : SIXBIT_ECUDA; }
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D row-major tensor [rows, cols] of `dtype`, box = 128 bytes of columns x
+// `box_rows` rows, 128-byte swizzle, out-of-bounds rows read as zero.
+static bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, int elem_bytes, int rows, int cols,
+                     int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem_bytes};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elem_bytes), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace sixbit
+
+using namespace sixbit;
+
+extern "C" {
+
+size_t sixbit_fp4_scale_bytes(int rows, int K) {
+  if (rows < 0 || K < 0) return 0;
+  return static_cast<size_t>((rows + 127) / 128) * 128 * static_cast<size_t>(K / 16);
+}
+
+size_t sixbit_fp4_scale_offset(int r, int kb, int K) {
+  return static_cast<size_t>(r / 128) * (128 * static_cast<size_t>(K / 16)) + static_cast<size_t>(kb / 4) * 512 +
+         static_cast<size_t>((r % 32) * 16 + ((r / 32) % 4) * 4 + (kb % 4));
+}
+
+size_t sixbit_stats_scratch_bytes(int64_t n) { return stats_scratch_bytes(n); }
+
+uint64_t sixbit_launch_count(void) { return g_launches.load(); }
+
+const char* sixbit_status_str(sixbit_status s) {
+  switch (s) {
+    case SIXBIT_OK: return "ok";
+    case SIXBIT_EINVAL: return "invalid argument";
+    case SIXBIT_ESHAPE: return "unsupported shape";
+    case SIXBIT_EALIGN: return "pointer not 16-byte aligned";
+    case SIXBIT_EUNSUPPORTED: return "no compute capability 10.3 device";
+    case SIXBIT_ECUDA: return "CUDA runtime error";
+    case SIXBIT_ETIMEOUT: return "device-side wait timed out";
+    case SIXBIT_EDEVICE: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+sixbit_status sixbit_check(int32_t* err_dev, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SIXBIT_ECUDA;
+  if (err_dev == nullptr) return SIXBIT_OK;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, err_dev, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SIXBIT_ECUDA;
+  if (v != 0) {
+    const int32_t z = 0;
+    cudaMemcpy(err_dev, &z, sizeof(z), cudaMemcpyHostToDevice);
+  }
+  return v;
+}
+
+sixbit_status sixbit_pack_weights(const float* W, int N, int K, int had_block, const sixbit_weights* out,
+                                  int32_t* err_dev, void* stream) {
+  (void)err_dev;
+  if (W == nullptr || out == nullptr || out->fp4_codes == nullptr || out->fp4_scales == nullptr ||
+      out->fp4_amax == nullptr || out->fp4_tensor_scale == nullptr || out->i4_codes == nullptr ||
+      out->i4_scales == nullptr || out->i4_operand == nullptr || out->bf16_w == nullptr)
+    return SIXBIT_EINVAL;
+  if (N <= 0 || K <= 0 || K % 128 != 0 || !valid_block(had_block) || K % had_block != 0) return SIXBIT_ESHAPE;
+  if (!aligned16(W) || !aligned16(out->fp4_codes) || !aligned16(out->i4_codes) || !aligned16(out->i4_operand) ||
+      !aligned16(out->bf16_w))
+    return SIXBIT_EALIGN;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+  return cuda_status(launch_pack_weights(W, N, K, had_block, out, static_cast<cudaStream_t>(stream)));
+}
+
+sixbit_status sixbit_hadamard_quant(const uint16_t* X, int M, int K, int had_block, int mode,
+                                    const int32_t* mode_dev, const float* tamax_in, const sixbit_qact* out,
+                                    int32_t* err_dev, void* stream) {
+  (void)err_dev;
+  if (X == nullptr || out == nullptr) return SIXBIT_EINVAL;
+  if (M <= 0 || K <= 0 || K % 128 != 0 || !valid_block(had_block) || K % had_block != 0) return SIXBIT_ESHAPE;
+  if (!aligned16(X) || (out->rotated && !aligned16(out->rotated))) return SIXBIT_EALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool want_fp4 = mode_dev != nullptr || mode == SIXBIT_MODE_NVFP4;
+  const bool want_i8 = mode_dev != nullptr || mode == SIXBIT_MODE_INT8;
+  if (mode_dev == nullptr && mode != SIXBIT_MODE_NVFP4 && mode != SIXBIT_MODE_INT8) {
+    if (mode == SIXBIT_MODE_BF16 || mode == SIXBIT_MODE_SKIP) return SIXBIT_OK;
+    return SIXBIT_EINVAL;
+  }
+  if (want_fp4 && (out->fp4_codes == nullptr || out->fp4_scales == nullptr || out->tensor_scale == nullptr ||
+                   (tamax_in == nullptr && out->tensor_amax == nullptr)))
+    return SIXBIT_EINVAL;
+  if (want_i8 && (out->i8_codes == nullptr || out->row_scale == nullptr)) return SIXBIT_EINVAL;
+  if (want_fp4 && !aligned16(out->fp4_codes)) return SIXBIT_EALIGN;
+  if (want_i8 && (!aligned16(out->i8_codes) || (out->i8_operand && !aligned16(out->i8_operand))))
+    return SIXBIT_EALIGN;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+  if (want_fp4) {
+    const float* amax = tamax_in;
+    if (amax == nullptr) {
+      cudaError_t e = launch_hq_amax(X, M, K, had_block, mode_dev, out->tensor_amax, st);
+      if (e != cudaSuccess) return SIXBIT_ECUDA;
+      amax = out->tensor_amax;
+    }
+    cudaError_t e = launch_hq_nvfp4(X, M, K, had_block, mode_dev, amax, out, st);
+    if (e != cudaSuccess) return SIXBIT_ECUDA;
+  }
+  if (want_i8) {
+    cudaError_t e = launch_hq_int8(X, M, K, had_block, mode_dev, out, st);
+    if (e != cudaSuccess) return SIXBIT_ECUDA;
+  }
+  return SIXBIT_OK;
+}
+
+sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W, int M, int N,
+                           int K, int mode, const int32_t* mode_dev, int epilogue, const uint16_t* residual,
+                           uint16_t* Y, float* Y_f32, int32_t* acc_dbg, int32_t* err_dev, void* stream) {
+  if (W == nullptr || (Y == nullptr && Y_f32 == nullptr)) return SIXBIT_EINVAL;
+  if (epilogue != SIXBIT_EPI_NONE && epilogue != SIXBIT_EPI_GELU && epilogue != SIXBIT_EPI_RESIDUAL)
+    return SIXBIT_EINVAL;
+  if (epilogue == SIXBIT_EPI_RESIDUAL && residual == nullptr) return SIXBIT_EINVAL;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 16 != 0) return SIXBIT_ESHAPE;
+  if ((Y && !aligned16(Y)) || (Y_f32 && !aligned16(Y_f32)) || (residual && !aligned16(residual)))
+    return SIXBIT_EALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool run_fp4 = mode_dev != nullptr || mode == SIXBIT_MODE_NVFP4;
+  const bool run_i8 = mode_dev != nullptr || mode == SIXBIT_MODE_INT8;
+  const bool run_bf = mode_dev != nullptr || mode == SIXBIT_MODE_BF16;
+  if (mode_dev == nullptr && !run_fp4 && !run_i8 && !run_bf) return mode == SIXBIT_MODE_SKIP ? SIXBIT_OK : SIXBIT_EINVAL;
+  if ((run_fp4 || run_i8) && A == nullptr) return SIXBIT_EINVAL;
+  if (run_fp4 && (A->fp4_codes == nullptr || A->fp4_scales == nullptr || A->tensor_scale == nullptr ||
+                  W->fp4_codes == nullptr || W->fp4_scales == nullptr || W->fp4_tensor_scale == nullptr))
+    return SIXBIT_EINVAL;
+  if (run_i8 && (A->i8_operand == nullptr || A->row_scale == nullptr || W->i4_operand == nullptr ||
+                 W->i4_scales == nullptr))
+    return SIXBIT_EINVAL;
+  if (run_bf && (X_bf16 == nullptr || W->bf16_w == nullptr)) return SIXBIT_EINVAL;
+  if ((run_fp4 && (!aligned16(A->fp4_codes) || !aligned16(A->fp4_scales) || !aligned16(W->fp4_codes) ||
+                   !aligned16(W->fp4_scales))) ||
+      (run_i8 && (!aligned16(A->i8_operand) || !aligned16(W->i4_operand))) ||
+      (run_bf && (!aligned16(X_bf16) || !aligned16(W->bf16_w))))
+    return SIXBIT_EALIGN;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+
+  GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.mode_dev = mode_dev;
+  p.epilogue = epilogue;
+  p.residual = residual;
+  p.Y = Y;
+  p.Yf = Y_f32;
+  p.err = err_dev;
+  if (run_fp4) {
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A->fp4_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, M, K / 2, 128) ||
+        !make_map(&mb, W->fp4_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, 128))
+      return SIXBIT_ECUDA;
+    GemmParams q = p;
+    q.want_mode = SIXBIT_MODE_NVFP4;
+    q.sfa = A->fp4_scales;
+    q.sfb = W->fp4_scales;
+    q.s_a = A->tensor_scale;
+    q.s_b = W->fp4_tensor_scale;
+    if (launch_qgemm_nvf4(ma, mb, q, st) != cudaSuccess) return SIXBIT_ECUDA;
+  }
+  if (run_i8) {
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A->i8_operand, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, 128) ||
+        !make_map(&mb, W->i4_operand, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, 128))
+      return SIXBIT_ECUDA;
+    GemmParams q = p;
+    q.want_mode = SIXBIT_MODE_INT8;
+    q.row_scale = A->row_scale;
+    q.grp_scale = W->i4_scales;
+    q.acc_dbg = acc_dbg;
+    if (launch_qgemm_int8(ma, mb, q, st) != cudaSuccess) return SIXBIT_ECUDA;
+  }
+  if (run_bf) {
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, X_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, 128) ||
+        !make_map(&mb, W->bf16_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, 128))
+      return SIXBIT_ECUDA;
+    GemmParams q = p;
+    q.want_mode = SIXBIT_MODE_BF16;
+    if (launch_qgemm_bf16(ma, mb, q, st) != cudaSuccess) return SIXBIT_ECUDA;
+  }
+  return SIXBIT_OK;
+}
+
+sixbit_status sixbit_block_stats(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta_cache, int64_t n,
+                                 const int32_t* mode_dev, sixbit_stats* stats_dev, void* scratch, int32_t* err_dev,
+                                 void* stream) {
+  (void)err_dev;
+  if (x_in == nullptr || x_out == nullptr || delta_cache == nullptr || stats_dev == nullptr || scratch == nullptr)
+    return SIXBIT_EINVAL;
+  if (n <= 0 || n % 8 != 0) return SIXBIT_ESHAPE;
+  if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(delta_cache) || !aligned16(scratch)) return SIXBIT_EALIGN;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+  return cuda_status(
+      launch_block_stats(x_in, x_out, delta_cache, n, mode_dev, stats_dev, scratch, static_cast<cudaStream_t>(stream)));
+}
+
+sixbit_status sixbit_tensor_stats(const uint16_t* x, int64_t n, double* out_dev, void* scratch, int32_t* err_dev,
+                                  void* stream) {
+  (void)err_dev;
+  if (x == nullptr || out_dev == nullptr || scratch == nullptr) return SIXBIT_EINVAL;
+  if (n <= 0 || n % 8 != 0) return SIXBIT_ESHAPE;
+  if (!aligned16(x) || !aligned16(scratch)) return SIXBIT_EALIGN;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+  return cuda_status(launch_tensor_stats(x, n, out_dev, scratch, static_cast<cudaStream_t>(stream)));
+}
+
+sixbit_status sixbit_skip_apply(const uint16_t* x_in, const uint16_t* delta_cache, uint16_t* x_out, int64_t n,
+                                const int32_t* mode_dev, sixbit_stats* stats_dev, void* scratch, int32_t* err_dev,
+                                void* stream) {
+  (void)err_dev;
+  if (x_in == nullptr || delta_cache == nullptr || x_out == nullptr || stats_dev == nullptr || scratch == nullptr)
+    return SIXBIT_EINVAL;
+  if (n <= 0 || n % 8 != 0) return SIXBIT_ESHAPE;
+  if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(delta_cache) || !aligned16(scratch)) return SIXBIT_EALIGN;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+  return cuda_status(
+      launch_skip_apply(x_in, delta_cache, x_out, n, mode_dev, stats_dev, scratch, static_cast<cudaStream_t>(stream)));
+}
+
+sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_state* state_dev,
+                                 const sixbit_stats* last_stats_dev, const double* in_stats_dev, int32_t* mode_dev,
+                                 int32_t* err_dev, void* stream) {
+  (void)err_dev;
+  if (cfg == nullptr || state_dev == nullptr || last_stats_dev == nullptr || in_stats_dev == nullptr ||
+      mode_dev == nullptr)
+    return SIXBIT_EINVAL;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+  return cuda_status(
+      launch_policy(*cfg, state_dev, last_stats_dev, in_stats_dev, mode_dev, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,440 @@
+// Online block-Hadamard rotation fused with dynamic NVFP4 / INT8 quantization
+// of activations, and the offline rotation + 4-bit packing of weights.
+//
+// Method: "6Bit-Diffusion" technical summary section 2.A (DMPQ: NVFP4 for
+// stable blocks, INT8 for volatile ones; online block Hadamard transform
+// against outliers) and section 4 (custom CUDA kernels fuse the
+// quantization with the block Hadamard transform).
+//
+// Work layout: one warp per row.  A row is walked in chunks of 256 elements;
+// lane l holds elements [8l, 8l+8) of the chunk, loaded with one 16-byte
+// non-coherent load.  A Hadamard block of b elements therefore lives in b/8
+// consecutive lanes: strides 1, 2, 4 of the butterfly are done in registers,
+// strides 8 .. b/2 with shfl.xor across lanes, in ascending order, each step
+// one IEEE FP32 add or subtract, then one exact multiply by 2^-log4(b).  The
+// 16-element NVFP4 groups are lane pairs; the 128-element INT4 weight groups
+// are 16-lane halves.
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace sixbit {
+
+constexpr int kHqWarps = 8;  // warps per CTA
+
+__device__ __forceinline__ size_t sf_offset(int r, int kb, int K) {
+  return static_cast<size_t>(r >> 7) * static_cast<size_t>(128 * (K >> 4)) + static_cast<size_t>(kb >> 2) * 512 +
+         static_cast<size_t>((r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3));
+}
+
+__device__ __forceinline__ uint4 ld_nc_16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& r, float (&v)[8]) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Fixed-order FP32 butterfly over a Hadamard block of B elements spread over
+// B/8 lanes (8 per lane), followed by the exact 1/sqrt(B) scaling.
+template <int B>
+__device__ __forceinline__ void fwht8(float (&v)[8], int lane) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], c = v[i + h];
+        v[i] = __fadd_rn(a, c);
+        v[i + h] = __fsub_rn(a, c);
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 8; h < B; h <<= 1) {
+    const int m = h >> 3;
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+      v[i] = upper ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
+    }
+  }
+  constexpr float s = B == 16 ? 0.25f : (B == 64 ? 0.125f : 0.0625f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], s);
+}
+
+__device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return r & 0xFFu;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c)));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// Eight FP32 values -> eight E2M1 codes, element 0 in the low nibble.
+__device__ __forceinline__ uint32_t f32x8_to_e2m1(const float (&q)[8]) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return out;
+}
+
+__device__ __forceinline__ bool mode_skips(const int32_t* mode_dev, int want) {
+  return mode_dev != nullptr && SIXBIT_MODE_OF(*mode_dev) != want;
+}
+
+__device__ __forceinline__ float warp_max(float m) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
+// Loads up to 4 chunks of a bf16 row (chunks c0..c0+3) into registers.
+__device__ __forceinline__ void load_chunks_bf16(const uint16_t* row, int K, int c0, int nch, int lane,
+                                                 uint4 (&raw)[4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int col = (c0 + u) * 256 + lane * 8;
+    raw[u] = make_uint4(0, 0, 0, 0);
+    if (c0 + u < nch && col < K) raw[u] = ld_nc_16(row + col);
+  }
+}
+
+// ------------------------------------------------ pass 1: tensor amax |y| --
+
+template <int B>
+__global__ void __launch_bounds__(kHqWarps * 32) hq_amax_kernel(const uint16_t* __restrict__ X, int M, int K,
+                                                                const int32_t* mode_dev, float* amax_out) {
+  if (mode_skips(mode_dev, SIXBIT_MODE_NVFP4)) return;
+  const int lane = threadIdx.x & 31;
+  const int warp = blockIdx.x * kHqWarps + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * kHqWarps;
+  const int nch = (K + 255) >> 8;
+  float m = 0.f;
+  for (int r = warp; r < M; r += nwarps) {
+    const uint16_t* row = X + static_cast<size_t>(r) * K;
+    for (int c0 = 0; c0 < nch; c0 += 4) {
+      uint4 raw[4];
+      load_chunks_bf16(row, K, c0, nch, lane, raw);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (c0 + u >= nch) break;
+        float v[8];
+        bf16x8_to_f32(raw[u], v);
+        fwht8<B>(v, lane);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+      }
+    }
+  }
+  m = warp_max(m);
+  __shared__ float red[kHqWarps];
+  if (lane == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = red[0];
+    for (int i = 1; i < kHqWarps; ++i) b = fmaxf(b, red[i]);
+    atomicMax(reinterpret_cast<unsigned int*>(amax_out), __float_as_uint(b));  // b >= 0
+  }
+}
+
+// ----------------------------------------------------- NVFP4 quantization --
+
+// One 256-element chunk of NVFP4 quantization for lane `lane` of row r.
+template <int B>
+__device__ __forceinline__ void nvfp4_chunk(float (&v)[8], int r, int col, bool row_ok, int K, int lane, float s_t,
+                                            uint8_t* codes, uint8_t* scales, float* rotated) {
+  const bool active = row_ok && col < K;
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
+  am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+  const float sb = __fdiv_rn(__fdiv_rn(am, 6.0f), s_t);
+  const uint32_t e = f32_to_e4m3(sb);
+  const float S = __fmul_rn(e4m3_to_f32(e), s_t);
+  float q[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) q[i] = (S != 0.f) ? __fdiv_rn(v[i], S) : 0.f;
+  const uint32_t packed = f32x8_to_e2m1(q);
+  if (active) {
+    *reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(r) * (K >> 1) + (col >> 1)) = packed;
+    if (rotated != nullptr) {
+      float4* dst = reinterpret_cast<float4*>(rotated + static_cast<size_t>(r) * K + col);
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  }
+  if ((lane & 1) == 0 && col < K) scales[sf_offset(r, col >> 4, K)] = row_ok ? static_cast<uint8_t>(e) : 0;
+}
+
+// Rows [0, M) are quantized; rows [M, round_up(M,128)) get zero scales so the
+// GEMM never multiplies by an undefined scale.
+template <int B>
+__global__ void __launch_bounds__(kHqWarps * 32) hq_nvfp4_kernel(const uint16_t* __restrict__ X, int M, int K,
+                                                                 const int32_t* mode_dev, const float* amax_src,
+                                                                 uint8_t* codes, uint8_t* scales, float* tscale_out,
+                                                                 float* rotated) {
+  if (mode_skips(mode_dev, SIXBIT_MODE_NVFP4)) return;
+  const float amax = *amax_src;
+  const float s_t = amax == 0.f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *tscale_out = s_t;
+  const int lane = threadIdx.x & 31;
+  const int warp = blockIdx.x * kHqWarps + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * kHqWarps;
+  const int nch = (K + 255) >> 8;
+  const int mpad = (M + 127) & ~127;
+  for (int r = warp; r < mpad; r += nwarps) {
+    const bool row_ok = r < M;
+    const uint16_t* row = X + static_cast<size_t>(row_ok ? r : 0) * K;
+    for (int c0 = 0; c0 < nch; c0 += 4) {
+      uint4 raw[4];
+      if (row_ok) {
+        load_chunks_bf16(row, K, c0, nch, lane, raw);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) raw[u] = make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (c0 + u >= nch) break;
+        float v[8];
+        bf16x8_to_f32(raw[u], v);
+        fwht8<B>(v, lane);
+        nvfp4_chunk<B>(v, r, (c0 + u) * 256 + lane * 8, row_ok, K, lane, s_t, codes, scales, rotated);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------ INT8 quantization --
+
+template <int B>
+__global__ void __launch_bounds__(kHqWarps * 32) hq_int8_kernel(const uint16_t* __restrict__ X, int M, int K,
+                                                                const int32_t* mode_dev, int8_t* codes,
+                                                                float* row_scale, uint16_t* operand,
+                                                                float* rotated) {
+  if (mode_skips(mode_dev, SIXBIT_MODE_INT8)) return;
+  const int lane = threadIdx.x & 31;
+  const int warp = blockIdx.x * kHqWarps + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * kHqWarps;
+  const int nch = (K + 255) >> 8;
+  for (int r = warp; r < M; r += nwarps) {
+    const uint16_t* row = X + static_cast<size_t>(r) * K;
+    // pass 1: row amax of the rotated values
+    float m = 0.f;
+    for (int c0 = 0; c0 < nch; c0 += 4) {
+      uint4 raw[4];
+      load_chunks_bf16(row, K, c0, nch, lane, raw);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (c0 + u >= nch) break;
+        float v[8];
+        bf16x8_to_f32(raw[u], v);
+        fwht8<B>(v, lane);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+      }
+    }
+    m = warp_max(m);
+    const float s = __fdiv_rn(m, 127.0f);
+    if (lane == 0) row_scale[r] = s;
+    // pass 2: the row again (from cache), rotate, quantize
+    for (int c0 = 0; c0 < nch; c0 += 4) {
+      uint4 raw[4];
+      load_chunks_bf16(row, K, c0, nch, lane, raw);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (c0 + u >= nch) break;
+        float v[8];
+        bf16x8_to_f32(raw[u], v);
+        fwht8<B>(v, lane);
+        const int col = (c0 + u) * 256 + lane * 8;
+        if (col < K) {
+          uint32_t qb[2] = {0, 0};
+          uint32_t ob[4] = {0, 0, 0, 0};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float q = 0.f;
+            if (s != 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(v[i], s)), -127.f), 127.f);
+            const int qi = static_cast<int>(q);
+            qb[i >> 2] |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * (i & 3));
+            ob[i >> 1] |= (__float_as_uint(q) >> 16) << (16 * (i & 1));  // integers |q|<=127 are exact in bf16
+          }
+          *reinterpret_cast<uint2*>(codes + static_cast<size_t>(r) * K + col) = make_uint2(qb[0], qb[1]);
+          if (operand != nullptr)
+            *reinterpret_cast<uint4*>(operand + static_cast<size_t>(r) * K + col) =
+                make_uint4(ob[0], ob[1], ob[2], ob[3]);
+          if (rotated != nullptr) {
+            float4* dst = reinterpret_cast<float4*>(rotated + static_cast<size_t>(r) * K + col);
+            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+          }
+        }
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------- weight packing --
+
+__device__ __forceinline__ void load8_f32(const float* p, float (&v)[8]) {
+  const uint4 a = ld_nc_16(p), b = ld_nc_16(p + 4);
+  v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+  v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+}
+
+template <int B>
+__global__ void __launch_bounds__(kHqWarps * 32) pack_amax_kernel(const float* __restrict__ W, int N, int K,
+                                                                  float* amax_out) {
+  const int lane = threadIdx.x & 31;
+  const int warp = blockIdx.x * kHqWarps + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * kHqWarps;
+  const int nch = (K + 255) >> 8;
+  float m = 0.f;
+  for (int r = warp; r < N; r += nwarps) {
+    for (int c = 0; c < nch; ++c) {
+      const int col = c * 256 + lane * 8;
+      float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (col < K) load8_f32(W + static_cast<size_t>(r) * K + col, v);
+      fwht8<B>(v, lane);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    }
+  }
+  m = warp_max(m);
+  if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(amax_out), __float_as_uint(m));
+}
+
+template <int B>
+__global__ void __launch_bounds__(kHqWarps * 32) pack_quant_kernel(const float* __restrict__ W, int N, int K,
+                                                                   const float* amax_src, sixbit_weights out) {
+  const float amax = *amax_src;
+  const float s_t = amax == 0.f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *out.fp4_tensor_scale = s_t;
+  const int lane = threadIdx.x & 31;
+  const int warp = blockIdx.x * kHqWarps + (threadIdx.x >> 5);
+  const int nwarps = gridDim.x * kHqWarps;
+  const int nch = (K + 255) >> 8;
+  const int npad = (N + 127) & ~127;
+  for (int r = warp; r < npad; r += nwarps) {
+    const bool row_ok = r < N;
+    for (int c = 0; c < nch; ++c) {
+      const int col = c * 256 + lane * 8;
+      const bool active = row_ok && col < K;
+      float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (active) {
+        load8_f32(W + static_cast<size_t>(r) * K + col, v);
+        uint32_t bw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+          bw[i] = *reinterpret_cast<const uint32_t*>(&p);
+        }
+        *reinterpret_cast<uint4*>(out.bf16_w + static_cast<size_t>(r) * K + col) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+      }
+      fwht8<B>(v, lane);
+      nvfp4_chunk<B>(v, r, col, row_ok, K, lane, s_t, out.fp4_codes, out.fp4_scales, nullptr);
+      // INT4, groups of 128 = 16 lanes
+      float am = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const float s = __fdiv_rn(am, 7.0f);
+      if (active) {
+        uint32_t nib = 0;
+        uint32_t ob[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float q = 0.f;
+          if (s != 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(v[i], s)), -7.f), 7.f);
+          nib |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFu) << (4 * i);
+          ob[i >> 1] |= (__float_as_uint(q) >> 16) << (16 * (i & 1));
+        }
+        *reinterpret_cast<uint32_t*>(out.i4_codes + static_cast<size_t>(r) * (K >> 1) + (col >> 1)) = nib;
+        *reinterpret_cast<uint4*>(out.i4_operand + static_cast<size_t>(r) * K + col) =
+            make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        if ((lane & 15) == 0) out.i4_scales[static_cast<size_t>(col >> 7) * N + r] = s;
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------- host launch --
+
+static int hq_grid(int rows) {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int want = (rows + kHqWarps - 1) / kHqWarps;
+  const int cap = sms * 8;
+  return want < cap ? (want > 0 ? want : 1) : cap;
+}
+
+#define SIXBIT_DISPATCH_B(b, KERNEL, ...)                                              \
+  do {                                                                                 \
+    if ((b) == 16) KERNEL<16><<<grid, kHqWarps * 32, 0, st>>>(__VA_ARGS__);            \
+    else if ((b) == 64) KERNEL<64><<<grid, kHqWarps * 32, 0, st>>>(__VA_ARGS__);       \
+    else KERNEL<256><<<grid, kHqWarps * 32, 0, st>>>(__VA_ARGS__);                     \
+    note_launch();                                                                     \
+  } while (0)
+
+cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, float* amax_out,
+                           cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  const int grid = hq_grid(M);
+  SIXBIT_DISPATCH_B(b, hq_amax_kernel, X, M, K, mode_dev, amax_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hq_nvfp4(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, const float* amax_src,
+                            const sixbit_qact* o, cudaStream_t st) {
+  const int grid = hq_grid((M + 127) & ~127);
+  SIXBIT_DISPATCH_B(b, hq_nvfp4_kernel, X, M, K, mode_dev, amax_src, o->fp4_codes, o->fp4_scales, o->tensor_scale,
+                    o->rotated);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hq_int8(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, const sixbit_qact* o,
+                           cudaStream_t st) {
+  const int grid = hq_grid(M);
+  SIXBIT_DISPATCH_B(b, hq_int8_kernel, X, M, K, mode_dev, o->i8_codes, o->row_scale, o->i8_operand, o->rotated);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_weights(const float* W, int N, int K, int b, const sixbit_weights* o, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(o->fp4_amax, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  int grid = hq_grid(N);
+  SIXBIT_DISPATCH_B(b, pack_amax_kernel, W, N, K, o->fp4_amax);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  grid = hq_grid((N + 127) & ~127);
+  SIXBIT_DISPATCH_B(b, pack_quant_kernel, W, N, K, o->fp4_amax, *o);
+  return cudaGetLastError();
+}
+
+}  // namespace sixbit

@@ -1,0 +1,51 @@
+// Internal interface between the C-ABI layer and the kernel translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "sixbit.h"
+
+namespace sixbit {
+
+struct GemmParams {
+  int M, N, K;
+  const int32_t* mode_dev;
+  int want_mode;
+  int epilogue;
+  const uint8_t* sfa;      // NVFP4 tiled scales of A
+  const uint8_t* sfb;      // NVFP4 tiled scales of B
+  const float* s_a;        // NVFP4 tensor scale of A
+  const float* s_b;        // NVFP4 tensor scale of B
+  const float* row_scale;  // INT8: s_m [M]
+  const float* grp_scale;  // INT8: s_w [K/128][N]
+  const uint16_t* residual;
+  uint16_t* Y;
+  float* Yf;
+  int32_t* acc_dbg;
+  int32_t* err;
+};
+
+cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, float* amax_out,
+                           cudaStream_t st);
+cudaError_t launch_hq_nvfp4(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, const float* amax_src,
+                            const sixbit_qact* o, cudaStream_t st);
+cudaError_t launch_hq_int8(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, const sixbit_qact* o,
+                           cudaStream_t st);
+cudaError_t launch_pack_weights(const float* W, int N, int K, int b, const sixbit_weights* o, cudaStream_t st);
+
+size_t stats_scratch_bytes(int64_t n);
+cudaError_t launch_tensor_stats(const uint16_t* x, int64_t n, double* out, void* scratch, cudaStream_t st);
+cudaError_t launch_block_stats(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta, int64_t n,
+                               const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st);
+cudaError_t launch_skip_apply(const uint16_t* x_in, const uint16_t* delta, uint16_t* x_out, int64_t n,
+                              const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st);
+cudaError_t launch_policy(const sixbit_policy_cfg& cfg, sixbit_policy_state* st_dev, const sixbit_stats* last,
+                          const double* in_stats, int32_t* mode_out, cudaStream_t st);
+
+cudaError_t launch_qgemm_nvf4(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st);
+cudaError_t launch_qgemm_bf16(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st);
+cudaError_t launch_qgemm_int8(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st);
+
+}  // namespace sixbit

@@ -1,0 +1,163 @@
+"""Torch-facing binding of libsixbit: argument marshalling only.
+
+Every function here allocates its output tensors with torch (device memory),
+passes raw pointers and the current CUDA stream to the C ABI, and raises
+``SixbitError`` on a non-zero status.  All arithmetic runs in the library's
+CUDA kernels; there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import abi
+from .abi import (EPI_GELU, EPI_NONE, EPI_RESIDUAL, MODE_BF16, MODE_INT8, MODE_NVFP4, MODE_SKIP,  # noqa: F401
+                  PolicyCfg, PolicyState, QAct, Stats, Weights, check, lib)
+
+_lib = lib()
+
+
+def _p(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def fp4_scale_bytes(rows: int, k: int) -> int:
+    return int(_lib.sixbit_fp4_scale_bytes(rows, k))
+
+
+def stats_scratch_bytes(n: int) -> int:
+    return int(_lib.sixbit_stats_scratch_bytes(n))
+
+
+def launch_count() -> int:
+    return int(_lib.sixbit_launch_count())
+
+
+class QActTensors:
+    """Device buffers of one quantized activation tensor [M, K]."""
+
+    def __init__(self, m: int, k: int, device="cuda", nvfp4=True, int8=True, rotated=False, i8_operand=True):
+        self.m, self.k = m, k
+        dev = torch.device(device)
+        u8, f32 = torch.uint8, torch.float32
+        self.fp4_codes = torch.empty((m, k // 2), dtype=u8, device=dev) if nvfp4 else None
+        self.fp4_scales = torch.zeros(fp4_scale_bytes(m, k), dtype=u8, device=dev) if nvfp4 else None
+        self.tensor_amax = torch.zeros(1, dtype=f32, device=dev) if nvfp4 else None
+        self.tensor_scale = torch.zeros(1, dtype=f32, device=dev) if nvfp4 else None
+        self.i8_codes = torch.empty((m, k), dtype=torch.int8, device=dev) if int8 else None
+        self.row_scale = torch.empty(m, dtype=f32, device=dev) if int8 else None
+        self.i8_operand = torch.empty((m, k), dtype=torch.bfloat16, device=dev) if (int8 and i8_operand) else None
+        self.rotated = torch.empty((m, k), dtype=f32, device=dev) if rotated else None
+
+    def c(self) -> QAct:
+        return QAct(*[_p(getattr(self, f)) for f, _ in QAct._fields_])
+
+
+class PackedWeights:
+    """Device buffers of one packed linear layer W [N, K]."""
+
+    def __init__(self, n: int, k: int, device="cuda"):
+        self.n, self.k = n, k
+        dev = torch.device(device)
+        self.fp4_codes = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
+        self.fp4_scales = torch.zeros(fp4_scale_bytes(n, k), dtype=torch.uint8, device=dev)
+        self.fp4_amax = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.fp4_tensor_scale = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.i4_codes = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
+        self.i4_scales = torch.empty((k // 128, n), dtype=torch.float32, device=dev)
+        self.i4_operand = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+        self.bf16_w = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+
+    def c(self) -> Weights:
+        return Weights(*[_p(getattr(self, f)) for f, _ in Weights._fields_])
+
+
+def pack_weights(w: torch.Tensor, had_block: int, out: PackedWeights | None = None, stream=None) -> PackedWeights:
+    assert w.dtype == torch.float32 and w.is_contiguous()
+    n, k = w.shape
+    out = out or PackedWeights(n, k, w.device)
+    cw = out.c()
+    check(_lib.sixbit_pack_weights(_p(w), n, k, had_block, C.byref(cw), None, _stream(stream)), "pack_weights")
+    return out
+
+
+def hadamard_quant(x: torch.Tensor, had_block: int, mode: int, out: QActTensors | None = None, mode_dev=None,
+                   tamax=None, stream=None) -> QActTensors:
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    m, k = x.shape
+    out = out or QActTensors(m, k, x.device)
+    ca = out.c()
+    check(_lib.sixbit_hadamard_quant(_p(x), m, k, had_block, mode, _p(mode_dev), _p(tamax), C.byref(ca), None,
+                                     _stream(stream)), "hadamard_quant")
+    return out
+
+
+def qgemm(a: QActTensors | None, x_bf16, w: PackedWeights, mode: int, epilogue: int = EPI_NONE, residual=None,
+          out=None, out_f32: bool = False, acc_dbg=None, mode_dev=None, err=None, stream=None, m: int | None = None):
+    n, k = w.n, w.k
+    m = m if m is not None else (a.m if a is not None else x_bf16.shape[0])
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float32 if out_f32 else torch.bfloat16, device=w.bf16_w.device)
+    ca = a.c() if a is not None else None
+    cw = w.c()
+    y = out if out.dtype == torch.bfloat16 else None
+    yf = out if out.dtype == torch.float32 else None
+    check(_lib.sixbit_qgemm(C.byref(ca) if ca is not None else None, _p(x_bf16), C.byref(cw), m, n, k, mode,
+                            _p(mode_dev), epilogue, _p(residual), _p(y), _p(yf), _p(acc_dbg), _p(err),
+                            _stream(stream)), "qgemm")
+    return out
+
+
+def tensor_stats(x: torch.Tensor, out: torch.Tensor, scratch: torch.Tensor, stream=None) -> torch.Tensor:
+    check(_lib.sixbit_tensor_stats(_p(x), x.numel(), _p(out), _p(scratch), None, _stream(stream)), "tensor_stats")
+    return out
+
+
+def block_stats(x_in, x_out, delta_cache, stats: torch.Tensor, scratch: torch.Tensor, mode_dev=None, stream=None):
+    check(_lib.sixbit_block_stats(_p(x_in), _p(x_out), _p(delta_cache), x_in.numel(), _p(mode_dev), _p(stats),
+                                  _p(scratch), None, _stream(stream)), "block_stats")
+    return stats
+
+
+def skip_apply(x_in, delta_cache, x_out, stats: torch.Tensor, scratch: torch.Tensor, mode_dev=None, stream=None):
+    check(_lib.sixbit_skip_apply(_p(x_in), _p(delta_cache), _p(x_out), x_in.numel(), _p(mode_dev), _p(stats),
+                                 _p(scratch), None, _stream(stream)), "skip_apply")
+    return x_out
+
+
+def policy_cfg(gamma_thr=0.1, cos_thr=0.99, err_cap=0.05, pdr_ratio=30.0, near_rel=1e-6, refresh_bf16=False):
+    return PolicyCfg(gamma_thr, cos_thr, err_cap, pdr_ratio, near_rel, int(refresh_bf16), 0)
+
+
+def policy_step(cfg: PolicyCfg, state: torch.Tensor, last_stats: torch.Tensor, in_stats: torch.Tensor,
+                mode_word: torch.Tensor, stream=None):
+    check(_lib.sixbit_policy_step(C.byref(cfg), _p(state), _p(last_stats), _p(in_stats), _p(mode_word), None,
+                                  _stream(stream)), "policy_step")
+    return mode_word
+
+
+def new_stats(device="cuda", count: int = 1) -> torch.Tensor:
+    """Zeroed device storage for `count` sixbit_stats records (float64 x 8 each)."""
+    return torch.zeros((count, 8), dtype=torch.float64, device=device)
+
+
+def new_policy_state(device="cuda", count: int = 1) -> torch.Tensor:
+    """Zeroed device storage for `count` sixbit_policy_state records (80 bytes each)."""
+    assert C.sizeof(PolicyState) == 80
+    return torch.zeros((count, 80), dtype=torch.uint8, device=device)
+
+
+def decode_state(raw: torch.Tensor) -> PolicyState:
+    b = bytes(raw.cpu().numpy().tobytes())
+    return PolicyState.from_buffer_copy(b)
+
+
+def new_scratch(n: int, device="cuda") -> torch.Tensor:
+    """Zeroed scratch for the statistics kernels (its counter must start at zero)."""
+    return torch.zeros(stats_scratch_bytes(n), dtype=torch.uint8, device=device)
