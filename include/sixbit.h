@@ -263,6 +263,29 @@ sixbit_status sixbit_skip_apply(const uint16_t* x_in, const uint16_t* delta_cach
                                 int64_t n, const int32_t* mode_dev, sixbit_stats* stats_dev,
                                 void* scratch, int32_t* err_dev, void* stream);
 
+/*
+ * Allocation-free variant of sixbit_block_stats.  The paper has no
+ * counterpart to this call; it exists for callers that cannot call
+ * cudaMalloc (code running under an allocator that owns all device memory,
+ * or in a host that forbids allocation after start-up) and so cannot provide
+ * the scratch buffer sixbit_block_stats asks for.  Same inputs, outputs and
+ * results as sixbit_block_stats (delta cache bit-identical, sums equal up to
+ * float64 summation order), but the reduction scratch is a fixed
+ * 256 KB array inside the library, which every GPU that loads the library
+ * holds until the process exits.  n must not exceed
+ * sixbit_block_stats_noalloc_max_elems() (268,435,456 elements); larger n
+ * returns SIXBIT_ESHAPE and launches nothing.  The call allocates no memory.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the one array: calls that overlap on the GPU race and
+ * corrupt each other's results, so order them (one stream, or events).
+ */
+sixbit_status sixbit_block_stats_noalloc(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta_cache,
+                                         int64_t n, const int32_t* mode_dev, sixbit_stats* stats_dev,
+                                         int32_t* err_dev, void* stream);
+/* Largest n sixbit_block_stats_noalloc accepts. */
+int64_t sixbit_block_stats_noalloc_max_elems(void);
+
 /* Synchronize `stream` and return the status recorded in err_dev (and clear it). */
 sixbit_status sixbit_check(int32_t* err_dev, void* stream);
 

@@ -1,6 +1,6 @@
 """Builds libsixbit.so in-tree with nvcc for sm_103a (no CMake, no torch extension).
 
-The four translation units compile in parallel and are linked with the static
+The translation units compile in parallel and are linked with the static
 CUDA runtime, so the library loads without a GPU driver present (calls then
 report SIXBIT_EUNSUPPORTED / SIXBIT_ECUDA).
 """
@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsixbit.so")
-SOURCES = ["api.cu", "hadamard_quant.cu", "stats_policy.cu", "qgemm.cu"]
+SOURCES = ["api.cu", "hadamard_quant.cu", "stats_policy.cu", "qgemm.cu", "noalloc.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 

@@ -56,6 +56,8 @@ EXPORTS = {
     "sixbit_policy_step": (C.c_int, [C.POINTER(PolicyCfg), c_p, c_p, c_p, c_p, c_p, c_p]),
     "sixbit_tensor_stats": (C.c_int, [c_p, C.c_int64, c_p, c_p, c_p, c_p]),
     "sixbit_skip_apply": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),
+    "sixbit_block_stats_noalloc": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p]),
+    "sixbit_block_stats_noalloc_max_elems": (C.c_int64, []),
     "sixbit_check": (C.c_int, [c_p, c_p]),
     "sixbit_status_str": (C.c_char_p, [C.c_int]),
     "sixbit_launch_count": (C.c_uint64, []),

@@ -39,6 +39,11 @@ size_t stats_scratch_bytes(int64_t n);
 cudaError_t launch_tensor_stats(const uint16_t* x, int64_t n, double* out, void* scratch, cudaStream_t st);
 cudaError_t launch_block_stats(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta, int64_t n,
                                const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st);
+// Elements one CTA of the fixed-grid statistics launch covers.
+constexpr int64_t kFixedElemsPerCta = 65536;
+cudaError_t launch_block_stats_fixed_grid(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta, int64_t n,
+                                          const int32_t* mode_dev, sixbit_stats* stats, void* scratch,
+                                          cudaStream_t st);
 cudaError_t launch_skip_apply(const uint16_t* x_in, const uint16_t* delta, uint16_t* x_out, int64_t n,
                               const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st);
 cudaError_t launch_policy(const sixbit_policy_cfg& cfg, sixbit_policy_state* st_dev, const sixbit_stats* last,

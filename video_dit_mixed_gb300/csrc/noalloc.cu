@@ -1,0 +1,81 @@
+// Allocation-free variant of sixbit_block_stats.
+//
+// Who needs it: callers that cannot call cudaMalloc -- code that runs where
+// the allocator is off limits (inside a custom memory pool that owns all
+// device memory, in a plugin host that forbids allocation after start-up, or
+// in a process whose allocations must all be accounted up front).  The
+// regular entry point takes the reduction scratch from the caller; this one
+// keeps it in a fixed array in the library's own device memory instead.
+//
+// The scratch lives in one file-scope __device__ array of
+// kNoallocScratchBytes (about 256 KB), which every GPU that loads the library
+// holds until the process exits.  Host code may not use the array's name as a
+// device address (on the host it names a shadow variable), so the device
+// address is looked up once per device with cudaGetSymbolAddress, with that
+// device current, during the first call on that device.  That first call
+// should come before any stream capture.  Every call shares the one array:
+// calls that overlap on the GPU (different streams, or different host
+// threads without ordering) race on it and corrupt each other's results.
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace sixbit {
+
+// Counter (16 bytes) + one 64-byte partial record per CTA.
+constexpr int64_t kNoallocMaxCtas = 4096;
+constexpr size_t kNoallocScratchBytes = 16 + static_cast<size_t>(kNoallocMaxCtas) * 64;
+constexpr int64_t kNoallocMaxElems = kNoallocMaxCtas * kFixedElemsPerCta;  // 268,435,456
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+static void* g_scratch_ptr[kMaxDevices] = {nullptr};
+static std::mutex g_scratch_mu;
+
+// Device address of g_noalloc_scratch on the current device (looked up once).
+static sixbit_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SIXBIT_ECUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SIXBIT_ECUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return SIXBIT_OK;
+}
+
+}  // namespace sixbit
+
+using namespace sixbit;
+
+extern "C" int64_t sixbit_block_stats_noalloc_max_elems(void) { return kNoallocMaxElems; }
+
+extern "C" sixbit_status sixbit_block_stats_noalloc(const uint16_t* x_in, const uint16_t* x_out,
+                                                    uint16_t* delta_cache, int64_t n, const int32_t* mode_dev,
+                                                    sixbit_stats* stats_dev, int32_t* err_dev, void* stream) {
+  (void)err_dev;
+  if (x_in == nullptr || x_out == nullptr || delta_cache == nullptr || stats_dev == nullptr) return SIXBIT_EINVAL;
+  if (n <= 0 || n % 8 != 0 || n > kNoallocMaxElems) return SIXBIT_ESHAPE;
+  if ((reinterpret_cast<uintptr_t>(x_in) | reinterpret_cast<uintptr_t>(x_out) |
+       reinterpret_cast<uintptr_t>(delta_cache)) & 15u)
+    return SIXBIT_EALIGN;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SIXBIT_EUNSUPPORTED;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return SIXBIT_EUNSUPPORTED;
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return SIXBIT_EUNSUPPORTED;
+  void* scratch = nullptr;
+  sixbit_status s = noalloc_scratch(&scratch);
+  if (s != SIXBIT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the completion counter must start at zero (the kernel also leaves it zero)
+  if (cudaMemsetAsync(scratch, 0, 16, st) != cudaSuccess) return SIXBIT_ECUDA;
+  return launch_block_stats_fixed_grid(x_in, x_out, delta_cache, n, mode_dev, stats_dev, scratch, st) == cudaSuccess
+             ? SIXBIT_OK
+             : SIXBIT_ECUDA;
+}

@@ -364,6 +364,19 @@ cudaError_t launch_block_stats(const uint16_t* x_in, const uint16_t* x_out, uint
   return cudaGetLastError();
 }
 
+// Same kernel with a fixed amount of work per CTA (kFixedElemsPerCta), so the
+// grid -- and with it the per-CTA partials in scratch -- grows with n.  Used
+// by the allocation-free entry point, whose scratch has a fixed capacity.
+cudaError_t launch_block_stats_fixed_grid(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta, int64_t n,
+                                          const int32_t* mode_dev, sixbit_stats* stats, void* scratch,
+                                          cudaStream_t st) {
+  const int64_t grid = (n + kFixedElemsPerCta - 1) / kFixedElemsPerCta;
+  block_stats_kernel<<<static_cast<unsigned int>(grid), kStThreads, 0, st>>>(x_in, x_out, delta, n, mode_dev, stats,
+                                                                             scratch);
+  note_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_skip_apply(const uint16_t* x_in, const uint16_t* delta, uint16_t* x_out, int64_t n,
                               const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st) {
   skip_apply_kernel<<<stats_grid(n), kStThreads, 0, st>>>(x_in, delta, x_out, n, mode_dev, stats, scratch);

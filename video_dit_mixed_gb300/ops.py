@@ -125,6 +125,17 @@ def block_stats(x_in, x_out, delta_cache, stats: torch.Tensor, scratch: torch.Te
     return stats
 
 
+def block_stats_noalloc(x_in, x_out, delta_cache, stats: torch.Tensor, mode_dev=None, stream=None):
+    """sixbit_block_stats without caller scratch (the library's fixed array is used).
+
+    For callers that cannot allocate device memory for scratch; calls must not
+    overlap on the GPU, since they share that array.
+    """
+    check(_lib.sixbit_block_stats_noalloc(_p(x_in), _p(x_out), _p(delta_cache), x_in.numel(), _p(mode_dev),
+                                          _p(stats), None, _stream(stream)), "block_stats_noalloc")
+    return stats
+
+
 def skip_apply(x_in, delta_cache, x_out, stats: torch.Tensor, scratch: torch.Tensor, mode_dev=None, stream=None):
     check(_lib.sixbit_skip_apply(_p(x_in), _p(delta_cache), _p(x_out), x_in.numel(), _p(mode_dev), _p(stats),
                                  _p(scratch), None, _stream(stream)), "skip_apply")
