@@ -37,7 +37,6 @@ namespace sixbit {
 
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kGemmThreads = 192;
 
 enum { KIND_BF16 = 0, KIND_NVF4 = 1 };
 
@@ -122,13 +121,38 @@ __device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, i
   }
 }
 
+// Stages of the shared-memory ring; the grouped (W4A8) kernel gives one stage
+// up for its staged group scales (up to K = 16768).
 template <int KIND, bool GROUPED>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__host__ __device__ constexpr int gemm_stages() {
+  return GROUPED ? 5 : GemmCfg<KIND>::kStages;
+}
+
+template <bool GROUPED>
+struct EpiCfg {
+  static constexpr int kWarps = GROUPED ? 8 : 4;    // epilogue warps
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kCols = kBN / (kWarps / 4);  // accumulator columns per epilogue thread
+};
+
+template <bool GROUPED>
+constexpr int gemm_threads() {
+  return 64 + EpiCfg<GROUPED>::kThreads;
+}
+
+// Persistent kernel: each CTA walks output tiles t = blockIdx.x, +gridDim.x,
+// ... (row tiles fastest, so the CTAs in flight share the same weight tiles).
+// Two accumulator buffers in tensor memory let the epilogue of one tile (or
+// K group) overlap the MMAs of the next.
+template <int KIND, bool GROUPED, bool DBG>
+__global__ void __launch_bounds__(gemm_threads<GROUPED>(), 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmParams p) {
   using C = GemmCfg<KIND>;
-  constexpr int S = C::kStages;
-  constexpr uint32_t kCols = (KIND == KIND_NVF4 || GROUPED) ? 256 : 128;
+  using E = EpiCfg<GROUPED>;
+  constexpr int S = gemm_stages<KIND, GROUPED>();
+  constexpr uint32_t kCols = (KIND == KIND_NVF4) ? 512 : 256;
+  constexpr uint32_t kSfCol = 2 * kBN;  // NVFP4 scale factors live after the two accumulators
   if (p.mode_dev != nullptr && SIXBIT_MODE_OF(*p.mode_dev) != p.want_mode) return;
 
   extern __shared__ uint8_t smem_raw[];
@@ -138,11 +162,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * stage_bytes<KIND>());
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
-  uint64_t* accf = bars + 2 * S;      // [2]
-  uint64_t* acce = bars + 2 * S + 2;  // [2]
+  uint64_t* accf = bars + 2 * S;      // [2] accumulator buffer ready
+  uint64_t* acce = bars + 2 * S + 2;  // [2] accumulator buffer drained
   uint64_t* drain = bars + 2 * S + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* sw_full = bars + 2 * S + 6;   // GROUPED: a tile's group scales are staged
+  uint64_t* sw_empty = bars + 2 * S + 7;  // GROUPED: ... and no longer read
+  float* sw_smem = reinterpret_cast<float*>(bars + 2 * S + 8);  // GROUPED: [K/128][128] group scales of a tile
 
   auto A_tile = [&](int s) { return tiles + s * stage_bytes<KIND>(); };
   auto B_tile = [&](int s) { return tiles + s * stage_bytes<KIND>() + kTileBytes; };
@@ -151,8 +178,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int m_tile = blockIdx.x, n_tile = blockIdx.y;
-  const int m0 = m_tile * kBM, n0 = n_tile * kBN;
+  const int tiles_m = (p.M + kBM - 1) / kBM;
+  const int tiles_n = (p.N + kBN - 1) / kBN;
+  const int ntiles = tiles_m * tiles_n;
   // NVFP4 stages hold 256 K-elements; a K that is an odd multiple of 128
   // leaves a half stage at the end (TMA zero-fills its missing columns; only
   // its valid scale chunks are copied and only its valid MMAs issued).
@@ -166,9 +194,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(&accf[0], 1);
     mbar_init(&accf[1], 1);
-    mbar_init(&acce[0], 128);
-    mbar_init(&acce[1], 128);
+    mbar_init(&acce[0], E::kThreads);
+    mbar_init(&acce[1], E::kThreads);
     mbar_init(drain, 1);
+    mbar_init(sw_full, E::kThreads);
+    mbar_init(sw_empty, E::kThreads);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -188,162 +218,201 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ producer --
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (kb / S) & 1;
-        if (kb >= S && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
-          set_error(p.err, SIXBIT_ETIMEOUT);
-          *abort_flag = 1;
-          break;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const int m_tile = t % tiles_m, n_tile = t / tiles_m;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (it >= S && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+            set_error(p.err, SIXBIT_ETIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          const int kvalid = min(C::kKStage, p.K - kb * C::kKStage);
+          const uint32_t sf_bytes = C::kSfBytes == 0 ? 0u : static_cast<uint32_t>(kvalid / 64) * 512u;
+          mbar_expect_tx(&full[s], 2 * kTileBytes + 2 * sf_bytes);
+          tma_load_2d(A_tile(s), &tmA, &full[s], kb * C::kKCoord, m_tile * kBM);
+          tma_load_2d(B_tile(s), &tmB, &full[s], kb * C::kKCoord, n_tile * kBN);
+          if constexpr (KIND == KIND_NVF4) {
+            const size_t row_bytes = static_cast<size_t>(128) * (p.K >> 4);
+            bulk_load(SFA(s), p.sfa + m_tile * row_bytes + static_cast<size_t>(kb) * 2048, sf_bytes, &full[s]);
+            bulk_load(SFB(s), p.sfb + n_tile * row_bytes + static_cast<size_t>(kb) * 2048, sf_bytes, &full[s]);
+          }
         }
-        const int kvalid = min(C::kKStage, p.K - kb * C::kKStage);
-        const uint32_t sf_bytes = C::kSfBytes == 0 ? 0u : static_cast<uint32_t>(kvalid / 64) * 512u;
-        mbar_expect_tx(&full[s], 2 * kTileBytes + 2 * sf_bytes);
-        tma_load_2d(A_tile(s), &tmA, &full[s], kb * C::kKCoord, m0);
-        tma_load_2d(B_tile(s), &tmB, &full[s], kb * C::kKCoord, n0);
-        if constexpr (KIND == KIND_NVF4) {
-          const size_t row_bytes = static_cast<size_t>(128) * (p.K >> 4);
-          bulk_load(SFA(s), p.sfa + m_tile * row_bytes + static_cast<size_t>(kb) * 2048, sf_bytes, &full[s]);
-          bulk_load(SFB(s), p.sfb + n_tile * row_bytes + static_cast<size_t>(kb) * 2048, sf_bytes, &full[s]);
-        }
-        issued = kb + 1;
       }
-      // make sure every copy this CTA started has landed before it can exit
-      for (int kb = (issued > S ? issued - S : 0); kb < issued; ++kb)
-        (void)mbar_wait(&full[kb % S], (kb / S) & 1, nullptr);
+      // every copy this CTA started lands before it can exit
+      for (uint32_t j = (it > S ? it - S : 0); j < it; ++j) (void)mbar_wait(&full[j % S], (j / S) & 1, nullptr);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------- MMA issuer --
+      uint32_t it = 0;   // stage counter
+      uint32_t ac = 0;   // accumulator-buffer use counter (tiles, or K groups when GROUPED)
       bool ok = true;
-      for (int kb = 0; kb < nk && ok; ++kb) {
-        const int s = kb % S;
-        const uint32_t ph = (kb / S) & 1;
-        int buf = 0;
-        bool first_in_acc = (kb == 0);
-        if constexpr (GROUPED) {
-          constexpr int spg = 128 / C::kKStage;  // stages per group
-          const int g = kb / spg;
-          buf = g & 1;
-          first_in_acc = (kb % spg) == 0;
-          if (first_in_acc && g >= 2 && !mbar_wait(&acce[buf], ((g >> 1) - 1) & 1, abort_flag)) {
+      constexpr int spg = 128 / C::kKStage > 0 ? 128 / C::kKStage : 1;  // stages per K group (bf16 kinds)
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        for (int kb = 0; kb < nk && ok; ++kb, ++it) {
+          const bool acc_start = GROUPED ? (kb % spg) == 0 : kb == 0;
+          const uint32_t buf = ac & 1;
+          if (acc_start && ac >= 2 && !mbar_wait(&acce[buf], ((ac >> 1) - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
-        }
-        if (!mbar_wait(&full[s], ph, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t a_base = smem_u32(A_tile(s));
-        const uint32_t b_base = smem_u32(B_tile(s));
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(buf * kBN);
-        if constexpr (KIND == KIND_NVF4) {
-          const int nmma = min(C::kKStage, p.K - kb * C::kKStage) / 64;
-#pragma unroll
-          for (int k = 0; k < C::kMmaPerStage; ++k) {
-            if (k < nmma) {
-              tmem_cp_32x128b_warpx4(tmem + 128 + 4 * k, sdesc_sf(smem_u32(SFA(s)) + 512 * k));
-              tmem_cp_32x128b_warpx4(tmem + 144 + 4 * k, sdesc_sf(smem_u32(SFB(s)) + 512 * k));
-            }
+          const int s = it % S;
+          if (!mbar_wait(&full[s], (it / S) & 1, abort_flag)) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(A_tile(s));
+          const uint32_t b_base = smem_u32(B_tile(s));
+          const uint32_t d_tmem = tmem + buf * kBN;
+          if constexpr (KIND == KIND_NVF4) {
+            const int nmma = min(C::kKStage, p.K - kb * C::kKStage) / 64;
 #pragma unroll
-          for (int k = 0; k < C::kMmaPerStage; ++k)
-            if (k < nmma)
-              mma_nvf4(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), C::kIdesc,
-                       tmem + 128 + 4 * k, tmem + 144 + 4 * k, (first_in_acc && k == 0) ? 0u : 1u);
-        } else {
+            for (int k = 0; k < C::kMmaPerStage; ++k) {
+              if (k < nmma) {
+                tmem_cp_32x128b_warpx4(tmem + kSfCol + 4 * k, sdesc_sf(smem_u32(SFA(s)) + 512 * k));
+                tmem_cp_32x128b_warpx4(tmem + kSfCol + 16 + 4 * k, sdesc_sf(smem_u32(SFB(s)) + 512 * k));
+              }
+            }
 #pragma unroll
-          for (int k = 0; k < C::kMmaPerStage; ++k)
-            mma_bf16(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), C::kIdesc,
-                     (first_in_acc && k == 0) ? 0u : 1u);
+            for (int k = 0; k < C::kMmaPerStage; ++k)
+              if (k < nmma)
+                mma_nvf4(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), C::kIdesc,
+                         tmem + kSfCol + 4 * k, tmem + kSfCol + 16 + 4 * k, (acc_start && k == 0) ? 0u : 1u);
+          } else {
+#pragma unroll
+            for (int k = 0; k < C::kMmaPerStage; ++k)
+              mma_bf16(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), C::kIdesc,
+                       (acc_start && k == 0) ? 0u : 1u);
+          }
+          tc_commit(&empty[s]);
+          const bool acc_end = GROUPED ? (kb % spg) == spg - 1 : kb == nk - 1;
+          if (acc_end) {
+            tc_commit(&accf[buf]);
+            ++ac;
+          }
         }
-        tc_commit(&empty[s]);
-        if constexpr (GROUPED) {
-          constexpr int spg = 128 / C::kKStage;
-          if ((kb % spg) == spg - 1) tc_commit(&accf[buf]);
-        }
-      }
-      if constexpr (!GROUPED) {
-        if (ok) tc_commit(&accf[0]);
       }
       if (!ok) {
         set_error(p.err, SIXBIT_ETIMEOUT);
         *abort_flag = 1;
       }
-      // all tensor-core work issued by this thread completes before exit
-      tc_commit(drain);
+      tc_commit(drain);  // all tensor-core work issued here completes before exit
       (void)mbar_wait(drain, 0, nullptr);
     }
   } else {
     // -------------------------------------------------------- epilogue --
-    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
-    const int row = m0 + 32 * q + lane;
+    const int ew = warp - 2;              // 0 .. kWarps-1
+    const int q = warp & 3;               // tensor-memory lane quarter this warp may read
+    const int col0 = (ew >> 2) * E::kCols;  // first accumulator column of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-    if constexpr (GROUPED) {
-      float sum[kBN];
-#pragma unroll
-      for (int j = 0; j < kBN; ++j) sum[j] = 0.f;
-      bool ok = true;
-      for (int g = 0; g < groups; ++g) {
-        const int buf = g & 1;
-        if (!mbar_wait(&accf[buf], (g >> 1) & 1, abort_flag)) {
-          set_error(p.err, SIXBIT_ETIMEOUT);
-          *abort_flag = 1;
+    uint32_t ac = 0;
+    uint32_t lt = 0;  // local tile counter
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
+      const int m_tile = t % tiles_m, n_tile = t / tiles_m;
+      const int row = m_tile * kBM + 32 * q + lane;
+      const int n0 = n_tile * kBN;
+      if constexpr (GROUPED) {
+        // the tile's group scales s_w[g][n0 .. n0+127] into shared memory, once
+        // every epilogue thread is done with the previous tile's (bounded waits)
+        if (lt >= 1 && !mbar_wait(sw_empty, (lt - 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const float* sw = p.grp_scale + static_cast<size_t>(g) * p.N + n0;
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(lane_addr + buf * kBN + c * 32, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int n = n0 + c * 32 + j;
-            const float a = __uint_as_float(r[j]);
-            const float s = (n < p.N) ? __ldg(sw + c * 32 + j) : 0.f;
-            sum[c * 32 + j] = fmaf(s, a, sum[c * 32 + j]);
-            if (p.acc_dbg != nullptr && row < p.M && n < p.N)
-              p.acc_dbg[(static_cast<size_t>(g) * p.M + row) * p.N + n] = __float2int_rn(a);
-          }
+        for (int i = threadIdx.x - 64; i < groups * kBN; i += E::kThreads) {
+          const int g = i / kBN, c = i % kBN;
+          sw_smem[i] = (n0 + c < p.N) ? __ldg(p.grp_scale + static_cast<size_t>(g) * p.N + n0 + c) : 0.f;
         }
-        tc_fence_before();
-        mbar_arrive(&acce[buf]);
-      }
-      if (ok) {
+        mbar_arrive(sw_full);
+        if (!mbar_wait(sw_full, lt & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        float sum[E::kCols];
+#pragma unroll
+        for (int j = 0; j < E::kCols; ++j) sum[j] = 0.f;
+        for (int g = 0; g < groups; ++g, ++ac) {
+          const uint32_t buf = ac & 1;
+          if (!mbar_wait(&accf[buf], (ac >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float4* sw4 = reinterpret_cast<const float4*>(sw_smem + g * kBN + col0);
+#pragma unroll
+          for (int c = 0; c < E::kCols / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(lane_addr + buf * kBN + col0 + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 s4 = sw4[c * 8 + j4];
+              const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int j = c * 32 + j4 * 4 + u;
+                sum[j] = fmaf(sv[u], __uint_as_float(r[j4 * 4 + u]), sum[j]);
+              }
+            }
+            if constexpr (DBG) {
+              if (row < p.M) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const int n = n0 + col0 + c * 32 + j;
+                  if (n < p.N)
+                    p.acc_dbg[(static_cast<size_t>(g) * p.M + row) * p.N + n] = __float2int_rn(__uint_as_float(r[j]));
+                }
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&acce[buf]);
+        }
+        if (!ok) break;
+        mbar_arrive(sw_empty);
         const float sm = (row < p.M) ? p.row_scale[row] : 0.f;
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = 0; c < E::kCols / 32; ++c) {
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(sum[c * 32 + j], sm);
-          if (n0 + c * 32 < p.N) epilogue_store32(p, row, n0 + c * 32, v);
+          if (n0 + col0 + c * 32 < p.N) epilogue_store32(p, row, n0 + col0 + c * 32, v);
         }
-      }
-    } else {
-      if (!mbar_wait(&accf[0], 0, abort_flag)) {
-        set_error(p.err, SIXBIT_ETIMEOUT);
-        *abort_flag = 1;
       } else {
+        const uint32_t buf = ac & 1;
+        if (!mbar_wait(&accf[buf], (ac >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         float alpha = 1.0f;
         if constexpr (KIND == KIND_NVF4) alpha = __fmul_rn(*p.s_a, *p.s_b);
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t r[32];
-          tmem_ld32(lane_addr + c * 32, r);
+          tmem_ld32(lane_addr + buf * kBN + c * 32, r);
           tmem_ld_wait();
+          if (c == kBN / 32 - 1) {  // buffer fully read: hand it back to the MMA warp
+            tc_fence_before();
+            mbar_arrive(&acce[buf]);
+          }
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
           if (n0 + c * 32 < p.N) epilogue_store32(p, row, n0 + c * 32, v);
         }
+        ++ac;
       }
+    }
+    if (!ok) {
+      set_error(p.err, SIXBIT_ETIMEOUT);
+      *abort_flag = 1;
     }
     tc_fence_before();
   }
@@ -356,29 +425,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ------------------------------------------------------------ host launch --
 
-template <int KIND, bool GROUPED>
-static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
-  static bool attr_done = false;
-  constexpr int smem = gemm_smem_bytes<KIND>();
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(qgemm_kernel<KIND, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
+static int num_sms() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
   }
-  dim3 grid((p.M + kBM - 1) / kBM, (p.N + kBN - 1) / kBN);
-  qgemm_kernel<KIND, GROUPED><<<grid, kGemmThreads, smem, st>>>(a, b, p);
+  return sms;
+}
+
+template <int KIND, bool GROUPED, bool DBG>
+static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
+  static int attr_done = 0;
+  const int smem = gemm_stages<KIND, GROUPED>() * stage_bytes<KIND>() + 1024 + 256 +
+                   (GROUPED ? (p.K / 128) * kBN * 4 : 0);
+  if (smem > attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(qgemm_kernel<KIND, GROUPED, DBG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_done = smem;
+  }
+  const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
+  const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  qgemm_kernel<KIND, GROUPED, DBG><<<grid, gemm_threads<GROUPED>(), smem, st>>>(a, b, p);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_qgemm_nvf4(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
-  return launch_one<KIND_NVF4, false>(a, b, p, st);
+  return launch_one<KIND_NVF4, false, false>(a, b, p, st);
 }
 cudaError_t launch_qgemm_bf16(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
-  return launch_one<KIND_BF16, false>(a, b, p, st);
+  return launch_one<KIND_BF16, false, false>(a, b, p, st);
 }
 cudaError_t launch_qgemm_int8(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
-  return launch_one<KIND_BF16, true>(a, b, p, st);
+  if (p.acc_dbg != nullptr) return launch_one<KIND_BF16, true, true>(a, b, p, st);
+  return launch_one<KIND_BF16, true, false>(a, b, p, st);
 }
 
 }  // namespace sixbit
