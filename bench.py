@@ -1,20 +1,32 @@
-"""Throughput of the quantized-linear hot path on one GB300 (or N, as replicas).
+"""Throughput of the quantized-linear hot path on one GB300 (N GPUs run as replicas).
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-Workloads (synthetic inputs of the shapes and distributions of the method's
-CogVideoX-shaped layers; no model weights or datasets are used):
-  qkv_2b  one step = input statistics, policy step, fused Hadamard + NVFP4
-          quantization, W4A4 GEMM, fused Hadamard + INT8 quantization, W4A8
-          GEMM and the BF16 (PDR) GEMM of a 17776 x 1920 -> 5760 linear layer.
+Workloads (synthetic inputs shaped like the method's CogVideoX-2B/5B layers;
+random weights, no checkpoints or datasets):
+  dit_2b        (default) one step = one denoising step of a 30-block
+                residual-MLP DiT (hidden 1920, FFN 7680, 17776 tokens) through
+                the whole hot path: input statistics, per-block policy, TDC
+                skip, fused Hadamard + NVFP4/INT8 quantization, W4A4 / W4A8 /
+                BF16 GEMMs with GELU and residual epilogues, block statistics
+                and delta cache.  Input trajectory x_s = x_{s-1} + sigma_s N(0,1),
+                sigma 0.5 -> 0.01 over 50 steps.  Metric: DiT steps/s.
+  dit_2b_gated  the same with a seeded per-block residual gate in [0.02, 0.5]
+                so Gamma straddles the 0.1 threshold (exercises NVFP4).
+  dit_5b        42 blocks, hidden 3072, FFN 12288.
+  qkv_2b        one step = both quantizers and all three GEMM kinds of a
+                17776 x 1920 -> 5760 linear layer.  Metric: TFLOP/s.
 
-Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on
-the launching stream; between steps a 256 MB buffer is written to flush the
-129 MB L2 (outside the events).  Barrier + synchronize around the timed
-region; the max over ranks is reported.  N > 1 runs independent replicas
-(weak scaling; the path needs no collective for independent inputs).
-`--impl reference` times the CPU oracle on a bounded sample of the same
-workload instead.
+Timing rules: W untimed warm-up steps, then K timed steps (the DiT restarts
+its 50-step trajectory at step 0, so the default K = 50 times one whole
+video's denoising, fully computed early steps included) on the device with
+CUDA events on the launching stream, barrier + synchronize on both sides,
+max over ranks.  The DiT working set (weights 4.5 GB, activations, delta
+caches) is far larger than the 129 MB L2; the linear workload writes a 256 MB
+buffer between steps (outside the events).  The DiT steps are CUDA-graph
+replays; a second, eager pass with one event pair per library call gives the
+per-kernel durations behind the roofline.  `--impl reference` times the CPU
+oracle on a bounded sample instead.
 """
 from __future__ import annotations
 
@@ -29,22 +41,18 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-import numpy as np  # noqa: E402
-
 METRIC = "W4A4/W4A8 qGEMM TFLOPS+%peak; Hadamard-quant GB/s; MLP-DiT step/s"
+FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio (FP4 13.5 PFLOP/s, BF16 2.25 PFLOP/s)
+MODE_NAMES = {1: "nvfp4", 2: "int8", 3: "bf16", 4: "skip"}
 
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
-                    src="measured")
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained") or
+                    d["bf16_tflops"], src="measured")
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
-
-
-# nominal dense ratios to bf16 (2.25 PFLOP/s): fp8 x2, fp4 x6
-FP4_OVER_BF16 = 13.5 / 2.25
 
 
 class Clocks:
@@ -71,25 +79,33 @@ class Clocks:
             return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        rows = [r.split(", ") for r in out.strip().splitlines() if r.strip()]
-        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        rows = [[v.strip() for v in r.split(",")] for r in out.strip().splitlines() if r.strip()]
+        rows = [r for r in rows if len(r) >= 9]
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows if len(r) >= 9 for i in range(4) if r[5 + i].strip() == "Active"})
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
         return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
-                    reasons=reasons, samples=len(rows))
+                    power_w_max=max(pw) if pw else None, reasons=reasons, samples=len(rows))
 
 
 # ------------------------------------------------------------------ workloads --
 
 class QkvLinear:
-    """The QKV-shaped linear (17776 x 1920 -> 5760), all three GEMM kinds per step."""
+    """The QKV-shaped linear (17776 x 1920 -> 5760), both quantizers and all three GEMM kinds per step."""
 
-    name = "qkv_2b"
+    unit = "TFLOP/s"
 
-    def __init__(self, torch, ops, device):
+    def __init__(self, name, torch, ops, device):
         import synthgen
-        self.t, self.ops = torch, ops
+        self.name, self.t, self.ops, self.dev = name, torch, ops, device
         x, w, c = synthgen.linear_inputs("qkv_2b")
         self.b = c["had_block"]
         self.m, self.k = x.shape
@@ -107,13 +123,13 @@ class QkvLinear:
         self.word = torch.zeros(1, dtype=torch.int32, device=device)
         self.cfg = ops.policy_cfg()
         self.gemm_flops = 2.0 * self.m * self.n * self.k
-        self.flops_per_step = 3 * self.gemm_flops
-        self.unit = "TFLOP/s"
+        self.flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)
         self.h2d_bytes = self.x.numel() * 2
         self.d2h_bytes = self.m * self.n * 2
+        self.config = dict(workload=name, tokens=self.m, k=self.k, n=self.n, had_block=self.b,
+                           l2="256 MB buffer written between steps")
 
-    def kernels(self):
-        """(label, callable) of the step, in order."""
+    def calls(self):
         o, b = self.ops, self.b
         return [
             ("tensor_stats", lambda: o.tensor_stats(self.x, self.ins, self.scratch)),
@@ -125,38 +141,297 @@ class QkvLinear:
             ("qgemm_bf16", lambda: o.qgemm(None, self.x, self.pw, o.MODE_BF16, out=self.y["bf"])),
         ]
 
-    def step(self):
-        for _, f in self.kernels():
-            f()
+    def warmup(self, w):
+        for _ in range(w):
+            for _, f in self.calls():
+                f()
 
-    def step_e2e(self, stream):
-        self.x.copy_(self.x_host, non_blocking=True)
-        self.step()
-        self.y_host.copy_(self.y["i8"], non_blocking=True)
+    def timed(self, k, stream):
+        """(per-step ms, {label: [per-call ms]}) -- one event pair per call, L2 flushed between steps."""
+        T = self.t
+        recs = []
+        for _ in range(k):
+            self.flush.fill_(1.0)
+            evs = [T.cuda.Event(enable_timing=True)]
+            evs[0].record(stream)
+            for _, f in self.calls():
+                f()
+                e = T.cuda.Event(enable_timing=True)
+                e.record(stream)
+                evs.append(e)
+            recs.append(evs)
+        T.cuda.synchronize()
+        labels = [l for l, _ in self.calls()]
+        per = {l: [] for l in labels}
+        steps = []
+        for evs in recs:
+            steps.append(evs[0].elapsed_time(evs[-1]))
+            for i, l in enumerate(labels):
+                per[l].append(evs[i].elapsed_time(evs[i + 1]))
+        return steps, per
 
-    def value(self, seconds_per_step):
-        return self.flops_per_step / seconds_per_step / 1e12
+    def profile(self, k, stream):
+        return self.timed(k, stream)[1]
 
-    # algorithmic work of each kernel per launch, for the roofline
-    def algorithmic(self, label):
+    def e2e(self, k, stream):
+        T = self.t
+        pairs = []
+        for _ in range(k):
+            self.flush.fill_(1.0)
+            a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+            a.record(stream)
+            self.x.copy_(self.x_host, non_blocking=True)
+            for _, f in self.calls():
+                f()
+            self.y_host.copy_(self.y["i8"], non_blocking=True)
+            b.record(stream)
+            pairs.append((a, b))
+        T.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in pairs]
+
+    def value(self, ms):
+        return 3 * self.gemm_flops / (ms / 1e3) / 1e12
+
+    def work(self, label):
         mk = self.m * self.k
         if label.startswith("qgemm"):
-            return ("tensor", self.gemm_flops)
+            return ("tensor", self.gemm_flops, "nvfp4" in label)
         if label == "hq_nvfp4":
-            # read X once (bf16), write E2M1 codes and E4M3 scales
-            return ("hbm", mk * 2 + mk // 2 + mk // 16)
+            return ("hbm", mk * 2 + mk // 2 + mk // 16, False)
         if label == "hq_int8":
-            # read X once, write int8 codes and row scales
-            return ("hbm", mk * 2 + mk + self.m * 4)
+            return ("hbm", mk * 2 + mk + self.m * 4, False)
         if label == "tensor_stats":
-            return ("hbm", mk * 2)
-        return (None, 0)
+            return ("hbm", mk * 2, False)
+        return (None, 0, False)
+
+    def launches(self):
+        return None
+
+    def extra(self):
+        return {}
 
 
-WORKLOADS = {"qkv_2b": QkvLinear}
+class DitStep:
+    """One denoising step of the synthetic residual-MLP DiT (all hot-path rows)."""
+
+    unit = "step/s"
+
+    def __init__(self, name, torch, ops, device):
+        import synthgen
+        from video_dit_mixed_gb300 import dit
+        self.name, self.t, self.ops, self.dev = name, torch, ops, device
+        c = synthgen.DIT_CONFIGS[name]
+        self.c = c
+        T, H, F, L, b = c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"]
+        self.T, self.H, self.F, self.L, self.b = T, H, F, L, b
+        gen = torch.Generator(device=device)
+        gen.manual_seed(1000 + c["seed"])
+        gates = synthgen.dit_gates(name)
+        packed = []
+        for l in range(L):
+            wu = torch.randn((F, H), generator=gen, device=device, dtype=torch.float32) * c["w_std"]
+            wd = torch.randn((H, F), generator=gen, device=device, dtype=torch.float32) * (c["w_std"] * gates[l])
+            packed.append((ops.pack_weights(wu, b), ops.pack_weights(wd, b)))
+            del wu, wd
+        self.model = dit.DiT(T, H, F, L, b, packed, device=device)
+        # input trajectory, resident in HBM before timing
+        x0 = synthgen.activations(c["seed"], T, H, "laplace", 0.005, 50.0)
+        sig = synthgen.sigmas(c["steps"])
+        self.traj = torch.empty((c["steps"], T, H), dtype=torch.bfloat16, device=device)
+        self.traj[0].copy_(torch.from_numpy(x0).to(torch.bfloat16))
+        for s in range(1, c["steps"]):
+            z = torch.randn((T, H), generator=gen, device=device, dtype=torch.float32)
+            self.traj[s].copy_((self.traj[s - 1].float() + float(sig[s - 1]) * z).to(torch.bfloat16))
+        self.traj_host = None
+        self.out_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        self.s = 0
+        self.h2d_bytes = T * H * 2
+        self.d2h_bytes = T * H * 2
+        self.config = dict(workload=name, tokens=T, hidden=H, ffn=F, blocks=L, steps_per_run=c["steps"],
+                           had_block=b, gate=c["gate"], policy="gamma 0.1, cos 0.99, err_cap 0.05, pdr 30",
+                           l2="working set > 10 GB, no flush needed", cuda_graph=True)
+        self.mode_log = []
+        self.timed_steps = []
+
+    def _next_input(self):
+        if self.s >= self.c["steps"]:       # trajectory exhausted: start a new video
+            self.s = 0
+            self.model.reset()
+        x = self.traj[self.s]
+        self.s += 1
+        return x
+
+    def warmup(self, w):
+        self.model.step(self._next_input())          # eager: sets kernel attributes
+        self.t.cuda.synchronize()
+        self.model.capture()
+        for _ in range(max(0, w - 1)):
+            self.model.step(self._next_input())
+        # timed steps start a fresh trajectory at its first (fully computed) step
+        self.t.cuda.synchronize()
+        self.model.reset()
+        self.s = 0
+
+    def timed(self, k, stream):
+        T = self.t
+        pairs = []
+        self.timed_steps = []
+        for _ in range(k):
+            a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+            a.record(stream)
+            self.timed_steps.append(self.s % self.c["steps"])
+            self.model.step(self._next_input())
+            b.record(stream)
+            pairs.append((a, b))
+        T.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in pairs], None
+
+    # kernels one block runs per decision inside the switched graph: NVFP4
+    # (amax + quant for x and h, two GEMMs, stats), INT8, BF16, SKIP; every
+    # block also runs the policy kernel and the switch selector
+    BODY_KERNELS = {1: 7, 2: 5, 3: 3, 4: 1}
+
+    def launches(self):
+        """Kernels run in the timed steps (from the device decision log of the same trajectory)."""
+        if len(self.mode_log) == 0:
+            return None
+        import numpy as np
+        low = np.asarray(self.mode_log) & 0xFF
+        n = 0
+        for s in self.timed_steps:
+            n += 1 + sum(2 + self.BODY_KERNELS.get(int(v), 0) for v in low[s])
+        return n
+
+    def profile(self, k, stream):
+        """Eager pass over a full trajectory: event pairs around every call, attributed to the block's mode."""
+        T = self.t
+        m = self.model
+        m.reset()
+        self.s = 0
+        recs = []
+        modes = T.zeros((self.c["steps"], self.L), dtype=T.int32, device=self.dev)
+        for s in range(self.c["steps"]):
+            m.x_in.copy_(self.traj[s])
+            evs = []
+            e0 = T.cuda.Event(enable_timing=True)
+            e0.record(stream)
+
+            def note(label, block, evs=evs):
+                e = T.cuda.Event(enable_timing=True)
+                e.record(stream)
+                evs.append((label, block, e))
+            m.enqueue_step(after_call=note)
+            modes[s].copy_(m.modes)
+            recs.append((e0, evs))
+        T.cuda.synchronize()
+        mh = modes.cpu().numpy()
+        per = {}
+        for s, (e0, evs) in enumerate(recs):
+            prev = e0
+            for label, block, e in evs:
+                key = label if block < 0 else f"{label}:{MODE_NAMES.get(int(mh[s, block]) & 0xFF, '?')}"
+                per.setdefault(key, []).append(prev.elapsed_time(e))
+                prev = e
+        self.mode_log = mh
+        m.reset()
+        self.s = 0
+        return per
+
+    def e2e(self, k, stream):
+        """Host trajectory (pinned) -> device, step, output -> host; from the trajectory's first step."""
+        T = self.t
+        if self.traj_host is None:
+            self.traj_host = self.traj.cpu().pin_memory()
+        self.model.reset()
+        self.s = 0
+        pairs = []
+        for _ in range(k):
+            if self.s >= self.c["steps"]:
+                self.s = 0
+                self.model.reset()
+            a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+            a.record(stream)
+            self.model.step(self.traj_host[self.s])
+            self.s += 1
+            self.out_host.copy_(self.model.out, non_blocking=True)
+            b.record(stream)
+            pairs.append((a, b))
+        T.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in pairs]
+
+    def value(self, ms):
+        return 1e3 / ms
+
+    def work(self, key):
+        label, _, mode = key.partition(":")
+        T, H, F = self.T, self.H, self.F
+        if mode == "skip" and label != "skip_apply":
+            return (None, 0, False)
+        if label in ("qgemm_up", "qgemm_down"):
+            return ("tensor", 2.0 * T * H * F, mode == "nvfp4")
+        if label in ("hq_x", "hq_h"):
+            n = T * (H if label == "hq_x" else F)
+            if mode == "nvfp4":
+                return ("hbm", n * 2 + n // 2 + n // 16, False)
+            if mode == "int8":
+                return ("hbm", n * 3 + T * 4, False)
+            return (None, 0, False)
+        if label == "block_stats":
+            return ("hbm", 8 * T * H, False)
+        if label == "skip_apply" and mode == "skip":
+            return ("hbm", 6 * T * H, False)
+        if label == "tensor_stats":
+            return ("hbm", 2 * T * H, False)
+        return (None, 0, False)
+
+    def extra(self):
+        import numpy as np
+        if len(self.mode_log) == 0:
+            return {}
+        words = np.asarray(self.mode_log)
+        low = words & 0xFF
+        hist = {MODE_NAMES[k]: int((low == k).sum()) for k in (1, 2, 3, 4)}
+        return dict(decisions=hist, refresh=int(((words & 256) != 0).sum()), pdr=int(((words & 512) != 0).sum()),
+                    near_threshold=int(((words & 2048) != 0).sum()), block_steps=int(low.size))
+
+
+WORKLOADS = {"qkv_2b": QkvLinear, "dit_2b": DitStep, "dit_2b_gated": DitStep, "dit_5b": DitStep}
 
 
 # --------------------------------------------------------------------- timing --
+
+def _roofline(wl, per, peaks):
+    """Per-kernel table and the dominant kernel's roofline from per-call durations (ms)."""
+    table = {}
+    for key, v in per.items():
+        kind, work, fp4 = wl.work(key)
+        avg = sum(v) / len(v)
+        ent = dict(calls=len(v), avg_us=round(avg * 1e3, 2), total_ms=round(sum(v), 3))
+        if kind == "tensor":
+            pk = peaks["bf16"] * (FP4_OVER_BF16 if fp4 else 1.0)
+            ach = work / (avg / 1e3) / 1e12
+            ent.update(tflops=round(ach, 1), frac=round(ach / pk, 4))
+        elif kind == "hbm":
+            ach = work / (avg / 1e3) / 1e9
+            ent.update(gbs=round(ach, 1), frac=round(ach / peaks["hbm"], 4))
+        table[key] = ent
+    cands = {k: sum(v) for k, v in per.items() if wl.work(k)[0] is not None}
+    dom = max(cands, key=cands.get)
+    kind, work, fp4 = wl.work(dom)
+    avg = sum(per[dom]) / len(per[dom]) / 1e3
+    if kind == "tensor":
+        pk = peaks["bf16"] * (FP4_OVER_BF16 if fp4 else 1.0)
+        ach = work / avg / 1e12
+        roof = dict(bound="tensor", kernel=dom, achieved=round(ach, 1), peak=round(pk, 1), unit="TFLOP/s",
+                    frac=round(ach / pk, 4), traffic=None, work_per_launch=work,
+                    peak_source=f"{peaks['src']} bf16 burst" + (" x6 nominal fp4/bf16" if fp4 else ""))
+    else:
+        ach = work / avg / 1e9
+        roof = dict(bound="hbm", kernel=dom, achieved=round(ach, 1), peak=peaks["hbm"], unit="GB/s",
+                    frac=round(ach / peaks["hbm"], 4), traffic=None, work_per_launch=work,
+                    peak_source=f"{peaks['src']} copy")
+    return roof, table
+
 
 def run_ours(args):
     import torch
@@ -174,9 +449,8 @@ def run_ours(args):
     __graft_entry__.build()
     from video_dit_mixed_gb300 import ops
 
-    wl = WORKLOADS[args.workload](torch, ops, dev)
+    wl = WORKLOADS[args.workload](args.workload, torch, ops, dev)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
     def barrier():
         torch.cuda.synchronize()
@@ -184,95 +458,44 @@ def run_ours(args):
             dist.barrier()
             torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
-        wl.step()
-    barrier()
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
 
-    # ---- device-resident timed region: one event pair per step, L2 flushed between steps
-    labels = [l for l, _ in wl.kernels()]
-    per_kernel = {l: 0.0 for l in labels}
+    wl.warmup(args.warmup)
+    barrier()
     clocks = Clocks(local)
     clocks.start()
     launches0 = ops.launch_count()
-    step_ms = []
+    t0 = time.perf_counter()
+    steps_ms, per = wl.timed(args.steps, stream)
     barrier()
-    t_wall0 = time.perf_counter()
-    for _ in range(args.steps):
-        flush.fill_(1.0)
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(labels) + 1)]
-        evs[0].record(stream)
-        for i, (_, f) in enumerate(wl.kernels()):
-            f()
-            evs[i + 1].record(stream)
-        torch.cuda.synchronize()
-        step_ms.append(evs[0].elapsed_time(evs[-1]))
-        for i, l in enumerate(labels):
-            per_kernel[l] += evs[i].elapsed_time(evs[i + 1])
-    barrier()
-    wall = time.perf_counter() - t_wall0
+    wall = time.perf_counter() - t0
     launches = ops.launch_count() - launches0
     clk = clocks.stop()
-    ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(steps_ms) / len(steps_ms))
 
-    # ---- end to end: pinned host input -> device -> hot path -> host output, per step
+    if per is None:
+        per = wl.profile(args.steps, stream)
     barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e2e_ms = []
-    for _ in range(max(1, args.steps)):
-        flush.fill_(1.0)
-        e0.record(stream)
-        wl.step_e2e(stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms.append(e0.elapsed_time(e1))
-    e2e = sum(e2e_ms) / len(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e_ms = max_over_ranks(statistics.fmean(wl.e2e(args.steps, stream)))
+    if wl.launches() is not None:
+        launches = wl.launches()
 
     if rank == 0:
         peaks = _peaks()
-        kavg = {l: per_kernel[l] / args.steps for l in labels}
-        dom = max(kavg, key=kavg.get)
-        kind, work = wl.algorithmic(dom)
-        dur = kavg[dom] / 1e3
-        if kind == "tensor":
-            peak = peaks["bf16"] * (FP4_OVER_BF16 if "nvfp4" in dom else 1.0)
-            achieved = work / dur / 1e12
-            roof = dict(bound="tensor", kernel=dom, achieved=round(achieved, 1), peak=round(peak, 1),
-                        unit="TFLOP/s", frac=round(achieved / peak, 4), traffic=None,
-                        peak_source=f"{peaks['src']} bf16 burst" + (" x6 nominal fp4/bf16" if "nvfp4" in dom else ""))
-        else:
-            achieved = work / dur / 1e9
-            roof = dict(bound="hbm", kernel=dom, achieved=round(achieved, 1), peak=peaks["hbm"], unit="GB/s",
-                        frac=round(achieved / peaks["hbm"], 4), traffic=None, peak_source=peaks["src"])
-        kernels = {}
-        for l in labels:
-            kd, wk = wl.algorithmic(l)
-            d = kavg[l] / 1e3
-            ent = dict(us=round(kavg[l] * 1e3, 2))
-            if kd == "tensor":
-                pk = peaks["bf16"] * (FP4_OVER_BF16 if "nvfp4" in l else 1.0)
-                ent.update(tflops=round(wk / d / 1e12, 1), frac=round(wk / d / 1e12 / pk, 4))
-            elif kd == "hbm":
-                ent.update(gbs=round(wk / d / 1e9, 1), frac=round(wk / d / 1e9 / peaks["hbm"], 4))
-            kernels[l] = ent
-        value = wl.value(ms / 1e3) * world
-        line = dict(metric=METRIC, value=round(value, 3), unit=wl.unit, n_gpus=world, steps=args.steps,
-                    warmup=args.warmup, ms_per_step=round(ms, 4), higher_is_better=True, scaling="weak",
-                    vs_baseline=None, dtype="nvfp4/int8/bf16 operands, fp32 accumulate", data="synthetic",
-                    config=dict(workload=wl.name, tokens=wl.m, k=wl.k, n=wl.n, had_block=wl.b,
-                                l2="flushed between steps (256 MB write)", parallelism=f"replicas x{world}"),
-                    e2e=dict(value=round(wl.value(e2e / 1e3) * world, 3), unit=wl.unit,
+        roof, table = _roofline(wl, per, peaks)
+        line = dict(metric=METRIC, value=round(wl.value(ms) * world, 4), unit=wl.unit, n_gpus=world,
+                    steps=args.steps, warmup=args.warmup, ms_per_step=round(ms, 4), higher_is_better=True,
+                    scaling="weak", vs_baseline=None, dtype="nvfp4/int8/bf16 operands, fp32 accumulate",
+                    data="synthetic", config=dict(wl.config, parallelism=f"replicas x{world}"),
+                    e2e=dict(value=round(wl.value(e2e_ms) * world, 4), unit=wl.unit,
                              h2d_bytes_per_step=wl.h2d_bytes, d2h_bytes_per_step=wl.d2h_bytes),
-                    gpu_launches=launches, roofline=roof, kernels=kernels, clocks=clk,
-                    wall_s=round(wall, 3))
+                    gpu_launches=launches, roofline=roof, kernels=table, clocks=clk, wall_s=round(wall, 3))
+        line.update(wl.extra())
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
         print(json.dumps(line), flush=True)
@@ -283,33 +506,68 @@ def run_ours(args):
 
 # ------------------------------------------------------------ CPU oracle leg --
 
-def cpu_baseline(workload: str, budget_s: float = 15.0):
-    """The oracle, as it stands, on a bounded sample of the workload (host cores)."""
+def _oracle_linear_sample(workload, budget_s):
     import synthgen
     from oracle import gemm, quant
-    cores = os.cpu_count()
     c = synthgen.CONFIGS[workload]
     rows = 128
     x, w, _ = synthgen.linear_inputs(workload, m=rows)
     b = c["had_block"]
+    pw = quant.pack_weights(w, b)
     t0 = time.perf_counter()
-    done_rows = 0
+    done = 0
     while True:
         qx = quant.hadamard_quant(x, b, "nvfp4")
-        pw = quant.pack_weights(w, b)
         gemm.nvfp4_gemm_ref(qx["codes"], qx["scales"], qx["s_t"], pw["nvfp4"]["codes"], pw["nvfp4"]["scales"],
                             pw["nvfp4"]["s_t"])
         q8 = quant.hadamard_quant(x, b, "int8")
         gemm.int8_gemm_ref(q8["q"], q8["s"], pw["int4"]["q"], pw["int4"]["s"])
         gemm.bf16_gemm_ref(x, w)
-        done_rows += rows
+        done += rows
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
-    flops = 3 * 2.0 * done_rows * c["n"] * c["k"]
-    return dict(value=round(flops / dt / 1e12, 6), unit="TFLOP/s", cores=cores, kind="oracle",
-                sample=f"{done_rows} of {c['m']} token rows of {workload} (oracle quantizers, weight packing "
-                       f"and float64 reference GEMMs of all three kinds), {dt:.1f} s")
+    flops = 3 * 2.0 * done * c["n"] * c["k"]
+    return dict(value=round(flops / dt / 1e12, 6), unit="TFLOP/s", cores=os.cpu_count(), kind="oracle",
+                sample=f"{done} of {c['m']} token rows of {workload}: oracle quantizers and float64 reference "
+                       f"GEMMs of all three kinds (weights packed once, untimed), {dt:.1f} s")
+
+
+def _oracle_dit_sample(workload, budget_s):
+    """One INT8 block (both linears, quantizers, statistics) on a token sample, extrapolated to a DiT step."""
+    import numpy as np
+
+    import synthgen
+    from oracle import dit as odit
+    from oracle import policy, quant, stats
+    c = synthgen.DIT_CONFIGS[workload]
+    rows = 64
+    x = synthgen.activations(c["seed"], rows, c["hidden"], "laplace", 0.005, 50.0)
+    wu = synthgen.weights(c["seed"], c["ffn"], c["hidden"], c["w_std"], stream=100)
+    wd = synthgen.weights(c["seed"], c["hidden"], c["ffn"], c["w_std"], stream=101)
+    pu, pd = quant.pack_weights(wu, c["had_block"]), quant.pack_weights(wd, c["had_block"])
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        h = odit.linear(x, pu, policy.INT8, c["had_block"], "gelu")
+        out = odit.linear(h, pd, policy.INT8, c["had_block"], "residual", x)
+        stats.block_stats(x, out, np.zeros_like(x))
+        done += rows
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    sec_per_step = dt / done * c["tokens"] * c["blocks"]
+    return dict(value=round(1.0 / sec_per_step, 8), unit="step/s", cores=os.cpu_count(), kind="oracle",
+                sample=f"{done} token rows of one INT8 block (up GEMM + GELU, down GEMM + residual, both "
+                       f"quantizers, block statistics; weights packed once, untimed) in {dt:.1f} s, "
+                       f"extrapolated to {c['tokens']} tokens x {c['blocks']} blocks per step (all computed)")
+
+
+def cpu_baseline(workload: str, budget_s: float = 15.0):
+    """The oracle, as it stands, on a bounded sample of the workload (host cores)."""
+    if workload.startswith("dit"):
+        return _oracle_dit_sample(workload, budget_s)
+    return _oracle_linear_sample(workload, budget_s)
 
 
 def run_reference(args):
@@ -317,18 +575,21 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    t_steps = []
+    per_step = max(1.0, args.cpu_budget / max(1, args.steps))
+    vals, times = [], []
     cb = None
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        cb = cpu_baseline(args.workload, budget_s=args.cpu_budget / max(1, args.steps))
+        cb = cpu_baseline(args.workload, budget_s=per_step if i >= args.warmup else 0.5)
         if i >= args.warmup:
-            t_steps.append(time.perf_counter() - t0)
-    v = cb["value"]
+            times.append(time.perf_counter() - t0)
+            vals.append(cb["value"])
+    v = statistics.fmean(vals)
+    cb = dict(cb, value=v)
     line = dict(impl="reference", metric=METRIC, value=v, unit=cb["unit"], n_gpus=world, steps=args.steps,
-                warmup=args.warmup, ms_per_step=round(1e3 * sum(t_steps) / len(t_steps), 3),
-                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64 reference, f32 quantizers",
-                data="synthetic", config=dict(workload=args.workload), cpu_baseline=cb,
+                warmup=args.warmup, ms_per_step=round(1e3 * statistics.fmean(times), 3), higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64 reference GEMMs, f32 quantizers", data="synthetic",
+                config=dict(workload=args.workload), cpu_baseline=cb,
                 e2e=dict(value=v, unit=cb["unit"], h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
 
@@ -336,9 +597,9 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="qkv_2b", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="dit_2b", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -286,6 +286,30 @@ sixbit_status sixbit_block_stats_noalloc(const uint16_t* x_in, const uint16_t* x
 /* Largest n sixbit_block_stats_noalloc accepts. */
 int64_t sixbit_block_stats_noalloc_max_elems(void);
 
+/* ---- device-decided branches in a captured CUDA graph ------------------- */
+
+/*
+ * The policy decides per block on the device (technical summary sections
+ * 2.A-2.C), so a captured denoising step needs a branch the GPU resolves.
+ * While `stream` is being captured into a CUDA graph, sixbit_graph_switch_begin
+ * appends a one-thread selector kernel and a SWITCH conditional node with
+ * `nbranches` bodies: when the graph runs, body i executes when the low byte
+ * of *mode_dev equals first_mode + i, and no body executes otherwise.  Fill
+ * each body with sixbit_graph_branch_begin (returns `body_stream`, a
+ * caller-owned stream other than `stream`, now capturing into that body;
+ * enqueue the body's work there) and sixbit_graph_branch_end, then close with
+ * sixbit_graph_switch_end; capture of `stream` continues after the node.
+ * nbranches <= 8.  The returned object is
+ * owned by the library and freed by sixbit_graph_switch_end.  Errors:
+ * SIXBIT_EINVAL when `stream` is not capturing or calls are out of order.
+ */
+typedef struct sixbit_switch sixbit_switch;
+sixbit_status sixbit_graph_switch_begin(void* stream, void* body_stream, const int32_t* mode_dev, int first_mode,
+                                        int nbranches, sixbit_switch** sw);
+sixbit_status sixbit_graph_branch_begin(sixbit_switch* sw, int branch, void** body_stream);
+sixbit_status sixbit_graph_branch_end(sixbit_switch* sw);
+sixbit_status sixbit_graph_switch_end(sixbit_switch* sw);
+
 /* Synchronize `stream` and return the status recorded in err_dev (and clear it). */
 sixbit_status sixbit_check(int32_t* err_dev, void* stream);
 

@@ -1,0 +1,78 @@
+"""A synthetic residual-MLP diffusion transformer run end to end (oracle; test infrastructure only).
+
+Each block maps x -> x + W_d . GELU(W_u . x); per denoising step and block
+the policy ("6Bit-Diffusion" technical summary sections 2.A-2.C; popular
+summary sections 1-3) picks NVFP4 / INT8 / BF16 compute or a TDC skip, both
+linear layers of a computed block use the chosen precision, and the block's
+statistics (Gamma, delta cosine, the next block's input outlier ratio) feed
+the next decision.  The GEMM outputs are the float64 references rounded to
+FP32 and then to bf16, as a bf16 activation tensor is stored.
+
+This chains every other oracle module; it is compared with the GPU path on
+small sizes only.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import gemm, policy, quant, stats
+from .formats import bf16_round
+
+
+def _round_bf16(v64):
+    return bf16_round(np.asarray(v64, dtype=np.float64).astype(np.float32))
+
+
+def linear(x, pk, mode, b, epilogue, residual=None):
+    """One quantized linear layer in the given mode; returns bf16-valued float32."""
+    if mode == policy.NVFP4:
+        q = quant.hadamard_quant(x, b, "nvfp4")
+        nv = pk["nvfp4"]
+        ref, _ = gemm.nvfp4_gemm_ref(q["codes"], q["scales"], q["s_t"], nv["codes"], nv["scales"], nv["s_t"])
+    elif mode == policy.INT8:
+        q = quant.hadamard_quant(x, b, "int8")
+        i4 = pk["int4"]
+        ref, _, _ = gemm.int8_gemm_ref(q["q"], q["s"], i4["q"], i4["s"])
+    elif mode == policy.BF16:
+        ref = np.asarray(x, np.float64) @ pk["bf16"].astype(np.float64).T
+    else:
+        raise ValueError(mode)
+    return _round_bf16(gemm.epilogue(ref, epilogue, residual))
+
+
+class OracleDiT:
+    def __init__(self, weights, had_block, cfg: policy.PolicyConfig | None = None):
+        """weights: list of (W_up [F, H], W_down [H, F]) float32 per block."""
+        self.b = had_block
+        self.cfg = cfg or policy.PolicyConfig()
+        self.packs = [(quant.pack_weights(wu, had_block), quant.pack_weights(wd, had_block)) for wu, wd in weights]
+        self.L = len(weights)
+        self.states = [policy.PolicyState() for _ in range(self.L)]
+        self.deltas = [None] * self.L
+        self.trace = []          # per step: list of Decision per block
+
+    def step(self, x0):
+        x = np.asarray(x0, np.float32)
+        ratio = stats.outlier_ratio(stats.tensor_stats(x))
+        decisions = []
+        for l in range(self.L):
+            st = self.states[l]
+            d = policy.decide(st, ratio, self.cfg)
+            decisions.append(d)
+            if self.deltas[l] is None:
+                self.deltas[l] = np.zeros_like(x)
+            if d.mode == policy.SKIP:
+                out = stats.skip_apply(x, self.deltas[l])
+                out_stats = stats.tensor_stats(out)
+            else:
+                pu, pd = self.packs[l]
+                h = linear(x, pu, d.mode, self.b, "gelu")
+                out = linear(h, pd, d.mode, self.b, "residual", x)
+                bs = stats.block_stats(x, out, self.deltas[l])
+                self.deltas[l] = bs["delta"]
+                policy.fold(st, bs["gamma"], bs["cos"])
+                out_stats = bs["out"]
+            ratio = stats.outlier_ratio(out_stats)
+            x = out
+        self.trace.append(decisions)
+        return x

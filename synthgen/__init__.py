@@ -119,3 +119,64 @@ def linear_inputs(name: str, m: int | None = None):
     x = activations(c["seed"], mm, c["k"], c["dist"], c["outlier_frac"], c["outlier_scale"])
     w = weights(c["seed"], c["n"], c["k"])
     return x, w, c
+
+
+# Synthetic residual-MLP DiTs: block l maps x -> x + g_l W_d GELU(W_u x).
+# tokens x hidden, ffn, blocks, denoising steps; x_0 like the QKV input
+# (Laplace, 0.5% channels x50); x_s = bf16(x_{s-1} + sigma_s z_s) with sigma
+# falling linearly from 0.5 (s = 1) to 0.01 (last step).  gate: None (all 1)
+# or (lo, hi) for a seeded log-uniform per-block gate folded into W_d.
+DIT_CONFIGS = {
+    # small enough for the oracle to run end to end; its 20 steps x 4 blocks
+    # take every branch: PDR -> BF16, NVFP4, INT8, SKIP, refresh after skips
+    "dit_tiny": dict(seed=12, tokens=256, hidden=256, ffn=1024, blocks=4, steps=20, had_block=64,
+                     w_std=0.05, gate=(0.02, 0.5), outlier_frac=0.01, outlier_scale=4.0),
+    "dit_2b": dict(seed=3, tokens=TOKENS, hidden=1920, ffn=7680, blocks=30, steps=50, had_block=64,
+                   w_std=0.02, gate=None),
+    "dit_2b_gated": dict(seed=3, tokens=TOKENS, hidden=1920, ffn=7680, blocks=30, steps=50, had_block=64,
+                         w_std=0.02, gate=(0.02, 0.5)),
+    "dit_5b": dict(seed=4, tokens=TOKENS, hidden=3072, ffn=12288, blocks=42, steps=50, had_block=64,
+                   w_std=0.02, gate=None),
+}
+
+
+def sigmas(steps: int) -> np.ndarray:
+    """sigma_s for s = 1 .. steps-1, linear from 0.5 to 0.01."""
+    if steps <= 1:
+        return np.zeros(0)
+    return np.linspace(0.5, 0.01, steps - 1)
+
+
+def dit_gates(name: str) -> np.ndarray:
+    c = DIT_CONFIGS[name]
+    if c["gate"] is None:
+        return np.ones(c["blocks"])
+    lo, hi = c["gate"]
+    u = uniform(c["seed"], 40, c["blocks"])
+    return np.exp(np.log(lo) + u * (np.log(hi) - np.log(lo)))
+
+
+def dit_weights(name: str):
+    """[(W_up [ffn, hidden], W_down [hidden, ffn])] float32, the gate folded into W_down."""
+    c = DIT_CONFIGS[name]
+    g = dit_gates(name)
+    out = []
+    for l in range(c["blocks"]):
+        wu = (normal(c["seed"], 100 + 2 * l, c["ffn"] * c["hidden"]) * c["w_std"]).astype(np.float32)
+        wd = (normal(c["seed"], 101 + 2 * l, c["hidden"] * c["ffn"]) * c["w_std"] * g[l]).astype(np.float32)
+        out.append((wu.reshape(c["ffn"], c["hidden"]), wd.reshape(c["hidden"], c["ffn"])))
+    return out
+
+
+def dit_trajectory(name: str):
+    """List of bf16-valued float32 inputs x_0 .. x_{steps-1} [tokens, hidden]."""
+    c = DIT_CONFIGS[name]
+    x = activations(c["seed"], c["tokens"], c["hidden"], "laplace", c.get("outlier_frac", 0.005),
+                    c.get("outlier_scale", 50.0))
+    xs = [x]
+    n = c["tokens"] * c["hidden"]
+    for s, sg in enumerate(sigmas(c["steps"]), start=1):
+        z = normal(c["seed"], 1000 + s, n).reshape(c["tokens"], c["hidden"])
+        x = bf16_rne((x + sg * z).astype(np.float32))
+        xs.append(x)
+    return xs

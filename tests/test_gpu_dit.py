@@ -1,0 +1,103 @@
+"""A small residual-MLP DiT run end to end on the GPU path vs the oracle's own chain.
+
+Both sides start from the same seeded weights and input trajectory and run
+every step independently (the oracle never sees a GPU tensor).  Bar:
+- every per-block decision (mode and refresh / PDR / post-skip flags) is
+  identical, except where the oracle's deciding statistic is within 1e-3
+  (relative) of its threshold: along a chain the two sides' statistics
+  differ by the bf16 rounding of intermediate activations, not only by the
+  policy's 1e-6 band; comparison stops at such a point;
+- each step's output agrees to 1e-2 relative (Frobenius norm);
+- the run takes every branch: BF16 (PDR), NVFP4, INT8, SKIP and a refresh;
+- the CUDA-graph replay of a step gives bit-identical results to eager launches.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synthgen
+from oracle import policy
+from oracle.dit import OracleDiT
+
+pytestmark = pytest.mark.gpu
+NAMES = {1: "NVFP4", 2: "INT8", 3: "BF16", 4: "SKIP"}
+
+
+def _margin(st, ratio, cfg):
+    m = [abs(ratio - cfg.pdr_ratio) / cfg.pdr_ratio]
+    if st.n_computed >= 2:
+        m.append(abs(st.cos - cfg.cos_thr) / cfg.cos_thr)
+        if st.cos >= cfg.cos_thr:
+            m.append(abs(st.acc + 1 - st.cos - cfg.err_cap) / cfg.err_cap)
+    if st.have_gamma:
+        m.append(abs(st.gamma - cfg.gamma_thr) / cfg.gamma_thr)
+    return min(m)
+
+
+def _run_gpu(name, graph, switched=True):
+    from video_dit_mixed_gb300 import dit, ops
+    c = synthgen.DIT_CONFIGS[name]
+    packed = dit.pack_block_weights(synthgen.dit_weights(name), c["had_block"])
+    model = dit.DiT(c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"], packed)
+    xs = [torch.from_numpy(x).to(torch.bfloat16).cuda() for x in synthgen.dit_trajectory(name)]
+    outs, words = [], []
+    for s, x in enumerate(xs):
+        if graph and s == 1:
+            model.capture(switched=switched)
+        y = model.step(x)
+        torch.cuda.synchronize()
+        outs.append(y.float().cpu().numpy())
+        words.append(model.modes.cpu().numpy().copy())
+    return outs, words, model
+
+
+def test_tiny_dit_against_oracle_chain():
+    name = "dit_tiny"
+    c = synthgen.DIT_CONFIGS[name]
+    outs, words, _ = _run_gpu(name, graph=False)
+    cfg = policy.PolicyConfig()
+    ref = OracleDiT(synthgen.dit_weights(name), c["had_block"], cfg)
+    # record the oracle's distance to its thresholds at every decision
+    margins = []
+    orig = policy.decide
+
+    def decide(st, ratio, cf):
+        margins.append(_margin(st, ratio, cf))
+        return orig(st, ratio, cf)
+
+    import oracle.dit as odit
+    odit.policy.decide = decide
+    try:
+        seen = set()
+        for s, x in enumerate(synthgen.dit_trajectory(name)):
+            y = ref.step(x)
+            stop = False
+            for l, d in enumerate(ref.trace[-1]):
+                w = int(words[s][l])
+                gpu = (NAMES[w & 0xFF], bool(w & 256), bool(w & 512), bool(w & 1024))
+                ora = (d.mode, d.refresh, d.pdr, d.post_skip)
+                seen.add(d.mode)
+                if d.refresh:
+                    seen.add("REFRESH")
+                if gpu != ora:
+                    assert margins[s * c["blocks"] + l] < 1e-3, (s, l, gpu, ora)
+                    stop = True
+                    break
+            if stop:
+                break
+            err = np.linalg.norm(outs[s].astype(np.float64) - y) / np.linalg.norm(y)
+            assert err <= 1e-2, (s, err)
+        assert {"BF16", "NVFP4", "INT8", "SKIP", "REFRESH"} <= seen, seen
+    finally:
+        odit.policy.decide = orig
+
+
+@pytest.mark.parametrize("switched", [False, True])
+def test_graph_replay_matches_eager(switched):
+    o_eager, w_eager, _ = _run_gpu("dit_tiny", graph=False)
+    o_graph, w_graph, m = _run_gpu("dit_tiny", graph=True, switched=switched)
+    assert m.graph is not None
+    for a, b in zip(w_eager, w_graph):
+        np.testing.assert_array_equal(a, b)
+    for a, b in zip(o_eager, o_graph):
+        np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))

@@ -58,6 +58,10 @@ EXPORTS = {
     "sixbit_skip_apply": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),
     "sixbit_block_stats_noalloc": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p]),
     "sixbit_block_stats_noalloc_max_elems": (C.c_int64, []),
+    "sixbit_graph_switch_begin": (C.c_int, [c_p, c_p, c_p, C.c_int, C.c_int, C.POINTER(c_p)]),
+    "sixbit_graph_branch_begin": (C.c_int, [c_p, C.c_int, C.POINTER(c_p)]),
+    "sixbit_graph_branch_end": (C.c_int, [c_p]),
+    "sixbit_graph_switch_end": (C.c_int, [c_p]),
     "sixbit_check": (C.c_int, [c_p, c_p]),
     "sixbit_status_str": (C.c_char_p, [C.c_int]),
     "sixbit_launch_count": (C.c_uint64, []),

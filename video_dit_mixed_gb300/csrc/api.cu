@@ -210,7 +210,7 @@ sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const s
   if (run_fp4) {
     CUtensorMap ma, mb;
     if (!make_map(&ma, A->fp4_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, M, K / 2, 128) ||
-        !make_map(&mb, W->fp4_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, 128))
+        !make_map(&mb, W->fp4_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, N, K / 2, 256))
       return SIXBIT_ECUDA;
     GemmParams q = p;
     q.want_mode = SIXBIT_MODE_NVFP4;
@@ -223,7 +223,7 @@ sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const s
   if (run_i8) {
     CUtensorMap ma, mb;
     if (!make_map(&ma, A->i8_operand, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, 128) ||
-        !make_map(&mb, W->i4_operand, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, 128))
+        !make_map(&mb, W->i4_operand, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, 256))
       return SIXBIT_ECUDA;
     GemmParams q = p;
     q.want_mode = SIXBIT_MODE_INT8;
@@ -235,7 +235,7 @@ sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const s
   if (run_bf) {
     CUtensorMap ma, mb;
     if (!make_map(&ma, X_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, 128) ||
-        !make_map(&mb, W->bf16_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, 128))
+        !make_map(&mb, W->bf16_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, 256))
       return SIXBIT_ECUDA;
     GemmParams q = p;
     q.want_mode = SIXBIT_MODE_BF16;

@@ -4,27 +4,32 @@
 // INT8 activations against 4-bit weights: W4A4 / W4A8) and 2.C (PDR's
 // FP16/BF16 recompute); popular summary section 4 (custom CUDA kernels).
 //
-// One CTA computes one 128 x 128 output tile with three warp roles:
+// A persistent CTA per SM walks 128 x 256 output tiles with three warp roles:
 //   warp 0      TMA producer: A/B tiles (128-byte swizzle) and, for NVFP4,
-//               the 2 KB scale-factor chunks, into a ring of shared-memory
-//               stages guarded by full/empty mbarriers;
+//               the scale-factor chunks, into a ring of shared-memory stages
+//               guarded by full/empty mbarriers;
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma (and,
 //               for NVFP4, tcgen05.cp of the scale factors into tensor
-//               memory) and tcgen05.commit to release stages;
-//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulators (warp w reads
-//               lanes 32*(w%4)..+31 = tile rows), scaling, GELU or residual,
-//               bf16 (or fp32) stores.
+//               memory) and tcgen05.commit to release stages and accumulators;
+//   warps 2..9  epilogue: tcgen05.ld of the FP32 accumulators (warp w reads
+//               lanes 32*(w%4)..+31 = tile rows, one 128-column half),
+//               scaling, GELU or residual, bf16 (or fp32) stores.
 // Kinds:
 //   NVFP4  kind::mxf4nvf4.block_scale.scale_vec::4X, E2M1 x E2M1 with one
-//          E4M3 scale per 16 elements, 256 K-elements (128 bytes) per stage.
-//   BF16   kind::f16 with bf16 operands, 64 K-elements per stage.  Used for
-//          the PDR path and, with "grouped" accumulation, for W4A8: INT8
-//          activation codes and INT4 weight codes are small integers, exact
-//          in bf16, every product and every 128-term group sum (|.| < 2^17)
-//          is an integer exactly representable in FP32, so each group's FP32
-//          accumulator holds the exact integer sum.  Groups alternate
-//          between two accumulator buffers in tensor memory; the epilogue
-//          folds s_w[g][n] * acc_g into registers while the next group runs.
+//          E4M3 scale per 16 elements, 256 K-elements (128 bytes) per stage;
+//          a 128 x 256 tile is two N = 128 MMAs per K step sharing A.  One
+//          accumulator buffer (256 columns) plus the scale factors fill
+//          tensor memory; the epilogue drains the accumulator to registers
+//          and releases it before its stores, so they overlap the next tile.
+//   BF16   kind::f16 with bf16 operands, N = 256 MMAs, 64 K-elements per
+//          stage, two accumulator buffers.  Used for the PDR path and, with
+//          "grouped" accumulation, for W4A8: INT8 activation codes and INT4
+//          weight codes are small integers, exact in bf16, every product and
+//          every 128-term group sum (|.| < 2^17) is an integer exactly
+//          representable in FP32, so each group's FP32 accumulator holds the
+//          exact integer sum.  Groups alternate between the two buffers; the
+//          epilogue folds s_w[g][n] * acc_g into registers while the next
+//          group runs.
 // Every mbarrier wait is bounded (2 s); on expiry the kernel records
 // SIXBIT_ETIMEOUT in the error word, drains its in-flight copies and tensor
 // core work with bounded waits, frees tensor memory and returns.
@@ -36,7 +41,11 @@
 namespace sixbit {
 
 constexpr int kBM = 128;
-constexpr int kBN = 128;
+constexpr int kBN = 256;       // output tile columns
+constexpr int kEpiWarps = 8;   // two per tensor-memory lane quarter, 128 columns each
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kEpiCols = kBN / (kEpiWarps / 4);
+constexpr int kGemmThreads = 64 + kEpiThreads;
 
 enum { KIND_BF16 = 0, KIND_NVF4 = 1 };
 
@@ -44,35 +53,37 @@ template <int KIND>
 struct GemmCfg;
 template <>
 struct GemmCfg<KIND_BF16> {
-  static constexpr int kStages = 6;
+  static constexpr int kStages = 4;
   static constexpr int kKStage = 64;      // K elements per stage
   static constexpr int kKCoord = 64;      // TMA x coordinate step per stage
   static constexpr int kMmaPerStage = 4;  // K = 16 per MMA
-  static constexpr int kSfBytes = 0;
+  static constexpr int kSfaBytes = 0;
+  static constexpr int kSfbBytes = 0;
   static constexpr uint32_t kIdesc = idesc_bf16(kBM, kBN);
 };
 template <>
 struct GemmCfg<KIND_NVF4> {
-  static constexpr int kStages = 5;
+  static constexpr int kStages = 4;
   static constexpr int kKStage = 256;
   static constexpr int kKCoord = 128;     // bytes of packed E2M1
   static constexpr int kMmaPerStage = 4;  // K = 64 per MMA
-  static constexpr int kSfBytes = 2048;   // 128 rows x 16 scales
-  static constexpr uint32_t kIdesc = idesc_nvf4(kBM, kBN);
+  static constexpr int kSfaBytes = 2048;  // 128 rows x 16 scales
+  static constexpr int kSfbBytes = 4096;  // 256 rows x 16 scales (two 128-row chunks)
+  static constexpr uint32_t kIdesc = idesc_nvf4(kBM, 128);
 };
 
-constexpr int kTileBytes = kBM * 128;  // one 128 x 128-byte operand tile
+constexpr int kATileBytes = kBM * 128;  // 128 rows x 128 bytes
+constexpr int kBTileBytes = kBN * 128;  // 256 rows x 128 bytes
 
 template <int KIND>
 __host__ __device__ constexpr int stage_bytes() {
-  return 2 * kTileBytes + 2 * GemmCfg<KIND>::kSfBytes;
+  return kATileBytes + kBTileBytes + GemmCfg<KIND>::kSfaBytes + GemmCfg<KIND>::kSfbBytes;
 }
-template <int KIND>
+template <int KIND, bool GROUPED>
 __host__ __device__ constexpr int gemm_smem_bytes() {
-  return GemmCfg<KIND>::kStages * stage_bytes<KIND>() + 1024 /*align*/ + 256 /*barriers*/;
+  return GemmCfg<KIND>::kStages * stage_bytes<KIND>() + 1024 /*align*/ + 256 /*barriers*/ +
+         (GROUPED ? kEpiWarps * kEpiCols * 4 : 0) /*per-warp group scales*/;
 }
-
-
 
 __device__ __forceinline__ float gelu_erf(float v) {
   return 0.5f * v * (1.0f + erff(v * 0.7071067811865475244f));
@@ -121,38 +132,19 @@ __device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, i
   }
 }
 
-// Stages of the shared-memory ring; the grouped (W4A8) kernel gives one stage
-// up for its staged group scales (up to K = 16768).
-template <int KIND, bool GROUPED>
-__host__ __device__ constexpr int gemm_stages() {
-  return GROUPED ? 5 : GemmCfg<KIND>::kStages;
-}
-
-template <bool GROUPED>
-struct EpiCfg {
-  static constexpr int kWarps = GROUPED ? 8 : 4;    // epilogue warps
-  static constexpr int kThreads = kWarps * 32;
-  static constexpr int kCols = kBN / (kWarps / 4);  // accumulator columns per epilogue thread
-};
-
-template <bool GROUPED>
-constexpr int gemm_threads() {
-  return 64 + EpiCfg<GROUPED>::kThreads;
-}
-
 // Persistent kernel: each CTA walks output tiles t = blockIdx.x, +gridDim.x,
 // ... (row tiles fastest, so the CTAs in flight share the same weight tiles).
-// Two accumulator buffers in tensor memory let the epilogue of one tile (or
-// K group) overlap the MMAs of the next.
 template <int KIND, bool GROUPED, bool DBG>
-__global__ void __launch_bounds__(gemm_threads<GROUPED>(), 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmParams p) {
   using C = GemmCfg<KIND>;
-  using E = EpiCfg<GROUPED>;
-  constexpr int S = gemm_stages<KIND, GROUPED>();
-  constexpr uint32_t kCols = (KIND == KIND_NVF4) ? 512 : 256;
-  constexpr uint32_t kSfCol = 2 * kBN;  // NVFP4 scale factors live after the two accumulators
+  constexpr int S = C::kStages;
+  constexpr bool kNvf4 = KIND == KIND_NVF4;
+  constexpr uint32_t kCols = 512;
+  constexpr uint32_t kSfaCol = 256;  // NVFP4: SFA [256, 272), SFB [272, 304)
+  constexpr uint32_t kSfbCol = 272;
+  constexpr uint32_t kBufs = kNvf4 ? 1 : 2;  // accumulator buffers of kBN columns
   if (p.mode_dev != nullptr && SIXBIT_MODE_OF(*p.mode_dev) != p.want_mode) return;
 
   extern __shared__ uint8_t smem_raw[];
@@ -167,14 +159,12 @@ __global__ void __launch_bounds__(gemm_threads<GROUPED>(), 1)
   uint64_t* drain = bars + 2 * S + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  uint64_t* sw_full = bars + 2 * S + 6;   // GROUPED: a tile's group scales are staged
-  uint64_t* sw_empty = bars + 2 * S + 7;  // GROUPED: ... and no longer read
-  float* sw_smem = reinterpret_cast<float*>(bars + 2 * S + 8);  // GROUPED: [K/128][128] group scales of a tile
+  float* sw_smem = reinterpret_cast<float*>(smem + S * stage_bytes<KIND>() + 256);  // GROUPED: per-warp scales
 
   auto A_tile = [&](int s) { return tiles + s * stage_bytes<KIND>(); };
-  auto B_tile = [&](int s) { return tiles + s * stage_bytes<KIND>() + kTileBytes; };
-  auto SFA = [&](int s) { return tiles + s * stage_bytes<KIND>() + 2 * kTileBytes; };
-  auto SFB = [&](int s) { return tiles + s * stage_bytes<KIND>() + 2 * kTileBytes + C::kSfBytes; };
+  auto B_tile = [&](int s) { return tiles + s * stage_bytes<KIND>() + kATileBytes; };
+  auto SFA = [&](int s) { return tiles + s * stage_bytes<KIND>() + kATileBytes + kBTileBytes; };
+  auto SFB = [&](int s) { return tiles + s * stage_bytes<KIND>() + kATileBytes + kBTileBytes + C::kSfaBytes; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -194,11 +184,9 @@ __global__ void __launch_bounds__(gemm_threads<GROUPED>(), 1)
     }
     mbar_init(&accf[0], 1);
     mbar_init(&accf[1], 1);
-    mbar_init(&acce[0], E::kThreads);
-    mbar_init(&acce[1], E::kThreads);
+    mbar_init(&acce[0], kEpiThreads);
+    mbar_init(&acce[1], kEpiThreads);
     mbar_init(drain, 1);
-    mbar_init(sw_full, E::kThreads);
-    mbar_init(sw_empty, E::kThreads);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -220,8 +208,10 @@ __global__ void __launch_bounds__(gemm_threads<GROUPED>(), 1)
       // ------------------------------------------------------ producer --
       uint32_t it = 0;
       bool ok = true;
+      const size_t sf_rows_bytes = static_cast<size_t>(128) * (p.K >> 4);  // one 128-row scale tile
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         const int m_tile = t % tiles_m, n_tile = t / tiles_m;
+        const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;  // 128-row halves of B that exist
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % S;
           const uint32_t ph = (it / S) & 1;
@@ -232,14 +222,15 @@ __global__ void __launch_bounds__(gemm_threads<GROUPED>(), 1)
             break;
           }
           const int kvalid = min(C::kKStage, p.K - kb * C::kKStage);
-          const uint32_t sf_bytes = C::kSfBytes == 0 ? 0u : static_cast<uint32_t>(kvalid / 64) * 512u;
-          mbar_expect_tx(&full[s], 2 * kTileBytes + 2 * sf_bytes);
+          const uint32_t sf_bytes = kNvf4 ? static_cast<uint32_t>(kvalid / 64) * 512u : 0u;
+          mbar_expect_tx(&full[s], kATileBytes + kBTileBytes + sf_bytes * (1 + (kNvf4 ? nj : 0)));
           tma_load_2d(A_tile(s), &tmA, &full[s], kb * C::kKCoord, m_tile * kBM);
           tma_load_2d(B_tile(s), &tmB, &full[s], kb * C::kKCoord, n_tile * kBN);
-          if constexpr (KIND == KIND_NVF4) {
-            const size_t row_bytes = static_cast<size_t>(128) * (p.K >> 4);
-            bulk_load(SFA(s), p.sfa + m_tile * row_bytes + static_cast<size_t>(kb) * 2048, sf_bytes, &full[s]);
-            bulk_load(SFB(s), p.sfb + n_tile * row_bytes + static_cast<size_t>(kb) * 2048, sf_bytes, &full[s]);
+          if constexpr (kNvf4) {
+            bulk_load(SFA(s), p.sfa + m_tile * sf_rows_bytes + static_cast<size_t>(kb) * 2048, sf_bytes, &full[s]);
+            for (int j = 0; j < nj; ++j)
+              bulk_load(SFB(s) + 2048 * j, p.sfb + (2 * n_tile + j) * sf_rows_bytes + static_cast<size_t>(kb) * 2048,
+                        sf_bytes, &full[s]);
           }
         }
       }
@@ -249,15 +240,18 @@ __global__ void __launch_bounds__(gemm_threads<GROUPED>(), 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------- MMA issuer --
-      uint32_t it = 0;   // stage counter
-      uint32_t ac = 0;   // accumulator-buffer use counter (tiles, or K groups when GROUPED)
+      uint32_t it = 0;  // stage counter
+      uint32_t ac = 0;  // accumulator-buffer use counter (tiles, or K groups when GROUPED)
       bool ok = true;
       constexpr int spg = 128 / C::kKStage > 0 ? 128 / C::kKStage : 1;  // stages per K group (bf16 kinds)
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const int n_tile = t / tiles_m;
+        const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;
         for (int kb = 0; kb < nk && ok; ++kb, ++it) {
           const bool acc_start = GROUPED ? (kb % spg) == 0 : kb == 0;
-          const uint32_t buf = ac & 1;
-          if (acc_start && ac >= 2 && !mbar_wait(&acce[buf], ((ac >> 1) - 1) & 1, abort_flag)) {
+          const uint32_t buf = ac % kBufs;
+          // the buffer's previous contents must have been drained by the epilogue
+          if (acc_start && ac >= kBufs && !mbar_wait(&acce[buf], ((ac / kBufs) - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -270,20 +264,25 @@ __global__ void __launch_bounds__(gemm_threads<GROUPED>(), 1)
           const uint32_t a_base = smem_u32(A_tile(s));
           const uint32_t b_base = smem_u32(B_tile(s));
           const uint32_t d_tmem = tmem + buf * kBN;
-          if constexpr (KIND == KIND_NVF4) {
+          if constexpr (kNvf4) {
             const int nmma = min(C::kKStage, p.K - kb * C::kKStage) / 64;
 #pragma unroll
             for (int k = 0; k < C::kMmaPerStage; ++k) {
               if (k < nmma) {
-                tmem_cp_32x128b_warpx4(tmem + kSfCol + 4 * k, sdesc_sf(smem_u32(SFA(s)) + 512 * k));
-                tmem_cp_32x128b_warpx4(tmem + kSfCol + 16 + 4 * k, sdesc_sf(smem_u32(SFB(s)) + 512 * k));
+                tmem_cp_32x128b_warpx4(tmem + kSfaCol + 4 * k, sdesc_sf(smem_u32(SFA(s)) + 512 * k));
+                for (int j = 0; j < nj; ++j)
+                  tmem_cp_32x128b_warpx4(tmem + kSfbCol + 8 * k + 4 * j, sdesc_sf(smem_u32(SFB(s)) + 2048 * j + 512 * k));
               }
             }
 #pragma unroll
-            for (int k = 0; k < C::kMmaPerStage; ++k)
-              if (k < nmma)
-                mma_nvf4(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), C::kIdesc,
-                         tmem + kSfCol + 4 * k, tmem + kSfCol + 16 + 4 * k, (acc_start && k == 0) ? 0u : 1u);
+            for (int k = 0; k < C::kMmaPerStage; ++k) {
+              if (k < nmma) {
+                for (int j = 0; j < nj; ++j)
+                  mma_nvf4(d_tmem + 128 * j, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 16384 * j + 32 * k),
+                           C::kIdesc, tmem + kSfaCol + 4 * k, tmem + kSfbCol + 8 * k + 4 * j,
+                           (acc_start && k == 0) ? 0u : 1u);
+              }
+            }
           } else {
 #pragma unroll
             for (int k = 0; k < C::kMmaPerStage; ++k)
@@ -307,64 +306,78 @@ __global__ void __launch_bounds__(gemm_threads<GROUPED>(), 1)
     }
   } else {
     // -------------------------------------------------------- epilogue --
-    const int ew = warp - 2;              // 0 .. kWarps-1
-    const int q = warp & 3;               // tensor-memory lane quarter this warp may read
-    const int col0 = (ew >> 2) * E::kCols;  // first accumulator column of this thread
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    const int ew = warp - 2;                      // 0 .. kEpiWarps-1
+    const int q = warp & 3;                       // tensor-memory lane quarter this warp may read
+    const int col0 = (ew >> 2) * kEpiCols;        // first accumulator column of this thread
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16) + col0;
+    float* my_sw = sw_smem + ew * kEpiCols;       // GROUPED: this warp's group scales
     uint32_t ac = 0;
-    uint32_t lt = 0;  // local tile counter
     bool ok = true;
-    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++lt) {
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       const int m_tile = t % tiles_m, n_tile = t / tiles_m;
       const int row = m_tile * kBM + 32 * q + lane;
-      const int n0 = n_tile * kBN;
+      const int nb = n_tile * kBN + col0;         // first output column of this thread
+      if (nb >= p.N) {                            // nothing of this half exists (ragged N)
+        if constexpr (GROUPED) {
+          for (int g = 0; g < groups && ok; ++g, ++ac) {
+            const uint32_t buf = ac & 1;
+            if (!mbar_wait(&accf[buf], (ac >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_before();
+            mbar_arrive(&acce[buf]);
+          }
+        } else {
+          const uint32_t buf = ac % kBufs;
+          if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_before();
+          mbar_arrive(&acce[buf]);
+          ++ac;
+        }
+        continue;
+      }
       if constexpr (GROUPED) {
-        // the tile's group scales s_w[g][n0 .. n0+127] into shared memory, once
-        // every epilogue thread is done with the previous tile's (bounded waits)
-        if (lt >= 1 && !mbar_wait(sw_empty, (lt - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        for (int i = threadIdx.x - 64; i < groups * kBN; i += E::kThreads) {
-          const int g = i / kBN, c = i % kBN;
-          sw_smem[i] = (n0 + c < p.N) ? __ldg(p.grp_scale + static_cast<size_t>(g) * p.N + n0 + c) : 0.f;
-        }
-        mbar_arrive(sw_full);
-        if (!mbar_wait(sw_full, lt & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        float sum[E::kCols];
+        float sum[kEpiCols];
 #pragma unroll
-        for (int j = 0; j < E::kCols; ++j) sum[j] = 0.f;
+        for (int j = 0; j < kEpiCols; ++j) sum[j] = 0.f;
+        auto load_sw = [&](int g) {
+          const int n = nb + 4 * lane;
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (g < groups && n < p.N) v = __ldg(reinterpret_cast<const float4*>(p.grp_scale + static_cast<size_t>(g) * p.N + n));
+          return v;
+        };
+        float4 sw_next = load_sw(0);
         for (int g = 0; g < groups; ++g, ++ac) {
+          const float4 sw_now = sw_next;
+          sw_next = load_sw(g + 1);                // prefetch the next group's scales
+          __syncwarp();
+          reinterpret_cast<float4*>(my_sw)[lane] = sw_now;
+          __syncwarp();
           const uint32_t buf = ac & 1;
           if (!mbar_wait(&accf[buf], (ac >> 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const float4* sw4 = reinterpret_cast<const float4*>(sw_smem + g * kBN + col0);
+          const float4* sw4 = reinterpret_cast<const float4*>(my_sw);
 #pragma unroll
-          for (int c = 0; c < E::kCols / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(lane_addr + buf * kBN + col0 + c * 32, r);
+          for (int c = 0; c < kEpiCols / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + buf * kBN + c * 16, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-              const float4 s4 = sw4[c * 8 + j4];
+            for (int j4 = 0; j4 < 4; ++j4) {
+              const float4 s4 = sw4[c * 4 + j4];
               const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                const int j = c * 32 + j4 * 4 + u;
+                const int j = c * 16 + j4 * 4 + u;
                 sum[j] = fmaf(sv[u], __uint_as_float(r[j4 * 4 + u]), sum[j]);
               }
             }
             if constexpr (DBG) {
               if (row < p.M) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  const int n = n0 + col0 + c * 32 + j;
+                for (int j = 0; j < 16; ++j) {
+                  const int n = nb + c * 16 + j;
                   if (n < p.N)
                     p.acc_dbg[(static_cast<size_t>(g) * p.M + row) * p.N + n] = __float2int_rn(__uint_as_float(r[j]));
                 }
@@ -375,37 +388,53 @@ __global__ void __launch_bounds__(gemm_threads<GROUPED>(), 1)
           mbar_arrive(&acce[buf]);
         }
         if (!ok) break;
-        mbar_arrive(sw_empty);
         const float sm = (row < p.M) ? p.row_scale[row] : 0.f;
 #pragma unroll
-        for (int c = 0; c < E::kCols / 32; ++c) {
+        for (int c = 0; c < kEpiCols / 32; ++c) {
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(sum[c * 32 + j], sm);
-          if (n0 + col0 + c * 32 < p.N) epilogue_store32(p, row, n0 + col0 + c * 32, v);
+          if (nb + c * 32 < p.N) epilogue_store32(p, row, nb + c * 32, v);
         }
       } else {
-        const uint32_t buf = ac & 1;
-        if (!mbar_wait(&accf[buf], (ac >> 1) & 1, abort_flag)) {
+        const uint32_t buf = ac % kBufs;
+        if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         float alpha = 1.0f;
-        if constexpr (KIND == KIND_NVF4) alpha = __fmul_rn(*p.s_a, *p.s_b);
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(lane_addr + buf * kBN + c * 32, r);
-          tmem_ld_wait();
-          if (c == kBN / 32 - 1) {  // buffer fully read: hand it back to the MMA warp
-            tc_fence_before();
-            mbar_arrive(&acce[buf]);
-          }
-          float v[32];
+        if constexpr (kNvf4) alpha = __fmul_rn(*p.s_a, *p.s_b);
+        if constexpr (kNvf4) {
+          // single accumulator: drain all of this thread's columns, release, then store
+          uint32_t r[kEpiCols / 32][32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
-          if (n0 + c * 32 < p.N) epilogue_store32(p, row, n0 + c * 32, v);
+          for (int c = 0; c < kEpiCols / 32; ++c) tmem_ld32(lane_addr + c * 32, r[c]);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&acce[buf]);
+#pragma unroll
+          for (int c = 0; c < kEpiCols / 32; ++c) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[c][j]), alpha);
+            if (nb + c * 32 < p.N) epilogue_store32(p, row, nb + c * 32, v);
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < kEpiCols / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(lane_addr + buf * kBN + c * 32, r);
+            tmem_ld_wait();
+            if (c == kEpiCols / 32 - 1) {  // buffer fully read: hand it back to the MMA warp
+              tc_fence_before();
+              mbar_arrive(&acce[buf]);
+            }
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
+            if (nb + c * 32 < p.N) epilogue_store32(p, row, nb + c * 32, v);
+          }
         }
         ++ac;
       }
@@ -438,18 +467,17 @@ static int num_sms() {
 
 template <int KIND, bool GROUPED, bool DBG>
 static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
-  static int attr_done = 0;
-  const int smem = gemm_stages<KIND, GROUPED>() * stage_bytes<KIND>() + 1024 + 256 +
-                   (GROUPED ? (p.K / 128) * kBN * 4 : 0);
-  if (smem > attr_done) {
+  static bool attr_done = false;
+  constexpr int smem = gemm_smem_bytes<KIND, GROUPED>();
+  if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(qgemm_kernel<KIND, GROUPED, DBG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_done = smem;
+    attr_done = true;
   }
   const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  qgemm_kernel<KIND, GROUPED, DBG><<<grid, gemm_threads<GROUPED>(), smem, st>>>(a, b, p);
+  qgemm_kernel<KIND, GROUPED, DBG><<<grid, kGemmThreads, smem, st>>>(a, b, p);
   note_launch();
   return cudaGetLastError();
 }

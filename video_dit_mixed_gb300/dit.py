@@ -1,0 +1,176 @@
+"""Runs a residual-MLP diffusion transformer through the hot path, one denoising step at a time.
+
+Every block maps x -> x + W_d . GELU(W_u . x).  Per step and block the
+policy kernel writes a mode word on the device; every later kernel of the
+block reads it and does its work only when the mode is its own, so one step
+is a fixed sequence of launches with no host synchronisation, and it is
+captured once into a CUDA graph and replayed.
+
+Per block l (all on one stream):
+  policy_step(state[l], stats[l], in_stats) -> mode[l]
+  skip_apply(x, delta[l]) -> out                         (SKIP)
+  hadamard_quant(x) -> qa_x                              (NVFP4 / INT8)
+  qgemm(qa_x | x, W_up[l], GELU) -> h                    (NVFP4 / INT8 / BF16)
+  hadamard_quant(h) -> qa_h
+  qgemm(qa_h | h, W_down[l], + x) -> out
+  block_stats(x, out, delta[l]) -> stats[l], delta[l]    (not SKIP)
+in_stats of block 0 come from tensor_stats(x_0), of block l from stats[l-1].
+"""
+from __future__ import annotations
+
+import torch
+
+from . import ops
+
+
+class DiT:
+    def __init__(self, tokens: int, hidden: int, ffn: int, blocks: int, had_block: int, packed, cfg=None,
+                 device="cuda"):
+        """packed: list of (PackedWeights up [ffn, hidden], PackedWeights down [hidden, ffn])."""
+        assert len(packed) == blocks
+        dev = torch.device(device)
+        self.T, self.H, self.F, self.L, self.b = tokens, hidden, ffn, blocks, had_block
+        self.packed = packed
+        self.cfg = cfg or ops.policy_cfg()
+        bf = torch.bfloat16
+        self.x_in = torch.zeros((tokens, hidden), dtype=bf, device=dev)
+        self.bufs = [torch.zeros((tokens, hidden), dtype=bf, device=dev) for _ in range(2)]
+        self.h = torch.zeros((tokens, ffn), dtype=bf, device=dev)
+        self.deltas = torch.zeros((blocks, tokens, hidden), dtype=bf, device=dev)
+        self.qa_x = ops.QActTensors(tokens, hidden, dev)
+        self.qa_h = ops.QActTensors(tokens, ffn, dev)
+        self.tstats = torch.zeros(4, dtype=torch.float64, device=dev)
+        self.stats = ops.new_stats(dev, blocks)
+        self.state = ops.new_policy_state(dev, blocks)
+        self.modes = torch.zeros(blocks, dtype=torch.int32, device=dev)
+        self.scratch = ops.new_scratch(tokens * ffn, dev)
+        self.graph = None
+        self.out = self.bufs[(blocks - 1) % 2]
+
+    def reset(self):
+        """Back to the state before the first denoising step."""
+        self.deltas.zero_()
+        self.stats.zero_()
+        self.state.zero_()
+        self.modes.zero_()
+
+    def _in_stats(self, l):
+        return self.tstats if l == 0 else self.stats[l - 1, 4:7]
+
+    CALLS = ("policy_step", "skip_apply", "hq_x", "qgemm_up", "hq_h", "qgemm_down", "block_stats")
+
+    def enqueue_step(self, after_call=None):
+        """Enqueue one denoising step on the current stream (input: self.x_in).
+
+        after_call(label, block) is invoked on the host after each library call
+        (e.g. to record a CUDA event for per-call timing); labels are
+        "tensor_stats" (block -1) and DiT.CALLS.
+        """
+        o = ops
+        note = after_call or (lambda label, block: None)
+        o.tensor_stats(self.x_in, self.tstats, self.scratch)
+        note("tensor_stats", -1)
+        x = self.x_in
+        for l in range(self.L):
+            out = self.bufs[l % 2]
+            mode = self.modes[l:l + 1]
+            st = self.stats[l]
+            up, down = self.packed[l]
+            o.policy_step(self.cfg, self.state[l], st, self._in_stats(l), mode)
+            note("policy_step", l)
+            o.skip_apply(x, self.deltas[l], out, st, self.scratch, mode_dev=mode)
+            note("skip_apply", l)
+            o.hadamard_quant(x, self.b, 0, out=self.qa_x, mode_dev=mode)
+            note("hq_x", l)
+            o.qgemm(self.qa_x, x, up, 0, epilogue=o.EPI_GELU, out=self.h, mode_dev=mode)
+            note("qgemm_up", l)
+            o.hadamard_quant(self.h, self.b, 0, out=self.qa_h, mode_dev=mode)
+            note("hq_h", l)
+            o.qgemm(self.qa_h, self.h, down, 0, epilogue=o.EPI_RESIDUAL, residual=x, out=out, mode_dev=mode)
+            note("qgemm_down", l)
+            o.block_stats(x, out, self.deltas[l], st, self.scratch, mode_dev=mode)
+            note("block_stats", l)
+            x = out
+        return x
+
+    def _compute_body(self, x, out, l, mode):
+        """The kernels of one computed block in a fixed mode (no mode word)."""
+        o = ops
+        up, down = self.packed[l]
+        quant = mode != o.MODE_BF16
+        if quant:
+            o.hadamard_quant(x, self.b, mode, out=self.qa_x)
+        o.qgemm(self.qa_x if quant else None, x, up, mode, epilogue=o.EPI_GELU, out=self.h, m=self.T)
+        if quant:
+            o.hadamard_quant(self.h, self.b, mode, out=self.qa_h)
+        o.qgemm(self.qa_h if quant else None, self.h, down, mode, epilogue=o.EPI_RESIDUAL, residual=x, out=out,
+                m=self.T)
+        o.block_stats(x, out, self.deltas[l], self.stats[l], self.scratch)
+
+    def enqueue_step_switched(self, body_stream):
+        """One step for graph capture: per block a device-selected SWITCH over the
+        NVFP4 / INT8 / BF16 / SKIP bodies, so only the chosen body's kernels run."""
+        o = ops
+        stream = torch.cuda.current_stream()
+        o.tensor_stats(self.x_in, self.tstats, self.scratch)
+        x = self.x_in
+        for l in range(self.L):
+            out = self.bufs[l % 2]
+            mode = self.modes[l:l + 1]
+            o.policy_step(self.cfg, self.state[l], self.stats[l], self._in_stats(l), mode)
+            sw = o.GraphSwitch(stream, body_stream, mode, o.MODE_NVFP4, 4)
+            for i, m in enumerate((o.MODE_NVFP4, o.MODE_INT8, o.MODE_BF16)):
+                with sw.branch(i):
+                    self._compute_body(x, out, l, m)
+            with sw.branch(3):
+                o.skip_apply(x, self.deltas[l], out, self.stats[l], self.scratch)
+            sw.close()
+            x = out
+        return x
+
+    def capture(self, switched: bool = True):
+        """Capture one step into a CUDA graph (call after at least one eager step).
+
+        switched=True uses device-selected SWITCH nodes (only the chosen body
+        runs); False captures the flat launch sequence whose kernels return at
+        once when the mode word is not theirs.
+        """
+        g = torch.cuda.CUDAGraph()
+        body_stream = torch.cuda.Stream()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            if switched:
+                self.enqueue_step_switched(body_stream)
+            else:
+                self.enqueue_step()
+        self.graph = g
+        self._body_stream = body_stream
+        return g
+
+    def step(self, x_s: torch.Tensor | None = None):
+        """One denoising step on input x_s (copied into the graph's input buffer)."""
+        if x_s is not None:
+            self.x_in.copy_(x_s, non_blocking=True)
+        if self.graph is not None:
+            self.graph.replay()
+        else:
+            self.enqueue_step()
+        return self.out
+
+    def decision_counts(self):
+        """Per block: (n_nvfp4, n_int8, n_bf16, n_skip, n_refresh, n_pdr, n_near) from the device state."""
+        out = []
+        for l in range(self.L):
+            s = ops.decode_state(self.state[l])
+            out.append((s.n_nvfp4, s.n_int8, s.n_bf16, s.n_skip, s.n_refresh, s.n_pdr, s.n_near))
+        return out
+
+
+def pack_block_weights(weights, had_block, device="cuda"):
+    """[(W_up fp32 [F, H], W_down fp32 [H, F])] (host or device) -> packed per block."""
+    out = []
+    for wu, wd in weights:
+        wu = torch.as_tensor(wu).to(device=device, dtype=torch.float32).contiguous()
+        wd = torch.as_tensor(wd).to(device=device, dtype=torch.float32).contiguous()
+        out.append((ops.pack_weights(wu, had_block), ops.pack_weights(wd, had_block)))
+    torch.cuda.synchronize()
+    return out

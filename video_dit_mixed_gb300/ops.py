@@ -153,6 +153,43 @@ def policy_step(cfg: PolicyCfg, state: torch.Tensor, last_stats: torch.Tensor, i
     return mode_word
 
 
+class GraphSwitch:
+    """A device-selected branch in the CUDA graph being captured on `stream` (sixbit_graph_switch_*).
+
+    Body i runs when the low byte of mode_word equals first_mode + i.  Use
+    ``with sw.branch(i):`` to capture body i: inside it the current torch
+    stream is `body_stream`, which is capturing into that body.
+    """
+
+    def __init__(self, stream, body_stream, mode_word: torch.Tensor, first_mode: int, nbranches: int):
+        self.h = C.c_void_p()
+        self.body_stream = body_stream
+        check(_lib.sixbit_graph_switch_begin(C.c_void_p(stream.cuda_stream), C.c_void_p(body_stream.cuda_stream),
+                                             _p(mode_word), first_mode, nbranches, C.byref(self.h)),
+              "graph_switch_begin")
+
+    def branch(self, i: int):
+        sw = self
+
+        class _Branch:
+            def __enter__(self):
+                s = C.c_void_p()
+                check(_lib.sixbit_graph_branch_begin(sw.h, i, C.byref(s)), "graph_branch_begin")
+                self.ctx = torch.cuda.stream(sw.body_stream)
+                self.ctx.__enter__()
+                return sw.body_stream
+
+            def __exit__(self, *exc):
+                self.ctx.__exit__(*exc)
+                check(_lib.sixbit_graph_branch_end(sw.h), "graph_branch_end")
+                return False
+
+        return _Branch()
+
+    def close(self):
+        check(_lib.sixbit_graph_switch_end(self.h), "graph_switch_end")
+
+
 def new_stats(device="cuda", count: int = 1) -> torch.Tensor:
     """Zeroed device storage for `count` sixbit_stats records (float64 x 8 each)."""
     return torch.zeros((count, 8), dtype=torch.float64, device=device)
