@@ -220,7 +220,9 @@ class DitStep:
         import synthgen
         from video_dit_mixed_gb300 import dit
         self.name, self.t, self.ops, self.dev = name, torch, ops, device
-        c = synthgen.DIT_CONFIGS[name]
+        c = dict(synthgen.DIT_CONFIGS[name])
+        if getattr(self, "blocks_override", None):
+            c["blocks"] = self.blocks_override
         self.c = c
         T, H, F, L, b = c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"]
         self.T, self.H, self.F, self.L, self.b = T, H, F, L, b
@@ -235,7 +237,8 @@ class DitStep:
             del wu, wd
         self.model = dit.DiT(T, H, F, L, b, packed, device=device)
         # input trajectory, resident in HBM before timing
-        x0 = synthgen.activations(c["seed"], T, H, "laplace", 0.005, 50.0)
+        x0 = synthgen.activations(c["seed"], T, H, "laplace", c.get("outlier_frac", 0.005),
+                                  c.get("outlier_scale", 50.0))
         sig = synthgen.sigmas(c["steps"])
         self.traj = torch.empty((c["steps"], T, H), dtype=torch.bfloat16, device=device)
         self.traj[0].copy_(torch.from_numpy(x0).to(torch.bfloat16))
@@ -449,7 +452,10 @@ def run_ours(args):
     __graft_entry__.build()
     from video_dit_mixed_gb300 import ops
 
-    wl = WORKLOADS[args.workload](args.workload, torch, ops, dev)
+    cls = WORKLOADS[args.workload]
+    if args.blocks:
+        cls = type(cls.__name__, (cls,), dict(blocks_override=args.blocks))
+    wl = cls(args.workload, torch, ops, dev)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -603,6 +609,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--blocks", type=int, default=0,
+                    help="DiT workloads: use only this many blocks (profiling runs on a smaller device footprint)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

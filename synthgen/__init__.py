@@ -133,8 +133,11 @@ DIT_CONFIGS = {
                      w_std=0.05, gate=(0.02, 0.5), outlier_frac=0.01, outlier_scale=4.0),
     "dit_2b": dict(seed=3, tokens=TOKENS, hidden=1920, ffn=7680, blocks=30, steps=50, had_block=64,
                    w_std=0.02, gate=None),
+    # a deviation that exercises the NVFP4 branch: per-block residual gates
+    # put Gamma around 0.1, and milder outlier channels (x2) keep the PDR
+    # ratio below 30
     "dit_2b_gated": dict(seed=3, tokens=TOKENS, hidden=1920, ffn=7680, blocks=30, steps=50, had_block=64,
-                         w_std=0.02, gate=(0.02, 0.5)),
+                         w_std=0.02, gate=(0.02, 0.5), outlier_frac=0.005, outlier_scale=2.0),
     "dit_5b": dict(seed=4, tokens=TOKENS, hidden=3072, ffn=12288, blocks=42, steps=50, had_block=64,
                    w_std=0.02, gate=None),
 }
