@@ -16,6 +16,8 @@ random weights, no checkpoints or datasets):
   dit_5b        42 blocks, hidden 3072, FFN 12288.
   qkv_2b        one step = both quantizers and all three GEMM kinds of a
                 17776 x 1920 -> 5760 linear layer.  Metric: TFLOP/s.
+  gemm_sweep_5b one step = quantization + W4A4 and W4A8 GEMM at K = N = 3072
+                for M = 1024 .. 35552.  Metric: TFLOP/s.
 
 Timing rules: W untimed warm-up steps, then K timed steps (the DiT restarts
 its 50-step trajectory at step 0, so the default K = 50 times one whole
@@ -306,7 +308,12 @@ class DitStep:
         return n
 
     def profile(self, k, stream):
-        """Eager pass over a full trajectory: event pairs around every call, attributed to the block's mode."""
+        """Eager pass over a full trajectory: event pairs around every call, attributed to the block's mode.
+
+        Eager launches of the kernels whose mode is not the block's return at
+        once (a few microseconds each); the CUDA-graph steps timed above do not
+        launch them at all.
+        """
         T = self.t
         m = self.model
         m.reset()
@@ -314,6 +321,10 @@ class DitStep:
         recs = []
         modes = T.zeros((self.c["steps"], self.L), dtype=T.int32, device=self.dev)
         for s in range(self.c["steps"]):
+            # a GPU-side pause lets the host enqueue the whole step before the GPU
+            # reaches it, so the event pairs bracket device work, not launch gaps
+            T.cuda.synchronize()
+            T.cuda._sleep(int(40e6))
             m.x_in.copy_(self.traj[s])
             evs = []
             e0 = T.cuda.Event(enable_timing=True)
@@ -398,7 +409,87 @@ class DitStep:
                     near_threshold=int(((words & 2048) != 0).sum()), block_steps=int(low.size))
 
 
-WORKLOADS = {"qkv_2b": QkvLinear, "dit_2b": DitStep, "dit_2b_gated": DitStep, "dit_5b": DitStep}
+class GemmSweep:
+    """The 5B-shaped quantized-GEMM sweep: K = N = 3072, M = 1024 .. 35552, W4A4 and W4A8.
+
+    One step = for every M, fused Hadamard + quantization of X then the GEMM,
+    in NVFP4 and in INT8.  Metric: aggregate GEMM TFLOP/s over the step.
+    """
+
+    unit = "TFLOP/s"
+
+    def __init__(self, name, torch, ops, device):
+        import synthgen
+        self.name, self.t, self.ops, self.dev = name, torch, ops, device
+        c = synthgen.GEMM_SWEEP
+        self.b, self.k, self.n, self.ms = c["had_block"], c["k"], c["n"], c["ms"]
+        x, w = synthgen.sweep_inputs(max(self.ms))
+        self.x_host = torch.from_numpy(x).to(torch.bfloat16).pin_memory()
+        self.x = self.x_host.to(device)
+        self.pw = ops.pack_weights(torch.from_numpy(w).to(device), self.b)
+        self.qa = {m: ops.QActTensors(m, self.k, device) for m in self.ms}
+        self.y = torch.empty((max(self.ms), self.n), dtype=torch.bfloat16, device=device)
+        self.y_host = torch.empty((max(self.ms), self.n), dtype=torch.bfloat16).pin_memory()
+        self.flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)
+        self.flops = {m: 2.0 * m * self.n * self.k for m in self.ms}
+        self.h2d_bytes = max(self.ms) * self.k * 2
+        self.d2h_bytes = max(self.ms) * self.n * 2
+        self.config = dict(workload=name, k=self.k, n=self.n, m=list(self.ms), had_block=self.b,
+                           l2="256 MB buffer written between steps")
+
+    def calls(self):
+        o = self.ops
+        out = []
+        for m in self.ms:
+            xm = self.x[:m]
+            for mode, code in (("nvfp4", o.MODE_NVFP4), ("int8", o.MODE_INT8)):
+                out.append((f"hq_{mode}:M{m}", lambda xm=xm, m=m, code=code:
+                            o.hadamard_quant(xm, self.b, code, out=self.qa[m])))
+                out.append((f"qgemm_{mode}:M{m}", lambda xm=xm, m=m, code=code:
+                            o.qgemm(self.qa[m], xm, self.pw, code, out=self.y[:m], m=m)))
+        return out
+
+    warmup = QkvLinear.warmup
+    timed = QkvLinear.timed
+    profile = QkvLinear.profile
+
+    def e2e(self, k, stream):
+        T = self.t
+        pairs = []
+        for _ in range(k):
+            self.flush.fill_(1.0)
+            a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+            a.record(stream)
+            self.x.copy_(self.x_host, non_blocking=True)
+            for _, f in self.calls():
+                f()
+            self.y_host.copy_(self.y, non_blocking=True)
+            b.record(stream)
+            pairs.append((a, b))
+        T.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in pairs]
+
+    def value(self, ms):
+        return 2 * sum(self.flops.values()) / (ms / 1e3) / 1e12
+
+    def work(self, label):
+        kind, _, mm = label.partition(":M")
+        m = int(mm)
+        if kind.startswith("qgemm"):
+            return ("tensor", self.flops[m], "nvfp4" in kind)
+        n = m * self.k
+        if kind == "hq_nvfp4":
+            return ("hbm", n * 2 + n // 2 + n // 16, False)
+        return ("hbm", n * 3 + m * 4, False)
+
+    def launches(self):
+        return None
+
+    def extra(self):
+        return {}
+
+
+WORKLOADS = {"qkv_2b": QkvLinear, "dit_2b": DitStep, "dit_2b_gated": DitStep, "dit_5b": DitStep, "gemm_sweep_5b": GemmSweep}
 
 
 # --------------------------------------------------------------------- timing --
@@ -436,6 +527,22 @@ def _roofline(wl, per, peaks):
     return roof, table
 
 
+def reduce_max(v: float, world: int, device) -> float:
+    """The largest of every rank's value (the slowest rank's time); a no-op on one rank."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(per_rank_value_at_max_time: float, world: int) -> float:
+    """Replicas do the same work each, so the job's throughput is N x one rank's at the slowest time."""
+    return per_rank_value_at_max_time * world
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -465,11 +572,7 @@ def run_ours(args):
             torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, world, dev)
 
     wl.warmup(args.warmup)
     barrier()
@@ -494,11 +597,11 @@ def run_ours(args):
     if rank == 0:
         peaks = _peaks()
         roof, table = _roofline(wl, per, peaks)
-        line = dict(metric=METRIC, value=round(wl.value(ms) * world, 4), unit=wl.unit, n_gpus=world,
+        line = dict(metric=METRIC, value=round(whole_job_value(wl.value(ms), world), 4), unit=wl.unit, n_gpus=world,
                     steps=args.steps, warmup=args.warmup, ms_per_step=round(ms, 4), higher_is_better=True,
                     scaling="weak", vs_baseline=None, dtype="nvfp4/int8/bf16 operands, fp32 accumulate",
                     data="synthetic", config=dict(wl.config, parallelism=f"replicas x{world}"),
-                    e2e=dict(value=round(wl.value(e2e_ms) * world, 4), unit=wl.unit,
+                    e2e=dict(value=round(whole_job_value(wl.value(e2e_ms), world), 4), unit=wl.unit,
                              h2d_bytes_per_step=wl.h2d_bytes, d2h_bytes_per_step=wl.d2h_bytes),
                     gpu_launches=launches, roofline=roof, kernels=table, clocks=clk, wall_s=round(wall, 3))
         line.update(wl.extra())

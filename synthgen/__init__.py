@@ -65,11 +65,12 @@ def laplace(seed: int, stream: int, n: int) -> np.ndarray:
 
 
 def bf16_rne(x) -> np.ndarray:
-    """Round to bf16 (RNE); returns float32 values (input preparation only)."""
+    """Round finite float32 values to bf16 (RNE); returns float32 values (input preparation only)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    r = ((u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)) << np.uint64(16)
-    return r.astype(np.uint32).view(np.float32).reshape(x.shape)
+    u = x.view(np.uint32)
+    # finite values stay below 0xFF800000, so the 32-bit sum cannot wrap
+    r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return r.view(np.float32).reshape(x.shape)
 
 
 def outlier_channels(seed: int, stream: int, k: int, frac: float) -> np.ndarray:
@@ -183,3 +184,26 @@ def dit_trajectory(name: str):
         x = bf16_rne((x + sg * z).astype(np.float32))
         xs.append(x)
     return xs
+
+
+# The 5B-shaped GEMM sweep: X [M, 3072] like the QKV input, W [3072, 3072].
+GEMM_SWEEP = dict(seed=5, ms=(1024, 2048, 4096, 8192, TOKENS, 2 * TOKENS), k=3072, n=3072, had_block=64)
+
+
+def sweep_inputs(m: int):
+    c = GEMM_SWEEP
+    x = activations(c["seed"], m, c["k"], "laplace", 0.005, 50.0)
+    w = weights(c["seed"], c["n"], c["k"])
+    return x, w
+
+
+def ffn_hidden(seed: int, m: int, f: int, tile: int = 8):
+    """A bf16 stand-in for GELU(W_up x) [m, f]: GELU of N(0, 0.9^2) samples (tanh form, input prep only).
+
+    f/tile columns are drawn and repeated `tile` times along the row (cheap to
+    generate at 17776 x 7680; the repetition does not matter to a GEMM test).
+    """
+    fc = f // tile
+    z = normal(seed, 7, m * fc).reshape(m, fc) * 0.9
+    g = 0.5 * z * (1.0 + np.tanh(0.7978845608028654 * (z + 0.044715 * z ** 3)))
+    return np.tile(bf16_rne(g.astype(np.float32)), (1, tile))

@@ -1,9 +1,13 @@
 """Parity: block statistics, delta cache, skip and the device policy step vs the oracle.
 
-Bar: bit-exact delta / skip outputs and maxima; float64 sums within
-1e-9 * sum of the absolute terms (the kernels accumulate each thread's
-exact FP32 terms as a TwoSum pair and combine in float64); policy decisions
-identical to the oracle's on the hand traces and on random statistics.
+Bar: bit-exact delta / skip outputs and maxima.  Sums, against the float64
+oracle: the three behind the delta cosine (sum Delta^2, Delta*Delta_prev,
+Delta_prev^2) within 1e-9 * sum|terms| (each thread keeps a TwoSum pair,
+float64 combine); the Kahan-compensated sums for Gamma and the outlier ratio
+(sum x_in^2, sum |x|, sum x^2) within 2.5e-7 * sum|terms| (Kahan's bound 2u
+per thread partial; the policy compares these statistics to thresholds with a
+1e-6 relative band, so 2.4e-7 cannot flip a decision outside it).  Policy
+decisions identical to the oracle's on the hand traces and random statistics.
 """
 import math
 import os
@@ -38,8 +42,11 @@ def _np_bits(a):
     return (np.ascontiguousarray(a, np.float32).view(np.uint32) >> 16).astype(np.uint16).view(np.int16)
 
 
-def _close(got, ref, absterms, what):
-    assert abs(got - ref) <= 1e-9 * absterms + 1e-300, (what, got, ref, absterms)
+def _close(got, ref, absterms, what, rel=1e-9):
+    assert abs(got - ref) <= rel * absterms + 1e-300, (what, got, ref, absterms)
+
+
+KAHAN = 2.5e-7
 
 
 SIZES = [8, 8 * 1000 + 8, 1920 * 257, 17776 * 1920]
@@ -53,8 +60,8 @@ def test_tensor_stats(ops, n):
     r = stats.tensor_stats(x)
     g = out.cpu().numpy()
     assert g[0] == r["max_abs"] and g[2] == n
-    _close(g[1], r["sum_abs"], r["sum_abs"], "sum_abs")
-    _close(g[3], r["sum_sq"], r["sum_sq"], "sum_sq")
+    _close(g[1], r["sum_abs"], r["sum_abs"], "sum_abs", KAHAN)
+    _close(g[3], r["sum_sq"], r["sum_sq"], "sum_sq", KAHAN)
 
 
 @pytest.mark.parametrize("n", SIZES)
@@ -75,11 +82,11 @@ def test_block_stats_and_delta_cache(ops, n):
     d = r["delta"].astype(np.float64)
     p = dp.astype(np.float64)
     _close(g[0], r["sum_d2"], r["sum_d2"], "sum_d2")
-    _close(g[1], r["sum_xin2"], r["sum_xin2"], "sum_xin2")
+    _close(g[1], r["sum_xin2"], r["sum_xin2"], "sum_xin2", KAHAN)
     _close(g[2], r["sum_ddp"], float(np.abs(d * p).sum()), "sum_ddp")
     _close(g[3], r["sum_dp2"], r["sum_dp2"], "sum_dp2")
     assert g[4] == r["out"]["max_abs"] and g[6] == n
-    _close(g[5], r["out"]["sum_abs"], r["out"]["sum_abs"], "sum_abs_out")
+    _close(g[5], r["out"]["sum_abs"], r["out"]["sum_abs"], "sum_abs_out", KAHAN)
 
 
 def test_skip_apply(ops):
@@ -97,7 +104,7 @@ def test_skip_apply(ops):
     assert list(g[:4]) == [1.0, 2.0, 3.0, 4.0]          # compute-side fields untouched
     t = stats.tensor_stats(ref)
     assert g[4] == t["max_abs"] and g[6] == n
-    _close(g[5], t["sum_abs"], t["sum_abs"], "sum_abs")
+    _close(g[5], t["sum_abs"], t["sum_abs"], "sum_abs", KAHAN)
 
 
 def test_mode_word_gates_stats_and_skip(ops):

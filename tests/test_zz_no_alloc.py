@@ -51,8 +51,11 @@ def test_noalloc_matches_regular_entry_point_twice_in_a_row():
         a = st.cpu().numpy()[0]
         b = st_ref.cpu().numpy()[0]
         assert a[4] == b[4] and a[6] == b[6] == n
-        for i in (0, 1, 3, 5):                      # sums of non-negative terms
-            assert abs(a[i] - b[i]) <= 1e-9 * abs(b[i]), (call, i, a[i], b[i])
+        # sums of non-negative terms: TwoSum-accumulated (0, 3) agree to 1e-9;
+        # Kahan-accumulated (1, 5) to twice Kahan's 2u bound, since the two
+        # entry points use different grids and so different summation orders
+        for i, rel in ((0, 1e-9), (1, 5e-7), (3, 1e-9), (5, 5e-7)):
+            assert abs(a[i] - b[i]) <= rel * abs(b[i]), (call, i, a[i], b[i])
         d = cache_ref.float().double()
         p = dp.float().double()
         assert abs(a[2] - b[2]) <= 1e-9 * float((d * p).abs().sum()), (call, a[2], b[2])

@@ -63,16 +63,36 @@ __device__ __forceinline__ void fwht8(float (&v)[8], int lane) {
 #pragma unroll
   for (int h = 8; h < B; h <<= 1) {
     const int m = h >> 3;
-    const bool upper = (lane & m) != 0;
+    // lower lane: v + o; upper lane: o - v.  fma(+-1, v, o) is that one sum
+    // with a single rounding, i.e. the same IEEE add or subtract.
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
-      v[i] = upper ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
+      v[i] = __fmaf_rn(sgn, v[i], o);
     }
   }
   constexpr float s = B == 16 ? 0.25f : (B == 64 ? 0.125f : 0.0625f);
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], s);
+}
+
+// Correctly rounded y / d from a correctly rounded reciprocal rd = RN(1/d):
+// q = RN(y*rd), then one FMA correction q + rd*(y - d*q) (Markstein's
+// theorem: with rd within half an ulp of 1/d and q within one ulp of y/d, the
+// corrected quotient is RN(y/d) barring overflow and underflow).  Callers use
+// it only when d and rd are normal numbers and fall back to the IEEE
+// division otherwise.
+__device__ __forceinline__ float div_by_recip(float y, float d, float rd) {
+  const float q = __fmul_rn(y, rd);
+  const float res = __fmaf_rn(-d, q, y);
+  return __fmaf_rn(res, rd, q);
+}
+
+// True when d is in the range where div_by_recip is exact (also excludes 0).
+__device__ __forceinline__ bool recip_ok(float d) {
+  const float a = fabsf(d);
+  return a >= 0x1p-100f && a <= 0x1p+100f;
 }
 
 __device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
@@ -175,8 +195,14 @@ __device__ __forceinline__ void nvfp4_chunk(float (&v)[8], int r, int col, bool 
   const uint32_t e = f32_to_e4m3(sb);
   const float S = __fmul_rn(e4m3_to_f32(e), s_t);
   float q[8];
+  if (recip_ok(S)) {
+    const float rS = __frcp_rn(S);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = (S != 0.f) ? __fdiv_rn(v[i], S) : 0.f;
+    for (int i = 0; i < 8; ++i) q[i] = div_by_recip(v[i], S, rS);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = (S != 0.f) ? __fdiv_rn(v[i], S) : 0.f;
+  }
   const uint32_t packed = f32x8_to_e2m1(q);
   if (active) {
     *reinterpret_cast<uint32_t*>(codes + static_cast<size_t>(r) * (K >> 1) + (col >> 1)) = packed;
@@ -259,6 +285,8 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_int8_kernel(const uint16_t* 
     }
     m = warp_max(m);
     const float s = __fdiv_rn(m, 127.0f);
+    const bool fast = recip_ok(s);
+    const float rs = fast ? __frcp_rn(s) : 0.f;
     if (lane == 0) row_scale[r] = s;
     // pass 2: the row again (from cache), rotate, quantize
     for (int c0 = 0; c0 < nch; c0 += 4) {
@@ -277,7 +305,7 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_int8_kernel(const uint16_t* 
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float q = 0.f;
-            if (s != 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(v[i], s)), -127.f), 127.f);
+            if (s != 0.f) q = fminf(fmaxf(rintf(fast ? div_by_recip(v[i], s, rs) : __fdiv_rn(v[i], s)), -127.f), 127.f);
             const int qi = static_cast<int>(q);
             qb[i >> 2] |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * (i & 3));
             ob[i >> 1] |= (__float_as_uint(q) >> 16) << (16 * (i & 1));  // integers |q|<=127 are exact in bf16

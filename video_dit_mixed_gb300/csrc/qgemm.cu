@@ -17,7 +17,7 @@
 // Kinds:
 //   NVFP4  kind::mxf4nvf4.block_scale.scale_vec::4X, E2M1 x E2M1 with one
 //          E4M3 scale per 16 elements, 256 K-elements (128 bytes) per stage;
-//          a 128 x 256 tile is two N = 128 MMAs per K step sharing A.  One
+//          a 128 x 256 tile is one N = 256 MMA per K step.  One
 //          accumulator buffer (256 columns) plus the scale factors fill
 //          tensor memory; the epilogue drains the accumulator to registers
 //          and releases it before its stores, so they overlap the next tile.
@@ -274,14 +274,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                   tmem_cp_32x128b_warpx4(tmem + kSfbCol + 8 * k + 4 * j, sdesc_sf(smem_u32(SFB(s)) + 2048 * j + 512 * k));
               }
             }
+            // one N = 256 MMA (B scale chunks for rows 0-127 and 128-255 in
+            // consecutive 4-column groups), or N = 128 when only half the tile exists
+            const uint32_t idesc = nj == 2 ? idesc_nvf4(kBM, 256) : C::kIdesc;
 #pragma unroll
             for (int k = 0; k < C::kMmaPerStage; ++k) {
-              if (k < nmma) {
-                for (int j = 0; j < nj; ++j)
-                  mma_nvf4(d_tmem + 128 * j, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 16384 * j + 32 * k),
-                           C::kIdesc, tmem + kSfaCol + 4 * k, tmem + kSfbCol + 8 * k + 4 * j,
-                           (acc_start && k == 0) ? 0u : 1u);
-              }
+              if (k < nmma)
+                mma_nvf4(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), idesc,
+                         tmem + kSfaCol + 4 * k, tmem + kSfbCol + 8 * k, (acc_start && k == 0) ? 0u : 1u);
             }
           } else {
 #pragma unroll
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int c = 0; c < kEpiCols / 16; ++c) {
             uint32_t r[16];
             tmem_ld16(lane_addr + buf * kBN + c * 16, r);
-            tmem_ld_wait();
+            tmem_ld_wait(r);
 #pragma unroll
             for (int j4 = 0; j4 < 4; ++j4) {
               const float4 s4 = sw4[c * 4 + j4];
@@ -410,7 +410,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint32_t r[kEpiCols / 32][32];
 #pragma unroll
           for (int c = 0; c < kEpiCols / 32; ++c) tmem_ld32(lane_addr + c * 32, r[c]);
-          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < kEpiCols / 32; ++c) tmem_ld_wait(r[c]);
           tc_fence_before();
           mbar_arrive(&acce[buf]);
 #pragma unroll
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int c = 0; c < kEpiCols / 32; ++c) {
             uint32_t r[32];
             tmem_ld32(lane_addr + buf * kBN + c * 32, r);
-            tmem_ld_wait();
+            tmem_ld_wait(r);
             if (c == kEpiCols / 32 - 1) {  // buffer fully read: hand it back to the MMA warp
               tc_fence_before();
               mbar_arrive(&acce[buf]);

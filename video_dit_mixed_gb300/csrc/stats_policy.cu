@@ -9,11 +9,13 @@
 // INT8 for every layer after a skip).
 //
 // The reductions are one pass over HBM with 16-byte loads.  Sums of squares
-// and products of bf16 values are exact in FP32 per term; each thread keeps
-// them as an unevaluated pair (s, c) updated with Knuth's TwoSum, so a
-// thread's partial carries about 48 bits; partials are combined in float64 in
-// a fixed order (warp shuffle tree, then CTA, then a last-CTA pass over the
-// per-CTA partials in scratch), so results are run-to-run deterministic.
+// and products of bf16 values are exact in FP32 per term.  The three sums
+// behind the delta cosine (whose threshold sits near 1) are kept per thread
+// as an unevaluated pair (s, c) updated with Knuth's TwoSum (about 48 bits);
+// the sums for Gamma and the outlier ratio use Kahan compensation.  Partials
+// are combined in float64 in a fixed order (warp shuffle tree, then CTA, then
+// a last-CTA pass over the per-CTA partials in scratch), so results are
+// run-to-run deterministic.
 #include <cstdint>
 
 #include "common.cuh"
@@ -38,6 +40,62 @@ __device__ __forceinline__ void two_add(TwoF& a, float x) {
 }
 
 __device__ __forceinline__ double to_d(const TwoF& a) { return static_cast<double>(a.s) + static_cast<double>(a.c); }
+
+// Kahan-compensated FP32 sum: error about 2u|S| for a thread's partial,
+// enough for the outlier ratio and Gamma (relative bands of 1e-6); the sums
+// behind the delta cosine keep the TwoSum pair.
+struct Kahan {
+  float s, c;
+};
+
+__device__ __forceinline__ void kahan_add(Kahan& k, float x) {
+  const float y = __fsub_rn(x, k.c);
+  const float t = __fadd_rn(k.s, y);
+  k.c = __fsub_rn(__fsub_rn(t, k.s), y);
+  k.s = t;
+}
+
+__device__ __forceinline__ double to_d(const Kahan& k) { return static_cast<double>(k.s) - static_cast<double>(k.c); }
+
+// The same two accumulators on packed FP32 pairs (two independent lanes per
+// instruction, lane-wise identical rounding); a thread accumulates even and
+// odd elements in the two lanes and adds the lanes in float64 at the end.
+struct TwoF2 {
+  uint64_t s, c;
+};
+
+__device__ __forceinline__ void two_add2(TwoF2& a, uint64_t x) {
+  const uint64_t s = f2_add(a.s, x);
+  const uint64_t bp = f2_sub(s, a.s);
+  const uint64_t err = f2_add(f2_sub(a.s, f2_sub(s, bp)), f2_sub(x, bp));
+  a.s = s;
+  a.c = f2_add(a.c, err);
+}
+
+__device__ __forceinline__ double to_d(const TwoF2& a) {
+  return (static_cast<double>(f2_lo(a.s)) + static_cast<double>(f2_lo(a.c))) +
+         (static_cast<double>(f2_hi(a.s)) + static_cast<double>(f2_hi(a.c)));
+}
+
+struct Kahan2 {
+  uint64_t s, c;
+};
+
+__device__ __forceinline__ void kahan_add2(Kahan2& k, uint64_t x) {
+  const uint64_t y = f2_sub(x, k.c);
+  const uint64_t t = f2_add(k.s, y);
+  k.c = f2_sub(f2_sub(t, k.s), y);
+  k.s = t;
+}
+
+__device__ __forceinline__ double to_d(const Kahan2& k) {
+  return (static_cast<double>(f2_lo(k.s)) - static_cast<double>(f2_lo(k.c))) +
+         (static_cast<double>(f2_hi(k.s)) - static_cast<double>(f2_hi(k.c)));
+}
+
+__device__ __forceinline__ float f2_max_abs(uint64_t v, float m) {
+  return fmaxf(m, fmaxf(fabsf(f2_lo(v)), fabsf(f2_hi(v))));
+}
 
 __device__ __forceinline__ uint4 ld16(const void* p) {
   uint4 v;
@@ -139,23 +197,40 @@ __device__ __forceinline__ bool mode_is(const int32_t* mode_dev, int want) {
   return mode_dev != nullptr && SIXBIT_MODE_OF(*mode_dev) == want;
 }
 
+// Each thread walks vectors of 8 elements (four packed pairs) with a grid
+// stride, two vectors per iteration (both loads issued before either is used).
+
+__device__ __forceinline__ void unpack4x2(const uint4& r, uint64_t (&v)[4]) {
+  v[0] = f2_from_bf16x2(r.x);
+  v[1] = f2_from_bf16x2(r.y);
+  v[2] = f2_from_bf16x2(r.z);
+  v[3] = f2_from_bf16x2(r.w);
+}
+
+__device__ __forceinline__ void tensor_stats_vec(const uint4& r, float& mx, Kahan2& sa, Kahan2& sq) {
+  uint64_t v[4];
+  unpack4x2(r, v);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    mx = f2_max_abs(v[j], mx);
+    kahan_add2(sa, f2_abs(v[j]));
+    kahan_add2(sq, f2_mul(v[j], v[j]));
+  }
+}
+
 // out[0..3] = {max |x|, sum |x|, count, sum x^2}
 __global__ void __launch_bounds__(kStThreads) tensor_stats_kernel(const uint16_t* __restrict__ x, int64_t n,
                                                                   double* out, void* scratch) {
   const int64_t n8 = n >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
   float mx = 0.f;
-  TwoF sa{0.f, 0.f}, sq{0.f, 0.f};
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * kStThreads) {
-    float v[8];
-    unpack8(ld16(x + 8 * i), v);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float a = fabsf(v[j]);
-      mx = fmaxf(mx, a);
-      two_add(sa, a);
-      two_add(sq, __fmul_rn(v[j], v[j]));
-    }
+  Kahan2 sa{0, 0}, sq{0, 0};
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8; i += 2 * stride) {
+    const bool two = i + stride < n8;
+    const uint4 r0 = ld16(x + 8 * i);
+    const uint4 r1 = two ? ld16(x + 8 * (i + stride)) : make_uint4(0, 0, 0, 0);
+    tensor_stats_vec(r0, mx, sa, sq);
+    tensor_stats_vec(r1, mx, sa, sq);   // zeros add nothing
   }
   double v[3] = {static_cast<double>(mx), to_d(sa), to_d(sq)};
   const bool is_max[3] = {true, false, false};
@@ -168,38 +243,51 @@ __global__ void __launch_bounds__(kStThreads) tensor_stats_kernel(const uint16_t
   }
 }
 
+__device__ __forceinline__ uint4 block_stats_vec(const uint4& ra, const uint4& rb, const uint4& rp, TwoF2& d2,
+                                                 Kahan2& xi2, TwoF2& ddp, TwoF2& dp2, float& mx, Kahan2& sa) {
+  uint64_t a[4], b[4], p[4];
+  unpack4x2(ra, a);
+  unpack4x2(rb, b);
+  unpack4x2(rp, p);
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    w[j] = f2_to_bf16x2(f2_sub(b[j], a[j]));      // Delta = bf16(x_out - x_in)
+    const uint64_t d = f2_from_bf16x2(w[j]);
+    two_add2(d2, f2_mul(d, d));
+    two_add2(ddp, f2_mul(d, p[j]));
+    two_add2(dp2, f2_mul(p[j], p[j]));
+    kahan_add2(xi2, f2_mul(a[j], a[j]));
+    mx = f2_max_abs(b[j], mx);
+    kahan_add2(sa, f2_abs(b[j]));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __global__ void __launch_bounds__(kStThreads) block_stats_kernel(const uint16_t* __restrict__ x_in,
                                                                  const uint16_t* __restrict__ x_out,
                                                                  uint16_t* delta, int64_t n, const int32_t* mode_dev,
                                                                  sixbit_stats* stats, void* scratch) {
   if (mode_is(mode_dev, SIXBIT_MODE_SKIP)) return;
   const int64_t n8 = n >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
   float mx = 0.f;
-  TwoF d2{0.f, 0.f}, xi2{0.f, 0.f}, ddp{0.f, 0.f}, dp2{0.f, 0.f}, sa{0.f, 0.f};
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * kStThreads) {
-    float a[8], b[8], p[8], d[8];
-    unpack8(ld16(x_in + 8 * i), a);
-    unpack8(ld16(x_out + 8 * i), b);
-    unpack8(*reinterpret_cast<const uint4*>(delta + 8 * i), p);
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      w[j] = pack2(__fsub_rn(b[2 * j], a[2 * j]), __fsub_rn(b[2 * j + 1], a[2 * j + 1]));
-      d[2 * j] = __uint_as_float(w[j] << 16);
-      d[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  TwoF2 d2{0, 0}, ddp{0, 0}, dp2{0, 0};
+  Kahan2 xi2{0, 0}, sa{0, 0};
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8; i += 2 * stride) {
+    const int64_t i1 = i + stride;
+    const bool two = i1 < n8;
+    const uint4 a0 = ld16(x_in + 8 * i), b0 = ld16(x_out + 8 * i);
+    const uint4 p0 = *reinterpret_cast<const uint4*>(delta + 8 * i);
+    uint4 a1 = make_uint4(0, 0, 0, 0), b1 = a1, p1 = a1;
+    if (two) {
+      a1 = ld16(x_in + 8 * i1);
+      b1 = ld16(x_out + 8 * i1);
+      p1 = *reinterpret_cast<const uint4*>(delta + 8 * i1);
     }
-    *reinterpret_cast<uint4*>(delta + 8 * i) = make_uint4(w[0], w[1], w[2], w[3]);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      two_add(d2, __fmul_rn(d[j], d[j]));
-      two_add(xi2, __fmul_rn(a[j], a[j]));
-      two_add(ddp, __fmul_rn(d[j], p[j]));
-      two_add(dp2, __fmul_rn(p[j], p[j]));
-      const float ab = fabsf(b[j]);
-      mx = fmaxf(mx, ab);
-      two_add(sa, ab);
-    }
+    *reinterpret_cast<uint4*>(delta + 8 * i) = block_stats_vec(a0, b0, p0, d2, xi2, ddp, dp2, mx, sa);
+    const uint4 w1 = block_stats_vec(a1, b1, p1, d2, xi2, ddp, dp2, mx, sa);  // zeros add nothing
+    if (two) *reinterpret_cast<uint4*>(delta + 8 * i1) = w1;
   }
   double v[6] = {to_d(d2), to_d(xi2), to_d(ddp), to_d(dp2), static_cast<double>(mx), to_d(sa)};
   const bool is_max[6] = {false, false, false, false, true, false};
@@ -215,29 +303,42 @@ __global__ void __launch_bounds__(kStThreads) block_stats_kernel(const uint16_t*
   }
 }
 
+__device__ __forceinline__ uint4 skip_vec(const uint4& ra, const uint4& rd, float& mx, Kahan2& sa) {
+  uint64_t a[4], d[4];
+  unpack4x2(ra, a);
+  unpack4x2(rd, d);
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    w[j] = f2_to_bf16x2(f2_add(a[j], d[j]));      // x_out = bf16(x_in + Delta)
+    const uint64_t o = f2_from_bf16x2(w[j]);
+    mx = f2_max_abs(o, mx);
+    kahan_add2(sa, f2_abs(o));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __global__ void __launch_bounds__(kStThreads) skip_apply_kernel(const uint16_t* __restrict__ x_in,
                                                                 const uint16_t* __restrict__ delta,
                                                                 uint16_t* x_out, int64_t n, const int32_t* mode_dev,
                                                                 sixbit_stats* stats, void* scratch) {
   if (mode_is_not(mode_dev, SIXBIT_MODE_SKIP)) return;
   const int64_t n8 = n >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
   float mx = 0.f;
-  TwoF sa{0.f, 0.f};
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8;
-       i += static_cast<int64_t>(gridDim.x) * kStThreads) {
-    float a[8], d[8];
-    unpack8(ld16(x_in + 8 * i), a);
-    unpack8(ld16(delta + 8 * i), d);
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      w[j] = pack2(__fadd_rn(a[2 * j], d[2 * j]), __fadd_rn(a[2 * j + 1], d[2 * j + 1]));
-      const float o0 = fabsf(__uint_as_float(w[j] << 16)), o1 = fabsf(__uint_as_float(w[j] & 0xFFFF0000u));
-      mx = fmaxf(mx, fmaxf(o0, o1));
-      two_add(sa, o0);
-      two_add(sa, o1);
+  Kahan2 sa{0, 0};
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8; i += 2 * stride) {
+    const int64_t i1 = i + stride;
+    const bool two = i1 < n8;
+    const uint4 a0 = ld16(x_in + 8 * i), d0 = ld16(delta + 8 * i);
+    uint4 a1 = make_uint4(0, 0, 0, 0), d1 = a1;
+    if (two) {
+      a1 = ld16(x_in + 8 * i1);
+      d1 = ld16(delta + 8 * i1);
     }
-    *reinterpret_cast<uint4*>(x_out + 8 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(x_out + 8 * i) = skip_vec(a0, d0, mx, sa);
+    const uint4 w1 = skip_vec(a1, d1, mx, sa);  // zeros add nothing
+    if (two) *reinterpret_cast<uint4*>(x_out + 8 * i1) = w1;
   }
   double v[2] = {static_cast<double>(mx), to_d(sa)};
   const bool is_max[2] = {true, false};
@@ -333,18 +434,23 @@ __global__ void policy_kernel(sixbit_policy_cfg cfg, sixbit_policy_state* st, co
 
 // ------------------------------------------------------------ host launch --
 
-static int stats_grid(int64_t n) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
+// One wave: as many CTAs as fit on the GPU at once (occupancy of `kernel`),
+// fewer for small n (at least 4 vectors per thread), never more than the
+// scratch holds.
+template <typename Kernel>
+static int stats_grid(Kernel kernel, int64_t n) {
+  static int resident = 0;  // per kernel instantiation of this template
+  if (resident == 0) {
+    int dev = 0, sms = 0, per_sm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 152;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kStThreads, 0);
+    resident = (sms > 0 ? sms : 152) * (per_sm > 0 ? per_sm : 4);
+    if (resident > kStMaxBlocks) resident = kStMaxBlocks;
   }
-  const int64_t per = static_cast<int64_t>(kStThreads) * 8 * 4;  // >= 4 iterations per thread
+  const int64_t per = static_cast<int64_t>(kStThreads) * 8 * 4;
   int64_t want = (n + per - 1) / per;
-  const int64_t cap = static_cast<int64_t>(sms) * 8 < kStMaxBlocks ? static_cast<int64_t>(sms) * 8 : kStMaxBlocks;
-  if (want > cap) want = cap;
+  if (want > resident) want = resident;
   if (want < 1) want = 1;
   return static_cast<int>(want);
 }
@@ -352,14 +458,14 @@ static int stats_grid(int64_t n) {
 size_t stats_scratch_bytes(int64_t) { return 16 + static_cast<size_t>(kStMaxBlocks) * kNumSums * sizeof(double); }
 
 cudaError_t launch_tensor_stats(const uint16_t* x, int64_t n, double* out, void* scratch, cudaStream_t st) {
-  tensor_stats_kernel<<<stats_grid(n), kStThreads, 0, st>>>(x, n, out, scratch);
+  tensor_stats_kernel<<<stats_grid(tensor_stats_kernel, n), kStThreads, 0, st>>>(x, n, out, scratch);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_block_stats(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta, int64_t n,
                                const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st) {
-  block_stats_kernel<<<stats_grid(n), kStThreads, 0, st>>>(x_in, x_out, delta, n, mode_dev, stats, scratch);
+  block_stats_kernel<<<stats_grid(block_stats_kernel, n), kStThreads, 0, st>>>(x_in, x_out, delta, n, mode_dev, stats, scratch);
   note_launch();
   return cudaGetLastError();
 }
@@ -379,7 +485,7 @@ cudaError_t launch_block_stats_fixed_grid(const uint16_t* x_in, const uint16_t* 
 
 cudaError_t launch_skip_apply(const uint16_t* x_in, const uint16_t* delta, uint16_t* x_out, int64_t n,
                               const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st) {
-  skip_apply_kernel<<<stats_grid(n), kStThreads, 0, st>>>(x_in, delta, x_out, n, mode_dev, stats, scratch);
+  skip_apply_kernel<<<stats_grid(skip_apply_kernel, n), kStThreads, 0, st>>>(x_in, delta, x_out, n, mode_dev, stats, scratch);
   note_launch();
   return cudaGetLastError();
 }
