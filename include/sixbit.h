@@ -73,10 +73,13 @@ enum { SIXBIT_EPI_NONE = 0, SIXBIT_EPI_GELU = 1, SIXBIT_EPI_RESIDUAL = 2 };
  *                unless an amax is supplied)
  *   tensor_scale [1] float: s_t = amax / 2688 (1 when amax == 0)
  * INT8 (technical summary section 2.A):
- *   i8_codes     [M, K] int8, symmetric, per token, in [-127, 127]
+ *   i8_codes     [M, K] int8, symmetric, per token, in [-127, 127]; optional
+ *                when i8_operand is given (the GEMM does not read it)
  *   row_scale    [M] float: s_m = row amax / 127
  *   i8_operand   [M, K] bf16 bit patterns of the same integers (the form the
- *                W4A8 GEMM reads); required by sixbit_qgemm in INT8 mode
+ *                W4A8 GEMM reads); required by sixbit_qgemm in INT8 mode.
+ *                sixbit_hadamard_quant writes whichever of i8_codes and
+ *                i8_operand is non-NULL (at least one must be).
  * Debug:
  *   rotated      [M, K] float, the rotated FP32 activations (optional)
  */

@@ -71,6 +71,37 @@ def test_int8_quant_bit_exact(ops, m, k, b):
     _check_int8(ops, synthgen.activations(200 + m, m, k, "normal", 0.01, 20.0), b)
 
 
+# Row lengths that exercise every team size of the one-pass INT8 kernel
+# (1, 2, 4, 8 and 16 warps per row, ragged last chunk) and, past 16384
+# elements, the two-pass kernel.
+INT8_WIDE = [(40, 1152, 64), (9, 2048, 256), (5, 3968, 16), (3, 8064, 64), (2, 16384, 256), (3, 12288, 64),
+             (2, 16640, 64)]
+
+
+@pytest.mark.parametrize("m,k,b", INT8_WIDE)
+def test_int8_quant_row_teams_bit_exact(ops, m, k, b):
+    _check_int8(ops, synthgen.activations(300 + k, m, k, "laplace", 0.01, 30.0), b)
+
+
+def test_int8_operand_without_codes(ops):
+    """i8_codes may be NULL when the bf16 operand is requested: same operand and scales."""
+    x = synthgen.activations(41, 96, 7680, "normal", 0.01, 20.0)
+    q = ops.QActTensors(96, 7680, nvfp4=False, i8_codes=False)
+    assert q.i8_codes is None
+    ops.hadamard_quant(_dev_bf16(x), 64, ops.MODE_INT8, out=q)
+    torch.cuda.synchronize()
+    ref = quant.hadamard_quant(x, 64, "int8")
+    np.testing.assert_array_equal(q.i8_operand.float().cpu().numpy(), ref["q"].astype(np.float32))
+    np.testing.assert_array_equal(_u32(q.row_scale.cpu().numpy()), _u32(ref["s"]))
+
+
+def test_int8_needs_codes_or_operand(ops):
+    q = ops.QActTensors(16, 256, nvfp4=False, i8_codes=False, i8_operand=False)
+    x = torch.zeros((16, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ops.abi.SixbitError):
+        ops.hadamard_quant(x, 64, ops.MODE_INT8, out=q)
+
+
 def test_tiny_linear_config(ops):
     c = synthgen.CONFIGS["tiny_linear"]
     x = synthgen.activations(c["seed"], c["m"], c["k"], c["dist"], c["outlier_frac"], c["outlier_scale"])

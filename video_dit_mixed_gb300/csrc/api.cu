@@ -143,9 +143,10 @@ sixbit_status sixbit_hadamard_quant(const uint16_t* X, int M, int K, int had_blo
   if (want_fp4 && (out->fp4_codes == nullptr || out->fp4_scales == nullptr || out->tensor_scale == nullptr ||
                    (tamax_in == nullptr && out->tensor_amax == nullptr)))
     return SIXBIT_EINVAL;
-  if (want_i8 && (out->i8_codes == nullptr || out->row_scale == nullptr)) return SIXBIT_EINVAL;
+  if (want_i8 && (out->row_scale == nullptr || (out->i8_codes == nullptr && out->i8_operand == nullptr)))
+    return SIXBIT_EINVAL;
   if (want_fp4 && !aligned16(out->fp4_codes)) return SIXBIT_EALIGN;
-  if (want_i8 && (!aligned16(out->i8_codes) || (out->i8_operand && !aligned16(out->i8_operand))))
+  if (want_i8 && ((out->i8_codes && !aligned16(out->i8_codes)) || (out->i8_operand && !aligned16(out->i8_operand))))
     return SIXBIT_EALIGN;
   sixbit_status s = check_device();
   if (s != SIXBIT_OK) return s;

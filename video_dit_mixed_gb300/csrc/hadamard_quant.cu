@@ -256,6 +256,32 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_nvfp4_kernel(const uint16_t*
 
 // ------------------------------------------------------ INT8 quantization --
 
+// Quantizes and stores one lane's 8 rotated values of row r at column col:
+// q = clamp(RN(y / s), -127, 127); codes (optional), the bf16 operand
+// (optional) and the rotated values (optional).
+__device__ __forceinline__ void int8_chunk_store(const float (&v)[8], int r, int col, int K, float s, bool fast,
+                                                 float rs, int8_t* codes, uint16_t* operand, float* rotated) {
+  uint32_t qb[2] = {0, 0};
+  uint32_t ob[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float q = 0.f;
+    if (s != 0.f) q = fminf(fmaxf(rintf(fast ? div_by_recip(v[i], s, rs) : __fdiv_rn(v[i], s)), -127.f), 127.f);
+    const int qi = static_cast<int>(q);
+    qb[i >> 2] |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * (i & 3));
+    ob[i >> 1] |= (__float_as_uint(q) >> 16) << (16 * (i & 1));  // integers |q|<=127 are exact in bf16
+  }
+  const size_t off = static_cast<size_t>(r) * K + col;
+  if (codes != nullptr) *reinterpret_cast<uint2*>(codes + off) = make_uint2(qb[0], qb[1]);
+  if (operand != nullptr) *reinterpret_cast<uint4*>(operand + off) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  if (rotated != nullptr) {
+    float4* dst = reinterpret_cast<float4*>(rotated + off);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+// Two passes per row (row amax, then the row again from cache); serves any K.
 template <int B>
 __global__ void __launch_bounds__(kHqWarps * 32) hq_int8_kernel(const uint16_t* __restrict__ X, int M, int K,
                                                                 const int32_t* mode_dev, int8_t* codes,
@@ -299,29 +325,66 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_int8_kernel(const uint16_t* 
         bf16x8_to_f32(raw[u], v);
         fwht8<B>(v, lane);
         const int col = (c0 + u) * 256 + lane * 8;
-        if (col < K) {
-          uint32_t qb[2] = {0, 0};
-          uint32_t ob[4] = {0, 0, 0, 0};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float q = 0.f;
-            if (s != 0.f) q = fminf(fmaxf(rintf(fast ? div_by_recip(v[i], s, rs) : __fdiv_rn(v[i], s)), -127.f), 127.f);
-            const int qi = static_cast<int>(q);
-            qb[i >> 2] |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * (i & 3));
-            ob[i >> 1] |= (__float_as_uint(q) >> 16) << (16 * (i & 1));  // integers |q|<=127 are exact in bf16
-          }
-          *reinterpret_cast<uint2*>(codes + static_cast<size_t>(r) * K + col) = make_uint2(qb[0], qb[1]);
-          if (operand != nullptr)
-            *reinterpret_cast<uint4*>(operand + static_cast<size_t>(r) * K + col) =
-                make_uint4(ob[0], ob[1], ob[2], ob[3]);
-          if (rotated != nullptr) {
-            float4* dst = reinterpret_cast<float4*>(rotated + static_cast<size_t>(r) * K + col);
-            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-          }
-        }
+        if (col < K) int8_chunk_store(v, r, col, K, s, fast, rs, codes, operand, rotated);
       }
     }
+  }
+}
+
+// One pass: a CTA of 16 warps takes 16 / R rows, R = 2^lr warps per row, and
+// each warp holds up to four 256-element chunks of its row (chunks t, t + R,
+// t + 2R, t + 3R for warp t of the row's team) in registers, so X is read
+// once.  The row amax is combined across the team through shared memory.
+// Serves rows of up to 16 * 4 * 256 elements, with the results of
+// hq_int8_kernel (same butterfly, same per-element division).
+constexpr int kHqRowWarps = 16;
+constexpr int kHqRowChunks = 4;
+
+template <int B>
+__global__ void __launch_bounds__(kHqRowWarps * 32) hq_int8_rows_kernel(const uint16_t* __restrict__ X, int M,
+                                                                        int K, int lr, const int32_t* mode_dev,
+                                                                        int8_t* codes, float* row_scale,
+                                                                        uint16_t* operand, float* rotated) {
+  if (mode_skips(mode_dev, SIXBIT_MODE_INT8)) return;
+  __shared__ float red[kHqRowWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int R = 1 << lr;
+  const int team = warp >> lr, t = warp & (R - 1);
+  const int r = blockIdx.x * (kHqRowWarps >> lr) + team;
+  const bool row_ok = r < M;
+  const int nch = (K + 255) >> 8;
+  const uint16_t* row = X + static_cast<size_t>(row_ok ? r : 0) * K;
+  uint4 raw[kHqRowChunks];
+#pragma unroll
+  for (int u = 0; u < kHqRowChunks; ++u) {
+    const int c = t + u * R;
+    const int col = c * 256 + lane * 8;
+    raw[u] = make_uint4(0, 0, 0, 0);
+    if (row_ok && c < nch && col < K) raw[u] = ld_nc_16(row + col);
+  }
+  float v[kHqRowChunks][8];
+  float m = 0.f;
+#pragma unroll
+  for (int u = 0; u < kHqRowChunks; ++u) {
+    bf16x8_to_f32(raw[u], v[u]);
+    if (t + u * R < nch) fwht8<B>(v[u], lane);  // warp-uniform condition
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[u][i]));
+  }
+  m = warp_max(m);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  m = red[team << lr];
+  for (int i = 1; i < R; ++i) m = fmaxf(m, red[(team << lr) + i]);
+  if (!row_ok) return;
+  const float s = __fdiv_rn(m, 127.0f);
+  const bool fast = recip_ok(s);
+  const float rs = fast ? __frcp_rn(s) : 0.f;
+  if (t == 0 && lane == 0) row_scale[r] = s;
+#pragma unroll
+  for (int u = 0; u < kHqRowChunks; ++u) {
+    const int col = (t + u * R) * 256 + lane * 8;
+    if (t + u * R < nch && col < K) int8_chunk_store(v[u], r, col, K, s, fast, rs, codes, operand, rotated);
   }
 }
 
@@ -448,6 +511,24 @@ cudaError_t launch_hq_nvfp4(const uint16_t* X, int M, int K, int b, const int32_
 
 cudaError_t launch_hq_int8(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, const sixbit_qact* o,
                            cudaStream_t st) {
+  const int nch = (K + 255) / 256;
+  int lr = 0;
+  while ((kHqRowChunks << lr) < nch && lr < 5) ++lr;
+  if ((kHqRowChunks << lr) >= nch && (1 << lr) <= kHqRowWarps) {
+    const int rows_per_cta = kHqRowWarps >> lr;
+    const int grid = (M + rows_per_cta - 1) / rows_per_cta;
+    if (b == 16)
+      hq_int8_rows_kernel<16><<<grid, kHqRowWarps * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes, o->row_scale,
+                                                                 o->i8_operand, o->rotated);
+    else if (b == 64)
+      hq_int8_rows_kernel<64><<<grid, kHqRowWarps * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes, o->row_scale,
+                                                                 o->i8_operand, o->rotated);
+    else
+      hq_int8_rows_kernel<256><<<grid, kHqRowWarps * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes, o->row_scale,
+                                                                  o->i8_operand, o->rotated);
+    note_launch();
+    return cudaGetLastError();
+  }
   const int grid = hq_grid(M);
   SIXBIT_DISPATCH_B(b, hq_int8_kernel, X, M, K, mode_dev, o->i8_codes, o->row_scale, o->i8_operand, o->rotated);
   return cudaGetLastError();

@@ -13,9 +13,9 @@
 // behind the delta cosine (whose threshold sits near 1) are kept per thread
 // as an unevaluated pair (s, c) updated with Knuth's TwoSum (about 48 bits);
 // the sums for Gamma and the outlier ratio use Kahan compensation.  Partials
-// are combined in float64 in a fixed order (warp shuffle tree, then CTA, then
-// a last-CTA pass over the per-CTA partials in scratch), so results are
-// run-to-run deterministic.
+// are combined as float-float pairs in a fixed order (warp shuffle tree, then
+// CTA, then a last-CTA pass over the per-CTA partials in scratch) and widened
+// to float64 once at the end, so results are run-to-run deterministic.
 #include <cstdint>
 
 #include "common.cuh"
@@ -27,39 +27,12 @@ constexpr int kStThreads = 256;
 constexpr int kStMaxBlocks = 1216;  // 152 SMs x 8
 constexpr int kNumSums = 8;
 
-struct TwoF {
-  float s, c;
-};
-
-__device__ __forceinline__ void two_add(TwoF& a, float x) {
-  const float s = __fadd_rn(a.s, x);
-  const float bp = __fsub_rn(s, a.s);
-  const float err = __fadd_rn(__fsub_rn(a.s, __fsub_rn(s, bp)), __fsub_rn(x, bp));
-  a.s = s;
-  a.c = __fadd_rn(a.c, err);
-}
-
-__device__ __forceinline__ double to_d(const TwoF& a) { return static_cast<double>(a.s) + static_cast<double>(a.c); }
-
-// Kahan-compensated FP32 sum: error about 2u|S| for a thread's partial,
-// enough for the outlier ratio and Gamma (relative bands of 1e-6); the sums
-// behind the delta cosine keep the TwoSum pair.
-struct Kahan {
-  float s, c;
-};
-
-__device__ __forceinline__ void kahan_add(Kahan& k, float x) {
-  const float y = __fsub_rn(x, k.c);
-  const float t = __fadd_rn(k.s, y);
-  k.c = __fsub_rn(__fsub_rn(t, k.s), y);
-  k.s = t;
-}
-
-__device__ __forceinline__ double to_d(const Kahan& k) { return static_cast<double>(k.s) - static_cast<double>(k.c); }
-
-// The same two accumulators on packed FP32 pairs (two independent lanes per
+// Per-thread accumulators on packed FP32 pairs (two independent lanes per
 // instruction, lane-wise identical rounding); a thread accumulates even and
-// odd elements in the two lanes and adds the lanes in float64 at the end.
+// odd elements in the two lanes.  TwoF2 keeps an unevaluated sum s + c with
+// Knuth's TwoSum (about 48 bits); Kahan2 keeps s - c with Kahan compensation
+// (error about 2u|S| for a thread's partial, enough for the outlier ratio and
+// Gamma, whose bands are relative 1e-6).
 struct TwoF2 {
   uint64_t s, c;
 };
@@ -70,11 +43,6 @@ __device__ __forceinline__ void two_add2(TwoF2& a, uint64_t x) {
   const uint64_t err = f2_add(f2_sub(a.s, f2_sub(s, bp)), f2_sub(x, bp));
   a.s = s;
   a.c = f2_add(a.c, err);
-}
-
-__device__ __forceinline__ double to_d(const TwoF2& a) {
-  return (static_cast<double>(f2_lo(a.s)) + static_cast<double>(f2_lo(a.c))) +
-         (static_cast<double>(f2_hi(a.s)) + static_cast<double>(f2_hi(a.c)));
 }
 
 struct Kahan2 {
@@ -88,9 +56,35 @@ __device__ __forceinline__ void kahan_add2(Kahan2& k, uint64_t x) {
   k.s = t;
 }
 
-__device__ __forceinline__ double to_d(const Kahan2& k) {
-  return (static_cast<double>(f2_lo(k.s)) - static_cast<double>(f2_lo(k.c))) +
-         (static_cast<double>(f2_hi(k.s)) - static_cast<double>(f2_hi(k.c)));
+// Float-float value hi + lo (|lo| <= ulp(hi)/2 after ff_add).  ff_add is the
+// double-float addition of Dekker / Bailey: TwoSum of the high parts, then the
+// low parts folded in and renormalised; its error is a few 2^-44 of |a| + |b|.
+// Combining partials this way keeps GB300's slow FP64 pipe off the reduction.
+struct FF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const float s = __fadd_rn(a.hi, b.hi);
+  const float bp = __fsub_rn(s, a.hi);
+  const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bp)), __fsub_rn(b.hi, bp));
+  const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), e);
+  const float hi = __fadd_rn(s, lo);
+  return FF{hi, __fsub_rn(lo, __fsub_rn(hi, s))};
+}
+
+__device__ __forceinline__ FF ff_max(FF a, FF b) { return FF{fmaxf(a.hi, b.hi), 0.f}; }
+
+__device__ __forceinline__ FF to_ff(const TwoF2& a) {
+  return ff_add(FF{f2_lo(a.s), f2_lo(a.c)}, FF{f2_hi(a.s), f2_hi(a.c)});
+}
+
+__device__ __forceinline__ FF to_ff(const Kahan2& k) {
+  return ff_add(FF{f2_lo(k.s), -f2_lo(k.c)}, FF{f2_hi(k.s), -f2_hi(k.c)});
+}
+
+__device__ __forceinline__ FF ff_shfl_xor(FF a, int o) {
+  return FF{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
 }
 
 __device__ __forceinline__ float f2_max_abs(uint64_t v, float m) {
@@ -119,42 +113,62 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 
 struct Scratch {
   unsigned int* counter;
-  double* partial;  // [gridDim.x][kNumSums]
+  FF* partial;  // [gridDim.x][kNumSums]
 };
 
 __device__ __forceinline__ Scratch scratch_view(void* p) {
   Scratch s;
   s.counter = reinterpret_cast<unsigned int*>(p);
-  s.partial = reinterpret_cast<double*>(reinterpret_cast<char*>(p) + 16);
+  s.partial = reinterpret_cast<FF*>(reinterpret_cast<char*>(p) + 16);
   return s;
 }
 
-// Reduces per-thread float64 values v[0..NS) (index NS-? as max where is_max)
-// across the grid in a fixed order.  Returns true in exactly one thread of the
-// last CTA to finish, with the totals in `tot`.
-template <int NS>
-__device__ bool grid_reduce(double (&v)[NS], const bool (&is_max)[NS], Scratch sc, double (&tot)[NS]) {
-  __shared__ double red[kStThreads / 32][NS];
-  __shared__ bool last;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Combines v[k] over a warp (xor-shuffle tree; sums with ff_add, maxima with
+// ff_max), leaving the result in every lane.
+template <int NS, int W = 32>
+__device__ __forceinline__ void warp_reduce(FF (&v)[NS], const bool (&is_max)[NS]) {
 #pragma unroll
-  for (int k = 0; k < NS; ++k) {
-    double x = v[k];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double y = __shfl_xor_sync(0xffffffffu, x, o);
-      x = is_max[k] ? fmax(x, y) : x + y;
-    }
-    if (lane == 0) red[warp][k] = x;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
+  for (int o = W / 2; o > 0; o >>= 1) {
 #pragma unroll
     for (int k = 0; k < NS; ++k) {
-      double x = red[0][k];
-      for (int w = 1; w < kStThreads / 32; ++w) x = is_max[k] ? fmax(x, red[w][k]) : x + red[w][k];
-      sc.partial[static_cast<size_t>(blockIdx.x) * kNumSums + k] = x;
+      const FF y = ff_shfl_xor(v[k], o);
+      v[k] = is_max[k] ? ff_max(v[k], y) : ff_add(v[k], y);
     }
+  }
+}
+
+// Combines the warps' values through shared memory; the CTA's result ends up
+// in warp 0.
+template <int NS>
+__device__ __forceinline__ void cta_reduce(FF (&v)[NS], const bool (&is_max)[NS], FF (*red)[NS]) {
+  constexpr int kWarps = kStThreads / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  warp_reduce<NS>(v, is_max);
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < NS; ++k) red[warp][k] = v[k];
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < NS; ++k) v[k] = lane < kWarps ? red[lane][k] : FF{0.f, 0.f};
+    warp_reduce<NS, kWarps>(v, is_max);
+  }
+}
+
+// Reduces per-thread values v[0..NS) (maxima where is_max, sums otherwise)
+// across the grid in a fixed order: warp tree, CTA, then the last CTA to finish
+// folds the per-CTA partials in scratch.  Returns true in exactly one thread,
+// with the totals in `tot`.  All values are non-negative except sums of
+// products, whose error stays relative to the sum of magnitudes.
+template <int NS>
+__device__ bool grid_reduce(FF (&v)[NS], const bool (&is_max)[NS], Scratch sc, double (&tot)[NS]) {
+  __shared__ FF red[kStThreads / 32][NS];
+  __shared__ bool last;
+  cta_reduce<NS>(v, is_max, red);
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 0; k < NS; ++k) sc.partial[static_cast<size_t>(blockIdx.x) * kNumSums + k] = v[k];
     __threadfence();
     const unsigned int done = atomicAdd(sc.counter, 1u);
     last = (done == gridDim.x - 1);
@@ -162,29 +176,23 @@ __device__ bool grid_reduce(double (&v)[NS], const bool (&is_max)[NS], Scratch s
   __syncthreads();
   if (!last) return false;
   __threadfence();
-  // last CTA: thread t folds partials t, t+256, ... then the same tree
+  // last CTA: thread t folds partials t, t + 256, ... then the same trees
 #pragma unroll
-  for (int k = 0; k < NS; ++k) {
-    double x = is_max[k] ? 0.0 : 0.0;
-    for (unsigned int b = threadIdx.x; b < gridDim.x; b += kStThreads) {
-      const double y = *reinterpret_cast<volatile double*>(&sc.partial[static_cast<size_t>(b) * kNumSums + k]);
-      x = is_max[k] ? fmax(x, y) : x + y;
-    }
+  for (int k = 0; k < NS; ++k) v[k] = FF{0.f, 0.f};
+  for (unsigned int b = threadIdx.x; b < gridDim.x; b += kStThreads) {
+    const float2* row = reinterpret_cast<const float2*>(sc.partial + static_cast<size_t>(b) * kNumSums);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const double y = __shfl_xor_sync(0xffffffffu, x, o);
-      x = is_max[k] ? fmax(x, y) : x + y;
+    for (int k = 0; k < NS; ++k) {
+      const float2 r = __ldcg(row + k);  // L2: written by other CTAs
+      const FF y{r.x, r.y};
+      v[k] = is_max[k] ? ff_max(v[k], y) : ff_add(v[k], y);
     }
-    if (lane == 0) red[warp][k] = x;
   }
-  __syncthreads();
+  __syncthreads();  // red is reused
+  cta_reduce<NS>(v, is_max, red);
   if (threadIdx.x != 0) return false;
 #pragma unroll
-  for (int k = 0; k < NS; ++k) {
-    double x = red[0][k];
-    for (int w = 1; w < kStThreads / 32; ++w) x = is_max[k] ? fmax(x, red[w][k]) : x + red[w][k];
-    tot[k] = x;
-  }
+  for (int k = 0; k < NS; ++k) tot[k] = static_cast<double>(v[k].hi) + static_cast<double>(v[k].lo);
   *sc.counter = 0;  // leave the scratch ready for the next call
   return true;
 }
@@ -232,7 +240,7 @@ __global__ void __launch_bounds__(kStThreads) tensor_stats_kernel(const uint16_t
     tensor_stats_vec(r0, mx, sa, sq);
     tensor_stats_vec(r1, mx, sa, sq);   // zeros add nothing
   }
-  double v[3] = {static_cast<double>(mx), to_d(sa), to_d(sq)};
+  FF v[3] = {FF{mx, 0.f}, to_ff(sa), to_ff(sq)};
   const bool is_max[3] = {true, false, false};
   double tot[3];
   if (grid_reduce<3>(v, is_max, scratch_view(scratch), tot)) {
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kStThreads) block_stats_kernel(const uint16_t*
     const uint4 w1 = block_stats_vec(a1, b1, p1, d2, xi2, ddp, dp2, mx, sa);  // zeros add nothing
     if (two) *reinterpret_cast<uint4*>(delta + 8 * i1) = w1;
   }
-  double v[6] = {to_d(d2), to_d(xi2), to_d(ddp), to_d(dp2), static_cast<double>(mx), to_d(sa)};
+  FF v[6] = {to_ff(d2), to_ff(xi2), to_ff(ddp), to_ff(dp2), FF{mx, 0.f}, to_ff(sa)};
   const bool is_max[6] = {false, false, false, false, true, false};
   double tot[6];
   if (grid_reduce<6>(v, is_max, scratch_view(scratch), tot)) {
@@ -340,7 +348,7 @@ __global__ void __launch_bounds__(kStThreads) skip_apply_kernel(const uint16_t* 
     const uint4 w1 = skip_vec(a1, d1, mx, sa);  // zeros add nothing
     if (two) *reinterpret_cast<uint4*>(x_out + 8 * i1) = w1;
   }
-  double v[2] = {static_cast<double>(mx), to_d(sa)};
+  FF v[2] = {FF{mx, 0.f}, to_ff(sa)};
   const bool is_max[2] = {true, false};
   double tot[2];
   if (grid_reduce<2>(v, is_max, scratch_view(scratch), tot)) {
@@ -455,7 +463,7 @@ static int stats_grid(Kernel kernel, int64_t n) {
   return static_cast<int>(want);
 }
 
-size_t stats_scratch_bytes(int64_t) { return 16 + static_cast<size_t>(kStMaxBlocks) * kNumSums * sizeof(double); }
+size_t stats_scratch_bytes(int64_t) { return 16 + static_cast<size_t>(kStMaxBlocks) * kNumSums * sizeof(FF); }
 
 cudaError_t launch_tensor_stats(const uint16_t* x, int64_t n, double* out, void* scratch, cudaStream_t st) {
   tensor_stats_kernel<<<stats_grid(tensor_stats_kernel, n), kStThreads, 0, st>>>(x, n, out, scratch);

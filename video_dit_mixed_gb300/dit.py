@@ -37,8 +37,9 @@ class DiT:
         self.bufs = [torch.zeros((tokens, hidden), dtype=bf, device=dev) for _ in range(2)]
         self.h = torch.zeros((tokens, ffn), dtype=bf, device=dev)
         self.deltas = torch.zeros((blocks, tokens, hidden), dtype=bf, device=dev)
-        self.qa_x = ops.QActTensors(tokens, hidden, dev)
-        self.qa_h = ops.QActTensors(tokens, ffn, dev)
+        # the W4A8 GEMM reads the bf16 operand form; the int8 codes are not kept
+        self.qa_x = ops.QActTensors(tokens, hidden, dev, i8_codes=False)
+        self.qa_h = ops.QActTensors(tokens, ffn, dev, i8_codes=False)
         self.tstats = torch.zeros(4, dtype=torch.float64, device=dev)
         self.stats = ops.new_stats(dev, blocks)
         self.state = ops.new_policy_state(dev, blocks)

@@ -42,7 +42,8 @@ def launch_count() -> int:
 class QActTensors:
     """Device buffers of one quantized activation tensor [M, K]."""
 
-    def __init__(self, m: int, k: int, device="cuda", nvfp4=True, int8=True, rotated=False, i8_operand=True):
+    def __init__(self, m: int, k: int, device="cuda", nvfp4=True, int8=True, rotated=False, i8_operand=True,
+                 i8_codes=True):
         self.m, self.k = m, k
         dev = torch.device(device)
         u8, f32 = torch.uint8, torch.float32
@@ -50,7 +51,7 @@ class QActTensors:
         self.fp4_scales = torch.zeros(fp4_scale_bytes(m, k), dtype=u8, device=dev) if nvfp4 else None
         self.tensor_amax = torch.zeros(1, dtype=f32, device=dev) if nvfp4 else None
         self.tensor_scale = torch.zeros(1, dtype=f32, device=dev) if nvfp4 else None
-        self.i8_codes = torch.empty((m, k), dtype=torch.int8, device=dev) if int8 else None
+        self.i8_codes = torch.empty((m, k), dtype=torch.int8, device=dev) if (int8 and i8_codes) else None
         self.row_scale = torch.empty(m, dtype=f32, device=dev) if int8 else None
         self.i8_operand = torch.empty((m, k), dtype=torch.bfloat16, device=dev) if (int8 and i8_operand) else None
         self.rotated = torch.empty((m, k), dtype=f32, device=dev) if rotated else None
