@@ -258,22 +258,35 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_nvfp4_kernel(const uint16_t*
 
 // Quantizes and stores one lane's 8 rotated values of row r at column col:
 // q = clamp(RN(y / s), -127, 127); codes (optional), the bf16 operand
-// (optional) and the rotated values (optional).
+// (optional) and the rotated values (optional).  Rounding to an integer is
+// done by adding 1.5 * 2^23: for |d| <= 127 the sum lies in [2^23, 2^24),
+// where the float spacing is 1, so the IEEE add rounds d to the nearest
+// integer with ties to even (rint) and the low mantissa bits hold q in two's
+// complement.  Clamping before rounding equals clamping after it (rounding
+// is monotone and +-127 are integers).  When s == 0 (all |y| rounded away)
+// the reciprocal is taken as 0, which gives q = 0.
 __device__ __forceinline__ void int8_chunk_store(const float (&v)[8], int r, int col, int K, float s, bool fast,
                                                  float rs, int8_t* codes, uint16_t* operand, float* rotated) {
-  uint32_t qb[2] = {0, 0};
-  uint32_t ob[4] = {0, 0, 0, 0};
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  uint32_t t[8], o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float q = 0.f;
-    if (s != 0.f) q = fminf(fmaxf(rintf(fast ? div_by_recip(v[i], s, rs) : __fdiv_rn(v[i], s)), -127.f), 127.f);
-    const int qi = static_cast<int>(q);
-    qb[i >> 2] |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * (i & 3));
-    ob[i >> 1] |= (__float_as_uint(q) >> 16) << (16 * (i & 1));  // integers |q|<=127 are exact in bf16
+    float d = fast ? div_by_recip(v[i], s, rs) : __fdiv_rn(v[i], s);
+    d = fminf(fmaxf(d, -127.f), 127.f);
+    const float ti = __fadd_rn(d, kRound);
+    t[i] = __float_as_uint(ti);                     // 0x4B400000 + q
+    o[i] = __float_as_uint(__fsub_rn(ti, kRound));  // q as float, exact (and exact in bf16)
   }
   const size_t off = static_cast<size_t>(r) * K + col;
-  if (codes != nullptr) *reinterpret_cast<uint2*>(codes + off) = make_uint2(qb[0], qb[1]);
-  if (operand != nullptr) *reinterpret_cast<uint4*>(operand + off) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  if (codes != nullptr) {
+    const uint32_t lo = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+    const uint32_t hi = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
+    *reinterpret_cast<uint2*>(codes + off) = make_uint2(lo, hi);
+  }
+  if (operand != nullptr)
+    *reinterpret_cast<uint4*>(operand + off) =
+        make_uint4(__byte_perm(o[0], o[1], 0x7632), __byte_perm(o[2], o[3], 0x7632), __byte_perm(o[4], o[5], 0x7632),
+                   __byte_perm(o[6], o[7], 0x7632));
   if (rotated != nullptr) {
     float4* dst = reinterpret_cast<float4*>(rotated + off);
     dst[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -311,8 +324,8 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_int8_kernel(const uint16_t* 
     }
     m = warp_max(m);
     const float s = __fdiv_rn(m, 127.0f);
-    const bool fast = recip_ok(s);
-    const float rs = fast ? __frcp_rn(s) : 0.f;
+    const bool fast = recip_ok(s) || s == 0.f;
+    const float rs = s != 0.f ? __frcp_rn(s) : 0.f;
     if (lane == 0) row_scale[r] = s;
     // pass 2: the row again (from cache), rotate, quantize
     for (int c0 = 0; c0 < nch; c0 += 4) {
@@ -341,7 +354,7 @@ constexpr int kHqRowWarps = 16;
 constexpr int kHqRowChunks = 4;
 
 template <int B>
-__global__ void __launch_bounds__(kHqRowWarps * 32) hq_int8_rows_kernel(const uint16_t* __restrict__ X, int M,
+__global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const uint16_t* __restrict__ X, int M,
                                                                         int K, int lr, const int32_t* mode_dev,
                                                                         int8_t* codes, float* row_scale,
                                                                         uint16_t* operand, float* rotated) {
@@ -378,8 +391,8 @@ __global__ void __launch_bounds__(kHqRowWarps * 32) hq_int8_rows_kernel(const ui
   for (int i = 1; i < R; ++i) m = fmaxf(m, red[(team << lr) + i]);
   if (!row_ok) return;
   const float s = __fdiv_rn(m, 127.0f);
-  const bool fast = recip_ok(s);
-  const float rs = fast ? __frcp_rn(s) : 0.f;
+  const bool fast = recip_ok(s) || s == 0.f;
+  const float rs = s != 0.f ? __frcp_rn(s) : 0.f;
   if (t == 0 && lane == 0) row_scale[r] = s;
 #pragma unroll
   for (int u = 0; u < kHqRowChunks; ++u) {
