@@ -9,7 +9,8 @@ every step independently (the oracle never sees a GPU tensor).  Bar:
   policy's 1e-6 band; comparison stops at such a point;
 - each step's output agrees to 1e-2 relative (Frobenius norm);
 - the run takes every branch: BF16 (PDR), NVFP4, INT8, SKIP and a refresh;
-- the CUDA-graph replay of a step gives bit-identical results to eager launches.
+- the CUDA-graph replay of a step, and host-side dispatch on the mode word,
+  give bit-identical results to eager launches.
 """
 import numpy as np
 import pytest
@@ -34,7 +35,7 @@ def _margin(st, ratio, cfg):
     return min(m)
 
 
-def _run_gpu(name, graph, switched=True):
+def _run_gpu(name, graph, switched=True, host_dispatch=False):
     from video_dit_mixed_gb300 import dit, ops
     c = synthgen.DIT_CONFIGS[name]
     packed = dit.pack_block_weights(synthgen.dit_weights(name), c["had_block"])
@@ -44,7 +45,7 @@ def _run_gpu(name, graph, switched=True):
     for s, x in enumerate(xs):
         if graph and s == 1:
             model.capture(switched=switched)
-        y = model.step(x)
+        y = model.step_host_dispatch(x) if host_dispatch else model.step(x)
         torch.cuda.synchronize()
         outs.append(y.float().cpu().numpy())
         words.append(model.modes.cpu().numpy().copy())
@@ -100,4 +101,14 @@ def test_graph_replay_matches_eager(switched):
     for a, b in zip(w_eager, w_graph):
         np.testing.assert_array_equal(a, b)
     for a, b in zip(o_eager, o_graph):
+        np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_host_dispatch_matches_eager():
+    """Host-side dispatch on the mode word runs the same kernels as the switched graph."""
+    o_eager, w_eager, _ = _run_gpu("dit_tiny", graph=False)
+    o_host, w_host, _ = _run_gpu("dit_tiny", graph=False, host_dispatch=True)
+    for a, b in zip(w_eager, w_host):
+        np.testing.assert_array_equal(a, b)
+    for a, b in zip(o_eager, o_host):
         np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))

@@ -208,6 +208,11 @@ sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const s
   p.Y = Y;
   p.Yf = Y_f32;
   p.err = err_dev;
+  // Walk the shorter output dimension fastest: the CTAs in flight then share
+  // tiles of the larger operand, which streams from HBM once, while the
+  // smaller one is re-read from L2 (an A of 17776 x 7680 bf16 does not fit
+  // in L2 and would be re-read from HBM once per column-tile pass).
+  p.n_fastest = M > N ? 1 : 0;
   if (run_fp4) {
     CUtensorMap ma, mb;
     if (!make_map(&ma, A->fp4_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, M, K / 2, 128) ||

@@ -25,6 +25,7 @@ struct GemmParams {
   float* Yf;
   int32_t* acc_dbg;
   int32_t* err;
+  int n_fastest;           // tile order: 1 = output column tiles fastest, 0 = row tiles fastest
 };
 
 cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, float* amax_out,

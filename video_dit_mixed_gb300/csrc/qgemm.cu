@@ -82,11 +82,50 @@ __host__ __device__ constexpr int stage_bytes() {
 template <int KIND, bool GROUPED>
 __host__ __device__ constexpr int gemm_smem_bytes() {
   return GemmCfg<KIND>::kStages * stage_bytes<KIND>() + 1024 /*align*/ + 256 /*barriers*/ +
-         (GROUPED ? kEpiWarps * kEpiCols * 4 : 0) /*per-warp group scales*/;
+         (GROUPED ? 2 * kEpiWarps * kEpiCols * 4 : 0) /*per-warp group scales, double-buffered*/;
 }
 
 __device__ __forceinline__ float gelu_erf(float v) {
   return 0.5f * v * (1.0f + erff(v * 0.7071067811865475244f));
+}
+
+// W4A8 group folding: each epilogue thread reads its accumulator columns of
+// one K group from tensor memory in chunks of kFold columns and adds
+// s_w[g][n] * acc_g[n] to its running sums (128 of them: the register budget
+// of 168 per thread leaves no room for a second chunk in flight).
+constexpr int kFold = 16;
+constexpr int kFoldChunks = kEpiCols / kFold;
+
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
+
+__device__ __forceinline__ void fold_chunk(float (&sum)[kEpiCols], int c, const uint32_t (&r)[kFold],
+                                           const float4* sw4) {
+#pragma unroll
+  for (int j4 = 0; j4 < kFold / 4; ++j4) {
+    const float4 s4 = sw4[c * (kFold / 4) + j4];
+    const int j = c * kFold + 4 * j4;
+    sum[j] = fmaf(s4.x, __uint_as_float(r[4 * j4]), sum[j]);
+    sum[j + 1] = fmaf(s4.y, __uint_as_float(r[4 * j4 + 1]), sum[j + 1]);
+    sum[j + 2] = fmaf(s4.z, __uint_as_float(r[4 * j4 + 2]), sum[j + 2]);
+    sum[j + 3] = fmaf(s4.w, __uint_as_float(r[4 * j4 + 3]), sum[j + 3]);
+  }
+}
+
+// 16-byte global -> shared copy without a register round trip (zero-fill when
+// !valid; src must still be a valid address).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Hands an accumulator buffer back to the MMA warp: one arrival per warp,
+// after every lane's tensor-memory loads have completed.
+__device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
 }
 
 // Applies the epilogue to 32 consecutive columns [n, n+32) of one row and
@@ -133,7 +172,7 @@ __device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, i
 }
 
 // Persistent kernel: each CTA walks output tiles t = blockIdx.x, +gridDim.x,
-// ... (row tiles fastest, so the CTAs in flight share the same weight tiles).
+// ...; p.n_fastest picks whether row or column tiles vary fastest along t.
 template <int KIND, bool GROUPED, bool DBG>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -171,6 +210,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int tiles_m = (p.M + kBM - 1) / kBM;
   const int tiles_n = (p.N + kBN - 1) / kBN;
   const int ntiles = tiles_m * tiles_n;
+  auto tile_of = [&](int t, int& m_tile, int& n_tile) {
+    if (p.n_fastest) {
+      n_tile = t % tiles_n;
+      m_tile = t / tiles_n;
+    } else {
+      m_tile = t % tiles_m;
+      n_tile = t / tiles_m;
+    }
+  };
   // NVFP4 stages hold 256 K-elements; a K that is an odd multiple of 128
   // leaves a half stage at the end (TMA zero-fills its missing columns; only
   // its valid scale chunks are copied and only its valid MMAs issued).
@@ -184,8 +232,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(&accf[0], 1);
     mbar_init(&accf[1], 1);
-    mbar_init(&acce[0], kEpiThreads);
-    mbar_init(&acce[1], kEpiThreads);
+    mbar_init(&acce[0], kEpiWarps);
+    mbar_init(&acce[1], kEpiWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -210,7 +258,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       const size_t sf_rows_bytes = static_cast<size_t>(128) * (p.K >> 4);  // one 128-row scale tile
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const int m_tile = t % tiles_m, n_tile = t / tiles_m;
+        int m_tile, n_tile;
+        tile_of(t, m_tile, n_tile);
         const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;  // 128-row halves of B that exist
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % S;
@@ -245,7 +294,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       bool ok = true;
       constexpr int spg = 128 / C::kKStage > 0 ? 128 / C::kKStage : 1;  // stages per K group (bf16 kinds)
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        const int n_tile = t / tiles_m;
+        int m_tile, n_tile;
+        tile_of(t, m_tile, n_tile);
+        (void)m_tile;
         const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;
         for (int kb = 0; kb < nk && ok; ++kb, ++it) {
           const bool acc_start = GROUPED ? (kb % spg) == 0 : kb == 0;
@@ -310,11 +361,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;                       // tensor-memory lane quarter this warp may read
     const int col0 = (ew >> 2) * kEpiCols;        // first accumulator column of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16) + col0;
-    float* my_sw = sw_smem + ew * kEpiCols;       // GROUPED: this warp's group scales
+    float* my_sw = sw_smem + ew * 2 * kEpiCols;   // GROUPED: this warp's group scales (two buffers)
     uint32_t ac = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-      const int m_tile = t % tiles_m, n_tile = t / tiles_m;
+      int m_tile, n_tile;
+      tile_of(t, m_tile, n_tile);
       const int row = m_tile * kBM + 32 * q + lane;
       const int nb = n_tile * kBN + col0;         // first output column of this thread
       if (nb >= p.N) {                            // nothing of this half exists (ragged N)
@@ -322,14 +374,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int g = 0; g < groups && ok; ++g, ++ac) {
             const uint32_t buf = ac & 1;
             if (!mbar_wait(&accf[buf], (ac >> 1) & 1, abort_flag)) { ok = false; break; }
-            tc_fence_before();
-            mbar_arrive(&acce[buf]);
+            release_acc(&acce[buf], lane);
           }
         } else {
           const uint32_t buf = ac % kBufs;
           if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_before();
-          mbar_arrive(&acce[buf]);
+          release_acc(&acce[buf], lane);
           ++ac;
         }
         continue;
@@ -338,55 +388,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         float sum[kEpiCols];
 #pragma unroll
         for (int j = 0; j < kEpiCols; ++j) sum[j] = 0.f;
-        auto load_sw = [&](int g) {
+        // s_w[g][nb .. nb+128): lane l copies 4 scales; group g goes to buffer g & 1
+        auto fetch_sw = [&](int g) {
           const int n = nb + 4 * lane;
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (g < groups && n < p.N) v = __ldg(reinterpret_cast<const float4*>(p.grp_scale + static_cast<size_t>(g) * p.N + n));
-          return v;
+          const bool v = g < groups && n < p.N;
+          cp_async16(smem_u32(my_sw + (g & 1) * kEpiCols + 4 * lane),
+                     v ? p.grp_scale + static_cast<size_t>(g) * p.N + n : p.grp_scale, v);
         };
-        float4 sw_next = load_sw(0);
+        fetch_sw(0);
         for (int g = 0; g < groups; ++g, ++ac) {
-          const float4 sw_now = sw_next;
-          sw_next = load_sw(g + 1);                // prefetch the next group's scales
-          __syncwarp();
-          reinterpret_cast<float4*>(my_sw)[lane] = sw_now;
-          __syncwarp();
+          cp_async_wait_all();
+          __syncwarp();                            // group g's scales visible; group g-1's no longer read
+          fetch_sw(g + 1);                         // prefetch into the other buffer
           const uint32_t buf = ac & 1;
           if (!mbar_wait(&accf[buf], (ac >> 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const float4* sw4 = reinterpret_cast<const float4*>(my_sw);
-#pragma unroll
-          for (int c = 0; c < kEpiCols / 16; ++c) {
-            uint32_t r[16];
-            tmem_ld16(lane_addr + buf * kBN + c * 16, r);
-            tmem_ld_wait(r);
-#pragma unroll
-            for (int j4 = 0; j4 < 4; ++j4) {
-              const float4 s4 = sw4[c * 4 + j4];
-              const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int j = c * 16 + j4 * 4 + u;
-                sum[j] = fmaf(sv[u], __uint_as_float(r[j4 * 4 + u]), sum[j]);
-              }
-            }
+          const float4* sw4 = reinterpret_cast<const float4*>(my_sw + (g & 1) * kEpiCols);
+          const uint32_t acc_addr = lane_addr + buf * kBN;
+          auto dbg = [&](int c, const uint32_t (&r)[kFold]) {
             if constexpr (DBG) {
               if (row < p.M) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  const int n = nb + c * 16 + j;
+                for (int j = 0; j < kFold; ++j) {
+                  const int n = nb + c * kFold + j;
                   if (n < p.N)
                     p.acc_dbg[(static_cast<size_t>(g) * p.M + row) * p.N + n] = __float2int_rn(__uint_as_float(r[j]));
                 }
               }
             }
+          };
+#pragma unroll
+          for (int c = 0; c < kFoldChunks; ++c) {
+            uint32_t r[kFold];
+            tmem_ld(acc_addr + c * kFold, r);
+            tmem_ld_wait(r);
+            if (c == kFoldChunks - 1) release_acc(&acce[buf], lane);  // every load of this group has landed
+            dbg(c, r);
+            fold_chunk(sum, c, r, sw4);
           }
-          tc_fence_before();
-          mbar_arrive(&acce[buf]);
         }
+        cp_async_wait_all();                       // no scale copy outlives the loop
         if (!ok) break;
         const float sm = (row < p.M) ? p.row_scale[row] : 0.f;
 #pragma unroll
@@ -412,8 +456,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int c = 0; c < kEpiCols / 32; ++c) tmem_ld32(lane_addr + c * 32, r[c]);
 #pragma unroll
           for (int c = 0; c < kEpiCols / 32; ++c) tmem_ld_wait(r[c]);
-          tc_fence_before();
-          mbar_arrive(&acce[buf]);
+          release_acc(&acce[buf], lane);
 #pragma unroll
           for (int c = 0; c < kEpiCols / 32; ++c) {
             float v[32];
@@ -427,10 +470,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t r[32];
             tmem_ld32(lane_addr + buf * kBN + c * 32, r);
             tmem_ld_wait(r);
-            if (c == kEpiCols / 32 - 1) {  // buffer fully read: hand it back to the MMA warp
-              tc_fence_before();
-              mbar_arrive(&acce[buf]);
-            }
+            if (c == kEpiCols / 32 - 1) release_acc(&acce[buf], lane);  // buffer fully read
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);

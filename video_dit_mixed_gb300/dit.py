@@ -129,6 +129,30 @@ class DiT:
             x = out
         return x
 
+    def step_host_dispatch(self, x_s: torch.Tensor | None = None):
+        """One step without a graph: the host reads each block's mode word (one
+        synchronisation per block) and launches only that mode's kernels.
+
+        The same kernels as a switched-graph step, minus the selectors; meant
+        for profilers that cannot look inside graphs with conditional nodes.
+        """
+        o = ops
+        if x_s is not None:
+            self.x_in.copy_(x_s, non_blocking=True)
+        o.tensor_stats(self.x_in, self.tstats, self.scratch)
+        x = self.x_in
+        for l in range(self.L):
+            out = self.bufs[l % 2]
+            mode = self.modes[l:l + 1]
+            o.policy_step(self.cfg, self.state[l], self.stats[l], self._in_stats(l), mode)
+            m = int(mode.item()) & 0xFF
+            if m == o.MODE_SKIP:
+                o.skip_apply(x, self.deltas[l], out, self.stats[l], self.scratch)
+            else:
+                self._compute_body(x, out, l, m)
+            x = out
+        return x
+
     def capture(self, switched: bool = True):
         """Capture one step into a CUDA graph (call after at least one eager step).
 
