@@ -8,12 +8,13 @@
 //   warp 0      TMA producer: A/B tiles (128-byte swizzle) and, for NVFP4,
 //               the scale-factor chunks, into a ring of shared-memory stages
 //               guarded by full/empty mbarriers;
-//   warp 1      allocates tensor memory; one lane issues tcgen05.mma (and,
-//               for NVFP4, tcgen05.cp of the scale factors into tensor
-//               memory) and tcgen05.commit to release stages and accumulators;
+//   warp 1      allocates tensor memory; one lane issues tcgen05.mma and
+//               tcgen05.commit to release stages and accumulators;
 //   warps 2..9  epilogue: tcgen05.ld of the FP32 accumulators (warp w reads
 //               lanes 32*(w%4)..+31 = tile rows, one 128-column half),
-//               scaling, GELU or residual, bf16 (or fp32) stores.
+//               scaling, GELU or residual, bf16 (or fp32) stores;
+//   warp 10     (NVFP4) tcgen05.cp of each stage's scale factors into its
+//               own tensor-memory slot.
 // Kinds:
 //   NVFP4  kind::mxf4nvf4.block_scale.scale_vec::4X, E2M1 x E2M1 with one
 //          E4M3 scale per 16 elements, 256 K-elements (128 bytes) per stage;
@@ -49,6 +50,15 @@ constexpr int kGemmThreads = 64 + kEpiThreads;
 
 enum { KIND_BF16 = 0, KIND_NVF4 = 1 };
 
+// NVFP4 adds a warp that copies the scale factors into tensor memory: every
+// tcgen05 instruction costs its issuing thread tens of cycles, and twelve
+// copies per stage on the MMA thread would pace the main loop.  (Splitting
+// the copies over two warps was slower: the issue cost is shared.)
+template <int KIND>
+__host__ __device__ constexpr int gemm_threads() {
+  return kGemmThreads + (KIND == KIND_NVF4 ? 32 : 0);
+}
+
 template <int KIND>
 struct GemmCfg;
 template <>
@@ -79,10 +89,15 @@ template <int KIND>
 __host__ __device__ constexpr int stage_bytes() {
   return kATileBytes + kBTileBytes + GemmCfg<KIND>::kSfaBytes + GemmCfg<KIND>::kSfbBytes;
 }
+// W4A8: each epilogue warp keeps the scales of the next kSwRing groups in a
+// shared-memory ring, fetched kSwRing - 1 groups ahead (an L2 round trip
+// per group would otherwise pace the fold).
+constexpr int kSwRing = 4;
+
 template <int KIND, bool GROUPED>
 __host__ __device__ constexpr int gemm_smem_bytes() {
   return GemmCfg<KIND>::kStages * stage_bytes<KIND>() + 1024 /*align*/ + 256 /*barriers*/ +
-         (GROUPED ? 2 * kEpiWarps * kEpiCols * 4 : 0) /*per-warp group scales, double-buffered*/;
+         (GROUPED ? kSwRing * kEpiWarps * kEpiCols * 4 : 0) /*per-warp ring of group scales*/;
 }
 
 __device__ __forceinline__ float gelu_erf(float v) {
@@ -119,6 +134,9 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Waits until at most N of this thread's most recent cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_newest() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // Hands an accumulator buffer back to the MMA warp: one arrival per warp,
 // after every lane's tensor-memory loads have completed.
@@ -174,15 +192,18 @@ __device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, i
 // Persistent kernel: each CTA walks output tiles t = blockIdx.x, +gridDim.x,
 // ...; p.n_fastest picks whether row or column tiles vary fastest along t.
 template <int KIND, bool GROUPED, bool DBG>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmParams p) {
   using C = GemmCfg<KIND>;
   constexpr int S = C::kStages;
   constexpr bool kNvf4 = KIND == KIND_NVF4;
   constexpr uint32_t kCols = 512;
-  constexpr uint32_t kSfaCol = 256;  // NVFP4: SFA [256, 272), SFB [272, 304)
-  constexpr uint32_t kSfbCol = 272;
+  // NVFP4: the scale factors of stage s live in TMEM columns 256 + 64 s:
+  // SFA in [0, 16), SFB in [16, 48) of that slot; one slot per stage, so the
+  // copies for later stages never overwrite scales earlier MMAs still read.
+  constexpr uint32_t kSfSlot0 = 256, kSfSlotCols = 64, kSfbOff = 16;
+  static_assert(!kNvf4 || kSfSlot0 + S * kSfSlotCols <= 512, "scale-factor slots exceed tensor memory");
   constexpr uint32_t kBufs = kNvf4 ? 1 : 2;  // accumulator buffers of kBN columns
   if (p.mode_dev != nullptr && SIXBIT_MODE_OF(*p.mode_dev) != p.want_mode) return;
 
@@ -196,7 +217,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* accf = bars + 2 * S;      // [2] accumulator buffer ready
   uint64_t* acce = bars + 2 * S + 2;  // [2] accumulator buffer drained
   uint64_t* drain = bars + 2 * S + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  uint64_t* sf_full = bars + 2 * S + 5;  // NVFP4: [S] the stage's scale factors are in tensor memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sw_smem = reinterpret_cast<float*>(smem + S * stage_bytes<KIND>() + 256);  // GROUPED: per-warp scales
 
@@ -235,6 +257,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(&acce[0], kEpiWarps);
     mbar_init(&acce[1], kEpiWarps);
     mbar_init(drain, 1);
+    if constexpr (kNvf4)
+      for (int s = 0; s < S; ++s) mbar_init(&sf_full[s], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -317,14 +341,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t d_tmem = tmem + buf * kBN;
           if constexpr (kNvf4) {
             const int nmma = min(C::kKStage, p.K - kb * C::kKStage) / 64;
-#pragma unroll
-            for (int k = 0; k < C::kMmaPerStage; ++k) {
-              if (k < nmma) {
-                tmem_cp_32x128b_warpx4(tmem + kSfaCol + 4 * k, sdesc_sf(smem_u32(SFA(s)) + 512 * k));
-                for (int j = 0; j < nj; ++j)
-                  tmem_cp_32x128b_warpx4(tmem + kSfbCol + 8 * k + 4 * j, sdesc_sf(smem_u32(SFB(s)) + 2048 * j + 512 * k));
-              }
+            const uint32_t sfa_col = tmem + kSfSlot0 + kSfSlotCols * s;
+            const uint32_t sfb_col = sfa_col + kSfbOff;
+            if (!mbar_wait(&sf_full[s], (it / S) & 1, abort_flag)) {  // copied by the scale-factor warp
+              ok = false;
+              break;
             }
+            tc_fence_after();
             // one N = 256 MMA (B scale chunks for rows 0-127 and 128-255 in
             // consecutive 4-column groups), or N = 128 when only half the tile exists
             const uint32_t idesc = nj == 2 ? idesc_nvf4(kBM, 256) : C::kIdesc;
@@ -332,7 +355,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int k = 0; k < C::kMmaPerStage; ++k) {
               if (k < nmma)
                 mma_nvf4(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), idesc,
-                         tmem + kSfaCol + 4 * k, tmem + kSfbCol + 8 * k, (acc_start && k == 0) ? 0u : 1u);
+                         sfa_col + 4 * k, sfb_col + 8 * k, (acc_start && k == 0) ? 0u : 1u);
             }
           } else {
 #pragma unroll
@@ -355,13 +378,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_commit(drain);  // all tensor-core work issued here completes before exit
       (void)mbar_wait(drain, 0, nullptr);
     }
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // -------------------------------------------------------- epilogue --
     const int ew = warp - 2;                      // 0 .. kEpiWarps-1
     const int q = warp & 3;                       // tensor-memory lane quarter this warp may read
     const int col0 = (ew >> 2) * kEpiCols;        // first accumulator column of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16) + col0;
-    float* my_sw = sw_smem + ew * 2 * kEpiCols;   // GROUPED: this warp's group scales (two buffers)
+    float* my_sw = sw_smem + ew * kSwRing * kEpiCols;  // GROUPED: this warp's ring of group scales
     uint32_t ac = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -388,25 +411,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         float sum[kEpiCols];
 #pragma unroll
         for (int j = 0; j < kEpiCols; ++j) sum[j] = 0.f;
-        // s_w[g][nb .. nb+128): lane l copies 4 scales; group g goes to buffer g & 1
+        // s_w[g][nb .. nb+128): lane l copies 4 scales; group g goes to slot g % kSwRing.
+        // One cp.async group is committed per fetch (a zero-fill past the last group).
         auto fetch_sw = [&](int g) {
           const int n = nb + 4 * lane;
           const bool v = g < groups && n < p.N;
-          cp_async16(smem_u32(my_sw + (g & 1) * kEpiCols + 4 * lane),
+          cp_async16(smem_u32(my_sw + (g % kSwRing) * kEpiCols + 4 * lane),
                      v ? p.grp_scale + static_cast<size_t>(g) * p.N + n : p.grp_scale, v);
         };
-        fetch_sw(0);
+#pragma unroll
+        for (int g = 0; g < kSwRing - 1; ++g) fetch_sw(g);
         for (int g = 0; g < groups; ++g, ++ac) {
-          cp_async_wait_all();
-          __syncwarp();                            // group g's scales visible; group g-1's no longer read
-          fetch_sw(g + 1);                         // prefetch into the other buffer
+          __syncwarp();                            // every lane is done with slot (g - 1) % kSwRing
+          fetch_sw(g + kSwRing - 1);               // ... which now receives group g + kSwRing - 1
+          cp_async_wait_newest<kSwRing - 1>();     // this lane's copy of group g has landed
+          __syncwarp();                            // and every other lane's
           const uint32_t buf = ac & 1;
           if (!mbar_wait(&accf[buf], (ac >> 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const float4* sw4 = reinterpret_cast<const float4*>(my_sw + (g & 1) * kEpiCols);
+          const float4* sw4 = reinterpret_cast<const float4*>(my_sw + (g % kSwRing) * kEpiCols);
           const uint32_t acc_addr = lane_addr + buf * kBN;
           auto dbg = [&](int c, const uint32_t (&r)[kFold]) {
             if constexpr (DBG) {
@@ -430,7 +456,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             fold_chunk(sum, c, r, sw4);
           }
         }
-        cp_async_wait_all();                       // no scale copy outlives the loop
+        cp_async_wait_all();                       // no scale copy outlives the tile
+        __syncwarp();
         if (!ok) break;
         const float sm = (row < p.M) ? p.row_scale[row] : 0.f;
 #pragma unroll
@@ -485,6 +512,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       *abort_flag = 1;
     }
     tc_fence_before();
+  } else if constexpr (kNvf4) {
+    if (lane == 0) {
+      // ------------------------------------- scale factors -> tensor memory --
+      // Stage s's scales go to slot s once the MMAs that read the slot in the
+      // previous round are done (empty[s]) and the stage has landed (full[s]).
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        int m_tile, n_tile;
+        tile_of(t, m_tile, n_tile);
+        (void)m_tile;
+        const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % S;
+          if ((it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1, abort_flag)) ||
+              !mbar_wait(&full[s], (it / S) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nmma = min(C::kKStage, p.K - kb * C::kKStage) / 64;
+          const uint32_t sfa_col = tmem + kSfSlot0 + kSfSlotCols * s;
+          const uint32_t sfb_col = sfa_col + kSfbOff;
+#pragma unroll
+          for (int k = 0; k < C::kMmaPerStage; ++k) {
+            if (k < nmma) {
+              tmem_cp_32x128b_warpx4(sfa_col + 4 * k, sdesc_sf(smem_u32(SFA(s)) + 512 * k));
+              for (int j = 0; j < nj; ++j)
+                tmem_cp_32x128b_warpx4(sfb_col + 8 * k + 4 * j, sdesc_sf(smem_u32(SFB(s)) + 2048 * j + 512 * k));
+            }
+          }
+          tc_commit(&sf_full[s]);
+        }
+      }
+      if (!ok) {
+        set_error(p.err, SIXBIT_ETIMEOUT);
+        *abort_flag = 1;
+      }
+    }
   }
   __syncthreads();
   if (warp == 1) {
@@ -518,7 +584,7 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
   }
   const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  qgemm_kernel<KIND, GROUPED, DBG><<<grid, kGemmThreads, smem, st>>>(a, b, p);
+  qgemm_kernel<KIND, GROUPED, DBG><<<grid, gemm_threads<KIND>(), smem, st>>>(a, b, p);
   note_launch();
   return cudaGetLastError();
 }
