@@ -257,6 +257,7 @@ class DitStep:
                            l2="working set > 10 GB, no flush needed", cuda_graph=not self.host_dispatch)
         self.mode_log = []
         self.timed_steps = []
+        self.skip_run_bytes = 0
 
     def _next_input(self):
         if self.s >= self.c["steps"]:       # trajectory exhausted: start a new video
@@ -300,9 +301,10 @@ class DitStep:
         return [a.elapsed_time(b) for a, b in pairs], None
 
     # kernels one block runs per decision inside the switched graph: NVFP4
-    # (amax + quant for x and h, two GEMMs, stats), INT8, BF16, SKIP; every
-    # block also runs the policy kernel and the switch selector
-    BODY_KERNELS = {1: 7, 2: 5, 3: 3, 4: 1}
+    # (amax + quant for x and h, two GEMMs, stats), INT8, BF16, SKIP (none:
+    # the skip runs inside the policy kernel); every block also runs the
+    # policy kernel, which sets the graph's branch condition
+    BODY_KERNELS = {1: 7, 2: 5, 3: 3, 4: 0}
 
     def launches(self):
         """Kernels run in the timed steps (from the device decision log of the same trajectory)."""
@@ -312,7 +314,7 @@ class DitStep:
         low = np.asarray(self.mode_log) & 0xFF
         n = 0
         for s in self.timed_steps:
-            n += 1 + sum(2 + self.BODY_KERNELS.get(int(v), 0) for v in low[s])
+            n += 1 + sum(1 + self.BODY_KERNELS.get(int(v), 0) for v in low[s])
         return n
 
     def profile(self, k, stream):
@@ -347,13 +349,25 @@ class DitStep:
             recs.append((e0, evs))
         T.cuda.synchronize()
         mh = modes.cpu().numpy()
+        low = mh & 0xFF
         per = {}
+        run_bytes = []
         for s, (e0, evs) in enumerate(recs):
             prev = e0
             for label, block, e in evs:
                 key = label if block < 0 else f"{label}:{MODE_NAMES.get(int(mh[s, block]) & 0xFF, '?')}"
+                if label == "policy_skip" and low[s, block] == 4:
+                    if block > 0 and low[s, block - 1] == 4:
+                        key = "policy_skip:covered"      # applied by the run that started earlier
+                    else:                                # a run start: reads x and k deltas, writes x
+                        k = 1
+                        while block + k < self.L and low[s, block + k] == 4:
+                            k += 1
+                        key = "skip_run"
+                        run_bytes.append((4 + 2 * k) * self.T * self.H)
                 per.setdefault(key, []).append(prev.elapsed_time(e))
                 prev = e
+        self.skip_run_bytes = (sum(run_bytes) / len(run_bytes)) if run_bytes else 0
         self.mode_log = mh
         m.reset()
         self.s = 0
@@ -387,7 +401,9 @@ class DitStep:
     def work(self, key):
         label, _, mode = key.partition(":")
         T, H, F = self.T, self.H, self.F
-        if mode == "skip" and label != "skip_apply":
+        if label == "skip_run":
+            return ("hbm", self.skip_run_bytes, False)
+        if mode in ("skip", "covered"):
             return (None, 0, False)
         if label in ("qgemm_up", "qgemm_down"):
             return ("tensor", 2.0 * T * H * F, mode == "nvfp4")
@@ -400,8 +416,6 @@ class DitStep:
             return (None, 0, False)
         if label == "block_stats":
             return ("hbm", 8 * T * H, False)
-        if label == "skip_apply" and mode == "skip":
-            return ("hbm", 6 * T * H, False)
         if label == "tensor_stats":
             return ("hbm", 2 * T * H, False)
         return (None, 0, False)

@@ -250,6 +250,56 @@ sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_sta
                                  const sixbit_stats* last_stats_dev, const double* in_stats_dev,
                                  int32_t* mode_dev, int32_t* err_dev, void* stream);
 
+/*
+ * The per-block device state of a stack of L residual blocks evaluated in
+ * order, block l reading x_{l-1} (x_{-1} = x0) and writing x_l into
+ * buf[l % 2].  All pointers are DEVICE pointers owned by the caller.
+ *   states [L], stats [L], modes [L]  as for sixbit_policy_step, one per block
+ *   covered [L] uint32, zero before the first step (the library keeps it
+ *               zero between steps)
+ *   in_stats0   {max |x0|, sum |x0|, count} of the step input (float64)
+ *   x0 [n], buf[0], buf[1] [n] bf16; deltas [L][n] bf16, the Delta cache
+ * n % 8 == 0; 16-byte aligned tensors.
+ */
+typedef struct {
+  sixbit_policy_state* states;
+  sixbit_stats* stats;
+  int32_t* modes;
+  uint32_t* covered;
+  const double* in_stats0;
+  const uint16_t* x0;
+  uint16_t* buf[2];
+  const uint16_t* deltas;
+  int64_t n;
+  int32_t L;
+  int32_t reserved;
+} sixbit_dit_blocks;
+
+/*
+ * sixbit_policy_step for block l (input statistics taken from stats[l-1],
+ * or in_stats0 for l = 0; decision to modes[l]) fused with the TDC skip
+ * (technical summary section 2.B; popular summary section 2) of every block
+ * it starts a run of.  A skip depends only on the block's own state, so when
+ * block l skips, the consecutive blocks l+1 .. l+k-1 that will also skip at
+ * this step are known; their skips are applied in the same pass:
+ * x_{l+k-1} = bf16(...bf16(x_{l-1} + Delta_l)... + Delta_{l+k-1}) into
+ * buf[(l+k-1) % 2], its {max |x|, sum |x|, count} into
+ * stats[l+k-1].{max_abs_out, sum_abs_out, count}, and blocks l+1 .. l+k-1
+ * marked covered: their own calls then only make (and record) their
+ * decision.  Results are bit-identical to one sixbit_policy_step +
+ * sixbit_skip_apply per block; the skipped intermediate activations are not
+ * written.  Call once per block, in order, every step.
+ * cond_handle: 0, or a conditional handle from sixbit_graph_cond_create (the
+ * call is then being captured into that graph); it is set to
+ * mode - SIXBIT_MODE_NVFP4 when that lies in [0, cond_branches), else to
+ * cond_branches (no body).  scratch as for sixbit_block_stats.  cfg is a
+ * HOST pointer.  A covered block whose decision is not a skip (impossible
+ * unless the state was changed in between) records SIXBIT_EINVAL in err_dev.
+ */
+sixbit_status sixbit_policy_skip_run(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
+                                     uint64_t cond_handle, int cond_branches, void* scratch, int32_t* err_dev,
+                                     void* stream);
+
 /* ---- companions of the hot path ---------------------------------------- */
 
 /* Input statistics of a bf16 tensor (the first block's input): out_dev[0..3] =
@@ -309,6 +359,16 @@ int64_t sixbit_block_stats_noalloc_max_elems(void);
 typedef struct sixbit_switch sixbit_switch;
 sixbit_status sixbit_graph_switch_begin(void* stream, void* body_stream, const int32_t* mode_dev, int first_mode,
                                         int nbranches, sixbit_switch** sw);
+/*
+ * The same SWITCH node without the selector kernel: the condition is set by
+ * a kernel captured before it (sixbit_policy_skip_run with this handle).
+ * sixbit_graph_cond_create makes the handle in the graph `stream` is
+ * capturing (its value defaults to "no body" at every graph launch);
+ * sixbit_graph_switch_begin_cond appends the node.
+ */
+sixbit_status sixbit_graph_cond_create(void* stream, int nbranches, uint64_t* handle);
+sixbit_status sixbit_graph_switch_begin_cond(void* stream, void* body_stream, uint64_t handle, int nbranches,
+                                             sixbit_switch** sw);
 sixbit_status sixbit_graph_branch_begin(sixbit_switch* sw, int branch, void** body_stream);
 sixbit_status sixbit_graph_branch_end(sixbit_switch* sw);
 sixbit_status sixbit_graph_switch_end(sixbit_switch* sw);

@@ -43,6 +43,12 @@ class PolicyState(C.Structure):
                                          "n_bf16", "reserved")]
 
 
+class DitBlocks(C.Structure):
+    _fields_ = [("states", c_p), ("stats", c_p), ("modes", c_p), ("covered", c_p), ("in_stats0", c_p),
+                ("x0", c_p), ("buf", c_p * 2), ("deltas", c_p), ("n", C.c_int64), ("L", C.c_int32),
+                ("reserved", C.c_int32)]
+
+
 EXPORTS = {
     "sixbit_fp4_scale_bytes": (C.c_size_t, [C.c_int, C.c_int]),
     "sixbit_fp4_scale_offset": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
@@ -58,7 +64,11 @@ EXPORTS = {
     "sixbit_skip_apply": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),
     "sixbit_block_stats_noalloc": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p]),
     "sixbit_block_stats_noalloc_max_elems": (C.c_int64, []),
+    "sixbit_policy_skip_run": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), C.c_int, C.c_uint64, C.c_int,
+                                         c_p, c_p, c_p]),
     "sixbit_graph_switch_begin": (C.c_int, [c_p, c_p, c_p, C.c_int, C.c_int, C.POINTER(c_p)]),
+    "sixbit_graph_cond_create": (C.c_int, [c_p, C.c_int, C.POINTER(C.c_uint64)]),
+    "sixbit_graph_switch_begin_cond": (C.c_int, [c_p, c_p, C.c_uint64, C.c_int, C.POINTER(c_p)]),
     "sixbit_graph_branch_begin": (C.c_int, [c_p, C.c_int, C.POINTER(c_p)]),
     "sixbit_graph_branch_end": (C.c_int, [c_p]),
     "sixbit_graph_switch_end": (C.c_int, [c_p]),

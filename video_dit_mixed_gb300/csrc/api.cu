@@ -302,4 +302,24 @@ sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_sta
       launch_policy(*cfg, state_dev, last_stats_dev, in_stats_dev, mode_dev, static_cast<cudaStream_t>(stream)));
 }
 
+sixbit_status sixbit_policy_skip_run(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
+                                     uint64_t cond_handle, int cond_branches, void* scratch, int32_t* err_dev,
+                                     void* stream) {
+  if (cfg == nullptr || blocks == nullptr || scratch == nullptr) return SIXBIT_EINVAL;
+  const sixbit_dit_blocks& B = *blocks;
+  if (B.states == nullptr || B.stats == nullptr || B.modes == nullptr || B.covered == nullptr ||
+      B.in_stats0 == nullptr || B.x0 == nullptr || B.buf[0] == nullptr || B.buf[1] == nullptr ||
+      B.deltas == nullptr)
+    return SIXBIT_EINVAL;
+  if (B.L <= 0 || l < 0 || l >= B.L || B.n <= 0 || B.n % 8 != 0 || cond_branches < 0 || cond_branches > 8)
+    return SIXBIT_ESHAPE;
+  if (!aligned16(B.x0) || !aligned16(B.buf[0]) || !aligned16(B.buf[1]) || !aligned16(B.deltas) ||
+      !aligned16(scratch))
+    return SIXBIT_EALIGN;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+  return cuda_status(launch_policy_skip(*cfg, B, l, static_cast<unsigned long long>(cond_handle), cond_branches,
+                                        scratch, err_dev, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

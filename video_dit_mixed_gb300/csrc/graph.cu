@@ -33,6 +33,9 @@ __global__ void switch_select_kernel(cudaGraphConditionalHandle h, const int32_t
 
 using namespace sixbit;
 
+static sixbit_status add_switch_node(cudaStream_t st, cudaStream_t body_stream, cudaGraphConditionalHandle handle,
+                                     int nbranches, sixbit_switch** out);
+
 extern "C" sixbit_status sixbit_graph_switch_begin(void* stream, void* body_stream, const int32_t* mode_dev,
                                                    int first_mode, int nbranches, sixbit_switch** out) {
   if (stream == nullptr || body_stream == nullptr || body_stream == stream || mode_dev == nullptr ||
@@ -52,12 +55,21 @@ extern "C" sixbit_status sixbit_graph_switch_begin(void* stream, void* body_stre
   switch_select_kernel<<<1, 32, 0, st>>>(handle, mode_dev, first_mode, static_cast<unsigned int>(nbranches));
   note_launch();
   if (cudaGetLastError() != cudaSuccess) return SIXBIT_ECUDA;
+  return add_switch_node(st, static_cast<cudaStream_t>(body_stream), handle, nbranches, out);
+}
 
+// Appends a SWITCH node on `handle` with `nbranches` empty bodies after the
+// current capture dependencies of `st`.
+static sixbit_status add_switch_node(cudaStream_t st, cudaStream_t body_stream, cudaGraphConditionalHandle handle,
+                                     int nbranches, sixbit_switch** out) {
+  cudaStreamCaptureStatus status;
+  cudaGraph_t graph = nullptr;
   const cudaGraphNode_t* deps = nullptr;
   const cudaGraphEdgeData* edges = nullptr;
   size_t ndeps = 0;
   if (cudaStreamGetCaptureInfo(st, &status, nullptr, &graph, &deps, &edges, &ndeps) != cudaSuccess)
     return SIXBIT_ECUDA;
+  if (status != cudaStreamCaptureStatusActive || graph == nullptr) return SIXBIT_EINVAL;
   cudaGraphNodeParams params = {};
   params.type = cudaGraphNodeTypeConditional;
   params.conditional.handle = handle;
@@ -73,9 +85,33 @@ extern "C" sixbit_status sixbit_graph_switch_begin(void* stream, void* body_stre
   sw->n = nbranches;
   sw->open_branch = -1;
   for (int i = 0; i < nbranches; ++i) sw->bodies[i] = params.conditional.phGraph_out[i];
-  sw->body_stream = static_cast<cudaStream_t>(body_stream);
+  sw->body_stream = body_stream;
   *out = sw;
   return SIXBIT_OK;
+}
+
+extern "C" sixbit_status sixbit_graph_cond_create(void* stream, int nbranches, uint64_t* handle) {
+  if (stream == nullptr || handle == nullptr || nbranches < 1 || nbranches > 8) return SIXBIT_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus status;
+  cudaGraph_t graph = nullptr;
+  if (cudaStreamGetCaptureInfo(st, &status, nullptr, &graph) != cudaSuccess) return SIXBIT_ECUDA;
+  if (status != cudaStreamCaptureStatusActive || graph == nullptr) return SIXBIT_EINVAL;
+  cudaGraphConditionalHandle h;
+  if (cudaGraphConditionalHandleCreate(&h, graph, static_cast<unsigned int>(nbranches),
+                                       cudaGraphCondAssignDefault) != cudaSuccess)
+    return SIXBIT_ECUDA;
+  *handle = static_cast<uint64_t>(h);
+  return SIXBIT_OK;
+}
+
+extern "C" sixbit_status sixbit_graph_switch_begin_cond(void* stream, void* body_stream, uint64_t handle,
+                                                        int nbranches, sixbit_switch** out) {
+  if (stream == nullptr || body_stream == nullptr || body_stream == stream || out == nullptr || nbranches < 1 ||
+      nbranches > 8)
+    return SIXBIT_EINVAL;
+  return add_switch_node(static_cast<cudaStream_t>(stream), static_cast<cudaStream_t>(body_stream),
+                         static_cast<cudaGraphConditionalHandle>(handle), nbranches, out);
 }
 
 extern "C" sixbit_status sixbit_graph_branch_begin(sixbit_switch* sw, int branch, void** body_stream) {

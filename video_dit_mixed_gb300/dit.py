@@ -1,20 +1,22 @@
 """Runs a residual-MLP diffusion transformer through the hot path, one denoising step at a time.
 
 Every block maps x -> x + W_d . GELU(W_u . x).  Per step and block the
-policy kernel writes a mode word on the device; every later kernel of the
-block reads it and does its work only when the mode is its own, so one step
-is a fixed sequence of launches with no host synchronisation, and it is
-captured once into a CUDA graph and replayed.
+policy writes a mode word on the device; every later kernel of the block
+reads it and does its work only when the mode is its own, so one step is a
+fixed sequence of launches with no host synchronisation, and it is captured
+once into a CUDA graph and replayed.
 
 Per block l (all on one stream):
-  policy_step(state[l], stats[l], in_stats) -> mode[l]
-  skip_apply(x, delta[l]) -> out                         (SKIP)
+  policy_skip_run(l) -> mode[l]; when block l starts a run of skipping
+                        blocks l..l+k-1: x_{l+k-1} = x_{l-1} + the run's
+                        cached deltas, in one pass            (SKIP)
   hadamard_quant(x) -> qa_x                              (NVFP4 / INT8)
   qgemm(qa_x | x, W_up[l], GELU) -> h                    (NVFP4 / INT8 / BF16)
   hadamard_quant(h) -> qa_h
   qgemm(qa_h | h, W_down[l], + x) -> out
   block_stats(x, out, delta[l]) -> stats[l], delta[l]    (not SKIP)
 in_stats of block 0 come from tensor_stats(x_0), of block l from stats[l-1].
+Block l reads bufs[(l-1) % 2] (x_in for l = 0) and writes bufs[l % 2].
 """
 from __future__ import annotations
 
@@ -44,7 +46,10 @@ class DiT:
         self.stats = ops.new_stats(dev, blocks)
         self.state = ops.new_policy_state(dev, blocks)
         self.modes = torch.zeros(blocks, dtype=torch.int32, device=dev)
+        self.covered = torch.zeros(blocks, dtype=torch.int32, device=dev)
         self.scratch = ops.new_scratch(tokens * ffn, dev)
+        self.rec = ops.dit_blocks(self.state, self.stats, self.modes, self.covered, self.tstats, self.x_in,
+                                  self.bufs[0], self.bufs[1], self.deltas)
         self.graph = None
         self.out = self.bufs[(blocks - 1) % 2]
 
@@ -54,11 +59,9 @@ class DiT:
         self.stats.zero_()
         self.state.zero_()
         self.modes.zero_()
+        self.covered.zero_()
 
-    def _in_stats(self, l):
-        return self.tstats if l == 0 else self.stats[l - 1, 4:7]
-
-    CALLS = ("policy_step", "skip_apply", "hq_x", "qgemm_up", "hq_h", "qgemm_down", "block_stats")
+    CALLS = ("policy_skip", "hq_x", "qgemm_up", "hq_h", "qgemm_down", "block_stats")
 
     def enqueue_step(self, after_call=None):
         """Enqueue one denoising step on the current stream (input: self.x_in).
@@ -77,10 +80,8 @@ class DiT:
             mode = self.modes[l:l + 1]
             st = self.stats[l]
             up, down = self.packed[l]
-            o.policy_step(self.cfg, self.state[l], st, self._in_stats(l), mode)
-            note("policy_step", l)
-            o.skip_apply(x, self.deltas[l], out, st, self.scratch, mode_dev=mode)
-            note("skip_apply", l)
+            o.policy_skip_run(self.cfg, self.rec, l, self.scratch)
+            note("policy_skip", l)
             o.hadamard_quant(x, self.b, 0, out=self.qa_x, mode_dev=mode)
             note("hq_x", l)
             o.qgemm(self.qa_x, x, up, 0, epilogue=o.EPI_GELU, out=self.h, mode_dev=mode)
@@ -109,22 +110,21 @@ class DiT:
         o.block_stats(x, out, self.deltas[l], self.stats[l], self.scratch)
 
     def enqueue_step_switched(self, body_stream):
-        """One step for graph capture: per block a device-selected SWITCH over the
-        NVFP4 / INT8 / BF16 / SKIP bodies, so only the chosen body's kernels run."""
+        """One step for graph capture: per block a SWITCH over the NVFP4 / INT8 /
+        BF16 bodies whose condition the policy kernel sets, so only the chosen
+        body's kernels run (a skip runs none: its work is in the policy kernel)."""
         o = ops
         stream = torch.cuda.current_stream()
         o.tensor_stats(self.x_in, self.tstats, self.scratch)
         x = self.x_in
         for l in range(self.L):
             out = self.bufs[l % 2]
-            mode = self.modes[l:l + 1]
-            o.policy_step(self.cfg, self.state[l], self.stats[l], self._in_stats(l), mode)
-            sw = o.GraphSwitch(stream, body_stream, mode, o.MODE_NVFP4, 4)
+            cond = o.graph_cond_create(stream, 3)
+            o.policy_skip_run(self.cfg, self.rec, l, self.scratch, cond=cond, cond_branches=3)
+            sw = o.GraphSwitch(stream, body_stream, None, o.MODE_NVFP4, 3, cond=cond)
             for i, m in enumerate((o.MODE_NVFP4, o.MODE_INT8, o.MODE_BF16)):
                 with sw.branch(i):
                     self._compute_body(x, out, l, m)
-            with sw.branch(3):
-                o.skip_apply(x, self.deltas[l], out, self.stats[l], self.scratch)
             sw.close()
             x = out
         return x
@@ -143,12 +143,9 @@ class DiT:
         x = self.x_in
         for l in range(self.L):
             out = self.bufs[l % 2]
-            mode = self.modes[l:l + 1]
-            o.policy_step(self.cfg, self.state[l], self.stats[l], self._in_stats(l), mode)
-            m = int(mode.item()) & 0xFF
-            if m == o.MODE_SKIP:
-                o.skip_apply(x, self.deltas[l], out, self.stats[l], self.scratch)
-            else:
+            o.policy_skip_run(self.cfg, self.rec, l, self.scratch)
+            m = int(self.modes[l].item()) & 0xFF
+            if m != o.MODE_SKIP:
                 self._compute_body(x, out, l, m)
             x = out
         return x

@@ -13,7 +13,7 @@ import torch
 
 from . import abi
 from .abi import (EPI_GELU, EPI_NONE, EPI_RESIDUAL, MODE_BF16, MODE_INT8, MODE_NVFP4, MODE_SKIP,  # noqa: F401
-                  PolicyCfg, PolicyState, QAct, Stats, Weights, check, lib)
+                  DitBlocks, PolicyCfg, PolicyState, QAct, Stats, Weights, check, lib)
 
 _lib = lib()
 
@@ -154,6 +154,30 @@ def policy_step(cfg: PolicyCfg, state: torch.Tensor, last_stats: torch.Tensor, i
     return mode_word
 
 
+def dit_blocks(states, stats, modes, covered, in_stats0, x0, buf0, buf1, deltas) -> DitBlocks:
+    """The sixbit_dit_blocks record of a stack of residual blocks (device tensors; deltas [L, ...])."""
+    L = states.shape[0]
+    n = x0.numel()
+    assert stats.shape[0] == L and modes.numel() == L and covered.numel() == L and deltas.shape[0] == L
+    assert covered.dtype == torch.int32 and deltas.numel() == L * n
+    return DitBlocks(_p(states), _p(stats), _p(modes), _p(covered), _p(in_stats0), _p(x0),
+                     (C.c_void_p * 2)(buf0.data_ptr(), buf1.data_ptr()), _p(deltas), n, L, 0)
+
+
+def policy_skip_run(cfg: PolicyCfg, blocks: DitBlocks, l: int, scratch: torch.Tensor, cond: int = 0,
+                    cond_branches: int = 3, err=None, stream=None):
+    """sixbit_policy_skip_run: block l's decision fused with the skips of the run it starts."""
+    check(_lib.sixbit_policy_skip_run(C.byref(cfg), C.byref(blocks), l, cond, cond_branches, _p(scratch), _p(err),
+                                      _stream(stream)), "policy_skip_run")
+
+
+def graph_cond_create(stream, nbranches: int) -> int:
+    """A conditional handle in the graph `stream` is capturing (default value: no body)."""
+    h = C.c_uint64()
+    check(_lib.sixbit_graph_cond_create(C.c_void_p(stream.cuda_stream), nbranches, C.byref(h)), "graph_cond_create")
+    return int(h.value)
+
+
 class GraphSwitch:
     """A device-selected branch in the CUDA graph being captured on `stream` (sixbit_graph_switch_*).
 
@@ -162,12 +186,19 @@ class GraphSwitch:
     stream is `body_stream`, which is capturing into that body.
     """
 
-    def __init__(self, stream, body_stream, mode_word: torch.Tensor, first_mode: int, nbranches: int):
+    def __init__(self, stream, body_stream, mode_word: torch.Tensor | None, first_mode: int, nbranches: int,
+                 cond: int | None = None):
+        """With cond (a handle from graph_cond_create, set by a kernel already captured) no selector is added."""
         self.h = C.c_void_p()
         self.body_stream = body_stream
-        check(_lib.sixbit_graph_switch_begin(C.c_void_p(stream.cuda_stream), C.c_void_p(body_stream.cuda_stream),
-                                             _p(mode_word), first_mode, nbranches, C.byref(self.h)),
-              "graph_switch_begin")
+        if cond is not None:
+            check(_lib.sixbit_graph_switch_begin_cond(C.c_void_p(stream.cuda_stream),
+                                                      C.c_void_p(body_stream.cuda_stream), cond, nbranches,
+                                                      C.byref(self.h)), "graph_switch_begin_cond")
+        else:
+            check(_lib.sixbit_graph_switch_begin(C.c_void_p(stream.cuda_stream),
+                                                 C.c_void_p(body_stream.cuda_stream), _p(mode_word), first_mode,
+                                                 nbranches, C.byref(self.h)), "graph_switch_begin")
 
     def branch(self, i: int):
         sw = self
