@@ -401,6 +401,143 @@ __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const
   }
 }
 
+// ------------------------------- thread-per-block NVFP4 forms (b = 16, 64) --
+//
+// For b <= 64 one thread holds a whole Hadamard block (b contiguous elements
+// of a row, b/8 16-byte loads) and runs every butterfly stage in registers:
+// no shuffles (which otherwise occupy the load/store pipe) and fewer
+// instructions per element.  Same stage order (ascending strides, each an
+// IEEE add or subtract), same exact 1/sqrt(b) scaling and same per-16-group
+// NVFP4 and per-row INT8 arithmetic as the warp-per-row kernels above, so
+// the results are bit-identical.  Consecutive threads take consecutive
+// blocks of a row, so a warp's loads cover a contiguous 32*2b bytes.  (The
+// same layout for INT8, with the row amax combined in shared memory, was
+// slower than the row-team kernel: one 480-thread CTA per SM.)
+
+template <int B>
+__device__ __forceinline__ void load_block_bf16(const uint16_t* p, float (&v)[B]) {
+#pragma unroll
+  for (int c = 0; c < B / 8; ++c) {
+    float t[8];
+    bf16x8_to_f32(ld_nc_16(p + 8 * c), t);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[8 * c + i] = t[i];
+  }
+}
+
+template <int B>
+__device__ __forceinline__ void fwht_block(float (&v)[B]) {
+#pragma unroll
+  for (int h = 1; h < B; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < B; ++i) {
+      if ((i & h) == 0) {
+        const float a = v[i], c = v[i + h];
+        v[i] = __fadd_rn(a, c);
+        v[i + h] = __fsub_rn(a, c);
+      }
+    }
+  }
+  constexpr float s = B == 16 ? 0.25f : 0.125f;
+#pragma unroll
+  for (int i = 0; i < B; ++i) v[i] = __fmul_rn(v[i], s);
+}
+
+template <int B>
+__global__ void __launch_bounds__(256) hq_amax_tpb_kernel(const uint16_t* __restrict__ X, int M, int K,
+                                                          const int32_t* mode_dev, float* amax_out) {
+  if (mode_skips(mode_dev, SIXBIT_MODE_NVFP4)) return;
+  const int per_row = K / B;
+  const int64_t nblk = static_cast<int64_t>(M) * per_row;
+  float m = 0.f;
+  for (int64_t t = blockIdx.x * 256ll + threadIdx.x; t < nblk; t += static_cast<int64_t>(gridDim.x) * 256) {
+    float v[B];
+    load_block_bf16<B>(X + t * B, v);
+    fwht_block<B>(v);
+#pragma unroll
+    for (int i = 0; i < B; ++i) m = fmaxf(m, fabsf(v[i]));
+  }
+  m = warp_max(m);
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float b = red[0];
+    for (int i = 1; i < 8; ++i) b = fmaxf(b, red[i]);
+    atomicMax(reinterpret_cast<unsigned int*>(amax_out), __float_as_uint(b));  // b >= 0
+  }
+}
+
+// Rows [M, round_up(M,128)) get zero scales (no codes), as in hq_nvfp4_kernel.
+template <int B>
+__global__ void __launch_bounds__(256) hq_nvfp4_tpb_kernel(const uint16_t* __restrict__ X, int M, int K,
+                                                           const int32_t* mode_dev, const float* amax_src,
+                                                           uint8_t* codes, uint8_t* scales, float* tscale_out,
+                                                           float* rotated) {
+  if (mode_skips(mode_dev, SIXBIT_MODE_NVFP4)) return;
+  const float amax = *amax_src;
+  const float s_t = amax == 0.f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *tscale_out = s_t;
+  const int per_row = K / B;
+  const int mpad = (M + 127) & ~127;
+  const int64_t nblk = static_cast<int64_t>(mpad) * per_row;
+  for (int64_t t = blockIdx.x * 256ll + threadIdx.x; t < nblk; t += static_cast<int64_t>(gridDim.x) * 256) {
+    const int r = static_cast<int>(t / per_row);
+    const int col = static_cast<int>(t - static_cast<int64_t>(r) * per_row) * B;
+    if (r >= M) {  // pad row: zero scales
+#pragma unroll
+      for (int g = 0; g < B / 16; ++g) scales[sf_offset(r, (col >> 4) + g, K)] = 0;
+      continue;
+    }
+    float v[B];
+    load_block_bf16<B>(X + static_cast<size_t>(r) * K + col, v);
+    fwht_block<B>(v);
+    uint32_t packed[B / 8];
+    uint32_t sc = 0;
+#pragma unroll
+    for (int g = 0; g < B / 16; ++g) {
+      float am = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[16 * g + i]));
+      const float sb = __fdiv_rn(__fdiv_rn(am, 6.0f), s_t);
+      const uint32_t e = f32_to_e4m3(sb);
+      const float S = __fmul_rn(e4m3_to_f32(e), s_t);
+      float q[16];
+      if (recip_ok(S)) {
+        const float rS = __frcp_rn(S);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q[i] = div_by_recip(v[16 * g + i], S, rS);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q[i] = (S != 0.f) ? __fdiv_rn(v[16 * g + i], S) : 0.f;
+      }
+      float q0[8], q1[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        q0[i] = q[i];
+        q1[i] = q[8 + i];
+      }
+      packed[2 * g] = f32x8_to_e2m1(q0);
+      packed[2 * g + 1] = f32x8_to_e2m1(q1);
+      sc |= e << (8 * g);
+    }
+    uint8_t* cp = codes + static_cast<size_t>(r) * (K >> 1) + (col >> 1);
+    if constexpr (B == 64) {
+      reinterpret_cast<uint4*>(cp)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      reinterpret_cast<uint4*>(cp)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      *reinterpret_cast<uint32_t*>(scales + sf_offset(r, col >> 4, K)) = sc;  // 4 consecutive groups
+    } else {
+      *reinterpret_cast<uint2*>(cp) = make_uint2(packed[0], packed[1]);
+      scales[sf_offset(r, col >> 4, K)] = static_cast<uint8_t>(sc);
+    }
+    if (rotated != nullptr) {
+      float4* dst = reinterpret_cast<float4*>(rotated + static_cast<size_t>(r) * K + col);
+#pragma unroll
+      for (int i = 0; i < B / 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+  }
+}
+
 // --------------------------------------------------------- weight packing --
 
 __device__ __forceinline__ void load8_f32(const float* p, float (&v)[8]) {
@@ -505,10 +642,28 @@ static int hq_grid(int rows) {
     note_launch();                                                                     \
   } while (0)
 
+// Grid of the thread-per-block kernels: one thread per Hadamard block, at
+// most 16 CTAs of 256 per SM (the rest is walked with a grid stride).
+static int tpb_grid(int64_t nblk) {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (nblk + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sms) * 16;
+  return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
 cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, float* amax_out,
                            cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), st);
   if (e != cudaSuccess) return e;
+  if (b == 16 || b == 64) {
+    const int grid = tpb_grid(static_cast<int64_t>(M) * (K / b));
+    if (b == 16) hq_amax_tpb_kernel<16><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_out);
+    else hq_amax_tpb_kernel<64><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_out);
+    note_launch();
+    return cudaGetLastError();
+  }
   const int grid = hq_grid(M);
   SIXBIT_DISPATCH_B(b, hq_amax_kernel, X, M, K, mode_dev, amax_out);
   return cudaGetLastError();
@@ -516,6 +671,18 @@ cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t
 
 cudaError_t launch_hq_nvfp4(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, const float* amax_src,
                             const sixbit_qact* o, cudaStream_t st) {
+  // b = 64 stores its four group scales as one 32-bit word
+  if (b == 16 || (b == 64 && (reinterpret_cast<uintptr_t>(o->fp4_scales) & 3u) == 0)) {
+    const int grid = tpb_grid(static_cast<int64_t>((M + 127) & ~127) * (K / b));
+    if (b == 16)
+      hq_nvfp4_tpb_kernel<16><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_src, o->fp4_codes, o->fp4_scales,
+                                                    o->tensor_scale, o->rotated);
+    else
+      hq_nvfp4_tpb_kernel<64><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_src, o->fp4_codes, o->fp4_scales,
+                                                    o->tensor_scale, o->rotated);
+    note_launch();
+    return cudaGetLastError();
+  }
   const int grid = hq_grid((M + 127) & ~127);
   SIXBIT_DISPATCH_B(b, hq_nvfp4_kernel, X, M, K, mode_dev, amax_src, o->fp4_codes, o->fp4_scales, o->tensor_scale,
                     o->rotated);

@@ -503,24 +503,25 @@ __global__ void __launch_bounds__(kStThreads) policy_skip_kernel(sixbit_policy_c
       uint64_t v[4];
       unpack4x2(ld16(x_in + 8 * i), v);
       uint32_t w[4];
+      const uint16_t* dp = d0 + 8 * i;
       int j = 0;
-      for (; j + 2 <= k; j += 2) {  // two Delta loads in flight
-        const uint4 ra = ld16(d0 + static_cast<size_t>(j) * B.n + 8 * i);
-        const uint4 rb = ld16(d0 + static_cast<size_t>(j + 1) * B.n + 8 * i);
-        uint64_t da[4], db[4];
-        unpack4x2(ra, da);
-        unpack4x2(rb, db);
+      for (; j + 4 <= k; j += 4) {  // four Delta loads in flight, applied in order
+        uint4 r[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], da[q])));
-          v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], db[q])));
+        for (int u = 0; u < 4; ++u) r[u] = ld16(dp + static_cast<size_t>(j + u) * B.n);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint64_t d[4];
+          unpack4x2(r[u], d);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
         }
       }
-      if (j < k) {
-        uint64_t da[4];
-        unpack4x2(ld16(d0 + static_cast<size_t>(j) * B.n + 8 * i), da);
+      for (; j < k; ++j) {
+        uint64_t d[4];
+        unpack4x2(ld16(dp + static_cast<size_t>(j) * B.n), d);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], da[q])));
+        for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
