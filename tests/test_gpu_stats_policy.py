@@ -2,8 +2,8 @@
 
 Bar: bit-exact delta / skip outputs and maxima.  Sums, against the float64
 oracle: the three behind the delta cosine (sum Delta^2, Delta*Delta_prev,
-Delta_prev^2) within 1e-9 * sum|terms| (each thread keeps a TwoSum pair,
-float64 combine); the Kahan-compensated sums for Gamma and the outlier ratio
+Delta_prev^2) within 1e-9 * sum|terms| (each thread keeps a TwoSum pair;
+partials combine as float-float pairs, ~44 bits); the Kahan-compensated sums for Gamma and the outlier ratio
 (sum x_in^2, sum |x|, sum x^2) within 2.5e-7 * sum|terms| (Kahan's bound 2u
 per thread partial; the policy compares these statistics to thresholds with a
 1e-6 relative band, so 2.4e-7 cannot flip a decision outside it).  Policy
