@@ -374,26 +374,35 @@ class DitStep:
         return per
 
     def e2e(self, k, stream):
-        """Host trajectory (pinned) -> device, step, output -> host; from the trajectory's first step."""
+        """Host trajectory (pinned) -> device, step, output -> host (pinned), from the trajectory's
+        first step, through DiT.step_pipelined: each step's input copy overlaps the previous step's
+        compute and its output copy the next one's.  Timed from the first copy to the last
+        output's arrival on the host; per-step time = total / k."""
         T = self.t
         if self.traj_host is None:
             self.traj_host = self.traj.cpu().pin_memory()
+        outs = [T.empty_like(self.out_host).pin_memory() for _ in range(2)]
         self.model.reset()
         self.s = 0
-        pairs = []
-        for _ in range(k):
+        T.cuda.synchronize()
+        a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+        a.record(stream)
+        last = None
+        for j in range(k):
             if self.s >= self.c["steps"]:
                 self.s = 0
                 self.model.reset()
-            a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
-            a.record(stream)
-            self._step(self.traj_host[self.s])
+            if self.host_dispatch:
+                self._step(self.traj_host[self.s])
+                outs[j % 2].copy_(self.model.out, non_blocking=True)
+            else:
+                last = self.model.step_pipelined(self.traj_host[self.s], outs[j % 2])
             self.s += 1
-            self.out_host.copy_(self.model.out, non_blocking=True)
-            b.record(stream)
-            pairs.append((a, b))
+        if last is not None:
+            stream.wait_event(last)
+        b.record(stream)
         T.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in pairs]
+        return [a.elapsed_time(b) / k] * k
 
     def value(self, ms):
         return 1e3 / ms

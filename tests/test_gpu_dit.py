@@ -112,3 +112,24 @@ def test_host_dispatch_matches_eager():
         np.testing.assert_array_equal(a, b)
     for a, b in zip(o_eager, o_host):
         np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_pipelined_host_io_matches_eager():
+    """step_pipelined (host copies overlapped with the neighbouring steps) gives the eager outputs."""
+    from video_dit_mixed_gb300 import dit
+    o_eager, w_eager, _ = _run_gpu("dit_tiny", graph=False)
+    name = "dit_tiny"
+    c = synthgen.DIT_CONFIGS[name]
+    packed = dit.pack_block_weights(synthgen.dit_weights(name), c["had_block"])
+    model = dit.DiT(c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"], packed)
+    xs = [torch.from_numpy(x).to(torch.bfloat16).pin_memory() for x in synthgen.dit_trajectory(name)]
+    model.step(xs[0].cuda())
+    torch.cuda.synchronize()
+    model.capture()
+    model.reset()
+    outs = [torch.empty((c["tokens"], c["hidden"]), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    for x, o in zip(xs, outs):
+        model.step_pipelined(x, o)
+    torch.cuda.synchronize()
+    for a, b in zip(o_eager, outs):
+        np.testing.assert_array_equal(a.view(np.uint32), b.float().numpy().view(np.uint32))

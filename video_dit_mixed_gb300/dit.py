@@ -178,6 +178,46 @@ class DiT:
             self.enqueue_step()
         return self.out
 
+    def step_pipelined(self, x_host: torch.Tensor, out_host: torch.Tensor):
+        """One step with its host copies overlapped with the neighbouring steps.
+
+        x_host and out_host are pinned host tensors [T, H] bf16.  The input is
+        copied in on one side stream while the previous step computes, and
+        the result is copied back on another while the next step computes
+        (each through a device staging buffer, so the copies never race the
+        step's own buffers).  Returns the event after which out_host holds
+        this step's output.  Nothing here synchronises the host.
+        """
+        cs = torch.cuda.current_stream()
+        if getattr(self, "_pipe", None) is None:
+            dev = self.x_in.device
+            mk = lambda: [torch.empty_like(self.x_in) for _ in range(2)]  # noqa: E731
+            self._pipe = dict(
+                s_in=torch.cuda.Stream(device=dev), s_out=torch.cuda.Stream(device=dev), stage_in=mk(),
+                stage_out=mk(), k=0,
+                in_ready=[torch.cuda.Event() for _ in range(2)], in_free=[torch.cuda.Event() for _ in range(2)],
+                out_ready=[torch.cuda.Event() for _ in range(2)], out_free=[torch.cuda.Event() for _ in range(2)])
+            for e in self._pipe["in_free"] + self._pipe["out_free"]:
+                e.record(cs)
+        P = self._pipe
+        i = P["k"] % 2
+        P["s_in"].wait_event(P["in_free"][i])           # stage_in[i] consumed two steps ago
+        with torch.cuda.stream(P["s_in"]):
+            P["stage_in"][i].copy_(x_host, non_blocking=True)
+            P["in_ready"][i].record(P["s_in"])
+        cs.wait_event(P["in_ready"][i])
+        self.step(P["stage_in"][i])                     # device-to-device into x_in, then the graph
+        P["in_free"][i].record(cs)
+        cs.wait_event(P["out_free"][i])                 # stage_out[i] read back two steps ago
+        P["stage_out"][i].copy_(self.out)
+        P["out_ready"][i].record(cs)
+        P["s_out"].wait_event(P["out_ready"][i])
+        with torch.cuda.stream(P["s_out"]):
+            out_host.copy_(P["stage_out"][i], non_blocking=True)
+            P["out_free"][i].record(P["s_out"])
+        P["k"] += 1
+        return P["out_free"][i]
+
     def decision_counts(self):
         """Per block: (n_nvfp4, n_int8, n_bf16, n_skip, n_refresh, n_pdr, n_near) from the device state."""
         out = []
