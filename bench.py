@@ -301,9 +301,10 @@ class DitStep:
         return [a.elapsed_time(b) for a, b in pairs], None
 
     # kernels one block runs per decision inside the switched graph: NVFP4
-    # (amax + quant for x and h, two GEMMs, stats), INT8, BF16, SKIP (none:
-    # the skip runs inside the policy kernel); every block also runs the
-    # policy kernel, which sets the graph's branch condition
+    # (amax + quant for x and h, two GEMMs, stats), INT8, BF16, SKIP (one
+    # kernel applying the run when the block starts one, none when an earlier
+    # run covered it); every block also runs the one-thread policy kernel,
+    # which sets the graph's branch condition
     BODY_KERNELS = {1: 7, 2: 5, 3: 3, 4: 0}
 
     def launches(self):
@@ -314,7 +315,9 @@ class DitStep:
         low = np.asarray(self.mode_log) & 0xFF
         n = 0
         for s in self.timed_steps:
-            n += 1 + sum(1 + self.BODY_KERNELS.get(int(v), 0) for v in low[s])
+            row = [int(v) for v in low[s]]
+            n += 1 + sum(1 + self.BODY_KERNELS.get(v, 0) for v in row)
+            n += sum(1 for l, v in enumerate(row) if v == 4 and (l == 0 or row[l - 1] != 4))  # run starts
         return n
 
     def profile(self, k, stream):

@@ -255,8 +255,8 @@ sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_sta
  * order, block l reading x_{l-1} (x_{-1} = x0) and writing x_l into
  * buf[l % 2].  All pointers are DEVICE pointers owned by the caller.
  *   states [L], stats [L], modes [L]  as for sixbit_policy_step, one per block
- *   covered [L] uint32, zero before the first step (the library keeps it
- *               zero between steps)
+ *   covered [L], run_len [L] uint32, zero before the first step (the
+ *               library leaves them zero between steps)
  *   in_stats0   {max |x0|, sum |x0|, count} of the step input (float64)
  *   x0 [n], buf[0], buf[1] [n] bf16; deltas [L][n] bf16, the Delta cache
  * n % 8 == 0; 16-byte aligned tensors.
@@ -270,6 +270,7 @@ typedef struct {
   const uint16_t* x0;
   uint16_t* buf[2];
   const uint16_t* deltas;
+  uint32_t* run_len;
   int64_t n;
   int32_t L;
   int32_t reserved;
@@ -281,7 +282,7 @@ typedef struct {
  * (technical summary section 2.B; popular summary section 2) of every block
  * it starts a run of.  A skip depends only on the block's own state, so when
  * block l skips, the consecutive blocks l+1 .. l+k-1 that will also skip at
- * this step are known; their skips are applied in the same pass:
+ * this step are known; their skips are applied in one pass:
  * x_{l+k-1} = bf16(...bf16(x_{l-1} + Delta_l)... + Delta_{l+k-1}) into
  * buf[(l+k-1) % 2], its {max |x|, sum |x|, count} into
  * stats[l+k-1].{max_abs_out, sum_abs_out, count}, and blocks l+1 .. l+k-1
@@ -289,16 +290,25 @@ typedef struct {
  * decision.  Results are bit-identical to one sixbit_policy_step +
  * sixbit_skip_apply per block; the skipped intermediate activations are not
  * written.  Call once per block, in order, every step.
- * cond_handle: 0, or a conditional handle from sixbit_graph_cond_create (the
- * call is then being captured into that graph); it is set to
- * mode - SIXBIT_MODE_NVFP4 when that lies in [0, cond_branches), else to
- * cond_branches (no body).  scratch as for sixbit_block_stats.  cfg is a
- * HOST pointer.  A covered block whose decision is not a skip (impossible
- * unless the state was changed in between) records SIXBIT_EINVAL in err_dev.
+ * With cond_handle == 0 the call enqueues the decision and then the run's
+ * skip (which does nothing unless block l starts a run).  With a handle
+ * from sixbit_graph_cond_create (the call is being captured into that
+ * graph) it enqueues only the decision, which sets the condition to
+ * mode - SIXBIT_MODE_NVFP4 for a compute (0, 1, 2), 3 for a run start and
+ * cond_branches (no body) for a covered block or a value out of range; the
+ * caller puts sixbit_skip_run for block l in branch 3 of a switch with 4
+ * branches.  scratch as for sixbit_block_stats (unused with a handle).
+ * cfg is a HOST pointer.  A covered block whose decision is not a skip
+ * (impossible unless the state was changed in between) records
+ * SIXBIT_EINVAL in err_dev.
  */
 sixbit_status sixbit_policy_skip_run(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
                                      uint64_t cond_handle, int cond_branches, void* scratch, int32_t* err_dev,
                                      void* stream);
+/* The skip of the run block l starts, as recorded by its sixbit_policy_skip_run
+ * decision (returns at once on the device when block l starts no run). */
+sixbit_status sixbit_skip_run(const sixbit_dit_blocks* blocks, int l, void* scratch, int32_t* err_dev,
+                              void* stream);
 
 /* ---- companions of the hot path ---------------------------------------- */
 

@@ -51,8 +51,8 @@ def test_fused_runs_match_sequential_skips(ops, skipping):
     st_b, stats_b = _states(ops, L, skipping), ops.new_stats("cuda", L)
     modes_b = torch.zeros(L, dtype=torch.int32, device="cuda")
     bufs_b = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
-    covered = torch.zeros(L, dtype=torch.int32, device="cuda")
-    rec = ops.dit_blocks(st_b, stats_b, modes_b, covered, tstats, x0, bufs_b[0], bufs_b[1], deltas)
+    marks = torch.zeros((2, L), dtype=torch.int32, device="cuda")
+    rec = ops.dit_blocks(st_b, stats_b, modes_b, marks, tstats, x0, bufs_b[0], bufs_b[1], deltas)
 
     first_low = None
     for step in range(3):   # by the third step the copying blocks have two computes and skip too
@@ -77,7 +77,7 @@ def test_fused_runs_match_sequential_skips(ops, skipping):
         np.testing.assert_array_equal(modes_a.cpu().numpy(), modes_b.cpu().numpy())
         np.testing.assert_array_equal(st_a.cpu().numpy(), st_b.cpu().numpy())
         assert torch.equal(x.view(torch.int16), xb.view(torch.int16)), step
-        assert not covered.any()
+        assert not marks.any()
         # the statistics a later block reads: those of every run's last block
         low = modes_a.cpu().numpy() & 0xFF
         first_low = low if first_low is None else first_low

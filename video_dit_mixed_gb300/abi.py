@@ -45,7 +45,8 @@ class PolicyState(C.Structure):
 
 class DitBlocks(C.Structure):
     _fields_ = [("states", c_p), ("stats", c_p), ("modes", c_p), ("covered", c_p), ("in_stats0", c_p),
-                ("x0", c_p), ("buf", c_p * 2), ("deltas", c_p), ("n", C.c_int64), ("L", C.c_int32),
+                ("x0", c_p), ("buf", c_p * 2), ("deltas", c_p), ("run_len", c_p), ("n", C.c_int64),
+                ("L", C.c_int32),
                 ("reserved", C.c_int32)]
 
 
@@ -66,6 +67,7 @@ EXPORTS = {
     "sixbit_block_stats_noalloc_max_elems": (C.c_int64, []),
     "sixbit_policy_skip_run": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), C.c_int, C.c_uint64, C.c_int,
                                          c_p, c_p, c_p]),
+    "sixbit_skip_run": (C.c_int, [C.POINTER(DitBlocks), C.c_int, c_p, c_p, c_p]),
     "sixbit_graph_switch_begin": (C.c_int, [c_p, c_p, c_p, C.c_int, C.c_int, C.POINTER(c_p)]),
     "sixbit_graph_cond_create": (C.c_int, [c_p, C.c_int, C.POINTER(C.c_uint64)]),
     "sixbit_graph_switch_begin_cond": (C.c_int, [c_p, c_p, C.c_uint64, C.c_int, C.POINTER(c_p)]),

@@ -452,112 +452,109 @@ __global__ void policy_kernel(sixbit_policy_cfg cfg, sixbit_policy_state* st, co
 
 // ------------------------------------------------ policy + TDC skip runs --
 //
-// The decision of block l fused with the skip of the run of consecutive
-// blocks l, l+1, ..., l+k-1 that all skip at this step.  A skip decision
-// depends only on the block's own state (cos, acc, number of computes) and on
-// the statistics of its last compute, never on its input, so when block l
-// skips, the decisions of the blocks after it are already fixed and the run
-// is found by evaluating policy_decide on copies of their states.  The run's
-// output x_{l+k-1} = bf16(... bf16(bf16(x_{l-1} + D_l) + D_{l+1}) ... + D_{l+k-1})
-// is written in one pass (the same roundings as k separate skips; the
-// intermediate activations are never read, so they are not written), with
-// its {max, sum |x|, count} into stats[l+k-1]; blocks l+1 .. l+k-1 are
-// marked covered, and their own launches then only update their states.
-// Every CTA decides from the state as it was at launch; the last CTA to
-// finish (after every other CTA has read the state) writes the new state,
-// the mode word, the run's statistics and marks, and the graph condition.
+// The decision of block l and, when it starts a run of consecutive blocks
+// l, l+1, ..., l+k-1 that all skip at this step, the skip of the whole run in
+// one pass.  A skip decision depends only on the block's own state (cos, acc,
+// number of computes) and on the statistics of its last compute, never on
+// its input, so when block l skips, the decisions of the blocks after it are
+// already fixed and the run is found by evaluating policy_decide on copies
+// of their states.
+//
+// policy_run_kernel (one thread) decides block l, records its state and mode
+// word, and for a run start stores k in run_len[l] and marks blocks
+// l+1 .. l+k-1 covered (their own decisions then only clear the mark); it
+// sets the graph condition: compute modes to their branch, a run start to
+// branch 3 (when the switch has one), a covered block to no branch.
+// skip_run_kernel applies the run:
+// x_{l+k-1} = bf16(... bf16(bf16(x_{l-1} + D_l) + D_{l+1}) ... + D_{l+k-1})
+// (the same roundings as k separate skips; the intermediate activations are
+// never read, so they are not written), with its {max, sum |x|, count} into
+// stats[l+k-1], and clears run_len[l]; it returns at once when run_len[l] = 0.
 __device__ __forceinline__ const double* block_in_stats(const sixbit_dit_blocks& B, int l) {
   return l == 0 ? B.in_stats0 : &B.stats[l - 1].max_abs_out;  // {max, sum |x|, count}
 }
 
-__global__ void __launch_bounds__(kStThreads) policy_skip_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l,
-                                                                 unsigned long long cond, int cond_branches,
-                                                                 void* scratch, int32_t* err) {
-  __shared__ int sh_word, sh_k;
-  if (threadIdx.x == 0) {
-    sixbit_policy_state s = B.states[l];
-    const int word = policy_decide(cfg, s, &B.stats[l], block_in_stats(B, l));
-    int k = 0;
-    if (SIXBIT_MODE_OF(word) == SIXBIT_MODE_SKIP && B.covered[l] == 0) {
-      k = 1;
-      for (int j = l + 1; j < B.L; ++j) {
-        sixbit_policy_state sj = B.states[j];
-        if (SIXBIT_MODE_OF(policy_decide(cfg, sj, &B.stats[j], block_in_stats(B, j))) != SIXBIT_MODE_SKIP) break;
-        ++k;
-      }
+__global__ void policy_run_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l, unsigned long long cond,
+                                  int cond_branches, int32_t* err) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  sixbit_policy_state s = B.states[l];
+  const int word = policy_decide(cfg, s, &B.stats[l], block_in_stats(B, l));
+  B.states[l] = s;
+  B.modes[l] = word;
+  const bool is_skip = SIXBIT_MODE_OF(word) == SIXBIT_MODE_SKIP;
+  int branch = SIXBIT_MODE_OF(word) - SIXBIT_MODE_NVFP4;  // compute modes: 0, 1, 2
+  if (B.covered[l] != 0) {
+    if (!is_skip) set_error(err, SIXBIT_EINVAL);  // a covered block must skip
+    B.covered[l] = 0;
+    branch = cond_branches;  // applied by its run: no body
+  } else if (is_skip) {
+    int k = 1;
+    for (int j = l + 1; j < B.L; ++j) {
+      sixbit_policy_state sj = B.states[j];
+      if (SIXBIT_MODE_OF(policy_decide(cfg, sj, &B.stats[j], block_in_stats(B, j))) != SIXBIT_MODE_SKIP) break;
+      B.covered[j] = 1;
+      ++k;
     }
-    sh_word = word;
-    sh_k = k;
+    B.run_len[l] = static_cast<uint32_t>(k);
+    branch = 3;
   }
-  __syncthreads();
-  const int k = sh_k;
+  if (cond != 0)
+    cudaGraphSetConditional(static_cast<cudaGraphConditionalHandle>(cond),
+                            (branch >= 0 && branch < cond_branches) ? static_cast<unsigned int>(branch)
+                                                                    : static_cast<unsigned int>(cond_branches));
+}
+
+__global__ void __launch_bounds__(kStThreads) skip_run_kernel(sixbit_dit_blocks B, int l, void* scratch) {
+  const int k = static_cast<int>(B.run_len[l]);
+  if (k == 0) return;  // uniform across the grid: nothing to apply
+  const uint16_t* __restrict__ x_in = l == 0 ? B.x0 : B.buf[(l - 1) & 1];
+  uint16_t* x_out = B.buf[(l + k - 1) & 1];
+  const uint16_t* __restrict__ d0 = B.deltas + static_cast<size_t>(l) * B.n;
+  const int64_t n8 = B.n >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
   float mx = 0.f;
   Kahan2 sa{0, 0};
-  if (k > 0) {
-    const uint16_t* __restrict__ x_in = l == 0 ? B.x0 : B.buf[(l - 1) & 1];
-    uint16_t* x_out = B.buf[(l + k - 1) & 1];
-    const uint16_t* __restrict__ d0 = B.deltas + static_cast<size_t>(l) * B.n;
-    const int64_t n8 = B.n >> 3;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8; i += stride) {
-      uint64_t v[4];
-      unpack4x2(ld16(x_in + 8 * i), v);
-      uint32_t w[4];
-      const uint16_t* dp = d0 + 8 * i;
-      int j = 0;
-      for (; j + 4 <= k; j += 4) {  // four Delta loads in flight, applied in order
-        uint4 r[4];
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8; i += stride) {
+    uint64_t v[4];
+    unpack4x2(ld16(x_in + 8 * i), v);
+    const uint16_t* dp = d0 + 8 * i;
+    int j = 0;
+    for (; j + 4 <= k; j += 4) {  // four Delta loads in flight, applied in order
+      uint4 r[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) r[u] = ld16(dp + static_cast<size_t>(j + u) * B.n);
+      for (int u = 0; u < 4; ++u) r[u] = ld16(dp + static_cast<size_t>(j + u) * B.n);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint64_t d[4];
-          unpack4x2(r[u], d);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
-        }
-      }
-      for (; j < k; ++j) {
+      for (int u = 0; u < 4; ++u) {
         uint64_t d[4];
-        unpack4x2(ld16(dp + static_cast<size_t>(j) * B.n), d);
+        unpack4x2(r[u], d);
 #pragma unroll
         for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        w[q] = f2_to_bf16x2(v[q]);  // exact: v holds bf16 values
-        mx = f2_max_abs(v[q], mx);
-        kahan_add2(sa, f2_abs(v[q]));
-      }
-      *reinterpret_cast<uint4*>(x_out + 8 * i) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    for (; j < k; ++j) {
+      uint64_t d[4];
+      unpack4x2(ld16(dp + static_cast<size_t>(j) * B.n), d);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      w[q] = f2_to_bf16x2(v[q]);  // exact: v holds bf16 values
+      mx = f2_max_abs(v[q], mx);
+      kahan_add2(sa, f2_abs(v[q]));
+    }
+    *reinterpret_cast<uint4*>(x_out + 8 * i) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   FF v[2] = {FF{mx, 0.f}, to_ff(sa)};
   const bool is_max[2] = {true, false};
   double tot[2];
   if (grid_reduce<2>(v, is_max, scratch_view(scratch), tot)) {
-    sixbit_policy_state s = B.states[l];
-    const int word = policy_decide(cfg, s, &B.stats[l], block_in_stats(B, l));
-    B.states[l] = s;
-    B.modes[l] = word;
-    const bool is_skip = SIXBIT_MODE_OF(word) == SIXBIT_MODE_SKIP;
-    if (B.covered[l] != 0) {
-      if (!is_skip) set_error(err, SIXBIT_EINVAL);  // a covered block must skip
-      B.covered[l] = 0;
-    }
-    if (k > 0) {
-      sixbit_stats* o = &B.stats[l + k - 1];
-      o->max_abs_out = tot[0];
-      o->sum_abs_out = tot[1];
-      o->count = static_cast<double>(B.n);
-      for (int j = l + 1; j < l + k; ++j) B.covered[j] = 1;
-    }
-    if (cond != 0) {
-      const int v = SIXBIT_MODE_OF(word) - SIXBIT_MODE_NVFP4;
-      cudaGraphSetConditional(static_cast<cudaGraphConditionalHandle>(cond),
-                              (v >= 0 && v < cond_branches) ? static_cast<unsigned int>(v)
-                                                            : static_cast<unsigned int>(cond_branches));
-    }
+    sixbit_stats* o = &B.stats[l + k - 1];
+    o->max_abs_out = tot[0];
+    o->sum_abs_out = tot[1];
+    o->count = static_cast<double>(B.n);
+    B.run_len[l] = 0;  // every CTA has read it
   }
 }
 
@@ -619,11 +616,15 @@ cudaError_t launch_skip_apply(const uint16_t* x_in, const uint16_t* delta, uint1
   return cudaGetLastError();
 }
 
-cudaError_t launch_policy_skip(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l,
-                               unsigned long long cond, int cond_branches, void* scratch, int32_t* err,
-                               cudaStream_t st) {
-  policy_skip_kernel<<<stats_grid(policy_skip_kernel, B.n), kStThreads, 0, st>>>(cfg, B, l, cond, cond_branches,
-                                                                                 scratch, err);
+cudaError_t launch_policy_run(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l,
+                              unsigned long long cond, int cond_branches, int32_t* err, cudaStream_t st) {
+  policy_run_kernel<<<1, 32, 0, st>>>(cfg, B, l, cond, cond_branches, err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_skip_run(const sixbit_dit_blocks& B, int l, void* scratch, cudaStream_t st) {
+  skip_run_kernel<<<stats_grid(skip_run_kernel, B.n), kStThreads, 0, st>>>(B, l, scratch);
   note_launch();
   return cudaGetLastError();
 }

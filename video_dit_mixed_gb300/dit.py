@@ -46,9 +46,9 @@ class DiT:
         self.stats = ops.new_stats(dev, blocks)
         self.state = ops.new_policy_state(dev, blocks)
         self.modes = torch.zeros(blocks, dtype=torch.int32, device=dev)
-        self.covered = torch.zeros(blocks, dtype=torch.int32, device=dev)
+        self.marks = torch.zeros((2, blocks), dtype=torch.int32, device=dev)  # covered, run length
         self.scratch = ops.new_scratch(tokens * ffn, dev)
-        self.rec = ops.dit_blocks(self.state, self.stats, self.modes, self.covered, self.tstats, self.x_in,
+        self.rec = ops.dit_blocks(self.state, self.stats, self.modes, self.marks, self.tstats, self.x_in,
                                   self.bufs[0], self.bufs[1], self.deltas)
         self.graph = None
         self.out = self.bufs[(blocks - 1) % 2]
@@ -59,7 +59,7 @@ class DiT:
         self.stats.zero_()
         self.state.zero_()
         self.modes.zero_()
-        self.covered.zero_()
+        self.marks.zero_()
 
     CALLS = ("policy_skip", "hq_x", "qgemm_up", "hq_h", "qgemm_down", "block_stats")
 
@@ -111,20 +111,23 @@ class DiT:
 
     def enqueue_step_switched(self, body_stream):
         """One step for graph capture: per block a SWITCH over the NVFP4 / INT8 /
-        BF16 bodies whose condition the policy kernel sets, so only the chosen
-        body's kernels run (a skip runs none: its work is in the policy kernel)."""
+        BF16 bodies and the skip of a run starting at the block, whose condition
+        the policy kernel sets, so only the chosen body's kernels run (a block
+        covered by an earlier run runs none)."""
         o = ops
         stream = torch.cuda.current_stream()
         o.tensor_stats(self.x_in, self.tstats, self.scratch)
         x = self.x_in
         for l in range(self.L):
             out = self.bufs[l % 2]
-            cond = o.graph_cond_create(stream, 3)
-            o.policy_skip_run(self.cfg, self.rec, l, self.scratch, cond=cond, cond_branches=3)
-            sw = o.GraphSwitch(stream, body_stream, None, o.MODE_NVFP4, 3, cond=cond)
+            cond = o.graph_cond_create(stream, 4)
+            o.policy_skip_run(self.cfg, self.rec, l, None, cond=cond, cond_branches=4)
+            sw = o.GraphSwitch(stream, body_stream, None, o.MODE_NVFP4, 4, cond=cond)
             for i, m in enumerate((o.MODE_NVFP4, o.MODE_INT8, o.MODE_BF16)):
                 with sw.branch(i):
                     self._compute_body(x, out, l, m)
+            with sw.branch(3):
+                o.skip_run(self.rec, l, self.scratch)
             sw.close()
             x = out
         return x

@@ -154,21 +154,28 @@ def policy_step(cfg: PolicyCfg, state: torch.Tensor, last_stats: torch.Tensor, i
     return mode_word
 
 
-def dit_blocks(states, stats, modes, covered, in_stats0, x0, buf0, buf1, deltas) -> DitBlocks:
-    """The sixbit_dit_blocks record of a stack of residual blocks (device tensors; deltas [L, ...])."""
+def dit_blocks(states, stats, modes, marks, in_stats0, x0, buf0, buf1, deltas) -> DitBlocks:
+    """The sixbit_dit_blocks record of a stack of residual blocks (device tensors; deltas [L, ...];
+    marks: int32 [2, L], zeroed: the covered marks and the run lengths)."""
     L = states.shape[0]
     n = x0.numel()
-    assert stats.shape[0] == L and modes.numel() == L and covered.numel() == L and deltas.shape[0] == L
-    assert covered.dtype == torch.int32 and deltas.numel() == L * n
-    return DitBlocks(_p(states), _p(stats), _p(modes), _p(covered), _p(in_stats0), _p(x0),
-                     (C.c_void_p * 2)(buf0.data_ptr(), buf1.data_ptr()), _p(deltas), n, L, 0)
+    assert stats.shape[0] == L and modes.numel() == L and tuple(marks.shape) == (2, L) and deltas.shape[0] == L
+    assert marks.dtype == torch.int32 and marks.is_contiguous() and deltas.numel() == L * n
+    return DitBlocks(_p(states), _p(stats), _p(modes), _p(marks[0]), _p(in_stats0), _p(x0),
+                     (C.c_void_p * 2)(buf0.data_ptr(), buf1.data_ptr()), _p(deltas), _p(marks[1]), n, L, 0)
 
 
-def policy_skip_run(cfg: PolicyCfg, blocks: DitBlocks, l: int, scratch: torch.Tensor, cond: int = 0,
-                    cond_branches: int = 3, err=None, stream=None):
-    """sixbit_policy_skip_run: block l's decision fused with the skips of the run it starts."""
+def policy_skip_run(cfg: PolicyCfg, blocks: DitBlocks, l: int, scratch: torch.Tensor | None, cond: int = 0,
+                    cond_branches: int = 4, err=None, stream=None):
+    """sixbit_policy_skip_run: block l's decision fused with the skips of the run it starts
+    (with `cond`, only the decision; skip_run then belongs in branch 3)."""
     check(_lib.sixbit_policy_skip_run(C.byref(cfg), C.byref(blocks), l, cond, cond_branches, _p(scratch), _p(err),
                                       _stream(stream)), "policy_skip_run")
+
+
+def skip_run(blocks: DitBlocks, l: int, scratch: torch.Tensor, err=None, stream=None):
+    """sixbit_skip_run: apply the run of skips block l's decision recorded (nothing if none)."""
+    check(_lib.sixbit_skip_run(C.byref(blocks), l, _p(scratch), _p(err), _stream(stream)), "skip_run")
 
 
 def graph_cond_create(stream, nbranches: int) -> int:
