@@ -507,8 +507,9 @@ __global__ void policy_run_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, in
 __global__ void __launch_bounds__(kStThreads) skip_run_kernel(sixbit_dit_blocks B, int l, void* scratch) {
   const int k = static_cast<int>(B.run_len[l]);
   if (k == 0) return;  // uniform across the grid: nothing to apply
-  const uint16_t* __restrict__ x_in = l == 0 ? B.x0 : B.buf[(l - 1) & 1];
-  uint16_t* x_out = B.buf[(l + k - 1) & 1];
+  // (selects, not an index into the parameter array: that would copy B to local memory)
+  const uint16_t* __restrict__ x_in = l == 0 ? B.x0 : (((l - 1) & 1) ? B.buf[1] : B.buf[0]);
+  uint16_t* x_out = ((l + k - 1) & 1) ? B.buf[1] : B.buf[0];
   const uint16_t* __restrict__ d0 = B.deltas + static_cast<size_t>(l) * B.n;
   const int64_t n8 = B.n >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
@@ -519,7 +520,19 @@ __global__ void __launch_bounds__(kStThreads) skip_run_kernel(sixbit_dit_blocks 
     unpack4x2(ld16(x_in + 8 * i), v);
     const uint16_t* dp = d0 + 8 * i;
     int j = 0;
-    for (; j + 4 <= k; j += 4) {  // four Delta loads in flight, applied in order
+    for (; j + 8 <= k; j += 8) {  // eight Delta loads in flight, applied in order
+      uint4 r[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) r[u] = ld16(dp + static_cast<size_t>(j + u) * B.n);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint64_t d[4];
+        unpack4x2(r[u], d);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
+      }
+    }
+    if (j + 4 <= k) {
       uint4 r[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) r[u] = ld16(dp + static_cast<size_t>(j + u) * B.n);
@@ -530,6 +543,7 @@ __global__ void __launch_bounds__(kStThreads) skip_run_kernel(sixbit_dit_blocks 
 #pragma unroll
         for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
       }
+      j += 4;
     }
     for (; j < k; ++j) {
       uint64_t d[4];

@@ -181,6 +181,21 @@ class DiT:
             self.enqueue_step()
         return self.out
 
+    def pipeline_init(self):
+        """Allocate step_pipelined's side streams, staging buffers and events (once)."""
+        if getattr(self, "_pipe", None) is not None:
+            return
+        cs = torch.cuda.current_stream()
+        dev = self.x_in.device
+        mk = lambda: [torch.empty_like(self.x_in) for _ in range(2)]  # noqa: E731
+        self._pipe = dict(
+            s_in=torch.cuda.Stream(device=dev), s_out=torch.cuda.Stream(device=dev), stage_in=mk(),
+            stage_out=mk(), k=0,
+            in_ready=[torch.cuda.Event() for _ in range(2)], in_free=[torch.cuda.Event() for _ in range(2)],
+            out_ready=[torch.cuda.Event() for _ in range(2)], out_free=[torch.cuda.Event() for _ in range(2)])
+        for e in self._pipe["in_free"] + self._pipe["out_free"]:
+            e.record(cs)
+
     def step_pipelined(self, x_host: torch.Tensor, out_host: torch.Tensor):
         """One step with its host copies overlapped with the neighbouring steps.
 
@@ -192,16 +207,7 @@ class DiT:
         this step's output.  Nothing here synchronises the host.
         """
         cs = torch.cuda.current_stream()
-        if getattr(self, "_pipe", None) is None:
-            dev = self.x_in.device
-            mk = lambda: [torch.empty_like(self.x_in) for _ in range(2)]  # noqa: E731
-            self._pipe = dict(
-                s_in=torch.cuda.Stream(device=dev), s_out=torch.cuda.Stream(device=dev), stage_in=mk(),
-                stage_out=mk(), k=0,
-                in_ready=[torch.cuda.Event() for _ in range(2)], in_free=[torch.cuda.Event() for _ in range(2)],
-                out_ready=[torch.cuda.Event() for _ in range(2)], out_free=[torch.cuda.Event() for _ in range(2)])
-            for e in self._pipe["in_free"] + self._pipe["out_free"]:
-                e.record(cs)
+        self.pipeline_init()
         P = self._pipe
         i = P["k"] % 2
         P["s_in"].wait_event(P["in_free"][i])           # stage_in[i] consumed two steps ago
