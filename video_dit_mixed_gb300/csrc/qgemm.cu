@@ -93,6 +93,7 @@ __host__ __device__ constexpr int stage_bytes() {
 // shared-memory ring, fetched kSwRing - 1 groups ahead (an L2 round trip
 // per group would otherwise pace the fold).
 constexpr int kSwRing = 4;
+constexpr int kMaxBufs = 4;  // accumulator buffers the barrier area has room for
 
 template <int KIND, bool GROUPED>
 __host__ __device__ constexpr int gemm_smem_bytes() {
@@ -214,11 +215,13 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * stage_bytes<KIND>());
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
-  uint64_t* accf = bars + 2 * S;      // [2] accumulator buffer ready
-  uint64_t* acce = bars + 2 * S + 2;  // [2] accumulator buffer drained
-  uint64_t* drain = bars + 2 * S + 4;
-  uint64_t* sf_full = bars + 2 * S + 5;  // NVFP4: [S] the stage's scale factors are in tensor memory
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
+  uint64_t* accf = bars + 2 * S;                    // [kBufs] accumulator buffer ready
+  uint64_t* acce = bars + 2 * S + kMaxBufs;         // [kBufs] accumulator buffer drained
+  uint64_t* drain = bars + 2 * S + 2 * kMaxBufs;
+  uint64_t* sf_full = drain + 1;                    // NVFP4: [S] the stage's scale factors are in tensor memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + S);
+  static_assert((3 * S + 2 * kMaxBufs + 1) * 8 + 8 <= 256, "barrier area");
+  static_assert(kBufs <= kMaxBufs && kBufs * kBN + (kNvf4 ? S * 64 : 0) <= kCols, "tensor memory");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sw_smem = reinterpret_cast<float*>(smem + S * stage_bytes<KIND>() + 256);  // GROUPED: per-warp scales
 
@@ -252,10 +255,10 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(&accf[0], 1);
-    mbar_init(&accf[1], 1);
-    mbar_init(&acce[0], kEpiWarps);
-    mbar_init(&acce[1], kEpiWarps);
+    for (uint32_t b = 0; b < kBufs; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], kEpiWarps);
+    }
     mbar_init(drain, 1);
     if constexpr (kNvf4)
       for (int s = 0; s < S; ++s) mbar_init(&sf_full[s], 1);
@@ -395,8 +398,8 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
       if (nb >= p.N) {                            // nothing of this half exists (ragged N)
         if constexpr (GROUPED) {
           for (int g = 0; g < groups && ok; ++g, ++ac) {
-            const uint32_t buf = ac & 1;
-            if (!mbar_wait(&accf[buf], (ac >> 1) & 1, abort_flag)) { ok = false; break; }
+            const uint32_t buf = ac % kBufs;
+            if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) { ok = false; break; }
             release_acc(&acce[buf], lane);
           }
         } else {
@@ -426,8 +429,8 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
           fetch_sw(g + kSwRing - 1);               // ... which now receives group g + kSwRing - 1
           cp_async_wait_newest<kSwRing - 1>();     // this lane's copy of group g has landed
           __syncwarp();                            // and every other lane's
-          const uint32_t buf = ac & 1;
-          if (!mbar_wait(&accf[buf], (ac >> 1) & 1, abort_flag)) {
+          const uint32_t buf = ac % kBufs;
+          if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) {
             ok = false;
             break;
           }
