@@ -45,6 +45,20 @@ sys.path.insert(0, ROOT)
 
 METRIC = "W4A4/W4A8 qGEMM TFLOPS+%peak; Hadamard-quant GB/s; MLP-DiT step/s"
 FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio (FP4 13.5 PFLOP/s, BF16 2.25 PFLOP/s)
+
+# DRAM bytes (read + write) per launch from one ncu capture of the same kernels
+# on the same shapes (profiles/dram_traffic_dit_2b.md); an entry must be
+# removed when its kernel changes.
+MEASURED_TRAFFIC = {
+    ("dit_2b", "qgemm_up:int8"): 324860416,
+    ("dit_2b", "qgemm_down:int8"): 585031680,
+    ("dit_2b", "hq_x:int8"): 87123712,
+    ("dit_2b", "hq_h:int8"): 495252992,
+    ("dit_2b", "block_stats:int8"): 243543552,
+    ("dit_2b", "qgemm_up:bf16"): 322869504,
+    ("dit_2b", "qgemm_down:bf16"): 530436096,
+    ("dit_2b", "block_stats:bf16"): 243864064,
+}
 MODE_NAMES = {1: "nvfp4", 2: "int8", 3: "bf16", 4: "skip"}
 
 
@@ -321,55 +335,83 @@ class DitStep:
         return n
 
     def profile(self, k, stream):
-        """Eager pass over a full trajectory: event pairs around every call, attributed to the block's mode.
+        """Per-call device times over a full trajectory, with the kernels a graph step runs.
 
-        Eager launches of the kernels whose mode is not the block's return at
-        once (a few microseconds each); the CUDA-graph steps timed above do not
-        launch them at all.
+        Each block is dispatched on the host from its mode word (the kernels of
+        the switched graph, minus nothing but the branch selection); CUDA
+        events on the launching stream bracket every call.  Before each group
+        of calls a GPU-side pause lets the host enqueue them ahead of the GPU,
+        so the events bracket device work, not launch gaps.
         """
+        import numpy as np
         T = self.t
         m = self.model
+        o = self.ops
         m.reset()
         self.s = 0
-        recs = []
-        modes = T.zeros((self.c["steps"], self.L), dtype=T.int32, device=self.dev)
-        for s in range(self.c["steps"]):
-            # a GPU-side pause lets the host enqueue the whole step before the GPU
-            # reaches it, so the event pairs bracket device work, not launch gaps
-            T.cuda.synchronize()
-            T.cuda._sleep(int(40e6))
-            m.x_in.copy_(self.traj[s])
-            evs = []
-            e0 = T.cuda.Event(enable_timing=True)
-            e0.record(stream)
+        pause = int(4e5)          # ~0.2 ms of GPU cycles: covers the host's enqueue of a group of calls
+        recs = []                 # (key, start event, end event)
+        run_bytes = []
+        mh = np.zeros((self.c["steps"], self.L), dtype=np.int64)
 
-            def note(label, block, evs=evs):
-                e = T.cuda.Event(enable_timing=True)
-                e.record(stream)
-                evs.append((label, block, e))
-            m.enqueue_step(after_call=note)
-            modes[s].copy_(m.modes)
-            recs.append((e0, evs))
+        def timed(key, fn):
+            a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            recs.append((key, a, b))
+
+        for s in range(self.c["steps"]):
+            m.x_in.copy_(self.traj[s])
+            T.cuda.synchronize()
+            T.cuda._sleep(pause)
+            timed("tensor_stats", lambda: o.tensor_stats(m.x_in, m.tstats, m.scratch))
+            x = m.x_in
+            for l in range(self.L):
+                out = m.bufs[l % 2]
+                T.cuda.synchronize()
+                T.cuda._sleep(pause)
+                a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+                a.record(stream)
+                o.policy_skip_run(m.cfg, m.rec, l, m.scratch)    # decision (+ the run it starts)
+                b.record(stream)
+                word = int(m.modes[l].item())                  # synchronises
+                mh[s, l] = word
+                mode = word & 0xFF
+                if mode == 4:
+                    if l > 0 and (mh[s, l - 1] & 0xFF) == 4:
+                        recs.append(("policy_skip:covered", a, b))
+                    else:                                      # a run start (its length: from the log)
+                        recs.append(("skip_run", a, b))
+                        run_bytes.append((s, l))
+                else:
+                    recs.append((f"policy_skip:{MODE_NAMES.get(mode, '?')}", a, b))
+                    T.cuda._sleep(pause)
+                    last = [a]
+
+                    def note(label, last=last, mode=mode):
+                        e = T.cuda.Event(enable_timing=True)
+                        e.record(stream)
+                        recs.append((f"{label}:{MODE_NAMES.get(mode, '?')}", last[0], e))
+                        last[0] = e
+                    b2 = T.cuda.Event(enable_timing=True)
+                    b2.record(stream)
+                    last[0] = b2
+                    m._compute_body(x, out, l, mode, note=note)
+                x = out
         T.cuda.synchronize()
-        mh = modes.cpu().numpy()
         low = mh & 0xFF
         per = {}
-        run_bytes = []
-        for s, (e0, evs) in enumerate(recs):
-            prev = e0
-            for label, block, e in evs:
-                key = label if block < 0 else f"{label}:{MODE_NAMES.get(int(mh[s, block]) & 0xFF, '?')}"
-                if label == "policy_skip" and low[s, block] == 4:
-                    if block > 0 and low[s, block - 1] == 4:
-                        key = "policy_skip:covered"      # applied by the run that started earlier
-                    else:                                # a run start: reads x and k deltas, writes x
-                        k = 1
-                        while block + k < self.L and low[s, block + k] == 4:
-                            k += 1
-                        key = "skip_run"
-                        run_bytes.append((4 + 2 * k) * self.T * self.H)
-                per.setdefault(key, []).append(prev.elapsed_time(e))
-                prev = e
+        for key, a, b in recs:
+            per.setdefault(key, []).append(a.elapsed_time(b))
+        # bytes of each run start: x read, k deltas read, x written
+        sizes = []
+        for s, l in run_bytes:
+            k = 1
+            while l + k < self.L and low[s, l + k] == 4:
+                k += 1
+            sizes.append((4 + 2 * k) * self.T * self.H)
+        run_bytes = sizes
         self.skip_run_bytes = (sum(run_bytes) / len(run_bytes)) if run_bytes else 0
         self.mode_log = mh
         m.reset()
@@ -553,12 +595,13 @@ def _roofline(wl, per, peaks):
         pk = peaks["bf16"] * (FP4_OVER_BF16 if fp4 else 1.0)
         ach = work / avg / 1e12
         roof = dict(bound="tensor", kernel=dom, achieved=round(ach, 1), peak=round(pk, 1), unit="TFLOP/s",
-                    frac=round(ach / pk, 4), traffic=None, work_per_launch=work,
+                    frac=round(ach / pk, 4), traffic=MEASURED_TRAFFIC.get((wl.name, dom)), work_per_launch=work,
                     peak_source=f"{peaks['src']} bf16 burst" + (" x6 nominal fp4/bf16" if fp4 else ""))
     else:
         ach = work / avg / 1e9
         roof = dict(bound="hbm", kernel=dom, achieved=round(ach, 1), peak=peaks["hbm"], unit="GB/s",
-                    frac=round(ach / peaks["hbm"], 4), traffic=None, work_per_launch=work,
+                    frac=round(ach / peaks["hbm"], 4), traffic=MEASURED_TRAFFIC.get((wl.name, dom)),
+                    work_per_launch=work,
                     peak_source=f"{peaks['src']} copy")
     return roof, table
 

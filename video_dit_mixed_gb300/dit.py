@@ -95,19 +95,26 @@ class DiT:
             x = out
         return x
 
-    def _compute_body(self, x, out, l, mode):
-        """The kernels of one computed block in a fixed mode (no mode word)."""
+    def _compute_body(self, x, out, l, mode, note=None):
+        """The kernels of one computed block in a fixed mode (no mode word);
+        note(label) is called on the host after each call when given."""
         o = ops
+        note = note or (lambda label: None)
         up, down = self.packed[l]
         quant = mode != o.MODE_BF16
         if quant:
             o.hadamard_quant(x, self.b, mode, out=self.qa_x)
+            note("hq_x")
         o.qgemm(self.qa_x if quant else None, x, up, mode, epilogue=o.EPI_GELU, out=self.h, m=self.T)
+        note("qgemm_up")
         if quant:
             o.hadamard_quant(self.h, self.b, mode, out=self.qa_h)
+            note("hq_h")
         o.qgemm(self.qa_h if quant else None, self.h, down, mode, epilogue=o.EPI_RESIDUAL, residual=x, out=out,
                 m=self.T)
+        note("qgemm_down")
         o.block_stats(x, out, self.deltas[l], self.stats[l], self.scratch)
+        note("block_stats")
 
     def enqueue_step_switched(self, body_stream):
         """One step for graph capture: per block a SWITCH over the NVFP4 / INT8 /
