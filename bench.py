@@ -83,10 +83,13 @@ class Clocks:
         self.proc = None
 
     def start(self):
+        """Starts sampling every 50 ms; returns once the first sample (taken before the timed
+        region, and dropped) has been printed, so the sampler is running when timing starts."""
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc.stdout.readline()
         except OSError:
             self.proc = None
 
