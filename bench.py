@@ -318,10 +318,10 @@ class DitStep:
         return [a.elapsed_time(b) for a, b in pairs], None
 
     # kernels one block runs per decision inside the switched graph: NVFP4
-    # (amax + quant for x and h, two GEMMs, stats), INT8, BF16, SKIP (one
+    # (amax + quant for x and h, two GEMMs, block end), INT8, BF16, SKIP (one
     # kernel applying the run when the block starts one, none when an earlier
-    # run covered it); every block also runs the one-thread policy kernel,
-    # which sets the graph's branch condition
+    # run covered it); the decisions run at the tails of these kernels and of
+    # the step's first kernel
     BODY_KERNELS = {1: 7, 2: 5, 3: 3, 4: 0}
 
     def launches(self):
@@ -333,7 +333,7 @@ class DitStep:
         n = 0
         for s in self.timed_steps:
             row = [int(v) for v in low[s]]
-            n += 1 + sum(1 + self.BODY_KERNELS.get(v, 0) for v in row)
+            n += 1 + sum(self.BODY_KERNELS.get(v, 0) for v in row)
             n += sum(1 for l, v in enumerate(row) if v == 4 and (l == 0 or row[l - 1] != 4))  # run starts
         return n
 
@@ -368,29 +368,21 @@ class DitStep:
             m.x_in.copy_(self.traj[s])
             T.cuda.synchronize()
             T.cuda._sleep(pause)
-            timed("tensor_stats", lambda: o.tensor_stats(m.x_in, m.tstats, m.scratch))
+            timed("tensor_stats", lambda: o.dit_begin(m.cfg, m.rec, m.scratch))   # + block 0's decision
             x = m.x_in
             for l in range(self.L):
                 out = m.bufs[l % 2]
-                T.cuda.synchronize()
-                T.cuda._sleep(pause)
-                a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
-                a.record(stream)
-                o.policy_skip_run(m.cfg, m.rec, l, m.scratch)    # decision (+ the run it starts)
-                b.record(stream)
                 word = int(m.modes[l].item())                  # synchronises
                 mh[s, l] = word
                 mode = word & 0xFF
                 if mode == 4:
-                    if l > 0 and (mh[s, l - 1] & 0xFF) == 4:
-                        recs.append(("policy_skip:covered", a, b))
-                    else:                                      # a run start (its length: from the log)
-                        recs.append(("skip_run", a, b))
+                    if l == 0 or (mh[s, l - 1] & 0xFF) != 4:    # a run starts here (its length: from the log)
+                        T.cuda._sleep(pause)
+                        timed("skip_run", lambda l=l: o.dit_skip_run(m.cfg, m.rec, l, m.scratch))
                         run_bytes.append((s, l))
                 else:
-                    recs.append((f"policy_skip:{MODE_NAMES.get(mode, '?')}", a, b))
                     T.cuda._sleep(pause)
-                    last = [a]
+                    last = [None]
 
                     def note(label, last=last, mode=mode):
                         e = T.cuda.Event(enable_timing=True)

@@ -257,8 +257,11 @@ sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_sta
  *   states [L], stats [L], modes [L]  as for sixbit_policy_step, one per block
  *   covered [L], run_len [L] uint32, zero before the first step (the
  *               library leaves them zero between steps)
- *   in_stats0   {max |x0|, sum |x0|, count} of the step input (float64)
+ *   in_stats0   [4] float64, written by sixbit_dit_begin: {max |x0|,
+ *               sum |x0|, count, sum x0^2}
  *   x0 [n], buf[0], buf[1] [n] bf16; deltas [L][n] bf16, the Delta cache
+ *   conds       NULL, or [L] conditional handles (sixbit_graph_cond_create)
+ *               of the per-block switches of a captured graph
  * n % 8 == 0; 16-byte aligned tensors.
  */
 typedef struct {
@@ -266,49 +269,55 @@ typedef struct {
   sixbit_stats* stats;
   int32_t* modes;
   uint32_t* covered;
-  const double* in_stats0;
+  double* in_stats0;
   const uint16_t* x0;
   uint16_t* buf[2];
-  const uint16_t* deltas;
+  uint16_t* deltas;
   uint32_t* run_len;
+  const uint64_t* conds;
   int64_t n;
   int32_t L;
   int32_t reserved;
 } sixbit_dit_blocks;
 
 /*
- * sixbit_policy_step for block l (input statistics taken from stats[l-1],
- * or in_stats0 for l = 0; decision to modes[l]) fused with the TDC skip
- * (technical summary section 2.B; popular summary section 2) of every block
- * it starts a run of.  A skip depends only on the block's own state, so when
- * block l skips, the consecutive blocks l+1 .. l+k-1 that will also skip at
- * this step are known; their skips are applied in one pass:
- * x_{l+k-1} = bf16(...bf16(x_{l-1} + Delta_l)... + Delta_{l+k-1}) into
- * buf[(l+k-1) % 2], its {max |x|, sum |x|, count} into
- * stats[l+k-1].{max_abs_out, sum_abs_out, count}, and blocks l+1 .. l+k-1
- * marked covered: their own calls then only make (and record) their
- * decision.  Results are bit-identical to one sixbit_policy_step +
- * sixbit_skip_apply per block; the skipped intermediate activations are not
- * written.  Call once per block, in order, every step.
- * With cond_handle == 0 the call enqueues the decision and then the run's
- * skip (which does nothing unless block l starts a run).  With a handle
- * from sixbit_graph_cond_create (the call is being captured into that
- * graph) it enqueues only the decision, which sets the condition to
- * mode - SIXBIT_MODE_NVFP4 for a compute (0, 1, 2), 3 for a run start and
- * cond_branches (no body) for a covered block or a value out of range; the
- * caller puts sixbit_skip_run for block l in branch 3 of a switch with 4
- * branches.  scratch as for sixbit_block_stats (unused with a handle).
- * cfg is a HOST pointer.  A covered block whose decision is not a skip
- * (impossible unless the state was changed in between) records
- * SIXBIT_EINVAL in err_dev.
+ * One denoising step of the stack (technical summary sections 2.A-2.C;
+ * popular summary sections 1-3), with every per-block decision taken on the
+ * device at the tail of the kernel that produces the statistics it needs:
+ *   sixbit_dit_begin      statistics of x0, then block 0's decision;
+ *   sixbit_dit_block_end  for a block l that computed (its mode word is not
+ *                         SKIP): sixbit_block_stats of x_{l-1}, x_l and
+ *                         Delta_l into stats[l], then block l+1's decision;
+ *                         nothing for a skipped block;
+ *   sixbit_dit_skip_run   for a block l that starts a run of k skipping
+ *                         blocks: their TDC skips in one pass,
+ *                         x_{l+k-1} = bf16(...bf16(x_{l-1} + Delta_l)... +
+ *                         Delta_{l+k-1}) into buf[(l+k-1) % 2] with its
+ *                         {max |x|, sum |x|, count} into stats[l+k-1], then
+ *                         the decisions of l+1 .. l+k; nothing otherwise.
+ * A decision is sixbit_policy_step's (input statistics from stats[l-1], or
+ * in_stats0 for l = 0; the word to modes[l]).  A skip depends only on the
+ * block's own state, never on its input, so when block l skips, the blocks
+ * l+1 .. l+k-1 that will also skip are known: the decision records k in
+ * run_len[l] and marks them covered (their decisions, taken by the run, only
+ * clear the mark).  Results are bit-identical to one policy step + one skip
+ * (or the block's compute + block statistics) per block; the skipped
+ * intermediate activations are not written.  With conds, each decision also
+ * sets conds[l]: 0, 1, 2 for NVFP4, INT8, BF16 (the compute bodies, each
+ * ending with sixbit_dit_block_end), 3 for a run start (sixbit_dit_skip_run)
+ * and 4 (no body) for a covered block.  Eager use: after sixbit_dit_begin,
+ * per block the mode-gated compute calls, sixbit_dit_block_end and
+ * sixbit_dit_skip_run (each a no-op when it does not apply).  scratch as for
+ * sixbit_block_stats.  cfg is a HOST pointer.  A covered block whose
+ * decision is not a skip (impossible unless a state was changed in between)
+ * records SIXBIT_EINVAL in err_dev.
  */
-sixbit_status sixbit_policy_skip_run(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
-                                     uint64_t cond_handle, int cond_branches, void* scratch, int32_t* err_dev,
-                                     void* stream);
-/* The skip of the run block l starts, as recorded by its sixbit_policy_skip_run
- * decision (returns at once on the device when block l starts no run). */
-sixbit_status sixbit_skip_run(const sixbit_dit_blocks* blocks, int l, void* scratch, int32_t* err_dev,
-                              void* stream);
+sixbit_status sixbit_dit_begin(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, void* scratch,
+                               int32_t* err_dev, void* stream);
+sixbit_status sixbit_dit_block_end(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
+                                   void* scratch, int32_t* err_dev, void* stream);
+sixbit_status sixbit_dit_skip_run(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
+                                  void* scratch, int32_t* err_dev, void* stream);
 
 /* ---- companions of the hot path ---------------------------------------- */
 
@@ -371,8 +380,8 @@ sixbit_status sixbit_graph_switch_begin(void* stream, void* body_stream, const i
                                         int nbranches, sixbit_switch** sw);
 /*
  * The same SWITCH node without the selector kernel: the condition is set by
- * a kernel captured before it (sixbit_policy_skip_run with this handle).
- * sixbit_graph_cond_create makes the handle in the graph `stream` is
+ * kernels captured before it (the sixbit_dit_* calls, through the blocks'
+ * conds).  sixbit_graph_cond_create makes a handle in the graph `stream` is
  * capturing (its value defaults to "no body" at every graph launch);
  * sixbit_graph_switch_begin_cond appends the node.
  */

@@ -45,8 +45,8 @@ class PolicyState(C.Structure):
 
 class DitBlocks(C.Structure):
     _fields_ = [("states", c_p), ("stats", c_p), ("modes", c_p), ("covered", c_p), ("in_stats0", c_p),
-                ("x0", c_p), ("buf", c_p * 2), ("deltas", c_p), ("run_len", c_p), ("n", C.c_int64),
-                ("L", C.c_int32),
+                ("x0", c_p), ("buf", c_p * 2), ("deltas", c_p), ("run_len", c_p), ("conds", c_p),
+                ("n", C.c_int64), ("L", C.c_int32),
                 ("reserved", C.c_int32)]
 
 
@@ -65,9 +65,9 @@ EXPORTS = {
     "sixbit_skip_apply": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),
     "sixbit_block_stats_noalloc": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p]),
     "sixbit_block_stats_noalloc_max_elems": (C.c_int64, []),
-    "sixbit_policy_skip_run": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), C.c_int, C.c_uint64, C.c_int,
-                                         c_p, c_p, c_p]),
-    "sixbit_skip_run": (C.c_int, [C.POINTER(DitBlocks), C.c_int, c_p, c_p, c_p]),
+    "sixbit_dit_begin": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), c_p, c_p, c_p]),
+    "sixbit_dit_block_end": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), C.c_int, c_p, c_p, c_p]),
+    "sixbit_dit_skip_run": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), C.c_int, c_p, c_p, c_p]),
     "sixbit_graph_switch_begin": (C.c_int, [c_p, c_p, c_p, C.c_int, C.c_int, C.POINTER(c_p)]),
     "sixbit_graph_cond_create": (C.c_int, [c_p, C.c_int, C.POINTER(C.c_uint64)]),
     "sixbit_graph_switch_begin_cond": (C.c_int, [c_p, c_p, C.c_uint64, C.c_int, C.POINTER(c_p)]),

@@ -302,47 +302,40 @@ sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_sta
       launch_policy(*cfg, state_dev, last_stats_dev, in_stats_dev, mode_dev, static_cast<cudaStream_t>(stream)));
 }
 
-static sixbit_status check_blocks(const sixbit_dit_blocks* blocks, int l) {
-  if (blocks == nullptr) return SIXBIT_EINVAL;
+static sixbit_status check_blocks(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
+                                  void* scratch) {
+  if (cfg == nullptr || blocks == nullptr || scratch == nullptr) return SIXBIT_EINVAL;
   const sixbit_dit_blocks& B = *blocks;
   if (B.states == nullptr || B.stats == nullptr || B.modes == nullptr || B.covered == nullptr ||
       B.run_len == nullptr || B.in_stats0 == nullptr || B.x0 == nullptr || B.buf[0] == nullptr ||
       B.buf[1] == nullptr || B.deltas == nullptr)
     return SIXBIT_EINVAL;
   if (B.L <= 0 || l < 0 || l >= B.L || B.n <= 0 || B.n % 8 != 0) return SIXBIT_ESHAPE;
-  if (!aligned16(B.x0) || !aligned16(B.buf[0]) || !aligned16(B.buf[1]) || !aligned16(B.deltas))
+  if (!aligned16(B.x0) || !aligned16(B.buf[0]) || !aligned16(B.buf[1]) || !aligned16(B.deltas) ||
+      !aligned16(scratch))
     return SIXBIT_EALIGN;
-  return SIXBIT_OK;
+  return check_device();
 }
 
-sixbit_status sixbit_policy_skip_run(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
-                                     uint64_t cond_handle, int cond_branches, void* scratch, int32_t* err_dev,
-                                     void* stream) {
-  if (cfg == nullptr) return SIXBIT_EINVAL;
-  sixbit_status s = check_blocks(blocks, l);
+sixbit_status sixbit_dit_begin(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, void* scratch,
+                               int32_t* err_dev, void* stream) {
+  const sixbit_status s = check_blocks(cfg, blocks, 0, scratch);
   if (s != SIXBIT_OK) return s;
-  if (cond_branches < 0 || cond_branches > 8) return SIXBIT_ESHAPE;
-  if (cond_handle == 0 && (scratch == nullptr || !aligned16(scratch))) return scratch ? SIXBIT_EALIGN : SIXBIT_EINVAL;
-  s = check_device();
-  if (s != SIXBIT_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_policy_run(*cfg, *blocks, l, static_cast<unsigned long long>(cond_handle), cond_branches, err_dev,
-                        st) != cudaSuccess)
-    return SIXBIT_ECUDA;
-  if (cond_handle != 0) return SIXBIT_OK;  // the run is applied by sixbit_skip_run in branch 3
-  return cuda_status(launch_skip_run(*blocks, l, scratch, st));
+  return cuda_status(launch_dit_begin(*cfg, *blocks, scratch, err_dev, static_cast<cudaStream_t>(stream)));
 }
 
-sixbit_status sixbit_skip_run(const sixbit_dit_blocks* blocks, int l, void* scratch, int32_t* err_dev,
-                              void* stream) {
-  (void)err_dev;
-  sixbit_status s = check_blocks(blocks, l);
+sixbit_status sixbit_dit_block_end(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
+                                   void* scratch, int32_t* err_dev, void* stream) {
+  const sixbit_status s = check_blocks(cfg, blocks, l, scratch);
   if (s != SIXBIT_OK) return s;
-  if (scratch == nullptr) return SIXBIT_EINVAL;
-  if (!aligned16(scratch)) return SIXBIT_EALIGN;
-  s = check_device();
+  return cuda_status(launch_dit_block_end(*cfg, *blocks, l, scratch, err_dev, static_cast<cudaStream_t>(stream)));
+}
+
+sixbit_status sixbit_dit_skip_run(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
+                                  void* scratch, int32_t* err_dev, void* stream) {
+  const sixbit_status s = check_blocks(cfg, blocks, l, scratch);
   if (s != SIXBIT_OK) return s;
-  return cuda_status(launch_skip_run(*blocks, l, scratch, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_dit_skip_run(*cfg, *blocks, l, scratch, err_dev, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

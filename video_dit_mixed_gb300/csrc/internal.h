@@ -47,9 +47,12 @@ cudaError_t launch_block_stats_fixed_grid(const uint16_t* x_in, const uint16_t* 
                                           cudaStream_t st);
 cudaError_t launch_skip_apply(const uint16_t* x_in, const uint16_t* delta, uint16_t* x_out, int64_t n,
                               const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st);
-cudaError_t launch_policy_run(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l,
-                              unsigned long long cond, int cond_branches, int32_t* err, cudaStream_t st);
-cudaError_t launch_skip_run(const sixbit_dit_blocks& B, int l, void* scratch, cudaStream_t st);
+cudaError_t launch_dit_begin(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, void* scratch, int32_t* err,
+                             cudaStream_t st);
+cudaError_t launch_dit_block_end(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, void* scratch,
+                                 int32_t* err, cudaStream_t st);
+cudaError_t launch_dit_skip_run(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, void* scratch,
+                                int32_t* err, cudaStream_t st);
 cudaError_t launch_policy(const sixbit_policy_cfg& cfg, sixbit_policy_state* st_dev, const sixbit_stats* last,
                           const double* in_stats, int32_t* mode_out, cudaStream_t st);
 

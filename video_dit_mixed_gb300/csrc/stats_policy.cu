@@ -226,9 +226,9 @@ __device__ __forceinline__ void tensor_stats_vec(const uint4& r, float& mx, Kaha
   }
 }
 
-// out[0..3] = {max |x|, sum |x|, count, sum x^2}
-__global__ void __launch_bounds__(kStThreads) tensor_stats_kernel(const uint16_t* __restrict__ x, int64_t n,
-                                                                  double* out, void* scratch) {
+// Grid-wide {max |x|, sum |x|, sum x^2} of x[0..n); true in one thread of
+// the last CTA, with the totals in tot.
+__device__ bool tensor_stats_body(const uint16_t* __restrict__ x, int64_t n, void* scratch, double (&tot)[3]) {
   const int64_t n8 = n >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
   float mx = 0.f;
@@ -242,8 +242,14 @@ __global__ void __launch_bounds__(kStThreads) tensor_stats_kernel(const uint16_t
   }
   FF v[3] = {FF{mx, 0.f}, to_ff(sa), to_ff(sq)};
   const bool is_max[3] = {true, false, false};
+  return grid_reduce<3>(v, is_max, scratch_view(scratch), tot);
+}
+
+// out[0..3] = {max |x|, sum |x|, count, sum x^2}
+__global__ void __launch_bounds__(kStThreads) tensor_stats_kernel(const uint16_t* __restrict__ x, int64_t n,
+                                                                  double* out, void* scratch) {
   double tot[3];
-  if (grid_reduce<3>(v, is_max, scratch_view(scratch), tot)) {
+  if (tensor_stats_body(x, n, scratch, tot)) {
     out[0] = tot[0];
     out[1] = tot[1];
     out[2] = static_cast<double>(n);
@@ -272,11 +278,11 @@ __device__ __forceinline__ uint4 block_stats_vec(const uint4& ra, const uint4& r
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__global__ void __launch_bounds__(kStThreads) block_stats_kernel(const uint16_t* __restrict__ x_in,
-                                                                 const uint16_t* __restrict__ x_out,
-                                                                 uint16_t* delta, int64_t n, const int32_t* mode_dev,
-                                                                 sixbit_stats* stats, void* scratch) {
-  if (mode_is(mode_dev, SIXBIT_MODE_SKIP)) return;
+// One pass over x_in, x_out, Delta_prev: writes Delta_new over Delta_prev and
+// reduces {sum Delta^2, sum x_in^2, sum Delta*Delta_prev, sum Delta_prev^2,
+// max |x_out|, sum |x_out|}; true in one thread of the last CTA.
+__device__ bool block_stats_body(const uint16_t* __restrict__ x_in, const uint16_t* __restrict__ x_out,
+                                 uint16_t* delta, int64_t n, void* scratch, double (&tot)[6]) {
   const int64_t n8 = n >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
   float mx = 0.f;
@@ -299,16 +305,26 @@ __global__ void __launch_bounds__(kStThreads) block_stats_kernel(const uint16_t*
   }
   FF v[6] = {to_ff(d2), to_ff(xi2), to_ff(ddp), to_ff(dp2), FF{mx, 0.f}, to_ff(sa)};
   const bool is_max[6] = {false, false, false, false, true, false};
+  return grid_reduce<6>(v, is_max, scratch_view(scratch), tot);
+}
+
+__device__ __forceinline__ void write_block_stats(sixbit_stats* stats, const double (&tot)[6], int64_t n) {
+  stats->sum_d2 = tot[0];
+  stats->sum_xin2 = tot[1];
+  stats->sum_ddp = tot[2];
+  stats->sum_dp2 = tot[3];
+  stats->max_abs_out = tot[4];
+  stats->sum_abs_out = tot[5];
+  stats->count = static_cast<double>(n);
+}
+
+__global__ void __launch_bounds__(kStThreads) block_stats_kernel(const uint16_t* __restrict__ x_in,
+                                                                 const uint16_t* __restrict__ x_out,
+                                                                 uint16_t* delta, int64_t n, const int32_t* mode_dev,
+                                                                 sixbit_stats* stats, void* scratch) {
+  if (mode_is(mode_dev, SIXBIT_MODE_SKIP)) return;
   double tot[6];
-  if (grid_reduce<6>(v, is_max, scratch_view(scratch), tot)) {
-    stats->sum_d2 = tot[0];
-    stats->sum_xin2 = tot[1];
-    stats->sum_ddp = tot[2];
-    stats->sum_dp2 = tot[3];
-    stats->max_abs_out = tot[4];
-    stats->sum_abs_out = tot[5];
-    stats->count = static_cast<double>(n);
-  }
+  if (block_stats_body(x_in, x_out, delta, n, scratch, tot)) write_block_stats(stats, tot, n);
 }
 
 __device__ __forceinline__ uint4 skip_vec(const uint4& ra, const uint4& rd, float& mx, Kahan2& sa) {
@@ -450,33 +466,34 @@ __global__ void policy_kernel(sixbit_policy_cfg cfg, sixbit_policy_state* st, co
   *mode_out = word;
 }
 
-// ------------------------------------------------ policy + TDC skip runs --
+// ----------------------------------------------- the DiT step protocol --
 //
-// The decision of block l and, when it starts a run of consecutive blocks
-// l, l+1, ..., l+k-1 that all skip at this step, the skip of the whole run in
-// one pass.  A skip decision depends only on the block's own state (cos, acc,
-// number of computes) and on the statistics of its last compute, never on
-// its input, so when block l skips, the decisions of the blocks after it are
-// already fixed and the run is found by evaluating policy_decide on copies
-// of their states.
-//
-// policy_run_kernel (one thread) decides block l, records its state and mode
-// word, and for a run start stores k in run_len[l] and marks blocks
-// l+1 .. l+k-1 covered (their own decisions then only clear the mark); it
-// sets the graph condition: compute modes to their branch, a run start to
-// branch 3 (when the switch has one), a covered block to no branch.
-// skip_run_kernel applies the run:
-// x_{l+k-1} = bf16(... bf16(bf16(x_{l-1} + D_l) + D_{l+1}) ... + D_{l+k-1})
-// (the same roundings as k separate skips; the intermediate activations are
-// never read, so they are not written), with its {max, sum |x|, count} into
-// stats[l+k-1], and clears run_len[l]; it returns at once when run_len[l] = 0.
+// Per step, block l's decision needs the statistics of its input, which the
+// last kernel before it produces; so every decision is taken at the tail of
+// that kernel, by the thread that holds the totals:
+//   dit_begin_kernel     statistics of x0, then the decision of block 0;
+//   dit_block_end_kernel block statistics + Delta update of a computed block
+//                        l, then the decision of block l+1;
+//   dit_skip_run_kernel  the skip of the run of blocks l .. l+k-1 that block
+//                        l starts, then the decisions of l+1 .. l+k.
+// A skip decision depends only on the block's own state (cos, acc, number of
+// computes) and the statistics of its last compute, never on its input, so
+// when block l skips, the run of blocks that will skip after it is already
+// fixed: decide_block finds it by evaluating policy_decide on copies of
+// their states, records k in run_len[l] and marks l+1 .. l+k-1 covered.  The
+// run's output x_{l+k-1} = bf16(... bf16(bf16(x_{l-1} + D_l) + D_{l+1}) ... +
+// D_{l+k-1}) is written in one pass (the same roundings as k separate skips;
+// the intermediate activations are never read, so they are not written),
+// with its {max, sum |x|, count} into stats[l+k-1].  Each decision also sets
+// the block's graph condition when a handle array is given: a compute mode
+// to its body (0, 1, 2), a run start to 3, a covered block to none (4).
 __device__ __forceinline__ const double* block_in_stats(const sixbit_dit_blocks& B, int l) {
   return l == 0 ? B.in_stats0 : &B.stats[l - 1].max_abs_out;  // {max, sum |x|, count}
 }
 
-__global__ void policy_run_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l, unsigned long long cond,
-                                  int cond_branches, int32_t* err) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+constexpr int kDitBranches = 4;
+
+__device__ void decide_block(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, int32_t* err) {
   sixbit_policy_state s = B.states[l];
   const int word = policy_decide(cfg, s, &B.stats[l], block_in_stats(B, l));
   B.states[l] = s;
@@ -486,7 +503,7 @@ __global__ void policy_run_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, in
   if (B.covered[l] != 0) {
     if (!is_skip) set_error(err, SIXBIT_EINVAL);  // a covered block must skip
     B.covered[l] = 0;
-    branch = cond_branches;  // applied by its run: no body
+    branch = kDitBranches;  // applied by its run: no body
   } else if (is_skip) {
     int k = 1;
     for (int j = l + 1; j < B.L; ++j) {
@@ -498,18 +515,49 @@ __global__ void policy_run_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, in
     B.run_len[l] = static_cast<uint32_t>(k);
     branch = 3;
   }
-  if (cond != 0)
-    cudaGraphSetConditional(static_cast<cudaGraphConditionalHandle>(cond),
-                            (branch >= 0 && branch < cond_branches) ? static_cast<unsigned int>(branch)
-                                                                    : static_cast<unsigned int>(cond_branches));
+  if (B.conds != nullptr)
+    cudaGraphSetConditional(static_cast<cudaGraphConditionalHandle>(B.conds[l]),
+                            (branch >= 0 && branch < kDitBranches) ? static_cast<unsigned int>(branch)
+                                                                   : static_cast<unsigned int>(kDitBranches));
 }
 
-__global__ void __launch_bounds__(kStThreads) skip_run_kernel(sixbit_dit_blocks B, int l, void* scratch) {
+// (selects, not an index into the parameter array: that would copy B to local memory)
+__device__ __forceinline__ const uint16_t* block_input(const sixbit_dit_blocks& B, int l) {
+  return l == 0 ? B.x0 : (((l - 1) & 1) ? B.buf[1] : B.buf[0]);
+}
+__device__ __forceinline__ uint16_t* block_output(const sixbit_dit_blocks& B, int l) {
+  return (l & 1) ? B.buf[1] : B.buf[0];
+}
+
+__global__ void __launch_bounds__(kStThreads) dit_begin_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B,
+                                                               void* scratch, int32_t* err) {
+  double tot[3];
+  if (tensor_stats_body(B.x0, B.n, scratch, tot)) {
+    B.in_stats0[0] = tot[0];
+    B.in_stats0[1] = tot[1];
+    B.in_stats0[2] = static_cast<double>(B.n);
+    B.in_stats0[3] = tot[2];
+    decide_block(cfg, B, 0, err);
+  }
+}
+
+__global__ void __launch_bounds__(kStThreads) dit_block_end_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l,
+                                                                   void* scratch, int32_t* err) {
+  if (SIXBIT_MODE_OF(B.modes[l]) == SIXBIT_MODE_SKIP) return;  // uniform: a skipped block has no end
+  double tot[6];
+  if (block_stats_body(block_input(B, l), block_output(B, l), B.deltas + static_cast<size_t>(l) * B.n, B.n, scratch,
+                       tot)) {
+    write_block_stats(&B.stats[l], tot, B.n);
+    if (l + 1 < B.L) decide_block(cfg, B, l + 1, err);
+  }
+}
+
+__global__ void __launch_bounds__(kStThreads) dit_skip_run_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l,
+                                                                  void* scratch, int32_t* err) {
   const int k = static_cast<int>(B.run_len[l]);
-  if (k == 0) return;  // uniform across the grid: nothing to apply
-  // (selects, not an index into the parameter array: that would copy B to local memory)
-  const uint16_t* __restrict__ x_in = l == 0 ? B.x0 : (((l - 1) & 1) ? B.buf[1] : B.buf[0]);
-  uint16_t* x_out = ((l + k - 1) & 1) ? B.buf[1] : B.buf[0];
+  if (k == 0) return;  // uniform across the grid: block l starts no run
+  const uint16_t* __restrict__ x_in = block_input(B, l);
+  uint16_t* x_out = block_output(B, l + k - 1);
   const uint16_t* __restrict__ d0 = B.deltas + static_cast<size_t>(l) * B.n;
   const int64_t n8 = B.n >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
@@ -569,6 +617,7 @@ __global__ void __launch_bounds__(kStThreads) skip_run_kernel(sixbit_dit_blocks 
     o->sum_abs_out = tot[1];
     o->count = static_cast<double>(B.n);
     B.run_len[l] = 0;  // every CTA has read it
+    for (int j = l + 1; j <= l + k && j < B.L; ++j) decide_block(cfg, B, j, err);  // covered, then the next
   }
 }
 
@@ -630,15 +679,23 @@ cudaError_t launch_skip_apply(const uint16_t* x_in, const uint16_t* delta, uint1
   return cudaGetLastError();
 }
 
-cudaError_t launch_policy_run(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l,
-                              unsigned long long cond, int cond_branches, int32_t* err, cudaStream_t st) {
-  policy_run_kernel<<<1, 32, 0, st>>>(cfg, B, l, cond, cond_branches, err);
+cudaError_t launch_dit_begin(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, void* scratch, int32_t* err,
+                             cudaStream_t st) {
+  dit_begin_kernel<<<stats_grid(dit_begin_kernel, B.n), kStThreads, 0, st>>>(cfg, B, scratch, err);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_skip_run(const sixbit_dit_blocks& B, int l, void* scratch, cudaStream_t st) {
-  skip_run_kernel<<<stats_grid(skip_run_kernel, B.n), kStThreads, 0, st>>>(B, l, scratch);
+cudaError_t launch_dit_block_end(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, void* scratch,
+                                 int32_t* err, cudaStream_t st) {
+  dit_block_end_kernel<<<stats_grid(dit_block_end_kernel, B.n), kStThreads, 0, st>>>(cfg, B, l, scratch, err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dit_skip_run(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, void* scratch,
+                                int32_t* err, cudaStream_t st) {
+  dit_skip_run_kernel<<<stats_grid(dit_skip_run_kernel, B.n), kStThreads, 0, st>>>(cfg, B, l, scratch, err);
   note_launch();
   return cudaGetLastError();
 }

@@ -1,22 +1,23 @@
 """Runs a residual-MLP diffusion transformer through the hot path, one denoising step at a time.
 
-Every block maps x -> x + W_d . GELU(W_u . x).  Per step and block the
-policy writes a mode word on the device; every later kernel of the block
-reads it and does its work only when the mode is its own, so one step is a
-fixed sequence of launches with no host synchronisation, and it is captured
-once into a CUDA graph and replayed.
+Every block maps x -> x + W_d . GELU(W_u . x).  Every per-block decision is
+taken on the device, at the tail of the kernel that produces the statistics
+it needs (libsixbit's DiT step protocol), and every later kernel of the block
+reads the mode word and does its work only when the mode is its own, so one
+step is a fixed sequence of launches with no host synchronisation; it is
+captured once into a CUDA graph in which each block is a SWITCH node whose
+condition the deciding kernel sets.
 
-Per block l (all on one stream):
-  policy_skip_run(l) -> mode[l]; when block l starts a run of skipping
-                        blocks l..l+k-1: x_{l+k-1} = x_{l-1} + the run's
-                        cached deltas, in one pass            (SKIP)
+Per step:
+  dit_begin: statistics of x_0, decision of block 0
+Per block l (reads bufs[(l-1) % 2], x_in for l = 0; writes bufs[l % 2]):
   hadamard_quant(x) -> qa_x                              (NVFP4 / INT8)
   qgemm(qa_x | x, W_up[l], GELU) -> h                    (NVFP4 / INT8 / BF16)
   hadamard_quant(h) -> qa_h
   qgemm(qa_h | h, W_down[l], + x) -> out
-  block_stats(x, out, delta[l]) -> stats[l], delta[l]    (not SKIP)
-in_stats of block 0 come from tensor_stats(x_0), of block l from stats[l-1].
-Block l reads bufs[(l-1) % 2] (x_in for l = 0) and writes bufs[l % 2].
+  dit_block_end(l): block statistics, Delta cache; decision of block l+1
+  dit_skip_run(l): when block l starts a run of k skipping blocks, their
+                   skips in one pass; decisions of blocks l+1 .. l+k
 """
 from __future__ import annotations
 
@@ -48,10 +49,14 @@ class DiT:
         self.modes = torch.zeros(blocks, dtype=torch.int32, device=dev)
         self.marks = torch.zeros((2, blocks), dtype=torch.int32, device=dev)  # covered, run length
         self.scratch = ops.new_scratch(tokens * ffn, dev)
-        self.rec = ops.dit_blocks(self.state, self.stats, self.modes, self.marks, self.tstats, self.x_in,
-                                  self.bufs[0], self.bufs[1], self.deltas)
+        self.conds = torch.zeros(blocks, dtype=torch.int64, device=dev)  # graph condition handles
+        self.rec = self._record(None)
         self.graph = None
         self.out = self.bufs[(blocks - 1) % 2]
+
+    def _record(self, conds):
+        return ops.dit_blocks(self.state, self.stats, self.modes, self.marks, self.tstats, self.x_in,
+                              self.bufs[0], self.bufs[1], self.deltas, conds)
 
     def reset(self):
         """Back to the state before the first denoising step."""
@@ -61,27 +66,25 @@ class DiT:
         self.modes.zero_()
         self.marks.zero_()
 
-    CALLS = ("policy_skip", "hq_x", "qgemm_up", "hq_h", "qgemm_down", "block_stats")
+    CALLS = ("hq_x", "qgemm_up", "hq_h", "qgemm_down", "block_stats", "skip_run")
 
     def enqueue_step(self, after_call=None):
-        """Enqueue one denoising step on the current stream (input: self.x_in).
+        """Enqueue one denoising step on the current stream (input: self.x_in), every
+        kernel launched and gated on the device by the block's mode word.
 
         after_call(label, block) is invoked on the host after each library call
         (e.g. to record a CUDA event for per-call timing); labels are
-        "tensor_stats" (block -1) and DiT.CALLS.
+        "tensor_stats" (block -1, the step's first call) and DiT.CALLS.
         """
         o = ops
         note = after_call or (lambda label, block: None)
-        o.tensor_stats(self.x_in, self.tstats, self.scratch)
+        o.dit_begin(self.cfg, self.rec, self.scratch)
         note("tensor_stats", -1)
         x = self.x_in
         for l in range(self.L):
             out = self.bufs[l % 2]
             mode = self.modes[l:l + 1]
-            st = self.stats[l]
             up, down = self.packed[l]
-            o.policy_skip_run(self.cfg, self.rec, l, self.scratch)
-            note("policy_skip", l)
             o.hadamard_quant(x, self.b, 0, out=self.qa_x, mode_dev=mode)
             note("hq_x", l)
             o.qgemm(self.qa_x, x, up, 0, epilogue=o.EPI_GELU, out=self.h, mode_dev=mode)
@@ -90,15 +93,18 @@ class DiT:
             note("hq_h", l)
             o.qgemm(self.qa_h, self.h, down, 0, epilogue=o.EPI_RESIDUAL, residual=x, out=out, mode_dev=mode)
             note("qgemm_down", l)
-            o.block_stats(x, out, self.deltas[l], st, self.scratch, mode_dev=mode)
+            o.dit_block_end(self.cfg, self.rec, l, self.scratch)
             note("block_stats", l)
+            o.dit_skip_run(self.cfg, self.rec, l, self.scratch)
+            note("skip_run", l)
             x = out
         return x
 
-    def _compute_body(self, x, out, l, mode, note=None):
-        """The kernels of one computed block in a fixed mode (no mode word);
-        note(label) is called on the host after each call when given."""
+    def _compute_body(self, x, out, l, mode, rec=None, note=None):
+        """The kernels of one computed block in a fixed mode (no mode word), ending with
+        dit_block_end; note(label) is called on the host after each call when given."""
         o = ops
+        rec = rec or self.rec
         note = note or (lambda label: None)
         up, down = self.packed[l]
         quant = mode != o.MODE_BF16
@@ -113,31 +119,33 @@ class DiT:
         o.qgemm(self.qa_h if quant else None, self.h, down, mode, epilogue=o.EPI_RESIDUAL, residual=x, out=out,
                 m=self.T)
         note("qgemm_down")
-        o.block_stats(x, out, self.deltas[l], self.stats[l], self.scratch)
+        o.dit_block_end(self.cfg, rec, l, self.scratch)
         note("block_stats")
 
     def enqueue_step_switched(self, body_stream):
         """One step for graph capture: per block a SWITCH over the NVFP4 / INT8 /
-        BF16 bodies and the skip of a run starting at the block, whose condition
-        the policy kernel sets, so only the chosen body's kernels run (a block
-        covered by an earlier run runs none)."""
+        BF16 bodies and the skip run a block starts, whose condition the deciding
+        kernel sets, so only the chosen body's kernels run (a block covered by an
+        earlier run runs none).  Returns the handles (filled into self.conds by
+        capture())."""
         o = ops
         stream = torch.cuda.current_stream()
-        o.tensor_stats(self.x_in, self.tstats, self.scratch)
+        handles = [o.graph_cond_create(stream, 4) for _ in range(self.L)]
+        rec = self._record(self.conds)
+        o.dit_begin(self.cfg, rec, self.scratch)
         x = self.x_in
         for l in range(self.L):
             out = self.bufs[l % 2]
-            cond = o.graph_cond_create(stream, 4)
-            o.policy_skip_run(self.cfg, self.rec, l, None, cond=cond, cond_branches=4)
-            sw = o.GraphSwitch(stream, body_stream, None, o.MODE_NVFP4, 4, cond=cond)
+            sw = o.GraphSwitch(stream, body_stream, None, o.MODE_NVFP4, 4, cond=handles[l])
             for i, m in enumerate((o.MODE_NVFP4, o.MODE_INT8, o.MODE_BF16)):
                 with sw.branch(i):
-                    self._compute_body(x, out, l, m)
+                    self._compute_body(x, out, l, m, rec=rec)
             with sw.branch(3):
-                o.skip_run(self.rec, l, self.scratch)
+                o.dit_skip_run(self.cfg, rec, l, self.scratch)
             sw.close()
             x = out
-        return x
+        self._rec_graph = rec   # keeps the record's buffers referenced with the graph
+        return handles
 
     def step_host_dispatch(self, x_s: torch.Tensor | None = None):
         """One step without a graph: the host reads each block's mode word (one
@@ -149,14 +157,15 @@ class DiT:
         o = ops
         if x_s is not None:
             self.x_in.copy_(x_s, non_blocking=True)
-        o.tensor_stats(self.x_in, self.tstats, self.scratch)
+        o.dit_begin(self.cfg, self.rec, self.scratch)
         x = self.x_in
         for l in range(self.L):
             out = self.bufs[l % 2]
-            o.policy_skip_run(self.cfg, self.rec, l, self.scratch)
             m = int(self.modes[l].item()) & 0xFF
             if m != o.MODE_SKIP:
                 self._compute_body(x, out, l, m)
+            elif l == 0 or (int(self.modes[l - 1].item()) & 0xFF) != o.MODE_SKIP:
+                o.dit_skip_run(self.cfg, self.rec, l, self.scratch)   # a run starts here
             x = out
         return x
 
@@ -169,11 +178,16 @@ class DiT:
         """
         g = torch.cuda.CUDAGraph()
         body_stream = torch.cuda.Stream()
+        handles = None
         with torch.cuda.graph(g, capture_error_mode="thread_local"):
             if switched:
-                self.enqueue_step_switched(body_stream)
+                handles = self.enqueue_step_switched(body_stream)
             else:
                 self.enqueue_step()
+        if handles is not None:   # read by the deciding kernels when the graph runs
+            as_i64 = [h - (1 << 64) if h >= (1 << 63) else h for h in handles]
+            self.conds.copy_(torch.tensor(as_i64, dtype=torch.int64))
+            torch.cuda.synchronize()
         self.graph = g
         self._body_stream = body_stream
         return g

@@ -154,28 +154,36 @@ def policy_step(cfg: PolicyCfg, state: torch.Tensor, last_stats: torch.Tensor, i
     return mode_word
 
 
-def dit_blocks(states, stats, modes, marks, in_stats0, x0, buf0, buf1, deltas) -> DitBlocks:
+def dit_blocks(states, stats, modes, marks, in_stats0, x0, buf0, buf1, deltas, conds=None) -> DitBlocks:
     """The sixbit_dit_blocks record of a stack of residual blocks (device tensors; deltas [L, ...];
-    marks: int32 [2, L], zeroed: the covered marks and the run lengths)."""
+    marks: int32 [2, L], zeroed: the covered marks and the run lengths; conds: int64 [L] graph
+    condition handles, or None)."""
     L = states.shape[0]
     n = x0.numel()
     assert stats.shape[0] == L and modes.numel() == L and tuple(marks.shape) == (2, L) and deltas.shape[0] == L
     assert marks.dtype == torch.int32 and marks.is_contiguous() and deltas.numel() == L * n
+    assert in_stats0.dtype == torch.float64 and in_stats0.numel() >= 4
+    assert conds is None or (conds.dtype == torch.int64 and conds.numel() == L)
     return DitBlocks(_p(states), _p(stats), _p(modes), _p(marks[0]), _p(in_stats0), _p(x0),
-                     (C.c_void_p * 2)(buf0.data_ptr(), buf1.data_ptr()), _p(deltas), _p(marks[1]), n, L, 0)
+                     (C.c_void_p * 2)(buf0.data_ptr(), buf1.data_ptr()), _p(deltas), _p(marks[1]), _p(conds),
+                     n, L, 0)
 
 
-def policy_skip_run(cfg: PolicyCfg, blocks: DitBlocks, l: int, scratch: torch.Tensor | None, cond: int = 0,
-                    cond_branches: int = 4, err=None, stream=None):
-    """sixbit_policy_skip_run: block l's decision fused with the skips of the run it starts
-    (with `cond`, only the decision; skip_run then belongs in branch 3)."""
-    check(_lib.sixbit_policy_skip_run(C.byref(cfg), C.byref(blocks), l, cond, cond_branches, _p(scratch), _p(err),
-                                      _stream(stream)), "policy_skip_run")
+def dit_begin(cfg: PolicyCfg, blocks: DitBlocks, scratch: torch.Tensor, err=None, stream=None):
+    """sixbit_dit_begin: statistics of the step input, then block 0's decision."""
+    check(_lib.sixbit_dit_begin(C.byref(cfg), C.byref(blocks), _p(scratch), _p(err), _stream(stream)), "dit_begin")
 
 
-def skip_run(blocks: DitBlocks, l: int, scratch: torch.Tensor, err=None, stream=None):
-    """sixbit_skip_run: apply the run of skips block l's decision recorded (nothing if none)."""
-    check(_lib.sixbit_skip_run(C.byref(blocks), l, _p(scratch), _p(err), _stream(stream)), "skip_run")
+def dit_block_end(cfg: PolicyCfg, blocks: DitBlocks, l: int, scratch: torch.Tensor, err=None, stream=None):
+    """sixbit_dit_block_end: block l's statistics and Delta update (if it computed), then block l+1's decision."""
+    check(_lib.sixbit_dit_block_end(C.byref(cfg), C.byref(blocks), l, _p(scratch), _p(err), _stream(stream)),
+          "dit_block_end")
+
+
+def dit_skip_run(cfg: PolicyCfg, blocks: DitBlocks, l: int, scratch: torch.Tensor, err=None, stream=None):
+    """sixbit_dit_skip_run: the run of skips block l starts (if any), then the decisions up to its end + 1."""
+    check(_lib.sixbit_dit_skip_run(C.byref(cfg), C.byref(blocks), l, _p(scratch), _p(err), _stream(stream)),
+          "dit_skip_run")
 
 
 def graph_cond_create(stream, nbranches: int) -> int:
