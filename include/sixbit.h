@@ -255,8 +255,8 @@ sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_sta
  * order, block l reading x_{l-1} (x_{-1} = x0) and writing x_l into
  * buf[l % 2].  All pointers are DEVICE pointers owned by the caller.
  *   states [L], stats [L], modes [L]  as for sixbit_policy_step, one per block
- *   covered [L], run_len [L] uint32, zero before the first step (the
- *               library leaves them zero between steps)
+ *   run_len [L] uint32, zero before the first step (the library leaves
+ *               it zero between steps)
  *   in_stats0   [4] float64, written by sixbit_dit_begin: {max |x0|,
  *               sum |x0|, count, sum x0^2}
  *   x0 [n], buf[0], buf[1] [n] bf16; deltas [L][n] bf16, the Delta cache
@@ -268,7 +268,6 @@ typedef struct {
   sixbit_policy_state* states;
   sixbit_stats* stats;
   int32_t* modes;
-  uint32_t* covered;
   double* in_stats0;
   const uint16_t* x0;
   uint16_t* buf[2];
@@ -294,23 +293,22 @@ typedef struct {
  *                         x_{l+k-1} = bf16(...bf16(x_{l-1} + Delta_l)... +
  *                         Delta_{l+k-1}) into buf[(l+k-1) % 2] with its
  *                         {max |x|, sum |x|, count} into stats[l+k-1], then
- *                         the decisions of l+1 .. l+k; nothing otherwise.
+ *                         the decision of block l+k; nothing otherwise.
  * A decision is sixbit_policy_step's (input statistics from stats[l-1], or
  * in_stats0 for l = 0; the word to modes[l]).  A skip depends only on the
  * block's own state, never on its input, so when block l skips, the blocks
- * l+1 .. l+k-1 that will also skip are known: the decision records k in
- * run_len[l] and marks them covered (their decisions, taken by the run, only
- * clear the mark).  Results are bit-identical to one policy step + one skip
+ * l+1 .. l+k-1 that will also skip are known: block l's decision takes
+ * theirs too (they launch nothing) and records k in run_len[l].  Results
+ * are bit-identical to one policy step + one skip
  * (or the block's compute + block statistics) per block; the skipped
  * intermediate activations are not written.  With conds, each decision also
  * sets conds[l]: 0, 1, 2 for NVFP4, INT8, BF16 (the compute bodies, each
  * ending with sixbit_dit_block_end), 3 for a run start (sixbit_dit_skip_run)
- * and 4 (no body) for a covered block.  Eager use: after sixbit_dit_begin,
+ * and 4 (no body) for the other blocks of a run.  Eager use: after sixbit_dit_begin,
  * per block the mode-gated compute calls, sixbit_dit_block_end and
  * sixbit_dit_skip_run (each a no-op when it does not apply).  scratch as for
- * sixbit_block_stats.  cfg is a HOST pointer.  A covered block whose
- * decision is not a skip (impossible unless a state was changed in between)
- * records SIXBIT_EINVAL in err_dev.
+ * sixbit_block_stats.  cfg is a HOST pointer.  err_dev is reserved (no
+ * device-side error is possible).
  */
 sixbit_status sixbit_dit_begin(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, void* scratch,
                                int32_t* err_dev, void* stream);

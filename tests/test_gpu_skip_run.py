@@ -5,8 +5,8 @@ and sixbit_block_stats.
 
 Bar: bit-identical decisions, policy states, activations, Delta caches and the
 statistics later blocks read, over several steps of a stack whose skip runs start
-at block 0, in the middle and at the end; the covered marks and run lengths are
-back to zero after each step.  A block's compute is stood in for by a seeded
+at block 0, in the middle and at the end; the run lengths are back to zero
+after each step.  A block's compute is stood in for by a seeded
 perturbation of its input (the same on both sides).
 """
 import numpy as np
@@ -61,8 +61,8 @@ def test_protocol_matches_sequential_steps(ops, skipping):
     bufs_b = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     deltas_b = deltas0.clone()
     tstats_b = torch.zeros(4, dtype=torch.float64, device="cuda")
-    marks = torch.zeros((2, L), dtype=torch.int32, device="cuda")
-    rec = ops.dit_blocks(st_b, stats_b, modes_b, marks, tstats_b, x0, bufs_b[0], bufs_b[1], deltas_b)
+    run_len = torch.zeros(L, dtype=torch.int32, device="cuda")
+    rec = ops.dit_blocks(st_b, stats_b, modes_b, run_len, tstats_b, x0, bufs_b[0], bufs_b[1], deltas_b)
 
     first_low = None
     for step in range(3):   # by the third step the computing blocks have two computes and may skip too
@@ -93,7 +93,7 @@ def test_protocol_matches_sequential_steps(ops, skipping):
         assert torch.equal(x.view(torch.int16), xb.view(torch.int16)), step
         assert torch.equal(deltas_a.view(torch.int16), deltas_b.view(torch.int16)), step
         np.testing.assert_array_equal(tstats_a.cpu().numpy(), tstats_b.cpu().numpy())
-        assert not marks.any()
+        assert not run_len.any()
         low = modes_a.cpu().numpy() & 0xFF
         first_low = low if first_low is None else first_low
         for l in range(L):

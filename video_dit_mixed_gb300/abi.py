@@ -44,7 +44,7 @@ class PolicyState(C.Structure):
 
 
 class DitBlocks(C.Structure):
-    _fields_ = [("states", c_p), ("stats", c_p), ("modes", c_p), ("covered", c_p), ("in_stats0", c_p),
+    _fields_ = [("states", c_p), ("stats", c_p), ("modes", c_p), ("in_stats0", c_p),
                 ("x0", c_p), ("buf", c_p * 2), ("deltas", c_p), ("run_len", c_p), ("conds", c_p),
                 ("n", C.c_int64), ("L", C.c_int32),
                 ("reserved", C.c_int32)]

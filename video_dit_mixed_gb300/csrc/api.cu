@@ -306,9 +306,9 @@ static sixbit_status check_blocks(const sixbit_policy_cfg* cfg, const sixbit_dit
                                   void* scratch) {
   if (cfg == nullptr || blocks == nullptr || scratch == nullptr) return SIXBIT_EINVAL;
   const sixbit_dit_blocks& B = *blocks;
-  if (B.states == nullptr || B.stats == nullptr || B.modes == nullptr || B.covered == nullptr ||
-      B.run_len == nullptr || B.in_stats0 == nullptr || B.x0 == nullptr || B.buf[0] == nullptr ||
-      B.buf[1] == nullptr || B.deltas == nullptr)
+  if (B.states == nullptr || B.stats == nullptr || B.modes == nullptr || B.run_len == nullptr ||
+      B.in_stats0 == nullptr || B.x0 == nullptr || B.buf[0] == nullptr || B.buf[1] == nullptr ||
+      B.deltas == nullptr)
     return SIXBIT_EINVAL;
   if (B.L <= 0 || l < 0 || l >= B.L || B.n <= 0 || B.n % 8 != 0) return SIXBIT_ESHAPE;
   if (!aligned16(B.x0) || !aligned16(B.buf[0]) || !aligned16(B.buf[1]) || !aligned16(B.deltas) ||

@@ -402,8 +402,6 @@ __device__ int policy_decide(const sixbit_policy_cfg& cfg, sixbit_policy_state& 
     s.skipped_last = 0;
     s.pending = 0;
   }
-  const double mx = in_stats[0], sabs = in_stats[1], cnt = in_stats[2];
-  const double ratio = (sabs == 0.0) ? 0.0 : mx / (sabs / cnt);
   int word = 0;
   bool near = false, refresh = false;
   bool decided = false;
@@ -424,6 +422,10 @@ __device__ int policy_decide(const sixbit_policy_cfg& cfg, sixbit_policy_state& 
     }
   }
   if (!decided) {
+    // the input's max/mean ratio only matters when the block computes (two
+    // float64 divisions, slow on this GPU, are not spent on a skip)
+    const double mx = in_stats[0], sabs = in_stats[1], cnt = in_stats[2];
+    const double ratio = (sabs == 0.0) ? 0.0 : mx / (sabs / cnt);
     near |= near_thr(ratio, cfg.pdr_ratio, cfg.near_rel);
     if (ratio > cfg.pdr_ratio || (refresh && cfg.refresh_bf16)) {
       word = SIXBIT_MODE_BF16 | (ratio > cfg.pdr_ratio ? SIXBIT_FLAG_PDR : 0);
@@ -475,50 +477,72 @@ __global__ void policy_kernel(sixbit_policy_cfg cfg, sixbit_policy_state* st, co
 //   dit_block_end_kernel block statistics + Delta update of a computed block
 //                        l, then the decision of block l+1;
 //   dit_skip_run_kernel  the skip of the run of blocks l .. l+k-1 that block
-//                        l starts, then the decisions of l+1 .. l+k.
+//                        l starts, then the decision of block l+k.
 // A skip decision depends only on the block's own state (cos, acc, number of
 // computes) and the statistics of its last compute, never on its input, so
 // when block l skips, the run of blocks that will skip after it is already
-// fixed: decide_block finds it by evaluating policy_decide on copies of
-// their states, records k in run_len[l] and marks l+1 .. l+k-1 covered.  The
+// fixed: decide_block finds it, decides those blocks as well (recording
+// their states and mode words; they launch nothing) and records k in
+// run_len[l].  The
 // run's output x_{l+k-1} = bf16(... bf16(bf16(x_{l-1} + D_l) + D_{l+1}) ... +
 // D_{l+k-1}) is written in one pass (the same roundings as k separate skips;
 // the intermediate activations are never read, so they are not written),
 // with its {max, sum |x|, count} into stats[l+k-1].  Each decision also sets
 // the block's graph condition when a handle array is given: a compute mode
-// to its body (0, 1, 2), a run start to 3, a covered block to none (4).
+// to its body (0, 1, 2), a run start to 3, a block inside a run to none (4).
+// The protocol's kernels cap registers at 64 (launch bounds): the decisions
+// run in one thread at the tail and may spill; the streaming body may not.
 __device__ __forceinline__ const double* block_in_stats(const sixbit_dit_blocks& B, int l) {
   return l == 0 ? B.in_stats0 : &B.stats[l - 1].max_abs_out;  // {max, sum |x|, count}
 }
 
 constexpr int kDitBranches = 4;
 
-__device__ void decide_block(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, int32_t* err) {
-  sixbit_policy_state s = B.states[l];
-  const int word = policy_decide(cfg, s, &B.stats[l], block_in_stats(B, l));
-  B.states[l] = s;
-  B.modes[l] = word;
-  const bool is_skip = SIXBIT_MODE_OF(word) == SIXBIT_MODE_SKIP;
-  int branch = SIXBIT_MODE_OF(word) - SIXBIT_MODE_NVFP4;  // compute modes: 0, 1, 2
-  if (B.covered[l] != 0) {
-    if (!is_skip) set_error(err, SIXBIT_EINVAL);  // a covered block must skip
-    B.covered[l] = 0;
-    branch = kDitBranches;  // applied by its run: no body
-  } else if (is_skip) {
-    int k = 1;
-    for (int j = l + 1; j < B.L; ++j) {
-      sixbit_policy_state sj = B.states[j];
-      if (SIXBIT_MODE_OF(policy_decide(cfg, sj, &B.stats[j], block_in_stats(B, j))) != SIXBIT_MODE_SKIP) break;
-      B.covered[j] = 1;
-      ++k;
-    }
-    B.run_len[l] = static_cast<uint32_t>(k);
-    branch = 3;
-  }
+__device__ __forceinline__ void set_branch(const sixbit_dit_blocks& B, int l, int branch) {
   if (B.conds != nullptr)
     cudaGraphSetConditional(static_cast<cudaGraphConditionalHandle>(B.conds[l]),
                             (branch >= 0 && branch < kDitBranches) ? static_cast<unsigned int>(branch)
                                                                    : static_cast<unsigned int>(kDitBranches));
+}
+
+// Decides block l; when it starts a run, also decides (and records) the
+// blocks l+1 .. l+k-1 the run covers -- their skips are fixed by their own
+// states -- and gives them no body.
+__device__ void decide_block(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l) {
+  sixbit_policy_state s = B.states[l];
+  const int word = policy_decide(cfg, s, &B.stats[l], block_in_stats(B, l));
+  B.states[l] = s;
+  B.modes[l] = word;
+  if (SIXBIT_MODE_OF(word) != SIXBIT_MODE_SKIP) {
+    set_branch(B, l, SIXBIT_MODE_OF(word) - SIXBIT_MODE_NVFP4);  // compute modes: 0, 1, 2
+    return;
+  }
+  int k = 1;
+  // the next block's state and statistics are loaded while this one is decided
+  sixbit_stats prev = B.stats[l];
+  sixbit_policy_state sn;
+  sixbit_stats tn;
+  if (l + 1 < B.L) {
+    sn = B.states[l + 1];
+    tn = B.stats[l + 1];
+  }
+  for (int j = l + 1; j < B.L; ++j) {
+    sixbit_policy_state sj = sn;
+    const sixbit_stats tj = tn;
+    if (j + 1 < B.L) {
+      sn = B.states[j + 1];
+      tn = B.stats[j + 1];
+    }
+    const int wj = policy_decide(cfg, sj, &tj, &prev.max_abs_out);  // input stats: block j-1's output
+    if (SIXBIT_MODE_OF(wj) != SIXBIT_MODE_SKIP) break;  // decided later, from the run's statistics
+    B.states[j] = sj;
+    B.modes[j] = wj;
+    set_branch(B, j, kDitBranches);  // applied by the run: no body
+    prev = tj;
+    ++k;
+  }
+  B.run_len[l] = static_cast<uint32_t>(k);
+  set_branch(B, l, 3);
 }
 
 // (selects, not an index into the parameter array: that would copy B to local memory)
@@ -529,7 +553,7 @@ __device__ __forceinline__ uint16_t* block_output(const sixbit_dit_blocks& B, in
   return (l & 1) ? B.buf[1] : B.buf[0];
 }
 
-__global__ void __launch_bounds__(kStThreads) dit_begin_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B,
+__global__ void __launch_bounds__(kStThreads, 4) dit_begin_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B,
                                                                void* scratch, int32_t* err) {
   double tot[3];
   if (tensor_stats_body(B.x0, B.n, scratch, tot)) {
@@ -537,22 +561,22 @@ __global__ void __launch_bounds__(kStThreads) dit_begin_kernel(sixbit_policy_cfg
     B.in_stats0[1] = tot[1];
     B.in_stats0[2] = static_cast<double>(B.n);
     B.in_stats0[3] = tot[2];
-    decide_block(cfg, B, 0, err);
+    decide_block(cfg, B, 0);
   }
 }
 
-__global__ void __launch_bounds__(kStThreads) dit_block_end_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l,
+__global__ void __launch_bounds__(kStThreads, 4) dit_block_end_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l,
                                                                    void* scratch, int32_t* err) {
   if (SIXBIT_MODE_OF(B.modes[l]) == SIXBIT_MODE_SKIP) return;  // uniform: a skipped block has no end
   double tot[6];
   if (block_stats_body(block_input(B, l), block_output(B, l), B.deltas + static_cast<size_t>(l) * B.n, B.n, scratch,
                        tot)) {
     write_block_stats(&B.stats[l], tot, B.n);
-    if (l + 1 < B.L) decide_block(cfg, B, l + 1, err);
+    if (l + 1 < B.L) decide_block(cfg, B, l + 1);
   }
 }
 
-__global__ void __launch_bounds__(kStThreads) dit_skip_run_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l,
+__global__ void __launch_bounds__(kStThreads, 4) dit_skip_run_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l,
                                                                   void* scratch, int32_t* err) {
   const int k = static_cast<int>(B.run_len[l]);
   if (k == 0) return;  // uniform across the grid: block l starts no run
@@ -617,7 +641,7 @@ __global__ void __launch_bounds__(kStThreads) dit_skip_run_kernel(sixbit_policy_
     o->sum_abs_out = tot[1];
     o->count = static_cast<double>(B.n);
     B.run_len[l] = 0;  // every CTA has read it
-    for (int j = l + 1; j <= l + k && j < B.L; ++j) decide_block(cfg, B, j, err);  // covered, then the next
+    if (l + k < B.L) decide_block(cfg, B, l + k);
   }
 }
 

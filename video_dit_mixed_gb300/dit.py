@@ -17,7 +17,7 @@ Per block l (reads bufs[(l-1) % 2], x_in for l = 0; writes bufs[l % 2]):
   qgemm(qa_h | h, W_down[l], + x) -> out
   dit_block_end(l): block statistics, Delta cache; decision of block l+1
   dit_skip_run(l): when block l starts a run of k skipping blocks, their
-                   skips in one pass; decisions of blocks l+1 .. l+k
+                   skips in one pass; decision of block l+k
 """
 from __future__ import annotations
 
@@ -47,7 +47,7 @@ class DiT:
         self.stats = ops.new_stats(dev, blocks)
         self.state = ops.new_policy_state(dev, blocks)
         self.modes = torch.zeros(blocks, dtype=torch.int32, device=dev)
-        self.marks = torch.zeros((2, blocks), dtype=torch.int32, device=dev)  # covered, run length
+        self.run_len = torch.zeros(blocks, dtype=torch.int32, device=dev)   # per run start, within a step
         self.scratch = ops.new_scratch(tokens * ffn, dev)
         self.conds = torch.zeros(blocks, dtype=torch.int64, device=dev)  # graph condition handles
         self.rec = self._record(None)
@@ -55,7 +55,7 @@ class DiT:
         self.out = self.bufs[(blocks - 1) % 2]
 
     def _record(self, conds):
-        return ops.dit_blocks(self.state, self.stats, self.modes, self.marks, self.tstats, self.x_in,
+        return ops.dit_blocks(self.state, self.stats, self.modes, self.run_len, self.tstats, self.x_in,
                               self.bufs[0], self.bufs[1], self.deltas, conds)
 
     def reset(self):
@@ -64,7 +64,7 @@ class DiT:
         self.stats.zero_()
         self.state.zero_()
         self.modes.zero_()
-        self.marks.zero_()
+        self.run_len.zero_()
 
     CALLS = ("hq_x", "qgemm_up", "hq_h", "qgemm_down", "block_stats", "skip_run")
 
@@ -125,8 +125,8 @@ class DiT:
     def enqueue_step_switched(self, body_stream):
         """One step for graph capture: per block a SWITCH over the NVFP4 / INT8 /
         BF16 bodies and the skip run a block starts, whose condition the deciding
-        kernel sets, so only the chosen body's kernels run (a block covered by an
-        earlier run runs none).  Returns the handles (filled into self.conds by
+        kernel sets, so only the chosen body's kernels run (the other blocks of a
+        run run none).  Returns the handles (filled into self.conds by
         capture())."""
         o = ops
         stream = torch.cuda.current_stream()

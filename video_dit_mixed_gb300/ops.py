@@ -154,19 +154,17 @@ def policy_step(cfg: PolicyCfg, state: torch.Tensor, last_stats: torch.Tensor, i
     return mode_word
 
 
-def dit_blocks(states, stats, modes, marks, in_stats0, x0, buf0, buf1, deltas, conds=None) -> DitBlocks:
+def dit_blocks(states, stats, modes, run_len, in_stats0, x0, buf0, buf1, deltas, conds=None) -> DitBlocks:
     """The sixbit_dit_blocks record of a stack of residual blocks (device tensors; deltas [L, ...];
-    marks: int32 [2, L], zeroed: the covered marks and the run lengths; conds: int64 [L] graph
-    condition handles, or None)."""
+    run_len: int32 [L], zeroed; conds: int64 [L] graph condition handles, or None)."""
     L = states.shape[0]
     n = x0.numel()
-    assert stats.shape[0] == L and modes.numel() == L and tuple(marks.shape) == (2, L) and deltas.shape[0] == L
-    assert marks.dtype == torch.int32 and marks.is_contiguous() and deltas.numel() == L * n
+    assert stats.shape[0] == L and modes.numel() == L and run_len.numel() == L and deltas.shape[0] == L
+    assert run_len.dtype == torch.int32 and run_len.is_contiguous() and deltas.numel() == L * n
     assert in_stats0.dtype == torch.float64 and in_stats0.numel() >= 4
     assert conds is None or (conds.dtype == torch.int64 and conds.numel() == L)
-    return DitBlocks(_p(states), _p(stats), _p(modes), _p(marks[0]), _p(in_stats0), _p(x0),
-                     (C.c_void_p * 2)(buf0.data_ptr(), buf1.data_ptr()), _p(deltas), _p(marks[1]), _p(conds),
-                     n, L, 0)
+    return DitBlocks(_p(states), _p(stats), _p(modes), _p(in_stats0), _p(x0),
+                     (C.c_void_p * 2)(buf0.data_ptr(), buf1.data_ptr()), _p(deltas), _p(run_len), _p(conds), n, L, 0)
 
 
 def dit_begin(cfg: PolicyCfg, blocks: DitBlocks, scratch: torch.Tensor, err=None, stream=None):
