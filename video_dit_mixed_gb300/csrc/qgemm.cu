@@ -43,10 +43,17 @@ namespace sixbit {
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;       // output tile columns
-constexpr int kEpiWarps = 8;   // two per tensor-memory lane quarter, 128 columns each
-constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kEpiCols = kBN / (kEpiWarps / 4);
-constexpr int kGemmThreads = 64 + kEpiThreads;
+// Epilogue warps: the W4A8 fold keeps 128 running sums per thread, so it uses
+// two warps per tensor-memory lane quarter (128 columns each); the other
+// kinds use four per quarter (64 columns each), which spreads the GELU /
+// residual / store work of a tile over twice the threads (their registers
+// then fit the 96-per-thread budget of 576-608 threads).
+template <bool GROUPED>
+struct EpiCfg {
+  static constexpr int kWarps = GROUPED ? 8 : 16;
+  static constexpr int kCols = kBN / (kWarps / 4);  // accumulator columns per thread
+};
+constexpr int kGrpCols = EpiCfg<true>::kCols;       // 128
 
 enum { KIND_BF16 = 0, KIND_NVF4 = 1 };
 
@@ -54,9 +61,9 @@ enum { KIND_BF16 = 0, KIND_NVF4 = 1 };
 // tcgen05 instruction costs its issuing thread tens of cycles, and twelve
 // copies per stage on the MMA thread would pace the main loop.  (Splitting
 // the copies over two warps was slower: the issue cost is shared.)
-template <int KIND>
+template <int KIND, bool GROUPED>
 __host__ __device__ constexpr int gemm_threads() {
-  return kGemmThreads + (KIND == KIND_NVF4 ? 32 : 0);
+  return 64 + EpiCfg<GROUPED>::kWarps * 32 + (KIND == KIND_NVF4 ? 32 : 0);
 }
 
 template <int KIND>
@@ -98,7 +105,7 @@ constexpr int kMaxBufs = 4;  // accumulator buffers the barrier area has room fo
 template <int KIND, bool GROUPED>
 __host__ __device__ constexpr int gemm_smem_bytes() {
   return GemmCfg<KIND>::kStages * stage_bytes<KIND>() + 1024 /*align*/ + 256 /*barriers*/ +
-         (GROUPED ? kSwRing * kEpiWarps * kEpiCols * 4 : 0) /*per-warp ring of group scales*/;
+         (GROUPED ? kSwRing * EpiCfg<true>::kWarps * kGrpCols * 4 : 0) /*per-warp ring of group scales*/;
 }
 
 __device__ __forceinline__ float gelu_erf(float v) {
@@ -110,12 +117,12 @@ __device__ __forceinline__ float gelu_erf(float v) {
 // s_w[g][n] * acc_g[n] to its running sums (128 of them: the register budget
 // of 168 per thread leaves no room for a second chunk in flight).
 constexpr int kFold = 16;
-constexpr int kFoldChunks = kEpiCols / kFold;
+constexpr int kFoldChunks = kGrpCols / kFold;
 
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
 
-__device__ __forceinline__ void fold_chunk(float (&sum)[kEpiCols], int c, const uint32_t (&r)[kFold],
+__device__ __forceinline__ void fold_chunk(float (&sum)[kGrpCols], int c, const uint32_t (&r)[kFold],
                                            const float4* sw4) {
 #pragma unroll
   for (int j4 = 0; j4 < kFold / 4; ++j4) {
@@ -193,11 +200,13 @@ __device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, i
 // Persistent kernel: each CTA walks output tiles t = blockIdx.x, +gridDim.x,
 // ...; p.n_fastest picks whether row or column tiles vary fastest along t.
 template <int KIND, bool GROUPED, bool DBG>
-__global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
+__global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmParams p) {
   using C = GemmCfg<KIND>;
   constexpr int S = C::kStages;
+  constexpr int kEpiWarps = EpiCfg<GROUPED>::kWarps;
+  constexpr int kEpiCols = EpiCfg<GROUPED>::kCols;
   constexpr bool kNvf4 = KIND == KIND_NVF4;
   constexpr uint32_t kCols = 512;
   // NVFP4: the scale factors of stage s live in TMEM columns 256 + 64 s:
@@ -587,7 +596,7 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
   }
   const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  qgemm_kernel<KIND, GROUPED, DBG><<<grid, gemm_threads<KIND>(), smem, st>>>(a, b, p);
+  qgemm_kernel<KIND, GROUPED, DBG><<<grid, gemm_threads<KIND, GROUPED>(), smem, st>>>(a, b, p);
   note_launch();
   return cudaGetLastError();
 }
