@@ -54,8 +54,6 @@ MEASURED_TRAFFIC = {
     ("dit_2b", "qgemm_down:int8"): 585031680,
     ("dit_2b", "hq_x:int8"): 87123712,
     ("dit_2b", "hq_h:int8"): 495252992,
-    ("dit_2b", "qgemm_up:bf16"): 322869504,
-    ("dit_2b", "qgemm_down:bf16"): 530436096,
 }
 MODE_NAMES = {1: "nvfp4", 2: "int8", 3: "bf16", 4: "skip"}
 
