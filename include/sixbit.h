@@ -221,6 +221,20 @@ sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const s
                            int32_t* err_dev, void* stream);
 
 /*
+ * The NVFP4 sixbit_qgemm (bf16 output Y) whose epilogue also takes the first
+ * pass of the NVFP4 quantization of Y (technical summary section 4: the
+ * quantization fused with the kernels around it): *amax_out = max |y| over
+ * y = bf16(Y) . blockdiag(H_b / sqrt b), by the quantizer's own butterfly, so
+ * it equals the amax pass of sixbit_hadamard_quant(Y, b, NVFP4) and can be
+ * passed to it as tamax_in.  had_block in {16, 64}; N % 128 == 0; amax_out a
+ * device float (zeroed by the call).  With mode_dev, the kernel runs (and
+ * amax_out is written) only when the mode word is NVFP4.
+ */
+sixbit_status sixbit_qgemm_rotamax(const sixbit_qact* A, const sixbit_weights* W, int M, int N, int K,
+                                   const int32_t* mode_dev, int epilogue, const uint16_t* residual, uint16_t* Y,
+                                   int had_block, float* amax_out, int32_t* err_dev, void* stream);
+
+/*
  * Block statistics and delta cache update for a computed block step
  * (technical summary sections 2.A-2.C; popular summary sections 1-3):
  * Delta = bf16(f32(x_out) - f32(x_in)) overwrites delta_cache (which holds

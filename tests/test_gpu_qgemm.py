@@ -167,3 +167,24 @@ def test_device_mode_word_selects_the_kernel(ops):
     ops.qgemm(qa, xd, pw, 0, out=y, mode_dev=word)
     torch.cuda.synchronize()
     assert bool((y == 7.0).all())
+
+
+@pytest.mark.parametrize("m,n,k,b,epi", [(300, 256, 384, 64, "gelu"), (17, 512, 256, 16, "none"),
+                                         (1000, 7680, 1920, 64, "gelu")])
+def test_rotamax_epilogue_equals_quantizer_amax_pass(m, n, k, b, epi):
+    """qgemm_rotamax: the same Y as the NVFP4 qgemm, and an amax equal to the quantizer's own
+    amax pass over that Y (bit for bit)."""
+    from video_dit_mixed_gb300 import ops
+    x = synthgen.activations(77 + m, m, k, "laplace", 0.005, 20.0)
+    w = synthgen.weights(78, n, k)
+    pw = ops.pack_weights(torch.from_numpy(w).cuda(), b)
+    xd = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    qa = ops.hadamard_quant(xd, b, ops.MODE_NVFP4)
+    e = ops.EPI_GELU if epi == "gelu" else ops.EPI_NONE
+    y_ref = ops.qgemm(qa, xd, pw, ops.MODE_NVFP4, epilogue=e)
+    amax = torch.full((1,), 123.0, device="cuda")
+    y = ops.qgemm_rotamax(qa, pw, b, amax, epilogue=e)
+    qh = ops.hadamard_quant(y_ref, b, ops.MODE_NVFP4)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+    assert amax.item() == qh.tensor_amax.item() and amax.item() > 0

@@ -59,6 +59,8 @@ EXPORTS = {
                                         C.POINTER(QAct), c_p, c_p]),
     "sixbit_qgemm": (C.c_int, [C.POINTER(QAct), c_p, C.POINTER(Weights), C.c_int, C.c_int, C.c_int, C.c_int,
                                c_p, C.c_int, c_p, c_p, c_p, c_p, c_p, c_p]),
+    "sixbit_qgemm_rotamax": (C.c_int, [C.POINTER(QAct), C.POINTER(Weights), C.c_int, C.c_int, C.c_int, c_p, C.c_int,
+                                       c_p, c_p, C.c_int, c_p, c_p, c_p]),
     "sixbit_block_stats": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),
     "sixbit_policy_step": (C.c_int, [C.POINTER(PolicyCfg), c_p, c_p, c_p, c_p, c_p, c_p]),
     "sixbit_tensor_stats": (C.c_int, [c_p, C.c_int64, c_p, c_p, c_p, c_p]),

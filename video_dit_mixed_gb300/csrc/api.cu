@@ -167,9 +167,10 @@ sixbit_status sixbit_hadamard_quant(const uint16_t* X, int M, int K, int had_blo
   return SIXBIT_OK;
 }
 
-sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W, int M, int N,
-                           int K, int mode, const int32_t* mode_dev, int epilogue, const uint16_t* residual,
-                           uint16_t* Y, float* Y_f32, int32_t* acc_dbg, int32_t* err_dev, void* stream) {
+static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W, int M,
+                                int N, int K, int mode, const int32_t* mode_dev, int epilogue,
+                                const uint16_t* residual, uint16_t* Y, float* Y_f32, int32_t* acc_dbg,
+                                int32_t* err_dev, void* stream, int had_block, float* rot_amax) {
   if (W == nullptr || (Y == nullptr && Y_f32 == nullptr)) return SIXBIT_EINVAL;
   if (epilogue != SIXBIT_EPI_NONE && epilogue != SIXBIT_EPI_GELU && epilogue != SIXBIT_EPI_RESIDUAL)
     return SIXBIT_EINVAL;
@@ -178,9 +179,10 @@ sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const s
   if ((Y && !aligned16(Y)) || (Y_f32 && !aligned16(Y_f32)) || (residual && !aligned16(residual)))
     return SIXBIT_EALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool only_fp4 = rot_amax != nullptr;  // the rotated-amax epilogue exists for the NVFP4 kind only
   const bool run_fp4 = mode_dev != nullptr || mode == SIXBIT_MODE_NVFP4;
-  const bool run_i8 = mode_dev != nullptr || mode == SIXBIT_MODE_INT8;
-  const bool run_bf = mode_dev != nullptr || mode == SIXBIT_MODE_BF16;
+  const bool run_i8 = !only_fp4 && (mode_dev != nullptr || mode == SIXBIT_MODE_INT8);
+  const bool run_bf = !only_fp4 && (mode_dev != nullptr || mode == SIXBIT_MODE_BF16);
   if (mode_dev == nullptr && !run_fp4 && !run_i8 && !run_bf) return mode == SIXBIT_MODE_SKIP ? SIXBIT_OK : SIXBIT_EINVAL;
   if ((run_fp4 || run_i8) && A == nullptr) return SIXBIT_EINVAL;
   if (run_fp4 && (A->fp4_codes == nullptr || A->fp4_scales == nullptr || A->tensor_scale == nullptr ||
@@ -197,6 +199,7 @@ sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const s
     return SIXBIT_EALIGN;
   sixbit_status s = check_device();
   if (s != SIXBIT_OK) return s;
+  if (rot_amax != nullptr && cudaMemsetAsync(rot_amax, 0, sizeof(float), st) != cudaSuccess) return SIXBIT_ECUDA;
 
   GemmParams p{};
   p.M = M;
@@ -213,6 +216,8 @@ sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const s
   // smaller one is re-read from L2 (an A of 17776 x 7680 bf16 does not fit
   // in L2 and would be re-read from HBM once per column-tile pass).
   p.n_fastest = M > N ? 1 : 0;
+  p.rot_amax = rot_amax;
+  p.had_block = had_block;
   if (run_fp4) {
     CUtensorMap ma, mb;
     if (!make_map(&ma, A->fp4_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, M, K / 2, 128) ||
@@ -248,6 +253,22 @@ sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const s
     if (launch_qgemm_bf16(ma, mb, q, st) != cudaSuccess) return SIXBIT_ECUDA;
   }
   return SIXBIT_OK;
+}
+
+sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W, int M, int N,
+                           int K, int mode, const int32_t* mode_dev, int epilogue, const uint16_t* residual,
+                           uint16_t* Y, float* Y_f32, int32_t* acc_dbg, int32_t* err_dev, void* stream) {
+  return qgemm_impl(A, X_bf16, W, M, N, K, mode, mode_dev, epilogue, residual, Y, Y_f32, acc_dbg, err_dev, stream,
+                    0, nullptr);
+}
+
+sixbit_status sixbit_qgemm_rotamax(const sixbit_qact* A, const sixbit_weights* W, int M, int N, int K,
+                                   const int32_t* mode_dev, int epilogue, const uint16_t* residual, uint16_t* Y,
+                                   int had_block, float* amax_out, int32_t* err_dev, void* stream) {
+  if (Y == nullptr || amax_out == nullptr) return SIXBIT_EINVAL;
+  if ((had_block != 16 && had_block != 64) || N % 128 != 0) return SIXBIT_ESHAPE;
+  return qgemm_impl(A, nullptr, W, M, N, K, SIXBIT_MODE_NVFP4, mode_dev, epilogue, residual, Y, nullptr, nullptr,
+                    err_dev, stream, had_block, amax_out);
 }
 
 sixbit_status sixbit_block_stats(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta_cache, int64_t n,

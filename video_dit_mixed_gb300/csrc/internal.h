@@ -26,6 +26,8 @@ struct GemmParams {
   int32_t* acc_dbg;
   int32_t* err;
   int n_fastest;           // tile order: 1 = output column tiles fastest, 0 = row tiles fastest
+  float* rot_amax;         // NVFP4 epilogue: atomicMax of |bf16(Y) . blockdiag(H_b / sqrt b)| (or NULL)
+  int had_block;           // b of rot_amax (16 or 64)
 };
 
 cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, float* amax_out,

@@ -184,17 +184,52 @@ __device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, i
   } else {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      if (n + 8 * q + 8 <= p.N) {
-        uint32_t w[4];
+      uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
-          w[i] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-        *reinterpret_cast<uint4*>(p.Y + base + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&b);
+        v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);            // the stored value (read by rot_amax)
+        v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
       }
+      if (n + 8 * q + 8 <= p.N) *reinterpret_cast<uint4*>(p.Y + base + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
+}
+
+// max |y| over a thread's 64 output columns after the block Hadamard rotation
+// y = x . blockdiag(H_b / sqrt b), b in {16, 64}: the same FP32 butterfly
+// (ascending strides, exact power-of-two scale last) as the quantizer, so
+// the maximum over all threads equals its amax pass over the stored Y.
+template <int B>
+__device__ __forceinline__ float rot_amax64(float (&v)[2][32]) {
+#pragma unroll
+  for (int h = 1; h < 32 && h < B; h <<= 1) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if ((i & h) == 0) {
+          const float a = v[c][i], b = v[c][i + h];
+          v[c][i] = __fadd_rn(a, b);
+          v[c][i + h] = __fsub_rn(a, b);
+        }
+  }
+  constexpr float s = B == 16 ? 0.25f : 0.125f;
+  float m = 0.f;
+  if constexpr (B == 64) {  // the last stage pairs the two halves
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      m = fmaxf(m, fabsf(__fmul_rn(__fadd_rn(v[0][i], v[1][i]), s)));
+      m = fmaxf(m, fabsf(__fmul_rn(__fsub_rn(v[0][i], v[1][i]), s)));
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(__fmul_rn(v[c][i], s)));
+  }
+  return m;
 }
 
 // Persistent kernel: each CTA walks output tiles t = blockIdx.x, +gridDim.x,
@@ -496,12 +531,24 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
 #pragma unroll
           for (int c = 0; c < kEpiCols / 32; ++c) tmem_ld_wait(r[c]);
           release_acc(&acce[buf], lane);
+          float v[kEpiCols / 32][32];
 #pragma unroll
           for (int c = 0; c < kEpiCols / 32; ++c) {
-            float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[c][j]), alpha);
-            if (nb + c * 32 < p.N) epilogue_store32(p, row, nb + c * 32, v);
+            for (int j = 0; j < 32; ++j) v[c][j] = __fmul_rn(__uint_as_float(r[c][j]), alpha);
+            if (nb + c * 32 < p.N) epilogue_store32(p, row, nb + c * 32, v[c]);
+          }
+          if constexpr (kEpiCols == 64) {
+            if (p.rot_amax != nullptr) {  // the next quantizer's amax pass, on the stored values
+              float m = 0.f;
+              if (row < p.M && nb < p.N) m = p.had_block == 16 ? rot_amax64<16>(v) : rot_amax64<64>(v);
+              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+              if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(p.rot_amax), __float_as_uint(m));  // m >= 0
+            }
           }
         } else {
 #pragma unroll 1

@@ -108,13 +108,17 @@ class DiT:
         note = note or (lambda label: None)
         up, down = self.packed[l]
         quant = mode != o.MODE_BF16
+        fused = mode == o.MODE_NVFP4 and self.b in (16, 64)   # the up GEMM also takes h's amax pass
         if quant:
             o.hadamard_quant(x, self.b, mode, out=self.qa_x)
             note("hq_x")
-        o.qgemm(self.qa_x if quant else None, x, up, mode, epilogue=o.EPI_GELU, out=self.h, m=self.T)
+        if fused:
+            o.qgemm_rotamax(self.qa_x, up, self.b, self.qa_h.tensor_amax, epilogue=o.EPI_GELU, out=self.h, m=self.T)
+        else:
+            o.qgemm(self.qa_x if quant else None, x, up, mode, epilogue=o.EPI_GELU, out=self.h, m=self.T)
         note("qgemm_up")
         if quant:
-            o.hadamard_quant(self.h, self.b, mode, out=self.qa_h)
+            o.hadamard_quant(self.h, self.b, mode, out=self.qa_h, tamax=self.qa_h.tensor_amax if fused else None)
             note("hq_h")
         o.qgemm(self.qa_h if quant else None, self.h, down, mode, epilogue=o.EPI_RESIDUAL, residual=x, out=out,
                 m=self.T)

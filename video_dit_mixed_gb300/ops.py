@@ -115,6 +115,19 @@ def qgemm(a: QActTensors | None, x_bf16, w: PackedWeights, mode: int, epilogue: 
     return out
 
 
+def qgemm_rotamax(a: QActTensors, w: PackedWeights, had_block: int, amax_out: torch.Tensor, epilogue: int = EPI_NONE,
+                  residual=None, out=None, mode_dev=None, err=None, stream=None, m: int | None = None):
+    """NVFP4 qgemm whose epilogue also writes the rotated amax of its bf16 output to amax_out."""
+    n, k = w.n, w.k
+    m = m if m is not None else a.m
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=w.bf16_w.device)
+    ca, cw = a.c(), w.c()
+    check(_lib.sixbit_qgemm_rotamax(C.byref(ca), C.byref(cw), m, n, k, _p(mode_dev), epilogue, _p(residual), _p(out),
+                                    had_block, _p(amax_out), _p(err), _stream(stream)), "qgemm_rotamax")
+    return out
+
+
 def tensor_stats(x: torch.Tensor, out: torch.Tensor, scratch: torch.Tensor, stream=None) -> torch.Tensor:
     check(_lib.sixbit_tensor_stats(_p(x), x.numel(), _p(out), _p(scratch), None, _stream(stream)), "tensor_stats")
     return out
