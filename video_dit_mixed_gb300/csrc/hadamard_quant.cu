@@ -271,8 +271,11 @@ __device__ __forceinline__ void int8_chunk_store(const float (&v)[8], int r, int
   uint32_t t[8], o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float d = fast ? div_by_recip(v[i], s, rs) : __fdiv_rn(v[i], s);
-    d = fminf(fmaxf(d, -127.f), 127.f);
+    // With s = RN(amax / 127) normal, |RN(y / s)| <= 127 (1 + 2^-24): the clamp
+    // cannot bind, and is only applied on the IEEE-division path (s subnormal
+    // or huge, where s carries less precision).  (A NaN y gives an unspecified
+    // code on the fast path.)
+    const float d = fast ? div_by_recip(v[i], s, rs) : fminf(fmaxf(__fdiv_rn(v[i], s), -127.f), 127.f);
     const float ti = __fadd_rn(d, kRound);
     t[i] = __float_as_uint(ti);                     // 0x4B400000 + q
     o[i] = __float_as_uint(__fsub_rn(ti, kRound));  // q as float, exact (and exact in bf16)
