@@ -50,10 +50,6 @@ FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio (FP4 13.5 PFLOP/s, BF16 2.25
 # on the same shapes (profiles/dram_traffic_dit_2b.md); an entry must be
 # removed when its kernel changes.
 MEASURED_TRAFFIC = {
-    ("dit_2b", "qgemm_up:int8"): 324860416,
-    ("dit_2b", "qgemm_down:int8"): 585031680,
-    ("dit_2b", "hq_x:int8"): 87123712,
-    ("dit_2b", "hq_h:int8"): 495252992,
 }
 MODE_NAMES = {1: "nvfp4", 2: "int8", 3: "bf16", 4: "skip"}
 

@@ -63,6 +63,21 @@ static bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dtype
   return r == CUDA_SUCCESS;
 }
 
+// bf16 output Y [rows, cols] for the GEMM epilogue's TMA stores: box 32
+// columns (64 bytes) x 32 rows, 64-byte swizzle.
+static bool make_store_map(CUtensorMap* m, const uint16_t* Y, int rows, int cols) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(Y), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace sixbit
 
 using namespace sixbit;
@@ -218,6 +233,11 @@ static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, co
   p.n_fastest = M > N ? 1 : 0;
   p.rot_amax = rot_amax;
   p.had_block = had_block;
+  // The BF16 kind writes a bf16 Y through TMA stores (Y 16-byte aligned,
+  // N % 16 == 0 checked above); an FP32 Y is stored directly.
+  CUtensorMap my{};
+  p.y_tma = (Y_f32 == nullptr && run_bf) ? 1 : 0;
+  if (p.y_tma && !make_store_map(&my, Y, M, N)) return SIXBIT_ECUDA;
   if (run_fp4) {
     CUtensorMap ma, mb;
     if (!make_map(&ma, A->fp4_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, M, K / 2, 128) ||
@@ -241,7 +261,7 @@ static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, co
     q.row_scale = A->row_scale;
     q.grp_scale = W->i4_scales;
     q.acc_dbg = acc_dbg;
-    if (launch_qgemm_int8(ma, mb, q, st) != cudaSuccess) return SIXBIT_ECUDA;
+    if (launch_qgemm_int8(ma, mb, my, q, st) != cudaSuccess) return SIXBIT_ECUDA;
   }
   if (run_bf) {
     CUtensorMap ma, mb;
@@ -250,7 +270,7 @@ static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, co
       return SIXBIT_ECUDA;
     GemmParams q = p;
     q.want_mode = SIXBIT_MODE_BF16;
-    if (launch_qgemm_bf16(ma, mb, q, st) != cudaSuccess) return SIXBIT_ECUDA;
+    if (launch_qgemm_bf16(ma, mb, my, q, st) != cudaSuccess) return SIXBIT_ECUDA;
   }
   return SIXBIT_OK;
 }

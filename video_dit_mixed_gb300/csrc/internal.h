@@ -28,6 +28,7 @@ struct GemmParams {
   int n_fastest;           // tile order: 1 = output column tiles fastest, 0 = row tiles fastest
   float* rot_amax;         // NVFP4 epilogue: atomicMax of |bf16(Y) . blockdiag(H_b / sqrt b)| (or NULL)
   int had_block;           // b of rot_amax (16 or 64)
+  int y_tma;               // BF16 kind: bf16 Y is written by TMA stores through the Y tensor map
 };
 
 cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, float* amax_out,
@@ -59,7 +60,10 @@ cudaError_t launch_policy(const sixbit_policy_cfg& cfg, sixbit_policy_state* st_
                           const double* in_stats, int32_t* mode_out, cudaStream_t st);
 
 cudaError_t launch_qgemm_nvf4(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st);
-cudaError_t launch_qgemm_bf16(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st);
-cudaError_t launch_qgemm_int8(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st);
+// y: tensor map of the bf16 output (box 32 x 32, 64-byte swizzle), used when p.y_tma.
+cudaError_t launch_qgemm_bf16(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
+                              cudaStream_t st);
+cudaError_t launch_qgemm_int8(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
+                              cudaStream_t st);
 
 }  // namespace sixbit

@@ -102,11 +102,32 @@ __host__ __device__ constexpr int stage_bytes() {
 constexpr int kSwRing = 4;
 constexpr int kMaxBufs = 4;  // accumulator buffers the barrier area has room for
 
+// The BF16 kind stages each epilogue warp's 32 x 32 bf16 output chunk in
+// shared memory (64-byte rows, 64-byte TMA swizzle) and writes it with one
+// TMA store: a warp's direct stores would touch 32 rows, 16 bytes each
+// (310 vs 329 us at 17776 x 7680 x 1920).  NVFP4 has no shared memory left;
+// in W4A8 the store path's registers cost the group fold more than the
+// stores gain when the epilogue has GELU or a residual (540 vs 517 us), so
+// both store directly.
+template <int KIND, bool GROUPED>
+__host__ __device__ constexpr bool tma_y() {
+  return KIND != KIND_NVF4 && !GROUPED;
+}
+constexpr int kBoxBytes = 32 * 64;
+template <int KIND, bool GROUPED>
+__host__ __device__ constexpr int staging_bytes() {
+  return tma_y<KIND, GROUPED>() ? EpiCfg<GROUPED>::kWarps * kBoxBytes : 0;
+}
+
+// Layout: [stages | output staging | barriers (256 B) | W4A8 group-scale rings].
 template <int KIND, bool GROUPED>
 __host__ __device__ constexpr int gemm_smem_bytes() {
-  return GemmCfg<KIND>::kStages * stage_bytes<KIND>() + 1024 /*align*/ + 256 /*barriers*/ +
-         (GROUPED ? kSwRing * EpiCfg<true>::kWarps * kGrpCols * 4 : 0) /*per-warp ring of group scales*/;
+  return GemmCfg<KIND>::kStages * stage_bytes<KIND>() + staging_bytes<KIND, GROUPED>() + 1024 /*align*/ +
+         256 /*barriers*/ + (GROUPED ? kSwRing * EpiCfg<true>::kWarps * kGrpCols * 4 : 0) /*per-warp ring of group scales*/;
 }
+static_assert(gemm_smem_bytes<KIND_BF16, true>() <= 227 * 1024 && gemm_smem_bytes<KIND_BF16, false>() <= 227 * 1024 &&
+                  gemm_smem_bytes<KIND_NVF4, false>() <= 227 * 1024,
+              "shared memory per CTA");
 
 __device__ __forceinline__ float gelu_erf(float v) {
   return 0.5f * v * (1.0f + erff(v * 0.7071067811865475244f));
@@ -154,10 +175,9 @@ __device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
   if (lane == 0) mbar_arrive(bar);
 }
 
-// Applies the epilogue to 32 consecutive columns [n, n+32) of one row and
-// stores them (bf16 or fp32).
-__device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, int n, float (&v)[32]) {
-  if (row >= p.M) return;
+// Applies the epilogue (GELU, or the residual add) to 32 consecutive columns
+// [n, n+32) of row `row` < M.
+__device__ __forceinline__ void epilogue_apply32(const GemmParams& p, int row, int n, float (&v)[32]) {
   const size_t base = static_cast<size_t>(row) * p.N + n;
   if (p.epilogue == SIXBIT_EPI_GELU) {
 #pragma unroll
@@ -176,6 +196,14 @@ __device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, i
       }
     }
   }
+}
+
+// Applies the epilogue to 32 consecutive columns [n, n+32) of one row and
+// stores them (bf16 or fp32) directly.
+__device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, int n, float (&v)[32]) {
+  if (row >= p.M) return;
+  const size_t base = static_cast<size_t>(row) * p.N + n;
+  epilogue_apply32(p, row, n, v);
   if (p.Yf != nullptr) {
 #pragma unroll
     for (int q = 0; q < 8; ++q)
@@ -194,6 +222,23 @@ __device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, i
       }
       if (n + 8 * q + 8 <= p.N) *reinterpret_cast<uint4*>(p.Y + base + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+  }
+}
+
+// Writes row r's 32 values as bf16 (round to nearest even) into a 32-row box
+// of 64-byte rows, 16-byte chunk q of row r at chunk q ^ ((r >> 1) & 3): the
+// TMA 64-byte swizzle (box 512-byte aligned), which also spreads a warp's
+// 16-byte writes over all banks.
+__device__ __forceinline__ void stage_bf16x32(uint8_t* box, int r, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(box + r * 64 + ((q ^ ((r >> 1) & 3)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -237,7 +282,7 @@ __device__ __forceinline__ float rot_amax64(float (&v)[2][32]) {
 template <int KIND, bool GROUPED, bool DBG>
 __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const GemmParams p) {
+                 const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
   using C = GemmCfg<KIND>;
   constexpr int S = C::kStages;
   constexpr int kEpiWarps = EpiCfg<GROUPED>::kWarps;
@@ -256,7 +301,8 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* tiles = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * stage_bytes<KIND>());
+  uint8_t* staging = smem + S * stage_bytes<KIND>();  // [kEpiWarps] output boxes (BF16 kind)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + staging_bytes<KIND, GROUPED>());
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* accf = bars + 2 * S;                    // [kBufs] accumulator buffer ready
@@ -267,7 +313,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
   static_assert((3 * S + 2 * kMaxBufs + 1) * 8 + 8 <= 256, "barrier area");
   static_assert(kBufs <= kMaxBufs && kBufs * kBN + (kNvf4 ? S * 64 : 0) <= kCols, "tensor memory");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* sw_smem = reinterpret_cast<float*>(smem + S * stage_bytes<KIND>() + 256);  // GROUPED: per-warp scales
+  float* sw_smem = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);  // GROUPED: per-warp scales
 
   auto A_tile = [&](int s) { return tiles + s * stage_bytes<KIND>(); };
   auto B_tile = [&](int s) { return tiles + s * stage_bytes<KIND>() + kATileBytes; };
@@ -312,6 +358,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (tma_y<KIND, GROUPED>() && p.y_tma) prefetch_tmap(&tmY);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kCols);
@@ -413,7 +460,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
           tc_commit(&empty[s]);
           const bool acc_end = GROUPED ? (kb % spg) == spg - 1 : kb == nk - 1;
           if (acc_end) {
-            tc_commit(&accf[buf]);
+            if constexpr (!GROUPED) tc_commit(&accf[buf]);  // W4A8: the epilogue waits on empty[s]
             ++ac;
           }
         }
@@ -432,8 +479,36 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
     const int col0 = (ew >> 2) * kEpiCols;        // first accumulator column of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16) + col0;
     float* my_sw = sw_smem + ew * kSwRing * kEpiCols;  // GROUPED: this warp's ring of group scales
+    uint8_t* my_box = staging + ew * kBoxBytes;         // BF16 kind: this warp's output box
+    // Epilogue + store of columns [n, n + 32) of this lane's row (n < N, warp-uniform).
+    auto store32 = [&](int row, int n, float (&v)[32]) {
+      if constexpr (tma_y<KIND, GROUPED>()) {
+        if (p.y_tma) {
+          if (row < p.M) epilogue_apply32(p, row, n, v);
+          if (lane == 0) bulk_wait_read0();  // the previous box has been read out
+          __syncwarp();
+          stage_bf16x32(my_box, lane, v);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {  // rows >= M and columns >= N of the box are not written
+            tma_store_2d(&tmY, my_box, n, row - lane);
+            bulk_commit();
+          }
+          return;
+        }
+      }
+      epilogue_store32(p, row, n, v);
+    };
     uint32_t ac = 0;
     bool ok = true;
+    // W4A8: group ac's MMAs are complete when the commit after its last stage
+    // (stage counter 2 ac + 1) arrives on that stage's empty barrier, so no
+    // commit of its own is issued (each tcgen05.commit costs the MMA thread
+    // time per group).  The barrier cannot run a phase past this wait: its
+    // next phase needs the MMAs of group ac + 2, which wait for this group's
+    // buffer to be released.
+    auto grp_done = [&](uint32_t a) { return &empty[(2 * a + 1) % S]; };
+    auto grp_par = [&](uint32_t a) { return ((2 * a + 1) / S) & 1; };
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       int m_tile, n_tile;
       tile_of(t, m_tile, n_tile);
@@ -443,7 +518,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
         if constexpr (GROUPED) {
           for (int g = 0; g < groups && ok; ++g, ++ac) {
             const uint32_t buf = ac % kBufs;
-            if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(grp_done(ac), grp_par(ac), abort_flag)) { ok = false; break; }
             release_acc(&acce[buf], lane);
           }
         } else {
@@ -474,7 +549,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
           cp_async_wait_newest<kSwRing - 1>();     // this lane's copy of group g has landed
           __syncwarp();                            // and every other lane's
           const uint32_t buf = ac % kBufs;
-          if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) {
+          if (!mbar_wait(grp_done(ac), grp_par(ac), abort_flag)) {
             ok = false;
             break;
           }
@@ -512,7 +587,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(sum[c * 32 + j], sm);
-          if (nb + c * 32 < p.N) epilogue_store32(p, row, nb + c * 32, v);
+          if (nb + c * 32 < p.N) store32(row, nb + c * 32, v);
         }
       } else {
         const uint32_t buf = ac % kBufs;
@@ -560,7 +635,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
-            if (nb + c * 32 < p.N) epilogue_store32(p, row, nb + c * 32, v);
+            if (nb + c * 32 < p.N) store32(row, nb + c * 32, v);
           }
         }
         ++ac;
@@ -570,6 +645,8 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
       set_error(p.err, SIXBIT_ETIMEOUT);
       *abort_flag = 1;
     }
+    if (tma_y<KIND, GROUPED>() && lane == 0) bulk_wait0();  // every output box has been written
+    __syncwarp();
     tc_fence_before();
   } else if constexpr (kNvf4) {
     if (lane == 0) {
@@ -632,7 +709,8 @@ static int num_sms() {
 }
 
 template <int KIND, bool GROUPED, bool DBG>
-static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
+static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
+                              cudaStream_t st) {
   static bool attr_done = false;
   constexpr int smem = gemm_smem_bytes<KIND, GROUPED>();
   if (!attr_done) {
@@ -643,20 +721,24 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
   }
   const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  qgemm_kernel<KIND, GROUPED, DBG><<<grid, gemm_threads<KIND, GROUPED>(), smem, st>>>(a, b, p);
+  qgemm_kernel<KIND, GROUPED, DBG><<<grid, gemm_threads<KIND, GROUPED>(), smem, st>>>(a, b, y, p);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_qgemm_nvf4(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
-  return launch_one<KIND_NVF4, false, false>(a, b, p, st);
+  GemmParams q = p;
+  q.y_tma = 0;
+  return launch_one<KIND_NVF4, false, false>(a, b, a /*unused*/, q, st);
 }
-cudaError_t launch_qgemm_bf16(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
-  return launch_one<KIND_BF16, false, false>(a, b, p, st);
+cudaError_t launch_qgemm_bf16(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
+                              cudaStream_t st) {
+  return launch_one<KIND_BF16, false, false>(a, b, y, p, st);
 }
-cudaError_t launch_qgemm_int8(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
-  if (p.acc_dbg != nullptr) return launch_one<KIND_BF16, true, true>(a, b, p, st);
-  return launch_one<KIND_BF16, true, false>(a, b, p, st);
+cudaError_t launch_qgemm_int8(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
+                              cudaStream_t st) {
+  if (p.acc_dbg != nullptr) return launch_one<KIND_BF16, true, true>(a, b, y, p, st);
+  return launch_one<KIND_BF16, true, false>(a, b, y, p, st);
 }
 
 }  // namespace sixbit
