@@ -265,9 +265,25 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_nvfp4_kernel(const uint16_t*
 // complement.  Clamping before rounding equals clamping after it (rounding
 // is monotone and +-127 are integers).  When s == 0 (all |y| rounded away)
 // the reciprocal is taken as 0, which gives q = 0.
+constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+
+// Writes one lane's 8 results: t = the rounding sums (0x4B400000 + q), o = q
+// as floats; the codes as int8, the operand as bf16 (both optional).
+__device__ __forceinline__ void int8_write8(const uint32_t (&t)[8], const uint32_t (&o)[8], size_t off,
+                                            int8_t* codes, uint16_t* operand) {
+  if (codes != nullptr) {
+    const uint32_t lo = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+    const uint32_t hi = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
+    *reinterpret_cast<uint2*>(codes + off) = make_uint2(lo, hi);
+  }
+  if (operand != nullptr)
+    *reinterpret_cast<uint4*>(operand + off) =
+        make_uint4(__byte_perm(o[0], o[1], 0x7632), __byte_perm(o[2], o[3], 0x7632), __byte_perm(o[4], o[5], 0x7632),
+                   __byte_perm(o[6], o[7], 0x7632));
+}
+
 __device__ __forceinline__ void int8_chunk_store(const float (&v)[8], int r, int col, int K, float s, bool fast,
                                                  float rs, int8_t* codes, uint16_t* operand, float* rotated) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
   uint32_t t[8], o[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -281,15 +297,7 @@ __device__ __forceinline__ void int8_chunk_store(const float (&v)[8], int r, int
     o[i] = __float_as_uint(__fsub_rn(ti, kRound));  // q as float, exact (and exact in bf16)
   }
   const size_t off = static_cast<size_t>(r) * K + col;
-  if (codes != nullptr) {
-    const uint32_t lo = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
-    const uint32_t hi = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
-    *reinterpret_cast<uint2*>(codes + off) = make_uint2(lo, hi);
-  }
-  if (operand != nullptr)
-    *reinterpret_cast<uint4*>(operand + off) =
-        make_uint4(__byte_perm(o[0], o[1], 0x7632), __byte_perm(o[2], o[3], 0x7632), __byte_perm(o[4], o[5], 0x7632),
-                   __byte_perm(o[6], o[7], 0x7632));
+  int8_write8(t, o, off, codes, operand);
   if (rotated != nullptr) {
     float4* dst = reinterpret_cast<float4*>(rotated + off);
     dst[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -353,8 +361,43 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_int8_kernel(const uint16_t* 
 // once.  The row amax is combined across the team through shared memory.
 // Serves rows of up to 16 * 4 * 256 elements, with the results of
 // hq_int8_kernel (same butterfly, same per-element division).
+//
+// Chunks are processed in pairs on packed FP32 pairs: element i of chunk 2p
+// in the low lane, element i of chunk 2p + 1 in the high lane.  Both lanes
+// take the same butterfly position, so every stage and every step of the
+// division is one f32x2 instruction for two elements, each lane rounded
+// exactly as the scalar operation.  The exact 1/sqrt(b) scaling is folded
+// into the divisor: y / s = v / (s sqrt(b)) with both scalings exact, so
+// RN(y / s) is unchanged (when y = v / sqrt(b) is an inexact subnormal,
+// |y / s| < 2^-26 on this path and both round to q = 0).
 constexpr int kHqRowWarps = 16;
 constexpr int kHqRowChunks = 4;
+
+template <int B>
+__device__ __forceinline__ void fwht8x2(uint64_t (&v)[8], int lane) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & h) == 0) {
+        const uint64_t a = v[i], c = v[i + h];
+        v[i] = f2_add(a, c);
+        v[i + h] = f2_sub(a, c);
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 8; h < B; h <<= 1) {
+    const int m = h >> 3;
+    const float sgn = (lane & m) ? -1.0f : 1.0f;  // lower lane: v + o; upper lane: o - v (one rounding)
+    const uint64_t sg2 = f2_pack(sgn, sgn);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, static_cast<unsigned long long>(v[i]), m);
+      v[i] = f2_fma(sg2, v[i], o);
+    }
+  }
+}
 
 template <int B>
 __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const uint16_t* __restrict__ X, int M,
@@ -362,6 +405,7 @@ __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const
                                                                         int8_t* codes, float* row_scale,
                                                                         uint16_t* operand, float* rotated) {
   if (mode_skips(mode_dev, SIXBIT_MODE_INT8)) return;
+  constexpr float kScale = B == 16 ? 0.25f : (B == 64 ? 0.125f : 0.0625f);  // 1/sqrt(B), exact
   __shared__ float red[kHqRowWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = 1 << lr;
@@ -378,14 +422,18 @@ __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const
     raw[u] = make_uint4(0, 0, 0, 0);
     if (row_ok && c < nch && col < K) raw[u] = ld_nc_16(row + col);
   }
-  float v[kHqRowChunks][8];
+  uint64_t v[kHqRowChunks / 2][8];  // unscaled rotated values of chunk pairs (2p, 2p + 1)
   float m = 0.f;
 #pragma unroll
-  for (int u = 0; u < kHqRowChunks; ++u) {
-    bf16x8_to_f32(raw[u], v[u]);
-    if (t + u * R < nch) fwht8<B>(v[u], lane);  // warp-uniform condition
+  for (int p = 0; p < kHqRowChunks / 2; ++p) {
+    float a[8], b[8];
+    bf16x8_to_f32(raw[2 * p], a);
+    bf16x8_to_f32(raw[2 * p + 1], b);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[u][i]));
+    for (int i = 0; i < 8; ++i) v[p][i] = f2_pack(a[i], b[i]);
+    if (t + 2 * p * R < nch) fwht8x2<B>(v[p], lane);  // warp-uniform; an absent chunk holds zeros
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(f2_lo(v[p][i])), fabsf(f2_hi(v[p][i]))));
   }
   m = warp_max(m);
   if (lane == 0) red[warp] = m;
@@ -393,14 +441,63 @@ __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const
   m = red[team << lr];
   for (int i = 1; i < R; ++i) m = fmaxf(m, red[(team << lr) + i]);
   if (!row_ok) return;
-  const float s = __fdiv_rn(m, 127.0f);
+  // max |y| = RN(max |v| / sqrt(B)): rounding is monotone, so this is the
+  // maximum of the rounded rotated values.
+  const float s = __fdiv_rn(__fmul_rn(m, kScale), 127.0f);
   const bool fast = recip_ok(s) || s == 0.f;
   const float rs = s != 0.f ? __frcp_rn(s) : 0.f;
+  const uint64_t rs2 = f2_pack(rs * kScale, rs * kScale);  // RN(1 / (s sqrt(B))), exact; s sqrt(B) = s / kScale
+  const uint64_t kr2 = f2_pack(kRound, kRound);
   if (t == 0 && lane == 0) row_scale[r] = s;
+  const uint64_t ns2 = f2_pack(-(s / kScale), -(s / kScale));
 #pragma unroll
-  for (int u = 0; u < kHqRowChunks; ++u) {
-    const int col = (t + u * R) * 256 + lane * 8;
-    if (t + u * R < nch && col < K) int8_chunk_store(v[u], r, col, K, s, fast, rs, codes, operand, rotated);
+  for (int p = 0; p < kHqRowChunks / 2; ++p) {
+    // q as floats (the rounding sums are q + 1.5 * 2^23 again, exactly); the
+    // row-uniform branch keeps the IEEE-division fallback out of the fast loop.
+    if (rotated != nullptr) {  // the rotated values y = v / sqrt(B) (FP32, test output)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = t + (2 * p + h) * R;
+        const int col = c * 256 + lane * 8;
+        if (c >= nch || col >= K) continue;
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(h ? f2_hi(v[p][i]) : f2_lo(v[p][i]), kScale);
+        float4* dst = reinterpret_cast<float4*>(rotated + static_cast<size_t>(r) * K + col);
+        dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+        dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+      }
+    }
+    uint64_t oi[8];
+    if (fast) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // div_by_recip on both lanes
+        const uint64_t q = f2_mul(v[p][i], rs2);
+        const uint64_t d = f2_fma(f2_fma(ns2, q, v[p][i]), rs2, q);
+        oi[i] = f2_sub(f2_add(d, kr2), kr2);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float dl = fminf(fmaxf(__fdiv_rn(__fmul_rn(f2_lo(v[p][i]), kScale), s), -127.f), 127.f);
+        const float dh = fminf(fmaxf(__fdiv_rn(__fmul_rn(f2_hi(v[p][i]), kScale), s), -127.f), 127.f);
+        oi[i] = f2_sub(f2_add(f2_pack(dl, dh), kr2), kr2);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = t + (2 * p + h) * R;
+      const int col = c * 256 + lane * 8;
+      if (c >= nch || col >= K) continue;
+      uint32_t tt[8], oo[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) oo[i] = static_cast<uint32_t>(h ? (oi[i] >> 32) : oi[i]);
+      if (codes != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tt[i] = __float_as_uint(__fadd_rn(__uint_as_float(oo[i]), kRound));
+      }
+      int8_write8(tt, oo, static_cast<size_t>(r) * K + col, codes, operand);
+    }
   }
 }
 
