@@ -83,6 +83,22 @@ def test_int8_quant_row_teams_bit_exact(ops, m, k, b):
     _check_int8(ops, synthgen.activations(300 + k, m, k, "laplace", 0.01, 30.0), b)
 
 
+@pytest.mark.parametrize("k", [1920, 16640])
+def test_int8_extreme_row_magnitudes(ops, k):
+    """Rows whose scale s = amax/127 is below 2^-100 or above 2^100 take the
+    IEEE-division path; a row with amax ~1e-26 keeps the reciprocal path while
+    some of its rotated values are subnormal.  Bit-exact against the oracle in
+    both INT8 kernels (one-pass rows kernel, two-pass kernel past 16384)."""
+    x = synthgen.activations(77, 6, k, "normal", 0.0, 1.0)
+    x[0] *= 1e-30                      # s ~ 1e-32 < 2^-100
+    x[1] *= 1e35                       # s ~ 1e33 > 2^100
+    x[2] *= 1e-26
+    x[2, 64:128] = np.where(np.arange(64) % 3 == 0, 1.0, -1.0) * 2.0 ** -130  # a block of subnormals
+    x[3] = 0.0
+    x[3, 5] = 2.0 ** -120              # a lone tiny value: s subnormal
+    _check_int8(ops, synthgen.bf16_rne(x), 64)
+
+
 def test_int8_operand_without_codes(ops):
     """i8_codes may be NULL when the bf16 operand is requested: same operand and scales."""
     x = synthgen.activations(41, 96, 7680, "normal", 0.01, 20.0)
