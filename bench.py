@@ -50,9 +50,7 @@ FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio (FP4 13.5 PFLOP/s, BF16 2.25
 # on the same shapes (profiles/dram_traffic_dit_2b.md); an entry must be
 # removed when its kernel changes.
 MEASURED_TRAFFIC = {
-    ("dit_2b", "qgemm_up:int8"): 325239680,
     ("dit_2b", "qgemm_down:int8"): 597813504,
-    ("dit_2b", "qgemm_up:bf16"): 333118054,
     ("dit_2b", "qgemm_down:bf16"): 544985420,
     ("dit_2b", "hq_x:int8"): 86517376,
     ("dit_2b", "hq_h:int8"): 495358848,

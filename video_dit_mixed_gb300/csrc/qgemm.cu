@@ -129,8 +129,23 @@ static_assert(gemm_smem_bytes<KIND_BF16, true>() <= 227 * 1024 && gemm_smem_byte
                   gemm_smem_bytes<KIND_NVF4, false>() <= 227 * 1024,
               "shared memory per CTA");
 
+// GELU(v) = v Phi(v) with Phi(v) = (1 + erf(v / sqrt 2)) / 2.  erfc(z), z = |v| / sqrt 2,
+// is taken as t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2), t = 1 / (1 + p z)
+// (Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26: the
+// erf it gives is within 1.5e-7 of the exact one), then 1 + erf = 2 - erfc for
+// v >= 0 and erfc(|z|) for v < 0, so the negative tail keeps its relative
+// accuracy.  Branch-free; its GELU differs from the exact-erf one by at most
+// a few 1e-7 |v|, inside the FP32 epilogue's error budget.
 __device__ __forceinline__ float gelu_erf(float v) {
-  return 0.5f * v * (1.0f + erff(v * 0.7071067811865475244f));
+  const float z = fabsf(v) * 0.7071067811865475244f;
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
+  float q = fmaf(t, 1.061405429f, -1.453152027f);
+  q = fmaf(t, q, 1.421413741f);
+  q = fmaf(t, q, -0.284496736f);
+  q = fmaf(t, q, 0.254829592f);
+  const float c = t * q * __expf(-z * z);  // erfc(z)
+  const float w = v >= 0.f ? 2.0f - c : c;  // 1 + erf(v / sqrt 2)
+  return 0.5f * v * w;
 }
 
 // W4A8 group folding: each epilogue thread reads its accumulator columns of
