@@ -92,6 +92,23 @@ def test_gemm_fp32_within_bound(ops, mode, m, n, k, b):
 
 
 @pytest.mark.parametrize("mode", ["nvfp4", "int8", "bf16"])
+@pytest.mark.parametrize("m,n,k,b", SHAPES)
+def test_gemm_bf16_output_ragged(ops, mode, m, n, k, b):
+    """bf16 Y at ragged M and N (N = 144 and 16 end in half of a 32-column
+    output box; the BF16 kind stores through TMA, which must clip at N and M
+    rather than spill into the next row or past the last)."""
+    x = synthgen.activations(600 + m, m, k, "laplace", 0.005, 50.0)
+    w = synthgen.weights(700 + n, n, k)
+    ref, bound, _ = _ref(mode, x, w, b)
+    y, _ = _run(ops, mode, x, w, b, out_f32=False)
+    _assert_close(y, ref, TOL * bound + _half_ulp_bf16(ref) * 1.0001 + 1e-30, f"{mode} bf16 {m}x{n}x{k}")
+    r = synthgen.activations(800 + m, m, n, "normal", 0.0, 1.0)
+    y, _ = _run(ops, mode, x, w, b, epi=2, residual=r, out_f32=False)
+    e = gemm.epilogue(ref, "residual", r)
+    _assert_close(y, e, TOL * bound + 1.2e-7 * np.abs(e) + _half_ulp_bf16(e) * 1.0001 + 1e-30, "residual")
+
+
+@pytest.mark.parametrize("mode", ["nvfp4", "int8", "bf16"])
 def test_gemm_epilogues_bf16_output(ops, mode):
     m, n, k, b = 200, 256, 512, 64
     x = synthgen.activations(41, m, k, "laplace", 0.005, 50.0)
