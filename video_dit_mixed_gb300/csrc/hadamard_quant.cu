@@ -638,6 +638,188 @@ __global__ void __launch_bounds__(256) hq_nvfp4_tpb_kernel(const uint16_t* __res
   }
 }
 
+// ------------------------------------------- shared-memory-staged b = 64 forms --
+//
+// The thread-per-block kernels above load each thread's 128-byte block
+// directly, so one 16-byte warp load touches 32 lines (32 L1 wavefronts) and
+// the load/store pipe, not HBM, bounds them.  Here each warp stages its next
+// 32 consecutive blocks (4 KB, contiguous: K % 64 == 0) with coalesced
+// 16-byte cp.async copies, three tiles ahead, into its own shared-memory
+// ring; chunk q of block r lands at chunk q ^ (r & 7) of the block's 128-byte
+// row, so both the copies and each thread's eight 16-byte reads of its own
+// block are conflict-free.  The arithmetic is that of the thread-per-block
+// kernels (same stage order, same per-group divisions), so the results are
+// bit-identical.  Warps need no synchronization beyond their own lanes.
+constexpr int kStgWarps = 8;
+constexpr int kStgDepth = 3;
+constexpr int kStgTileBytes = 32 * 128;
+constexpr int kStgSmem = kStgWarps * kStgDepth * kStgTileBytes;  // 96 KB
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Copies tile `tile` (blocks 32 tile .. 32 tile + 31 of X, zero past nblk)
+// into the warp's slot at `slot` (shared address), one commit group.
+__device__ __forceinline__ void stage_tile(const uint16_t* X, int64_t nblk, int64_t tile, uint32_t slot, int lane) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int off = c * 512 + lane * 16;  // byte offset within the tile
+    const int r = off >> 7, q = (off >> 4) & 7;
+    const int64_t blk = tile * 32 + r;
+    const bool v = blk < nblk;
+    cp_async16_zfill(slot + r * 128 + ((q ^ (r & 7)) << 4),
+                     v ? reinterpret_cast<const uint8_t*>(X) + tile * kStgTileBytes + off : reinterpret_cast<const uint8_t*>(X), v);
+  }
+  cp_async_commit();
+}
+
+// This lane's block (row `lane` of the slot) as 64 floats.
+__device__ __forceinline__ void read_staged_block(const uint8_t* slot, int lane, float (&v)[64]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(slot + lane * 128 + ((c ^ (lane & 7)) << 4));
+    float t[8];
+    bf16x8_to_f32(raw, t);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[8 * c + i] = t[i];
+  }
+}
+
+// AMAX: max |rotated X| into amax_out (atomicMax of a non-negative float's
+// bits).  Otherwise: the NVFP4 codes and scales with s_t from *amax_src, as
+// hq_nvfp4_tpb_kernel<64>, including zero scales for the pad rows.
+template <bool AMAX>
+__global__ void __launch_bounds__(kStgWarps * 32) hq_nvfp4_staged_kernel(
+    const uint16_t* __restrict__ X, int M, int K, const int32_t* mode_dev, const float* amax_src, float* amax_out,
+    uint8_t* codes, uint8_t* scales, float* tscale_out, float* rotated) {
+  if (mode_skips(mode_dev, SIXBIT_MODE_NVFP4)) return;
+  extern __shared__ __align__(1024) uint8_t stg_smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per_row = K / 64;
+  const int64_t nblk = static_cast<int64_t>(M) * per_row;
+  const int64_t ntiles = (nblk + 31) / 32;
+  const int64_t G = static_cast<int64_t>(gridDim.x) * kStgWarps;  // warps in the grid
+  const int64_t w0 = static_cast<int64_t>(blockIdx.x) * kStgWarps + warp;
+  uint8_t* ring = stg_smem + warp * (kStgDepth * kStgTileBytes);
+  const uint32_t ring_s = smem_u32(ring);
+  float s_t = 1.0f;
+  if constexpr (!AMAX) {
+    const float amax = *amax_src;
+    s_t = amax == 0.f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *tscale_out = s_t;
+  }
+  float m = 0.f;
+#pragma unroll
+  for (int d = 0; d < kStgDepth; ++d) stage_tile(X, nblk, w0 + d * G, ring_s + d * kStgTileBytes, lane);
+  int it = 0;
+  for (int64_t tile = w0; tile < ntiles; tile += G, ++it) {
+    const int slot = it % kStgDepth;
+    cp_async_wait<kStgDepth - 1>();  // this lane's copies of this tile have landed
+    __syncwarp();                    // and every other lane's
+    float v[64];
+    read_staged_block(ring + slot * kStgTileBytes, lane, v);
+    __syncwarp();                    // the slot is free again
+    stage_tile(X, nblk, tile + kStgDepth * G, ring_s + slot * kStgTileBytes, lane);
+    const int64_t t = tile * 32 + lane;
+    if (t >= nblk) continue;
+    fwht_block<64>(v);
+    if constexpr (AMAX) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(v[i]));
+    } else {
+      const int r = static_cast<int>(t / per_row);
+      const int col = static_cast<int>(t - static_cast<int64_t>(r) * per_row) * 64;
+      uint32_t packed[8];
+      uint32_t sc = 0;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float am = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[16 * g + i]));
+        const float sb = __fdiv_rn(__fdiv_rn(am, 6.0f), s_t);
+        const uint32_t e = f32_to_e4m3(sb);
+        const float S = __fmul_rn(e4m3_to_f32(e), s_t);
+        float q[16];
+        if (recip_ok(S)) {
+          const float rS = __frcp_rn(S);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) q[i] = div_by_recip(v[16 * g + i], S, rS);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) q[i] = (S != 0.f) ? __fdiv_rn(v[16 * g + i], S) : 0.f;
+        }
+        float q0[8], q1[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          q0[i] = q[i];
+          q1[i] = q[8 + i];
+        }
+        packed[2 * g] = f32x8_to_e2m1(q0);
+        packed[2 * g + 1] = f32x8_to_e2m1(q1);
+        sc |= e << (8 * g);
+      }
+      uint8_t* cp = codes + static_cast<size_t>(r) * (K >> 1) + (col >> 1);
+      reinterpret_cast<uint4*>(cp)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      reinterpret_cast<uint4*>(cp)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      *reinterpret_cast<uint32_t*>(scales + sf_offset(r, col >> 4, K)) = sc;  // 4 consecutive groups
+      if (rotated != nullptr) {
+        float4* dst = reinterpret_cast<float4*>(rotated + static_cast<size_t>(r) * K + col);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+    }
+  }
+  cp_async_wait<0>();  // no copy outlives the kernel
+  if constexpr (AMAX) {
+    m = warp_max(m);
+    __shared__ float red[kStgWarps];
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float b = red[0];
+      for (int i = 1; i < kStgWarps; ++i) b = fmaxf(b, red[i]);
+      atomicMax(reinterpret_cast<unsigned int*>(amax_out), __float_as_uint(b));  // b >= 0
+    }
+  } else {
+    // rows [M, round_up(M, 128)): zero scales (one 32-bit word per 64 columns)
+    const int mpad = (M + 127) & ~127;
+    const int64_t npad = static_cast<int64_t>(mpad - M) * per_row;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < npad;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+      const int r = M + static_cast<int>(i / per_row);
+      const int col = static_cast<int>(i % per_row) * 64;
+      *reinterpret_cast<uint32_t*>(scales + sf_offset(r, col >> 4, K)) = 0u;
+    }
+  }
+}
+
+template <bool AMAX>
+static cudaError_t launch_staged(const uint16_t* X, int M, int K, const int32_t* mode_dev, const float* amax_src,
+                                 float* amax_out, const sixbit_qact* o, cudaStream_t st) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(hq_nvfp4_staged_kernel<AMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStgSmem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t ntiles = (static_cast<int64_t>(M) * (K / 64) + 31) / 32;
+  const int64_t want = (ntiles + kStgWarps - 1) / kStgWarps;
+  const int grid = static_cast<int>(want < 2 * sms ? (want < 1 ? 1 : want) : 2 * sms);
+  hq_nvfp4_staged_kernel<AMAX><<<grid, kStgWarps * 32, kStgSmem, st>>>(
+      X, M, K, mode_dev, amax_src, amax_out, AMAX ? nullptr : o->fp4_codes, AMAX ? nullptr : o->fp4_scales,
+      AMAX ? nullptr : o->tensor_scale, AMAX ? nullptr : o->rotated);
+  note_launch();
+  return cudaGetLastError();
+}
+
 // --------------------------------------------------------- weight packing --
 
 __device__ __forceinline__ void load8_f32(const float* p, float (&v)[8]) {
@@ -757,10 +939,10 @@ cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t
                            cudaStream_t st) {
   cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), st);
   if (e != cudaSuccess) return e;
-  if (b == 16 || b == 64) {
+  if (b == 64) return launch_staged<true>(X, M, K, mode_dev, nullptr, amax_out, nullptr, st);
+  if (b == 16) {
     const int grid = tpb_grid(static_cast<int64_t>(M) * (K / b));
-    if (b == 16) hq_amax_tpb_kernel<16><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_out);
-    else hq_amax_tpb_kernel<64><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_out);
+    hq_amax_tpb_kernel<16><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_out);
     note_launch();
     return cudaGetLastError();
   }
@@ -772,7 +954,9 @@ cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t
 cudaError_t launch_hq_nvfp4(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, const float* amax_src,
                             const sixbit_qact* o, cudaStream_t st) {
   // b = 64 stores its four group scales as one 32-bit word
-  if (b == 16 || (b == 64 && (reinterpret_cast<uintptr_t>(o->fp4_scales) & 3u) == 0)) {
+  if (b == 64 && (reinterpret_cast<uintptr_t>(o->fp4_scales) & 3u) == 0)
+    return launch_staged<false>(X, M, K, mode_dev, amax_src, nullptr, o, st);
+  if (b == 16) {
     const int grid = tpb_grid(static_cast<int64_t>((M + 127) & ~127) * (K / b));
     if (b == 16)
       hq_nvfp4_tpb_kernel<16><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_src, o->fp4_codes, o->fp4_scales,
