@@ -50,8 +50,6 @@ FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio (FP4 13.5 PFLOP/s, BF16 2.25
 # on the same shapes (profiles/dram_traffic_dit_2b.md); an entry must be
 # removed when its kernel changes.
 MEASURED_TRAFFIC = {
-    ("dit_2b", "qgemm_up:int8"): 324978816,
-    ("dit_2b", "qgemm_down:int8"): 603963520,
     ("dit_2b", "qgemm_up:bf16"): 333092480,
     ("dit_2b", "qgemm_down:bf16"): 543273190,
     ("dit_2b", "hq_x:int8"): 86626048,

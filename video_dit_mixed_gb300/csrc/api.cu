@@ -233,10 +233,11 @@ static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, co
   p.n_fastest = M > N ? 1 : 0;
   p.rot_amax = rot_amax;
   p.had_block = had_block;
-  // The BF16 kind writes a bf16 Y through TMA stores (Y 16-byte aligned,
-  // N % 16 == 0 checked above); an FP32 Y is stored directly.
+  // The bf16-operand kinds (BF16, W4A8) write a bf16 Y through TMA stores
+  // (Y 16-byte aligned, N % 16 == 0 checked above); an FP32 Y is stored
+  // directly.
   CUtensorMap my{};
-  p.y_tma = (Y_f32 == nullptr && run_bf) ? 1 : 0;
+  p.y_tma = (Y_f32 == nullptr && (run_bf || run_i8)) ? 1 : 0;
   if (p.y_tma && !make_store_map(&my, Y, M, N)) return SIXBIT_ECUDA;
   if (run_fp4) {
     CUtensorMap ma, mb;

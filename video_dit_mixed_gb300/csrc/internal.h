@@ -28,7 +28,7 @@ struct GemmParams {
   int n_fastest;           // tile order: 1 = output column tiles fastest, 0 = row tiles fastest
   float* rot_amax;         // NVFP4 epilogue: atomicMax of |bf16(Y) . blockdiag(H_b / sqrt b)| (or NULL)
   int had_block;           // b of rot_amax (16 or 64)
-  int y_tma;               // BF16 kind: bf16 Y is written by TMA stores through the Y tensor map
+  int y_tma;               // bf16-operand kinds: bf16 Y is written by TMA stores through the Y tensor map
 };
 
 cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, float* amax_out,

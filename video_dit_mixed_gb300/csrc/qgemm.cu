@@ -10,10 +10,12 @@
 //               guarded by full/empty mbarriers;
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma and
 //               tcgen05.commit to release stages and accumulators;
-//   warps 2..9  epilogue: tcgen05.ld of the FP32 accumulators (warp w reads
-//               lanes 32*(w%4)..+31 = tile rows, one 128-column half),
-//               scaling, GELU or residual, bf16 (or fp32) stores;
-//   warp 10     (NVFP4) tcgen05.cp of each stage's scale factors into its
+//   epilogue    16 warps from warp 2 (NVFP4, BF16) or 8 warps from warp 4
+//               (W4A8): tcgen05.ld of the FP32 accumulators (warp w reads
+//               lanes 32*(w%4)..+31 = tile rows, a 64- or 128-column part),
+//               scaling, GELU or residual, bf16 TMA stores (or direct
+//               stores: NVFP4, FP32 output);
+//   last warp   (NVFP4) tcgen05.cp of each stage's scale factors into its
 //               own tensor-memory slot.
 // Kinds:
 //   NVFP4  kind::mxf4nvf4.block_scale.scale_vec::4X, E2M1 x E2M1 with one
@@ -48,11 +50,31 @@ constexpr int kBN = 256;       // output tile columns
 // kinds use four per quarter (64 columns each), which spreads the GELU /
 // residual / store work of a tile over twice the threads (their registers
 // then fit the 96-per-thread budget of 576-608 threads).
+//
+// W4A8 runs 12 warps: warpgroup 0 holds the producer (warp 0), the MMA issuer
+// (warp 1) and two idle warps, and gives registers to the two fold
+// warpgroups (warps 4-11) with setmaxnreg: launched at 168 per thread, it
+// drops to 56 and the fold warps rise to 224 (4 x 56 + 8 x 224 = 12 x 168,
+// and per SM sub-partition 56 + 2 x 224 = 3 x 168), so the fold's 128
+// running sums, its loads and the TMA-store epilogue fit without spills.
+// Each warpgroup executes its setmaxnreg once, all four warps at the same
+// instruction; the host refuses the launch unless the kernel was compiled
+// to the 168 registers the split is sized for (an increase that the
+// released registers could not cover would wait forever).
 template <bool GROUPED>
 struct EpiCfg {
   static constexpr int kWarps = GROUPED ? 8 : 16;
   static constexpr int kCols = kBN / (kWarps / 4);  // accumulator columns per thread
+  static constexpr int kWarp0 = GROUPED ? 4 : 2;    // first epilogue warp
 };
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+constexpr int kGrpRegsLaunch = 168, kGrpRegsLow = 56, kGrpRegsHigh = 224;
+static_assert(4 * kGrpRegsLow + 8 * kGrpRegsHigh <= 12 * kGrpRegsLaunch &&
+                  kGrpRegsLow + 2 * kGrpRegsHigh <= 3 * kGrpRegsLaunch,
+              "the W4A8 register split must fit in what the CTA is launched with");
 constexpr int kGrpCols = EpiCfg<true>::kCols;       // 128
 
 enum { KIND_BF16 = 0, KIND_NVF4 = 1 };
@@ -63,7 +85,7 @@ enum { KIND_BF16 = 0, KIND_NVF4 = 1 };
 // the copies over two warps was slower: the issue cost is shared.)
 template <int KIND, bool GROUPED>
 __host__ __device__ constexpr int gemm_threads() {
-  return 64 + EpiCfg<GROUPED>::kWarps * 32 + (KIND == KIND_NVF4 ? 32 : 0);
+  return GROUPED ? 384 : 64 + EpiCfg<GROUPED>::kWarps * 32 + (KIND == KIND_NVF4 ? 32 : 0);
 }
 
 template <int KIND>
@@ -102,16 +124,14 @@ __host__ __device__ constexpr int stage_bytes() {
 constexpr int kSwRing = 4;
 constexpr int kMaxBufs = 4;  // accumulator buffers the barrier area has room for
 
-// The BF16 kind stages each epilogue warp's 32 x 32 bf16 output chunk in
-// shared memory (64-byte rows, 64-byte TMA swizzle) and writes it with one
+// The bf16-operand kinds stage each epilogue warp's 32 x 32 bf16 output chunk
+// in shared memory (64-byte rows, 64-byte TMA swizzle) and write it with one
 // TMA store: a warp's direct stores would touch 32 rows, 16 bytes each
-// (310 vs 329 us at 17776 x 7680 x 1920).  NVFP4 has no shared memory left;
-// in W4A8 the store path's registers cost the group fold more than the
-// stores gain when the epilogue has GELU or a residual (540 vs 517 us), so
-// both store directly.
+// (BF16 310 vs 329 us, W4A8 397 vs 460 us at 17776 x 7680 x 1920).  NVFP4
+// has no shared memory left and stores directly.
 template <int KIND, bool GROUPED>
 __host__ __device__ constexpr bool tma_y() {
-  return KIND != KIND_NVF4 && !GROUPED;
+  return KIND != KIND_NVF4;
 }
 constexpr int kBoxBytes = 32 * 64;
 template <int KIND, bool GROUPED>
@@ -316,7 +336,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* tiles = smem;
-  uint8_t* staging = smem + S * stage_bytes<KIND>();  // [kEpiWarps] output boxes (BF16 kind)
+  uint8_t* staging = smem + S * stage_bytes<KIND>();  // [kEpiWarps] output boxes (bf16-operand kinds)
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + staging_bytes<KIND, GROUPED>());
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
@@ -384,117 +404,121 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------ producer --
-      uint32_t it = 0;
-      bool ok = true;
-      const size_t sf_rows_bytes = static_cast<size_t>(128) * (p.K >> 4);  // one 128-row scale tile
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        int m_tile, n_tile;
-        tile_of(t, m_tile, n_tile);
-        const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;  // 128-row halves of B that exist
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % S;
-          const uint32_t ph = (it / S) & 1;
-          if (it >= S && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
-            set_error(p.err, SIXBIT_ETIMEOUT);
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          const int kvalid = min(C::kKStage, p.K - kb * C::kKStage);
-          const uint32_t sf_bytes = kNvf4 ? static_cast<uint32_t>(kvalid / 64) * 512u : 0u;
-          mbar_expect_tx(&full[s], kATileBytes + kBTileBytes + sf_bytes * (1 + (kNvf4 ? nj : 0)));
-          tma_load_2d(A_tile(s), &tmA, &full[s], kb * C::kKCoord, m_tile * kBM);
-          tma_load_2d(B_tile(s), &tmB, &full[s], kb * C::kKCoord, n_tile * kBN);
-          if constexpr (kNvf4) {
-            bulk_load(SFA(s), p.sfa + m_tile * sf_rows_bytes + static_cast<size_t>(kb) * 2048, sf_bytes, &full[s]);
-            for (int j = 0; j < nj; ++j)
-              bulk_load(SFB(s) + 2048 * j, p.sfb + (2 * n_tile + j) * sf_rows_bytes + static_cast<size_t>(kb) * 2048,
-                        sf_bytes, &full[s]);
+  if (warp < EpiCfg<GROUPED>::kWarp0) {
+    if constexpr (GROUPED) setmaxnreg_dec<kGrpRegsLow>();  // the whole warpgroup, one instruction
+    if (warp == 0) {
+      if (lane == 0) {
+        // ------------------------------------------------------ producer --
+        uint32_t it = 0;
+        bool ok = true;
+        const size_t sf_rows_bytes = static_cast<size_t>(128) * (p.K >> 4);  // one 128-row scale tile
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+          int m_tile, n_tile;
+          tile_of(t, m_tile, n_tile);
+          const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;  // 128-row halves of B that exist
+          for (int kb = 0; kb < nk; ++kb, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (it / S) & 1;
+            if (it >= S && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+              set_error(p.err, SIXBIT_ETIMEOUT);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            const int kvalid = min(C::kKStage, p.K - kb * C::kKStage);
+            const uint32_t sf_bytes = kNvf4 ? static_cast<uint32_t>(kvalid / 64) * 512u : 0u;
+            mbar_expect_tx(&full[s], kATileBytes + kBTileBytes + sf_bytes * (1 + (kNvf4 ? nj : 0)));
+            tma_load_2d(A_tile(s), &tmA, &full[s], kb * C::kKCoord, m_tile * kBM);
+            tma_load_2d(B_tile(s), &tmB, &full[s], kb * C::kKCoord, n_tile * kBN);
+            if constexpr (kNvf4) {
+              bulk_load(SFA(s), p.sfa + m_tile * sf_rows_bytes + static_cast<size_t>(kb) * 2048, sf_bytes, &full[s]);
+              for (int j = 0; j < nj; ++j)
+                bulk_load(SFB(s) + 2048 * j, p.sfb + (2 * n_tile + j) * sf_rows_bytes + static_cast<size_t>(kb) * 2048,
+                          sf_bytes, &full[s]);
+            }
           }
         }
+        // every copy this CTA started lands before it can exit
+        for (uint32_t j = (it > S ? it - S : 0); j < it; ++j) (void)mbar_wait(&full[j % S], (j / S) & 1, nullptr);
       }
-      // every copy this CTA started lands before it can exit
-      for (uint32_t j = (it > S ? it - S : 0); j < it; ++j) (void)mbar_wait(&full[j % S], (j / S) & 1, nullptr);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------------------------------------------- MMA issuer --
-      uint32_t it = 0;  // stage counter
-      uint32_t ac = 0;  // accumulator-buffer use counter (tiles, or K groups when GROUPED)
-      bool ok = true;
-      constexpr int spg = 128 / C::kKStage > 0 ? 128 / C::kKStage : 1;  // stages per K group (bf16 kinds)
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        int m_tile, n_tile;
-        tile_of(t, m_tile, n_tile);
-        (void)m_tile;
-        const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;
-        for (int kb = 0; kb < nk && ok; ++kb, ++it) {
-          const bool acc_start = GROUPED ? (kb % spg) == 0 : kb == 0;
-          const uint32_t buf = ac % kBufs;
-          // the buffer's previous contents must have been drained by the epilogue
-          if (acc_start && ac >= kBufs && !mbar_wait(&acce[buf], ((ac / kBufs) - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          const int s = it % S;
-          if (!mbar_wait(&full[s], (it / S) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(A_tile(s));
-          const uint32_t b_base = smem_u32(B_tile(s));
-          const uint32_t d_tmem = tmem + buf * kBN;
-          if constexpr (kNvf4) {
-            const int nmma = min(C::kKStage, p.K - kb * C::kKStage) / 64;
-            const uint32_t sfa_col = tmem + kSfSlot0 + kSfSlotCols * s;
-            const uint32_t sfb_col = sfa_col + kSfbOff;
-            if (!mbar_wait(&sf_full[s], (it / S) & 1, abort_flag)) {  // copied by the scale-factor warp
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ---------------------------------------------------- MMA issuer --
+        uint32_t it = 0;  // stage counter
+        uint32_t ac = 0;  // accumulator-buffer use counter (tiles, or K groups when GROUPED)
+        bool ok = true;
+        constexpr int spg = 128 / C::kKStage > 0 ? 128 / C::kKStage : 1;  // stages per K group (bf16 kinds)
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+          int m_tile, n_tile;
+          tile_of(t, m_tile, n_tile);
+          (void)m_tile;
+          const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;
+          for (int kb = 0; kb < nk && ok; ++kb, ++it) {
+            const bool acc_start = GROUPED ? (kb % spg) == 0 : kb == 0;
+            const uint32_t buf = ac % kBufs;
+            // the buffer's previous contents must have been drained by the epilogue
+            if (acc_start && ac >= kBufs && !mbar_wait(&acce[buf], ((ac / kBufs) - 1) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const int s = it % S;
+            if (!mbar_wait(&full[s], (it / S) & 1, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            // one N = 256 MMA (B scale chunks for rows 0-127 and 128-255 in
-            // consecutive 4-column groups), or N = 128 when only half the tile exists
-            const uint32_t idesc = nj == 2 ? idesc_nvf4(kBM, 256) : C::kIdesc;
-#pragma unroll
-            for (int k = 0; k < C::kMmaPerStage; ++k) {
-              if (k < nmma)
-                mma_nvf4(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), idesc,
-                         sfa_col + 4 * k, sfb_col + 8 * k, (acc_start && k == 0) ? 0u : 1u);
+            const uint32_t a_base = smem_u32(A_tile(s));
+            const uint32_t b_base = smem_u32(B_tile(s));
+            const uint32_t d_tmem = tmem + buf * kBN;
+            if constexpr (kNvf4) {
+              const int nmma = min(C::kKStage, p.K - kb * C::kKStage) / 64;
+              const uint32_t sfa_col = tmem + kSfSlot0 + kSfSlotCols * s;
+              const uint32_t sfb_col = sfa_col + kSfbOff;
+              if (!mbar_wait(&sf_full[s], (it / S) & 1, abort_flag)) {  // copied by the scale-factor warp
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              // one N = 256 MMA (B scale chunks for rows 0-127 and 128-255 in
+              // consecutive 4-column groups), or N = 128 when only half the tile exists
+              const uint32_t idesc = nj == 2 ? idesc_nvf4(kBM, 256) : C::kIdesc;
+  #pragma unroll
+              for (int k = 0; k < C::kMmaPerStage; ++k) {
+                if (k < nmma)
+                  mma_nvf4(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), idesc,
+                           sfa_col + 4 * k, sfb_col + 8 * k, (acc_start && k == 0) ? 0u : 1u);
+              }
+            } else {
+  #pragma unroll
+              for (int k = 0; k < C::kMmaPerStage; ++k)
+                mma_bf16(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), C::kIdesc,
+                         (acc_start && k == 0) ? 0u : 1u);
             }
-          } else {
-#pragma unroll
-            for (int k = 0; k < C::kMmaPerStage; ++k)
-              mma_bf16(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), C::kIdesc,
-                       (acc_start && k == 0) ? 0u : 1u);
-          }
-          tc_commit(&empty[s]);
-          const bool acc_end = GROUPED ? (kb % spg) == spg - 1 : kb == nk - 1;
-          if (acc_end) {
-            if constexpr (!GROUPED) tc_commit(&accf[buf]);  // W4A8: the epilogue waits on empty[s]
-            ++ac;
+            tc_commit(&empty[s]);
+            const bool acc_end = GROUPED ? (kb % spg) == spg - 1 : kb == nk - 1;
+            if (acc_end) {
+              if constexpr (!GROUPED) tc_commit(&accf[buf]);  // W4A8: the epilogue waits on empty[s]
+              ++ac;
+            }
           }
         }
+        if (!ok) {
+          set_error(p.err, SIXBIT_ETIMEOUT);
+          *abort_flag = 1;
+        }
+        tc_commit(drain);  // all tensor-core work issued here completes before exit
+        (void)mbar_wait(drain, 0, nullptr);
       }
-      if (!ok) {
-        set_error(p.err, SIXBIT_ETIMEOUT);
-        *abort_flag = 1;
-      }
-      tc_commit(drain);  // all tensor-core work issued here completes before exit
-      (void)mbar_wait(drain, 0, nullptr);
-    }
-  } else if (warp < 2 + kEpiWarps) {
+    }  // warps 2 and 3 of a W4A8 CTA are idle
+  } else if (warp < EpiCfg<GROUPED>::kWarp0 + kEpiWarps) {
+    if constexpr (GROUPED) setmaxnreg_inc<kGrpRegsHigh>();  // each fold warpgroup, one instruction
     // -------------------------------------------------------- epilogue --
-    const int ew = warp - 2;                      // 0 .. kEpiWarps-1
+    const int ew = warp - EpiCfg<GROUPED>::kWarp0;  // 0 .. kEpiWarps-1
     const int q = warp & 3;                       // tensor-memory lane quarter this warp may read
     const int col0 = (ew >> 2) * kEpiCols;        // first accumulator column of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16) + col0;
     float* my_sw = sw_smem + ew * kSwRing * kEpiCols;  // GROUPED: this warp's ring of group scales
-    uint8_t* my_box = staging + ew * kBoxBytes;         // BF16 kind: this warp's output box
+    uint8_t* my_box = staging + ew * kBoxBytes;         // bf16-operand kinds: this warp's output box
     // Epilogue + store of columns [n, n + 32) of this lane's row (n < N, warp-uniform).
     auto store32 = [&](int row, int n, float (&v)[32]) {
       if constexpr (tma_y<KIND, GROUPED>()) {
@@ -733,6 +757,16 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
+  }
+  if constexpr (GROUPED) {
+    static int regs = -1;
+    if (regs < 0) {
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, qgemm_kernel<KIND, GROUPED, DBG>);
+      if (e != cudaSuccess) return e;
+      regs = fa.numRegs;
+    }
+    if (regs < kGrpRegsLaunch || 4 * kGrpRegsLow + 8 * kGrpRegsHigh > 12 * regs) return cudaErrorInvalidConfiguration;
   }
   const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
