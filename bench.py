@@ -50,10 +50,12 @@ FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio (FP4 13.5 PFLOP/s, BF16 2.25
 # on the same shapes (profiles/dram_traffic_dit_2b.md); an entry must be
 # removed when its kernel changes.
 MEASURED_TRAFFIC = {
-    ("dit_2b", "qgemm_up:bf16"): 333092480,
-    ("dit_2b", "qgemm_down:bf16"): 543273190,
-    ("dit_2b", "hq_x:int8"): 86626048,
-    ("dit_2b", "hq_h:int8"): 495295360,
+    ("dit_2b", "qgemm_up:int8"): 335972608,
+    ("dit_2b", "qgemm_down:int8"): 632774656,
+    ("dit_2b", "qgemm_up:bf16"): 333682841,
+    ("dit_2b", "qgemm_down:bf16"): 543600844,
+    ("dit_2b", "hq_x:int8"): 86360960,
+    ("dit_2b", "hq_h:int8"): 495195520,
 }
 MODE_NAMES = {1: "nvfp4", 2: "int8", 3: "bf16", 4: "skip"}
 
