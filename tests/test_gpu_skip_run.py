@@ -6,7 +6,7 @@ and sixbit_block_stats.
 Bar: bit-identical decisions, policy states, activations, Delta caches and the
 statistics later blocks read, over several steps of a stack whose skip runs start
 at block 0, in the middle and at the end; the run lengths are back to zero
-after each step.  A block's compute is stood in for by a seeded
+after each step (runs of up to 40 blocks).  A block's compute is stood in for by a seeded
 perturbation of its input (the same on both sides).
 """
 import numpy as np
@@ -39,9 +39,13 @@ def _compute(x, out, bump):
     out.copy_((x.float() + bump).to(torch.bfloat16))
 
 
-@pytest.mark.parametrize("skipping", [{0, 1, 2}, {1, 2, 3}, {4, 5}, {2}, set(range(6))])
-def test_protocol_matches_sequential_steps(ops, skipping):
-    L, n = 6, 8 * 1536
+# Stacks of 36-40 blocks put a run across the 32-block groups in which a
+# run's blocks are decided in parallel (one per lane).
+@pytest.mark.parametrize("L,skipping", [(6, {0, 1, 2}), (6, {1, 2, 3}), (6, {4, 5}), (6, {2}), (6, set(range(6))),
+                                        (40, set(range(1, 38))), (40, set(range(40))), (40, set(range(10, 36))),
+                                        (36, set(range(3, 36))), (40, set(range(0, 33)) | {35, 36})])
+def test_protocol_matches_sequential_steps(ops, L, skipping):
+    n = 8 * 1536
     g = torch.Generator(device="cuda").manual_seed(7)
     x0 = (torch.randn(n, device="cuda", generator=g) * 3).to(torch.bfloat16)
     deltas0 = (torch.randn((L, n), device="cuda", generator=g) * 0.05).to(torch.bfloat16)

@@ -158,10 +158,11 @@ __device__ __forceinline__ void cta_reduce(FF (&v)[NS], const bool (&is_max)[NS]
 
 // Reduces per-thread values v[0..NS) (maxima where is_max, sums otherwise)
 // across the grid in a fixed order: warp tree, CTA, then the last CTA to finish
-// folds the per-CTA partials in scratch.  Returns true in exactly one thread,
-// with the totals in `tot`.  All values are non-negative except sums of
-// products, whose error stays relative to the sum of magnitudes.
-template <int NS>
+// folds the per-CTA partials in scratch.  Returns true in exactly one thread
+// (W0: in every lane of warp 0 of the last CTA), with the totals in `tot`.
+// All values are non-negative except sums of products, whose error stays
+// relative to the sum of magnitudes.
+template <int NS, bool W0 = false>
 __device__ bool grid_reduce(FF (&v)[NS], const bool (&is_max)[NS], Scratch sc, double (&tot)[NS]) {
   __shared__ FF red[kStThreads / 32][NS];
   __shared__ bool last;
@@ -190,11 +191,21 @@ __device__ bool grid_reduce(FF (&v)[NS], const bool (&is_max)[NS], Scratch sc, d
   }
   __syncthreads();  // red is reused
   cta_reduce<NS>(v, is_max, red);
-  if (threadIdx.x != 0) return false;
+  if constexpr (W0) {
+    if (threadIdx.x >= 32) return false;
 #pragma unroll
-  for (int k = 0; k < NS; ++k) tot[k] = static_cast<double>(v[k].hi) + static_cast<double>(v[k].lo);
-  *sc.counter = 0;  // leave the scratch ready for the next call
-  return true;
+    for (int k = 0; k < NS; ++k)  // lane 0 holds the result
+      tot[k] = static_cast<double>(__shfl_sync(0xffffffffu, v[k].hi, 0)) +
+               static_cast<double>(__shfl_sync(0xffffffffu, v[k].lo, 0));
+    if (threadIdx.x == 0) *sc.counter = 0;  // leave the scratch ready for the next call
+    return true;
+  } else {
+    if (threadIdx.x != 0) return false;
+#pragma unroll
+    for (int k = 0; k < NS; ++k) tot[k] = static_cast<double>(v[k].hi) + static_cast<double>(v[k].lo);
+    *sc.counter = 0;  // leave the scratch ready for the next call
+    return true;
+  }
 }
 
 __device__ __forceinline__ bool mode_is_not(const int32_t* mode_dev, int want) {
@@ -227,7 +238,8 @@ __device__ __forceinline__ void tensor_stats_vec(const uint4& r, float& mx, Kaha
 }
 
 // Grid-wide {max |x|, sum |x|, sum x^2} of x[0..n); true in one thread of
-// the last CTA, with the totals in tot.
+// the last CTA (W0: in its warp 0), with the totals in tot.
+template <bool W0 = false>
 __device__ bool tensor_stats_body(const uint16_t* __restrict__ x, int64_t n, void* scratch, double (&tot)[3]) {
   const int64_t n8 = n >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
@@ -242,7 +254,7 @@ __device__ bool tensor_stats_body(const uint16_t* __restrict__ x, int64_t n, voi
   }
   FF v[3] = {FF{mx, 0.f}, to_ff(sa), to_ff(sq)};
   const bool is_max[3] = {true, false, false};
-  return grid_reduce<3>(v, is_max, scratch_view(scratch), tot);
+  return grid_reduce<3, W0>(v, is_max, scratch_view(scratch), tot);
 }
 
 // out[0..3] = {max |x|, sum |x|, count, sum x^2}
@@ -280,7 +292,9 @@ __device__ __forceinline__ uint4 block_stats_vec(const uint4& ra, const uint4& r
 
 // One pass over x_in, x_out, Delta_prev: writes Delta_new over Delta_prev and
 // reduces {sum Delta^2, sum x_in^2, sum Delta*Delta_prev, sum Delta_prev^2,
-// max |x_out|, sum |x_out|}; true in one thread of the last CTA.
+// max |x_out|, sum |x_out|}; true in one thread of the last CTA (W0: in its
+// warp 0).
+template <bool W0 = false>
 __device__ bool block_stats_body(const uint16_t* __restrict__ x_in, const uint16_t* __restrict__ x_out,
                                  uint16_t* delta, int64_t n, void* scratch, double (&tot)[6]) {
   const int64_t n8 = n >> 3;
@@ -305,7 +319,7 @@ __device__ bool block_stats_body(const uint16_t* __restrict__ x_in, const uint16
   }
   FF v[6] = {to_ff(d2), to_ff(xi2), to_ff(ddp), to_ff(dp2), FF{mx, 0.f}, to_ff(sa)};
   const bool is_max[6] = {false, false, false, false, true, false};
-  return grid_reduce<6>(v, is_max, scratch_view(scratch), tot);
+  return grid_reduce<6, W0>(v, is_max, scratch_view(scratch), tot);
 }
 
 __device__ __forceinline__ void write_block_stats(sixbit_stats* stats, const double (&tot)[6], int64_t n) {
@@ -472,7 +486,7 @@ __global__ void policy_kernel(sixbit_policy_cfg cfg, sixbit_policy_state* st, co
 //
 // Per step, block l's decision needs the statistics of its input, which the
 // last kernel before it produces; so every decision is taken at the tail of
-// that kernel, by the thread that holds the totals:
+// that kernel, by warp 0 of the CTA that holds the totals:
 //   dit_begin_kernel     statistics of x0, then the decision of block 0;
 //   dit_block_end_kernel block statistics + Delta update of a computed block
 //                        l, then the decision of block l+1;
@@ -481,9 +495,9 @@ __global__ void policy_kernel(sixbit_policy_cfg cfg, sixbit_policy_state* st, co
 // A skip decision depends only on the block's own state (cos, acc, number of
 // computes) and the statistics of its last compute, never on its input, so
 // when block l skips, the run of blocks that will skip after it is already
-// fixed: decide_block finds it, decides those blocks as well (recording
-// their states and mode words; they launch nothing) and records k in
-// run_len[l].  The
+// fixed: decide_block finds it (the warp's lanes evaluate the following
+// blocks in parallel), decides those blocks as well (recording their states
+// and mode words; they launch nothing) and records k in run_len[l].  The
 // run's output x_{l+k-1} = bf16(... bf16(bf16(x_{l-1} + D_l) + D_{l+1}) ... +
 // D_{l+k-1}) is written in one pass (the same roundings as k separate skips;
 // the intermediate activations are never read, so they are not written),
@@ -491,7 +505,7 @@ __global__ void policy_kernel(sixbit_policy_cfg cfg, sixbit_policy_state* st, co
 // the block's graph condition when a handle array is given: a compute mode
 // to its body (0, 1, 2), a run start to 3, a block inside a run to none (4).
 // The protocol's kernels cap registers at 64 (launch bounds): the decisions
-// run in one thread at the tail and may spill; the streaming body may not.
+// run in one warp at the tail and may spill; the streaming body may not.
 __device__ __forceinline__ const double* block_in_stats(const sixbit_dit_blocks& B, int l) {
   return l == 0 ? B.in_stats0 : &B.stats[l - 1].max_abs_out;  // {max, sum |x|, count}
 }
@@ -505,44 +519,51 @@ __device__ __forceinline__ void set_branch(const sixbit_dit_blocks& B, int l, in
                                                                    : static_cast<unsigned int>(kDitBranches));
 }
 
-// Decides block l; when it starts a run, also decides (and records) the
-// blocks l+1 .. l+k-1 the run covers -- their skips are fixed by their own
-// states -- and gives them no body.
+// Decides block l (all 32 lanes of one warp call it; lane 0 decides).  When
+// block l starts a run, the blocks after it are evaluated 32 at a time, one
+// per lane -- a skip depends only on the block's own state and statistics,
+// so the evaluations are independent -- and the run is the leading skips
+// (__ballot_sync): only those blocks are recorded (state, mode word, no
+// body), exactly the ones a walk that stops at the first non-skip records;
+// the first non-skip is decided later, from the run's output statistics.
 __device__ void decide_block(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l) {
-  sixbit_policy_state s = B.states[l];
-  const int word = policy_decide(cfg, s, &B.stats[l], block_in_stats(B, l));
-  B.states[l] = s;
-  B.modes[l] = word;
-  if (SIXBIT_MODE_OF(word) != SIXBIT_MODE_SKIP) {
-    set_branch(B, l, SIXBIT_MODE_OF(word) - SIXBIT_MODE_NVFP4);  // compute modes: 0, 1, 2
-    return;
+  const int lane = threadIdx.x & 31;
+  int word = 0;
+  if (lane == 0) {
+    sixbit_policy_state s = B.states[l];
+    word = policy_decide(cfg, s, &B.stats[l], block_in_stats(B, l));
+    B.states[l] = s;
+    B.modes[l] = word;
+    if (SIXBIT_MODE_OF(word) != SIXBIT_MODE_SKIP) set_branch(B, l, SIXBIT_MODE_OF(word) - SIXBIT_MODE_NVFP4);
   }
+  word = __shfl_sync(0xffffffffu, word, 0);
+  if (SIXBIT_MODE_OF(word) != SIXBIT_MODE_SKIP) return;  // compute modes: branches 0, 1, 2
   int k = 1;
-  // the next block's state and statistics are loaded while this one is decided
-  sixbit_stats prev = B.stats[l];
-  sixbit_policy_state sn;
-  sixbit_stats tn;
-  if (l + 1 < B.L) {
-    sn = B.states[l + 1];
-    tn = B.stats[l + 1];
-  }
-  for (int j = l + 1; j < B.L; ++j) {
-    sixbit_policy_state sj = sn;
-    const sixbit_stats tj = tn;
-    if (j + 1 < B.L) {
-      sn = B.states[j + 1];
-      tn = B.stats[j + 1];
+  for (int base = l + 1; base < B.L; base += 32) {
+    const int j = base + lane;
+    sixbit_policy_state sj{};
+    int wj = 0;
+    bool skip = false;
+    if (j < B.L) {
+      sj = B.states[j];
+      const sixbit_stats tj = B.stats[j];
+      wj = policy_decide(cfg, sj, &tj, &B.stats[j - 1].max_abs_out);  // input stats: block j-1's output
+      skip = SIXBIT_MODE_OF(wj) == SIXBIT_MODE_SKIP;
     }
-    const int wj = policy_decide(cfg, sj, &tj, &prev.max_abs_out);  // input stats: block j-1's output
-    if (SIXBIT_MODE_OF(wj) != SIXBIT_MODE_SKIP) break;  // decided later, from the run's statistics
-    B.states[j] = sj;
-    B.modes[j] = wj;
-    set_branch(B, j, kDitBranches);  // applied by the run: no body
-    prev = tj;
-    ++k;
+    const unsigned sk = __ballot_sync(0xffffffffu, skip);
+    const int lead = sk == 0xffffffffu ? 32 : __ffs(~sk) - 1;  // leading skips (lanes past L vote no)
+    if (lane < lead) {
+      B.states[j] = sj;
+      B.modes[j] = wj;
+      set_branch(B, j, kDitBranches);  // applied by the run: no body
+    }
+    k += lead;
+    if (lead < 32) break;
   }
-  B.run_len[l] = static_cast<uint32_t>(k);
-  set_branch(B, l, 3);
+  if (lane == 0) {
+    B.run_len[l] = static_cast<uint32_t>(k);
+    set_branch(B, l, 3);
+  }
 }
 
 // (selects, not an index into the parameter array: that would copy B to local memory)
@@ -556,11 +577,14 @@ __device__ __forceinline__ uint16_t* block_output(const sixbit_dit_blocks& B, in
 __global__ void __launch_bounds__(kStThreads, 4) dit_begin_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B,
                                                                void* scratch, int32_t* err) {
   double tot[3];
-  if (tensor_stats_body(B.x0, B.n, scratch, tot)) {
-    B.in_stats0[0] = tot[0];
-    B.in_stats0[1] = tot[1];
-    B.in_stats0[2] = static_cast<double>(B.n);
-    B.in_stats0[3] = tot[2];
+  if (tensor_stats_body<true>(B.x0, B.n, scratch, tot)) {  // warp 0 of the last CTA
+    if (threadIdx.x == 0) {
+      B.in_stats0[0] = tot[0];
+      B.in_stats0[1] = tot[1];
+      B.in_stats0[2] = static_cast<double>(B.n);
+      B.in_stats0[3] = tot[2];
+    }
+    __syncwarp();
     decide_block(cfg, B, 0);
   }
 }
@@ -569,9 +593,10 @@ __global__ void __launch_bounds__(kStThreads, 4) dit_block_end_kernel(sixbit_pol
                                                                    void* scratch, int32_t* err) {
   if (SIXBIT_MODE_OF(B.modes[l]) == SIXBIT_MODE_SKIP) return;  // uniform: a skipped block has no end
   double tot[6];
-  if (block_stats_body(block_input(B, l), block_output(B, l), B.deltas + static_cast<size_t>(l) * B.n, B.n, scratch,
-                       tot)) {
-    write_block_stats(&B.stats[l], tot, B.n);
+  if (block_stats_body<true>(block_input(B, l), block_output(B, l), B.deltas + static_cast<size_t>(l) * B.n, B.n,
+                             scratch, tot)) {  // warp 0 of the last CTA
+    if (threadIdx.x == 0) write_block_stats(&B.stats[l], tot, B.n);
+    __syncwarp();
     if (l + 1 < B.L) decide_block(cfg, B, l + 1);
   }
 }
@@ -635,12 +660,15 @@ __global__ void __launch_bounds__(kStThreads, 4) dit_skip_run_kernel(sixbit_poli
   FF v[2] = {FF{mx, 0.f}, to_ff(sa)};
   const bool is_max[2] = {true, false};
   double tot[2];
-  if (grid_reduce<2>(v, is_max, scratch_view(scratch), tot)) {
-    sixbit_stats* o = &B.stats[l + k - 1];
-    o->max_abs_out = tot[0];
-    o->sum_abs_out = tot[1];
-    o->count = static_cast<double>(B.n);
-    B.run_len[l] = 0;  // every CTA has read it
+  if (grid_reduce<2, true>(v, is_max, scratch_view(scratch), tot)) {  // warp 0 of the last CTA
+    if (threadIdx.x == 0) {
+      sixbit_stats* o = &B.stats[l + k - 1];
+      o->max_abs_out = tot[0];
+      o->sum_abs_out = tot[1];
+      o->count = static_cast<double>(B.n);
+      B.run_len[l] = 0;  // every CTA has read it
+    }
+    __syncwarp();
     if (l + k < B.L) decide_block(cfg, B, l + k);
   }
 }
