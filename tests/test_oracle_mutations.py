@@ -7,8 +7,9 @@ checks that at least one pin test then fails.
 import numpy as np
 import pytest
 
-from oracle import formats, hadamard, policy, quant, stats
+from oracle import dit, formats, gemm, hadamard, policy, quant, stats
 
+import tests.test_oracle_dit as td
 import tests.test_oracle_formats as tf
 import tests.test_oracle_hadamard as th
 import tests.test_oracle_quant as tq
@@ -89,3 +90,21 @@ def test_policy_rule_mutation_is_caught(monkeypatch):
 def test_cosine_mutation_is_caught(monkeypatch):
     monkeypatch.setattr(stats, "cosine", lambda a, b, c: a / b if b else 0.0)
     assert _fails(ts.test_cosine_special_cases)
+
+
+def test_dit_block_mutations_are_caught(monkeypatch):
+    orig = dit.linear
+
+    def no_residual(x, pk, mode, b, epilogue, residual=None):   # x -> W_d . GELU(W_u . x)
+        return orig(x, pk, mode, b, "none" if epilogue == "residual" else epilogue)
+
+    def gelu_after_down(x, pk, mode, b, epilogue, residual=None):   # x -> x + GELU(W_d . W_u . x)
+        y = orig(x, pk, mode, b, "none")
+        if epilogue == "residual":
+            return dit._round_bf16(gemm.gelu(y.astype(np.float64)) + np.asarray(residual, np.float64))
+        return y
+
+    monkeypatch.setattr(dit, "linear", no_residual)
+    assert _fails(td.test_zero_weights_identity_and_decision_sequence)
+    monkeypatch.setattr(dit, "linear", gelu_after_down)
+    assert _fails(td.test_gelu_sits_between_the_projections)
