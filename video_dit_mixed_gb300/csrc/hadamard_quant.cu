@@ -501,10 +501,11 @@ __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const
   }
 }
 
-// ------------------------------- thread-per-block NVFP4 forms (b = 16, 64) --
+// ----------------------------------- thread-per-block NVFP4 forms (b = 16) --
 //
 // For b <= 64 one thread holds a whole Hadamard block (b contiguous elements
-// of a row, b/8 16-byte loads) and runs every butterfly stage in registers:
+// of a row, b/8 16-byte loads) and runs every butterfly stage in registers
+// (b = 64 stages its blocks through shared memory first: see below):
 // no shuffles (which otherwise occupy the load/store pipe) and fewer
 // instructions per element.  Same stage order (ascending strides, each an
 // IEEE add or subtract), same exact 1/sqrt(b) scaling and same per-16-group
@@ -691,7 +692,8 @@ __device__ __forceinline__ void read_staged_block(const uint8_t* slot, int lane,
 
 // AMAX: max |rotated X| into amax_out (atomicMax of a non-negative float's
 // bits).  Otherwise: the NVFP4 codes and scales with s_t from *amax_src, as
-// hq_nvfp4_tpb_kernel<64>, including zero scales for the pad rows.
+// the thread-per-block kernel computes them, including zero scales for the
+// pad rows.
 template <bool AMAX>
 __global__ void __launch_bounds__(kStgWarps * 32) hq_nvfp4_staged_kernel(
     const uint16_t* __restrict__ X, int M, int K, const int32_t* mode_dev, const float* amax_src, float* amax_out,
@@ -958,12 +960,8 @@ cudaError_t launch_hq_nvfp4(const uint16_t* X, int M, int K, int b, const int32_
     return launch_staged<false>(X, M, K, mode_dev, amax_src, nullptr, o, st);
   if (b == 16) {
     const int grid = tpb_grid(static_cast<int64_t>((M + 127) & ~127) * (K / b));
-    if (b == 16)
-      hq_nvfp4_tpb_kernel<16><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_src, o->fp4_codes, o->fp4_scales,
-                                                    o->tensor_scale, o->rotated);
-    else
-      hq_nvfp4_tpb_kernel<64><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_src, o->fp4_codes, o->fp4_scales,
-                                                    o->tensor_scale, o->rotated);
+    hq_nvfp4_tpb_kernel<16><<<grid, 256, 0, st>>>(X, M, K, mode_dev, amax_src, o->fp4_codes, o->fp4_scales,
+                                                  o->tensor_scale, o->rotated);
     note_launch();
     return cudaGetLastError();
   }
