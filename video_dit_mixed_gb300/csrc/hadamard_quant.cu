@@ -695,7 +695,7 @@ __device__ __forceinline__ void read_staged_block(const uint8_t* slot, int lane,
 // the thread-per-block kernel computes them, including zero scales for the
 // pad rows.
 template <bool AMAX>
-__global__ void __launch_bounds__(kStgWarps * 32) hq_nvfp4_staged_kernel(
+__global__ void __launch_bounds__(kStgWarps * 32, 2) hq_nvfp4_staged_kernel(
     const uint16_t* __restrict__ X, int M, int K, const int32_t* mode_dev, const float* amax_src, float* amax_out,
     uint8_t* codes, uint8_t* scales, float* tscale_out, float* rotated) {
   if (mode_skips(mode_dev, SIXBIT_MODE_NVFP4)) return;
@@ -728,41 +728,92 @@ __global__ void __launch_bounds__(kStgWarps * 32) hq_nvfp4_staged_kernel(
     stage_tile(X, nblk, tile + kStgDepth * G, ring_s + slot * kStgTileBytes, lane);
     const int64_t t = tile * 32 + lane;
     if (t >= nblk) continue;
-    fwht_block<64>(v);
+    // P[i] = (v[i], v[32 + i]): the block's two halves side by side.  Stages
+    // of stride 1 .. 16 pair equal positions of both halves, so each is one
+    // f32x2 add or subtract per two butterflies; the stride-32 stage pairs
+    // the two lanes of a register.  Every lane rounds as the scalar
+    // fwht_block<64> does, in the same order.
+    uint64_t P[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) P[i] = f2_pack(v[i], v[32 + i]);
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if ((i & h) == 0) {
+          const uint64_t a = P[i], c = P[i + h];
+          P[i] = f2_add(a, c);
+          P[i + h] = f2_sub(a, c);
+        }
+      }
+    }
+    const uint64_t eighth = f2_pack(0.125f, 0.125f);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float a = f2_lo(P[i]), c = f2_hi(P[i]);
+      P[i] = f2_mul(f2_pack(__fadd_rn(a, c), __fsub_rn(a, c)), eighth);
+    }
     if constexpr (AMAX) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) m = fmaxf(m, fabsf(v[i]));
+      for (int i = 0; i < 32; ++i) m = fmaxf(m, fmaxf(fabsf(f2_lo(P[i])), fabsf(f2_hi(P[i]))));
     } else {
       const int r = static_cast<int>(t / per_row);
       const int col = static_cast<int>(t - static_cast<int64_t>(r) * per_row) * 64;
-      uint32_t packed[8];
+      // 16-element groups: g = 0, 1 in the low lanes of P[0..15], P[16..31];
+      // g = 2, 3 in the high lanes of the same registers.
+      float S[4];
       uint32_t sc = 0;
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         float am = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(v[16 * g + i]));
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t y = P[16 * (g & 1) + i];
+          am = fmaxf(am, fabsf(g < 2 ? f2_lo(y) : f2_hi(y)));
+        }
         const float sb = __fdiv_rn(__fdiv_rn(am, 6.0f), s_t);
         const uint32_t e = f32_to_e4m3(sb);
-        const float S = __fmul_rn(e4m3_to_f32(e), s_t);
-        float q[16];
-        if (recip_ok(S)) {
-          const float rS = __frcp_rn(S);
+        S[g] = __fmul_rn(e4m3_to_f32(e), s_t);
+        sc |= e << (8 * g);
+      }
+      uint32_t packed[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) q[i] = div_by_recip(v[16 * g + i], S, rS);
+      for (int hg = 0; hg < 2; ++hg) {  // registers P[16 hg ..]: groups hg (low lanes) and hg + 2 (high lanes)
+        const float Sl = S[hg], Sh = S[hg + 2];
+        uint64_t q[16];
+        if (recip_ok(Sl) && recip_ok(Sh)) {  // div_by_recip on both lanes
+          const uint64_t R2 = f2_pack(__frcp_rn(Sl), __frcp_rn(Sh));
+          const uint64_t N2 = f2_pack(-Sl, -Sh);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t y = P[16 * hg + i];
+            const uint64_t q0 = f2_mul(y, R2);
+            q[i] = f2_fma(f2_fma(N2, q0, y), R2, q0);
+          }
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) q[i] = (S != 0.f) ? __fdiv_rn(v[16 * g + i], S) : 0.f;
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t y = P[16 * hg + i];
+            float ql, qh;
+            if (recip_ok(Sl)) ql = div_by_recip(f2_lo(y), Sl, __frcp_rn(Sl));
+            else ql = (Sl != 0.f) ? __fdiv_rn(f2_lo(y), Sl) : 0.f;
+            if (recip_ok(Sh)) qh = div_by_recip(f2_hi(y), Sh, __frcp_rn(Sh));
+            else qh = (Sh != 0.f) ? __fdiv_rn(f2_hi(y), Sh) : 0.f;
+            q[i] = f2_pack(ql, qh);
+          }
         }
-        float q0[8], q1[8];
+        float a0[8], a1[8], b0[8], b1[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          q0[i] = q[i];
-          q1[i] = q[8 + i];
+          a0[i] = f2_lo(q[i]);
+          a1[i] = f2_lo(q[8 + i]);
+          b0[i] = f2_hi(q[i]);
+          b1[i] = f2_hi(q[8 + i]);
         }
-        packed[2 * g] = f32x8_to_e2m1(q0);
-        packed[2 * g + 1] = f32x8_to_e2m1(q1);
-        sc |= e << (8 * g);
+        packed[2 * hg] = f32x8_to_e2m1(a0);
+        packed[2 * hg + 1] = f32x8_to_e2m1(a1);
+        packed[2 * (hg + 2)] = f32x8_to_e2m1(b0);
+        packed[2 * (hg + 2) + 1] = f32x8_to_e2m1(b1);
       }
       uint8_t* cp = codes + static_cast<size_t>(r) * (K >> 1) + (col >> 1);
       reinterpret_cast<uint4*>(cp)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -771,7 +822,10 @@ __global__ void __launch_bounds__(kStgWarps * 32) hq_nvfp4_staged_kernel(
       if (rotated != nullptr) {
         float4* dst = reinterpret_cast<float4*>(rotated + static_cast<size_t>(r) * K + col);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < 8; ++i) {
+          dst[i] = make_float4(f2_lo(P[4 * i]), f2_lo(P[4 * i + 1]), f2_lo(P[4 * i + 2]), f2_lo(P[4 * i + 3]));
+          dst[8 + i] = make_float4(f2_hi(P[4 * i]), f2_hi(P[4 * i + 1]), f2_hi(P[4 * i + 2]), f2_hi(P[4 * i + 3]));
+        }
       }
     }
   }
