@@ -22,7 +22,7 @@ The matrix products use numpy's float64 matmul as a library primitive.
 from __future__ import annotations
 
 import numpy as np
-from scipy.special import erf
+from scipy.special import erfc
 
 from . import formats
 from .quant import INT4_GROUP, nvfp4_dequant
@@ -71,9 +71,13 @@ def bf16_gemm_ref(x, w):
 
 
 def gelu(v):
-    """Exact-erf GELU in float64."""
+    """Exact-erf GELU in float64, 0.5 v (1 + erf(v / sqrt 2)).
+
+    Evaluated as 0.5 v erfc(-v / sqrt 2), the same function: 1 + erf(z) would
+    cancel to 0 for z below about -6 and lose the negative tail entirely.
+    """
     v = np.asarray(v, dtype=np.float64)
-    return 0.5 * v * (1.0 + erf(v / np.sqrt(2.0)))
+    return 0.5 * v * erfc(-v / np.sqrt(2.0))
 
 
 def epilogue(ref, kind: str, residual=None):

@@ -9,6 +9,7 @@ import pytest
 
 from oracle import dit, formats, gemm, hadamard, policy, quant, stats
 
+import tests.test_oracle_composition as tc
 import tests.test_oracle_dit as td
 import tests.test_oracle_formats as tf
 import tests.test_oracle_hadamard as th
@@ -17,9 +18,10 @@ import tests.test_oracle_stats_policy as ts
 
 
 def _fails(fn, *args):
+    """True when the pin rejects the mutant: a failed assertion, or an error the mutant raises."""
     try:
         fn(*args)
-    except AssertionError:
+    except Exception:  # noqa: BLE001 -- AssertionError included
         return True
     return False
 
@@ -108,3 +110,58 @@ def test_dit_block_mutations_are_caught(monkeypatch):
     assert _fails(td.test_zero_weights_identity_and_decision_sequence)
     monkeypatch.setattr(dit, "linear", gelu_after_down)
     assert _fails(td.test_gelu_sits_between_the_projections)
+
+
+def test_rotate_then_quantize_mutations_are_caught(monkeypatch):
+    orig_hq = quant.hadamard_quant
+
+    def unrotated(x, b, mode, s_t=None):      # quantizes x instead of its rotation
+        out = quant.nvfp4_quantize(np.asarray(x, np.float32), s_t) if mode == "nvfp4" else \
+            quant.int8_quantize(np.asarray(x, np.float32))
+        out["y"] = np.asarray(x, np.float32)
+        return out
+    monkeypatch.setattr(quant, "hadamard_quant", unrotated)
+    assert _fails(tc.test_hadamard_quant_nvfp4_one_hot_rows)
+    assert _fails(tc.test_hadamard_quant_int8_one_hot_rows)
+    assert _fails(tc.test_linear_exact_on_the_quantizer_grids, policy.NVFP4)
+    assert _fails(tc.test_linear_exact_on_the_quantizer_grids, policy.INT8)
+    monkeypatch.setattr(quant, "hadamard_quant", lambda x, b, mode, s_t=None: orig_hq(x, b, mode, np.float32(1.0)))
+    assert _fails(tc.test_hadamard_quant_nvfp4_one_hot_rows)            # s_t forced to 1
+
+
+def test_weight_packing_mutations_are_caught(monkeypatch):
+    orig = quant.pack_weights
+
+    def unrotated_weights(w, b):              # quantizes W instead of W . blockdiag(H / sqrt b)
+        out = orig(w, b)
+        w = np.asarray(w, np.float32)
+        return dict(out, w_rot=w, nvfp4=quant.nvfp4_quantize(w), int4=quant.int4_quantize_weights(w))
+    monkeypatch.setattr(quant, "pack_weights", unrotated_weights)
+    assert _fails(tc.test_pack_weights_of_the_hadamard_matrix_is_the_identity)
+    assert _fails(tc.test_linear_exact_on_the_quantizer_grids, policy.NVFP4)
+    assert _fails(tc.test_linear_exact_on_the_quantizer_grids, policy.INT8)
+
+
+def test_quantized_linear_mutations_are_caught(monkeypatch):
+    orig_lin = dit.linear
+    swapped = lambda x, pk, mode, b, epi, residual=None: orig_lin(  # noqa: E731 -- the packings swapped
+        x, dict(pk, nvfp4=pk["int4"], int4=pk["nvfp4"]), mode, b, epi, residual)
+    monkeypatch.setattr(dit, "linear", swapped)
+    for mode in (policy.NVFP4, policy.INT8):
+        assert _fails(tc.test_linear_with_the_hadamard_weight_closed_form, mode)
+    monkeypatch.undo()
+    orig_nv = gemm.nvfp4_gemm_ref
+    monkeypatch.setattr(gemm, "nvfp4_gemm_ref", lambda xc, xs, stx, wc, ws, stw: orig_nv(xc, xs, 1.0, wc, ws, stw))
+    assert _fails(tc.test_linear_with_the_hadamard_weight_closed_form, policy.NVFP4)   # activation s_t dropped
+    assert _fails(tc.test_linear_exact_on_the_quantizer_grids, policy.NVFP4)
+    monkeypatch.undo()
+    orig_i8 = gemm.int8_gemm_ref
+    monkeypatch.setattr(gemm, "int8_gemm_ref", lambda qx, sm, qw, sw: orig_i8(qx, np.ones_like(sm), qw, sw))
+    assert _fails(tc.test_linear_with_the_hadamard_weight_closed_form, policy.INT8)    # row scale dropped
+    assert _fails(tc.test_linear_exact_on_the_quantizer_grids, policy.INT8)
+    monkeypatch.undo()
+    monkeypatch.setattr(gemm, "int8_gemm_ref", lambda qx, sm, qw, sw: orig_i8(qx, sm, qw, sw[:, ::-1]))
+    assert _fails(tc.test_linear_exact_on_the_quantizer_grids, policy.INT8)            # group scales misindexed
+    monkeypatch.undo()
+    monkeypatch.setattr(gemm, "gelu", lambda v: 0.5 * np.asarray(v, np.float64) * (1 + np.tanh(np.asarray(v))))
+    assert _fails(tc.test_linear_with_the_hadamard_weight_closed_form, policy.BF16)    # a different activation
