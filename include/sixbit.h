@@ -352,17 +352,26 @@ sixbit_status sixbit_skip_apply(const uint16_t* x_in, const uint16_t* delta_cach
  * counterpart to this call; it exists for callers that cannot call
  * cudaMalloc (code running under an allocator that owns all device memory,
  * or in a host that forbids allocation after start-up) and so cannot provide
- * the scratch buffer sixbit_block_stats asks for.  Same inputs, outputs and
- * results as sixbit_block_stats (delta cache bit-identical, sums equal up to
- * float64 summation order), but the reduction scratch is a fixed
- * 256 KB array inside the library, which every GPU that loads the library
- * holds until the process exits.  n must not exceed
+ * the scratch buffer sixbit_block_stats asks for.  Same inputs and outputs as
+ * sixbit_block_stats; the delta cache, the maximum and the count are
+ * bit-identical to it, while the sums are reduced over a different grid and
+ * so in a different order: they agree to about 5e-7 relative (the
+ * Kahan-summed sum_xin2 and sum_abs_out) and 1e-9 (the others), and a
+ * policy decision can differ only for a statistic within the policy's 1e-6
+ * near band of its threshold.  The reduction scratch is a fixed 256 KB array
+ * inside the library, which every GPU that loads the library holds until
+ * the process exits.  n must not exceed
  * sixbit_block_stats_noalloc_max_elems() (268,435,456 elements); larger n
- * returns SIXBIT_ESHAPE and launches nothing.  The call allocates no memory.
- * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
- * All calls share the one array: calls that overlap on the GPU race and
- * corrupt each other's results, so order them (one stream, or events).
+ * returns SIXBIT_ESHAPE and launches nothing.  The call allocates no memory
+ * itself.  The library looks up the array's device address at its first
+ * call of any entry point on each device (and again after a device reset);
+ * under CUDA's lazy module loading that is when the driver creates the
+ * array, so make one library call before a memory pool claims all device
+ * memory, or set CUDA_MODULE_LOADING=EAGER.  Make that first call before any
+ * stream capture.  All calls share the one array: calls that overlap on the
+ * GPU race and corrupt each other's results, so order them (one stream, or
+ * events).  err_dev is unused (the kernel has no device-side error path) and
+ * may be NULL.
  */
 sixbit_status sixbit_block_stats_noalloc(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta_cache,
                                          int64_t n, const int32_t* mode_dev, sixbit_stats* stats_dev,

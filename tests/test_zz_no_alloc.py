@@ -72,3 +72,37 @@ def test_noalloc_rejects_oversized_input_without_launching():
     status = lib.sixbit_block_stats_noalloc(p, p, p, big, None, C.c_void_p(st.data_ptr()), None, None)
     assert status == 2 and lib.sixbit_status_str(status) == b"unsupported shape"
     assert lib.sixbit_launch_count() == before
+
+
+def test_noalloc_skip_mode_touches_nothing_then_still_matches():
+    """With the mode word at SKIP the kernel returns at once: the delta cache and the statistics keep
+    their contents.  The next computing call, which finds the shared array as the skipped call left
+    it, still matches the regular entry point."""
+    from video_dit_mixed_gb300 import abi, ops
+    lib = abi.lib()
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    n = 1920 * 520
+    xi, xo, dp = _inputs(13, n)
+    mode = torch.tensor([ops.MODE_SKIP], dtype=torch.int32, device="cuda")
+    cache = dp.clone()
+    st = torch.full((1, 8), -1.0, dtype=torch.float64, device="cuda")
+
+    def call():
+        return lib.sixbit_block_stats_noalloc(C.c_void_p(xi.data_ptr()), C.c_void_p(xo.data_ptr()),
+                                              C.c_void_p(cache.data_ptr()), n, C.c_void_p(mode.data_ptr()),
+                                              C.c_void_p(st.data_ptr()), None, stream)
+    assert call() == 0
+    torch.cuda.synchronize()
+    assert torch.equal(cache.view(torch.int16), dp.view(torch.int16))
+    assert bool((st == -1.0).all())
+    mode.fill_(ops.MODE_INT8)
+    assert call() == 0
+    cache_ref = dp.clone()
+    st_ref = ops.new_stats()
+    ops.block_stats(xi, xo, cache_ref, st_ref, ops.new_scratch(n), mode_dev=mode)
+    torch.cuda.synchronize()
+    assert torch.equal(cache.view(torch.int16), cache_ref.view(torch.int16))
+    a, b = st.cpu().numpy()[0], st_ref.cpu().numpy()[0]
+    assert a[4] == b[4] and a[6] == b[6] == n
+    for i, rel in ((0, 1e-9), (1, 5e-7), (3, 1e-9), (5, 5e-7)):
+        assert abs(a[i] - b[i]) <= rel * abs(b[i]), (i, a[i], b[i])

@@ -6,9 +6,48 @@
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "ctx_cache.h"
 #include "internal.h"
 
 namespace sixbit {
+
+uint64_t current_context_id() {
+  struct Fns {
+    PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    PFN_cuCtxGetId_v12000 get_id = nullptr;
+  };
+  static const Fns fns = [] {
+    Fns f;
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    return f;
+  }();
+  if (fns.get_current == nullptr || fns.get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (fns.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (fns.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return static_cast<uint64_t>(id);
+}
+
+int sm_count() {
+  static ContextCache<int> cache;
+  int sms = 0;
+  const cudaError_t e = cache.get(&sms, [](int* o) {
+    int dev = 0;
+    cudaError_t r = cudaGetDevice(&dev);
+    if (r == cudaSuccess) r = cudaDeviceGetAttribute(o, cudaDevAttrMultiProcessorCount, dev);
+    return (r == cudaSuccess && *o > 0) ? cudaSuccess : cudaErrorInvalidDevice;
+  });
+  return (e == cudaSuccess && sms > 0) ? sms : 148;
+}
 
 static std::atomic<uint64_t> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
@@ -17,33 +56,40 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static bool valid_block(int b) { return b == 16 || b == 64 || b == 256; }
 
-// Checks that the current device is a compute capability 10.3 GPU (once per device).
-static sixbit_status check_device() {
-  static int ok_dev = -1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SIXBIT_EUNSUPPORTED;
-  if (dev == ok_dev) return SIXBIT_OK;
-  int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
-    return SIXBIT_EUNSUPPORTED;
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3) return SIXBIT_EUNSUPPORTED;
-  ok_dev = dev;
-  return SIXBIT_OK;
+// Checks that the current device is a compute capability 10.3 GPU (once per
+// context); the first successful check in a context also resolves the device
+// address of the allocation-free entry point's scratch array, so its module
+// is loaded at the library's first call on each device.
+sixbit_status check_device() {
+  static ContextCache<int> ok;
+  int v = 0;
+  const cudaError_t e = ok.get(&v, [](int* o) {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return cudaErrorInvalidDevice;
+    if (major != 10 || minor != 3) return cudaErrorInvalidDevice;
+    void* scratch = nullptr;
+    (void)noalloc_scratch(&scratch);   // its own call reports a failure
+    *o = 1;
+    return cudaSuccess;
+  });
+  return e == cudaSuccess ? SIXBIT_OK : SIXBIT_EUNSUPPORTED;
 }
 
 static sixbit_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SIXBIT_OK : SIXBIT_ECUDA; }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     cudaDriverEntryPointQueryResult q;
     void* p = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 

@@ -17,6 +17,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "ctx_cache.h"
 #include "internal.h"
 
 namespace sixbit {
@@ -856,13 +857,8 @@ __global__ void __launch_bounds__(kStgWarps * 32, 2) hq_nvfp4_staged_kernel(
 template <bool AMAX>
 static cudaError_t launch_staged(const uint16_t* X, int M, int K, const int32_t* mode_dev, const float* amax_src,
                                  float* amax_out, const sixbit_qact* o, cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(hq_nvfp4_staged_kernel<AMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStgSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  const cudaError_t ae = set_smem_once<hq_nvfp4_staged_kernel<AMAX>>(kStgSmem);
+  if (ae != cudaSuccess) return ae;
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -964,9 +960,7 @@ __global__ void __launch_bounds__(kHqWarps * 32) pack_quant_kernel(const float* 
 // ----------------------------------------------------------- host launch --
 
 static int hq_grid(int rows) {
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = sm_count();
   const int want = (rows + kHqWarps - 1) / kHqWarps;
   const int cap = sms * 8;
   return want < cap ? (want > 0 ? want : 1) : cap;
@@ -983,9 +977,7 @@ static int hq_grid(int rows) {
 // Grid of the thread-per-block kernels: one thread per Hadamard block, at
 // most 16 CTAs of 256 per SM (the rest is walked with a grid stride).
 static int tpb_grid(int64_t nblk) {
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = sm_count();
   const int64_t want = (nblk + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sms) * 16;
   return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));

@@ -9,6 +9,13 @@
 
 namespace sixbit {
 
+// SIXBIT_OK when the current device is a compute capability 10.3 GPU (checked
+// once per context), else SIXBIT_EUNSUPPORTED.
+sixbit_status check_device();
+// Device address of the allocation-free entry point's scratch array in the
+// current context (resolved once per context).
+sixbit_status noalloc_scratch(void** out);
+
 struct GemmParams {
   int M, N, K;
   const int32_t* mode_dev;

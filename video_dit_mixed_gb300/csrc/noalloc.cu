@@ -11,15 +11,20 @@
 // kNoallocScratchBytes (about 256 KB), which every GPU that loads the library
 // holds until the process exits.  Host code may not use the array's name as a
 // device address (on the host it names a shadow variable), so the device
-// address is looked up once per device with cudaGetSymbolAddress, with that
-// device current, during the first call on that device.  That first call
-// should come before any stream capture.  Every call shares the one array:
-// calls that overlap on the GPU (different streams, or different host
-// threads without ordering) race on it and corrupt each other's results.
+// address is looked up with cudaGetSymbolAddress, with the device current,
+// once per device and CUDA context (again after a cudaDeviceReset, which can
+// move the array).  The library does that lookup at its first call of any
+// entry point on each device: under CUDA's lazy module loading that lookup is
+// when the driver creates the array, so a caller whose memory pool will own
+// all device memory makes one library call first (or runs with
+// CUDA_MODULE_LOADING=EAGER).  That first call should also come before any
+// stream capture.  Every call shares the one array: calls that overlap on the
+// GPU (different streams, or different host threads without ordering) race on
+// it and corrupt each other's results.
 #include <cstdint>
-#include <mutex>
 
 #include "common.cuh"
+#include "ctx_cache.h"
 #include "internal.h"
 
 namespace sixbit {
@@ -31,22 +36,15 @@ constexpr int64_t kNoallocMaxElems = kNoallocMaxCtas * kFixedElemsPerCta;  // 26
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-static void* g_scratch_ptr[kMaxDevices] = {nullptr};
-static std::mutex g_scratch_mu;
-
-// Device address of g_noalloc_scratch on the current device (looked up once).
-static sixbit_status noalloc_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SIXBIT_ECUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return SIXBIT_ECUDA;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return SIXBIT_OK;
+// Device address of g_noalloc_scratch in the current context.
+sixbit_status noalloc_scratch(void** out) {
+  static ContextCache<void*> cache;
+  const cudaError_t e = cache.get(out, [](void** p) {
+    *p = nullptr;
+    const cudaError_t r = cudaGetSymbolAddress(p, g_noalloc_scratch);
+    return (r == cudaSuccess && *p != nullptr) ? cudaSuccess : cudaErrorInvalidSymbol;
+  });
+  return e == cudaSuccess ? SIXBIT_OK : SIXBIT_ECUDA;
 }
 
 }  // namespace sixbit
@@ -58,19 +56,16 @@ extern "C" int64_t sixbit_block_stats_noalloc_max_elems(void) { return kNoallocM
 extern "C" sixbit_status sixbit_block_stats_noalloc(const uint16_t* x_in, const uint16_t* x_out,
                                                     uint16_t* delta_cache, int64_t n, const int32_t* mode_dev,
                                                     sixbit_stats* stats_dev, int32_t* err_dev, void* stream) {
-  (void)err_dev;
+  (void)err_dev;  // the statistics kernel has no device-side error path
   if (x_in == nullptr || x_out == nullptr || delta_cache == nullptr || stats_dev == nullptr) return SIXBIT_EINVAL;
   if (n <= 0 || n % 8 != 0 || n > kNoallocMaxElems) return SIXBIT_ESHAPE;
   if ((reinterpret_cast<uintptr_t>(x_in) | reinterpret_cast<uintptr_t>(x_out) |
        reinterpret_cast<uintptr_t>(delta_cache)) & 15u)
     return SIXBIT_EALIGN;
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SIXBIT_EUNSUPPORTED;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return SIXBIT_EUNSUPPORTED;
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3) return SIXBIT_EUNSUPPORTED;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
   void* scratch = nullptr;
-  sixbit_status s = noalloc_scratch(&scratch);
+  s = noalloc_scratch(&scratch);
   if (s != SIXBIT_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the completion counter must start at zero (the kernel also leaves it zero)

@@ -39,6 +39,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "ctx_cache.h"
 #include "internal.h"
 
 namespace sixbit {
@@ -736,40 +737,27 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
 
 // ------------------------------------------------------------ host launch --
 
-static int num_sms() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
-  return sms;
-}
-
 template <int KIND, bool GROUPED, bool DBG>
 static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
                               cudaStream_t st) {
-  static bool attr_done = false;
   constexpr int smem = gemm_smem_bytes<KIND, GROUPED>();
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(qgemm_kernel<KIND, GROUPED, DBG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  cudaError_t e = set_smem_once<qgemm_kernel<KIND, GROUPED, DBG>>(smem);
+  if (e != cudaSuccess) return e;
   if constexpr (GROUPED) {
-    static int regs = -1;
-    if (regs < 0) {
+    static ContextCache<int> regs_cache;
+    int regs = 0;
+    e = regs_cache.get(&regs, [](int* o) {
       cudaFuncAttributes fa;
-      cudaError_t e = cudaFuncGetAttributes(&fa, qgemm_kernel<KIND, GROUPED, DBG>);
-      if (e != cudaSuccess) return e;
-      regs = fa.numRegs;
-    }
+      const cudaError_t r = cudaFuncGetAttributes(&fa, qgemm_kernel<KIND, GROUPED, DBG>);
+      *o = fa.numRegs;
+      return r;
+    });
+    if (e != cudaSuccess) return e;
     if (regs < kGrpRegsLaunch || 4 * kGrpRegsLow + 8 * kGrpRegsHigh > 12 * regs) return cudaErrorInvalidConfiguration;
   }
   const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
-  const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  const int sms = sm_count();
+  const int grid = ntiles < sms ? ntiles : sms;
   qgemm_kernel<KIND, GROUPED, DBG><<<grid, gemm_threads<KIND, GROUPED>(), smem, st>>>(a, b, y, p);
   note_launch();
   return cudaGetLastError();

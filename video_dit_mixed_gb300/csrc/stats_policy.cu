@@ -19,6 +19,7 @@
 #include <cstdint>
 
 #include "common.cuh"
+#include "ctx_cache.h"
 #include "internal.h"
 
 namespace sixbit {
@@ -678,17 +679,18 @@ __global__ void __launch_bounds__(kStThreads, 4) dit_skip_run_kernel(sixbit_poli
 // One wave: as many CTAs as fit on the GPU at once (occupancy of `kernel`),
 // fewer for small n (at least 4 vectors per thread), never more than the
 // scratch holds.
-template <typename Kernel>
-static int stats_grid(Kernel kernel, int64_t n) {
-  static int resident = 0;  // per kernel instantiation of this template
-  if (resident == 0) {
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kStThreads, 0);
-    resident = (sms > 0 ? sms : 152) * (per_sm > 0 ? per_sm : 4);
-    if (resident > kStMaxBlocks) resident = kStMaxBlocks;
-  }
+template <auto KERNEL>
+static int stats_grid(int64_t n) {
+  static ContextCache<int> cache;  // per kernel and context
+  int resident = 0;
+  if (cache.get(&resident, [](int* o) {
+        int per_sm = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, KERNEL, kStThreads, 0);
+        *o = sm_count() * (per_sm > 0 ? per_sm : 4);
+        if (*o > kStMaxBlocks) *o = kStMaxBlocks;
+        return cudaSuccess;
+      }) != cudaSuccess)
+    resident = kStMaxBlocks;
   const int64_t per = static_cast<int64_t>(kStThreads) * 8 * 4;
   int64_t want = (n + per - 1) / per;
   if (want > resident) want = resident;
@@ -699,14 +701,14 @@ static int stats_grid(Kernel kernel, int64_t n) {
 size_t stats_scratch_bytes(int64_t) { return 16 + static_cast<size_t>(kStMaxBlocks) * kNumSums * sizeof(FF); }
 
 cudaError_t launch_tensor_stats(const uint16_t* x, int64_t n, double* out, void* scratch, cudaStream_t st) {
-  tensor_stats_kernel<<<stats_grid(tensor_stats_kernel, n), kStThreads, 0, st>>>(x, n, out, scratch);
+  tensor_stats_kernel<<<stats_grid<tensor_stats_kernel>(n), kStThreads, 0, st>>>(x, n, out, scratch);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_block_stats(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta, int64_t n,
                                const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st) {
-  block_stats_kernel<<<stats_grid(block_stats_kernel, n), kStThreads, 0, st>>>(x_in, x_out, delta, n, mode_dev, stats, scratch);
+  block_stats_kernel<<<stats_grid<block_stats_kernel>(n), kStThreads, 0, st>>>(x_in, x_out, delta, n, mode_dev, stats, scratch);
   note_launch();
   return cudaGetLastError();
 }
@@ -726,28 +728,28 @@ cudaError_t launch_block_stats_fixed_grid(const uint16_t* x_in, const uint16_t* 
 
 cudaError_t launch_skip_apply(const uint16_t* x_in, const uint16_t* delta, uint16_t* x_out, int64_t n,
                               const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st) {
-  skip_apply_kernel<<<stats_grid(skip_apply_kernel, n), kStThreads, 0, st>>>(x_in, delta, x_out, n, mode_dev, stats, scratch);
+  skip_apply_kernel<<<stats_grid<skip_apply_kernel>(n), kStThreads, 0, st>>>(x_in, delta, x_out, n, mode_dev, stats, scratch);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_dit_begin(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, void* scratch, int32_t* err,
                              cudaStream_t st) {
-  dit_begin_kernel<<<stats_grid(dit_begin_kernel, B.n), kStThreads, 0, st>>>(cfg, B, scratch, err);
+  dit_begin_kernel<<<stats_grid<dit_begin_kernel>(B.n), kStThreads, 0, st>>>(cfg, B, scratch, err);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_dit_block_end(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, void* scratch,
                                  int32_t* err, cudaStream_t st) {
-  dit_block_end_kernel<<<stats_grid(dit_block_end_kernel, B.n), kStThreads, 0, st>>>(cfg, B, l, scratch, err);
+  dit_block_end_kernel<<<stats_grid<dit_block_end_kernel>(B.n), kStThreads, 0, st>>>(cfg, B, l, scratch, err);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_dit_skip_run(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, void* scratch,
                                 int32_t* err, cudaStream_t st) {
-  dit_skip_run_kernel<<<stats_grid(dit_skip_run_kernel, B.n), kStThreads, 0, st>>>(cfg, B, l, scratch, err);
+  dit_skip_run_kernel<<<stats_grid<dit_skip_run_kernel>(B.n), kStThreads, 0, st>>>(cfg, B, l, scratch, err);
   note_launch();
   return cudaGetLastError();
 }
