@@ -47,16 +47,9 @@ METRIC = "W4A4/W4A8 qGEMM TFLOPS+%peak; Hadamard-quant GB/s; MLP-DiT step/s"
 FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense ratio (FP4 13.5 PFLOP/s, BF16 2.25 PFLOP/s)
 
 # DRAM bytes (read + write) per launch from one ncu capture of the same kernels
-# on the same shapes (profiles/dram_traffic_dit_2b.md); an entry must be
-# removed when its kernel changes.
-MEASURED_TRAFFIC = {
-    ("dit_2b", "qgemm_up:int8"): 335972608,
-    ("dit_2b", "qgemm_down:int8"): 632774656,
-    ("dit_2b", "qgemm_up:bf16"): 333682841,
-    ("dit_2b", "qgemm_down:bf16"): 543600844,
-    ("dit_2b", "hq_x:int8"): 86360960,
-    ("dit_2b", "hq_h:int8"): 495195520,
-}
+# on the same shapes (profiles/); an entry must be removed when its kernel
+# changes.
+MEASURED_TRAFFIC = {}
 MODE_NAMES = {1: "nvfp4", 2: "int8", 3: "bf16", 4: "skip"}
 
 
@@ -130,7 +123,7 @@ class QkvLinear:
         self.x_host = torch.from_numpy(x).to(torch.bfloat16).pin_memory()
         self.x = self.x_host.to(device)
         self.pw = ops.pack_weights(torch.from_numpy(w).to(device), self.b)
-        self.qa = ops.QActTensors(self.m, self.k, device, i8_codes=False)   # the GEMM reads the bf16 operand
+        self.qa = ops.QActTensors(self.m, self.k, device)
         self.y = {k: torch.empty((self.m, self.n), dtype=torch.bfloat16, device=device) for k in ("fp4", "i8", "bf")}
         self.y_host = torch.empty((self.m, self.n), dtype=torch.bfloat16).pin_memory()
         self.ins = torch.zeros(4, dtype=torch.float64, device=device)
@@ -215,8 +208,8 @@ class QkvLinear:
             return ("tensor", self.gemm_flops, "nvfp4" in label)
         if label == "hq_nvfp4":
             return ("hbm", mk * 2 + mk // 2 + mk // 16, False)
-        if label == "hq_int8":   # read X, write the bf16 integer operand and the row scales
-            return ("hbm", mk * 4 + self.m * 4, False)
+        if label == "hq_int8":   # read X, write the int8 codes and the row scales
+            return ("hbm", mk * 3 + self.m * 4, False)
         if label == "tensor_stats":
             return ("hbm", mk * 2, False)
         return (None, 0, False)
@@ -323,37 +316,40 @@ class DitStep:
     BODY_KERNELS = {1: 7, 2: 5, 3: 3, 4: 0}
 
     def launches(self):
-        """Kernels run in the timed steps (from the device decision log of the same trajectory)."""
+        """Kernels run in the timed steps (from the device decision log of the same steps)."""
         if len(self.mode_log) == 0:
             return None
         import numpy as np
         low = np.asarray(self.mode_log) & 0xFF
         n = 0
-        for s in self.timed_steps:
-            row = [int(v) for v in low[s]]
+        for row in low:
+            row = [int(v) for v in row]
             n += 1 + sum(self.BODY_KERNELS.get(v, 0) for v in row)
             n += sum(1 for l, v in enumerate(row) if v == 4 and (l == 0 or row[l - 1] != 4))  # run starts
         return n
 
     def profile(self, k, stream):
-        """Per-call device times over a full trajectory, with the kernels a graph step runs.
+        """Per-call device times over the timed window's own steps, with the kernels a graph step runs.
 
-        Each block is dispatched on the host from its mode word (the kernels of
-        the switched graph, minus nothing but the branch selection); CUDA
-        events on the launching stream bracket every call.  Before each group
-        of calls a GPU-side pause lets the host enqueue them ahead of the GPU,
-        so the events bracket device work, not launch gaps.
+        The same trajectory steps as the timed region are replayed (from the
+        first, with the model reset wherever the timed region started a new
+        video), each block dispatched on the host from its mode word (the
+        kernels of the switched graph, minus nothing but the branch selection);
+        CUDA events on the launching stream bracket every call.  Before each
+        group of calls a GPU-side pause lets the host enqueue them ahead of the
+        GPU, so the events bracket device work, not launch gaps.  The decision
+        log of these steps is what `decisions`, `gpu_launches` and the CPU
+        baseline's extrapolation use.
         """
         import numpy as np
         T = self.t
         m = self.model
         o = self.ops
-        m.reset()
-        self.s = 0
+        steps = list(self.timed_steps) if self.timed_steps else list(range(k))
         pause = int(4e5)          # ~0.2 ms of GPU cycles: covers the host's enqueue of a group of calls
         recs = []                 # (key, start event, end event)
         run_bytes = []
-        mh = np.zeros((self.c["steps"], self.L), dtype=np.int64)
+        mh = np.zeros((len(steps), self.L), dtype=np.int64)
 
         def timed(key, fn):
             a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
@@ -362,7 +358,9 @@ class DitStep:
             b.record(stream)
             recs.append((key, a, b))
 
-        for s in range(self.c["steps"]):
+        for j, s in enumerate(steps):
+            if j == 0 or s == 0:      # the timed region started a new video here
+                m.reset()
             m.x_in.copy_(self.traj[s])
             T.cuda.synchronize()
             T.cuda._sleep(pause)
@@ -371,13 +369,13 @@ class DitStep:
             for l in range(self.L):
                 out = m.bufs[l % 2]
                 word = int(m.modes[l].item())                  # synchronises
-                mh[s, l] = word
+                mh[j, l] = word
                 mode = word & 0xFF
                 if mode == 4:
-                    if l == 0 or (mh[s, l - 1] & 0xFF) != 4:    # a run starts here (its length: from the log)
+                    if l == 0 or (mh[j, l - 1] & 0xFF) != 4:    # a run starts here (its length: from the log)
                         T.cuda._sleep(pause)
                         timed("skip_run", lambda l=l: o.dit_skip_run(m.cfg, m.rec, l, m.scratch))
-                        run_bytes.append((s, l))
+                        run_bytes.append((j, l))
                 else:
                     T.cuda._sleep(pause)
                     last = [None]
@@ -399,13 +397,12 @@ class DitStep:
             per.setdefault(key, []).append(a.elapsed_time(b))
         # bytes of each run start: x read, k deltas read, x written
         sizes = []
-        for s, l in run_bytes:
-            k = 1
-            while l + k < self.L and low[s, l + k] == 4:
-                k += 1
-            sizes.append((4 + 2 * k) * self.T * self.H)
-        run_bytes = sizes
-        self.skip_run_bytes = (sum(run_bytes) / len(run_bytes)) if run_bytes else 0
+        for j, l in run_bytes:
+            kk = 1
+            while l + kk < self.L and low[j, l + kk] == 4:
+                kk += 1
+            sizes.append((4 + 2 * kk) * self.T * self.H)
+        self.skip_run_bytes = (sum(sizes) / len(sizes)) if sizes else 0
         self.mode_log = mh
         m.reset()
         self.s = 0
@@ -460,8 +457,8 @@ class DitStep:
             n = T * (H if label == "hq_x" else F)
             if mode == "nvfp4":
                 return ("hbm", n * 2 + n // 2 + n // 16, False)
-            if mode == "int8":   # read, bf16 integer operand, row scales
-                return ("hbm", n * 4 + T * 4, False)
+            if mode == "int8":   # read, int8 codes, row scales
+                return ("hbm", n * 3 + T * 4, False)
             return (None, 0, False)
         if label == "block_stats":
             return ("hbm", 8 * T * H, False)
@@ -477,7 +474,16 @@ class DitStep:
         low = words & 0xFF
         hist = {MODE_NAMES[k]: int((low == k).sum()) for k in (1, 2, 3, 4)}
         return dict(decisions=hist, refresh=int(((words & 256) != 0).sum()), pdr=int(((words & 512) != 0).sum()),
-                    near_threshold=int(((words & 2048) != 0).sum()), block_steps=int(low.size))
+                    near_threshold=int(((words & 2048) != 0).sum()), block_steps=int(low.size),
+                    window=f"trajectory steps {self.timed_steps[0]}..{self.timed_steps[-1]}" if self.timed_steps
+                    else None)
+
+    def trace(self):
+        """Per timed step, the list of per-block modes ('nvfp4' | 'int8' | 'bf16' | 'skip')."""
+        import numpy as np
+        if len(self.mode_log) == 0:
+            return None
+        return [[MODE_NAMES.get(int(v), "?") for v in row] for row in (np.asarray(self.mode_log) & 0xFF)]
 
 
 class GemmSweep:
@@ -498,7 +504,7 @@ class GemmSweep:
         self.x_host = torch.from_numpy(x).to(torch.bfloat16).pin_memory()
         self.x = self.x_host.to(device)
         self.pw = ops.pack_weights(torch.from_numpy(w).to(device), self.b)
-        self.qa = {m: ops.QActTensors(m, self.k, device, i8_codes=False) for m in self.ms}
+        self.qa = {m: ops.QActTensors(m, self.k, device) for m in self.ms}
         self.y = torch.empty((max(self.ms), self.n), dtype=torch.bfloat16, device=device)
         self.y_host = torch.empty((max(self.ms), self.n), dtype=torch.bfloat16).pin_memory()
         self.flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)
@@ -551,7 +557,7 @@ class GemmSweep:
         n = m * self.k
         if kind == "hq_nvfp4":
             return ("hbm", n * 2 + n // 2 + n // 16, False)
-        return ("hbm", n * 4 + m * 4, False)
+        return ("hbm", n * 3 + m * 4, False)     # INT8: read X, write the codes and the row scales
 
     def launches(self):
         return None
@@ -597,6 +603,83 @@ def _roofline(wl, per, peaks):
                     work_per_launch=work,
                     peak_source=f"{peaks['src']} copy")
     return roof, table
+
+
+def metric_parts(torch, ops, dev, peaks):
+    """The metric's kernel parts, timed with CUDA events on the current stream (median of 7, after 3 warm-up
+    launches; every input is larger than L2, and a 256 MB buffer is written between launches):
+      qgemm: W4A4 (NVFP4) and W4A8 (INT8, including its per-call INT4 -> fp16 weight expansion) at
+             M x N x K = 35552 x 3072 x 3072, TFLOP/s and the fraction of the dtype's peak;
+      hadamard_quant: the fused rotation + quantization of a 17776 x 7680 bf16 tensor (the FFN hidden
+             activation), GB/s over its algorithmic bytes (read 2 B, write 0.5625 B (NVFP4) or 1 B (INT8) per
+             element), with the NVFP4 amax pass separate or supplied by the producer.
+    Synthetic inputs: Laplace(0, 1) activations with 0.5% of channels x50, N(0, 0.02^2) weights, drawn on
+    the device from a seeded generator."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(77)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def laplace(m, k):
+        u = torch.rand((m, k), generator=gen, device=dev) - 0.5
+        x = -torch.sign(u) * torch.log1p(-2 * u.abs())
+        idx = torch.randperm(k, generator=gen, device=dev)[: max(1, round(0.005 * k))]
+        x[:, idx] *= 50.0
+        return x.to(torch.bfloat16)
+
+    def med_us(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(7):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return sorted(ts)[len(ts) // 2]
+
+    out = {}
+    m, n, k, b = 35552, 3072, 3072, 64
+    x = laplace(m, k)
+    w = torch.randn((n, k), generator=gen, device=dev) * 0.02
+    pw = ops.pack_weights(w, b)
+    qa = ops.QActTensors(m, k, dev)
+    ops.hadamard_quant(x, b, ops.MODE_NVFP4, out=qa)
+    ops.hadamard_quant(x, b, ops.MODE_INT8, out=qa)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(ops.qgemm_workspace_bytes(n, k), dtype=torch.uint8, device=dev)
+    flops = 2.0 * m * n * k
+    g = {}
+    for name, code, pk, pk_src in (("w4a4_nvfp4", ops.MODE_NVFP4, peaks["bf16"] * FP4_OVER_BF16,
+                                    "bf16 burst x6 nominal fp4/bf16"),
+                                   ("w4a8_int8", ops.MODE_INT8, peaks["bf16"], "bf16 burst (fp16 MMAs)")):
+        us = med_us(lambda: ops.qgemm(qa, x, pw, code, out=y, ws=ws))
+        tf = flops / us / 1e6
+        g[name] = dict(us=round(us, 1), tflops=round(tf, 1), peak=round(pk, 1), frac=round(tf / pk, 4),
+                       peak_source=f"{peaks['src']} {pk_src}")
+    out["qgemm"] = dict(shape=[m, n, k], **g)
+    del x, qa, y, w, pw, ws
+    m, k = 17776, 7680
+    x = laplace(m, k)
+    qa = ops.QActTensors(m, k, dev)
+    nel = m * k
+    hq = {}
+    us2 = med_us(lambda: ops.hadamard_quant(x, b, ops.MODE_NVFP4, out=qa))
+    amax = qa.tensor_amax.clone()
+    us1 = med_us(lambda: ops.hadamard_quant(x, b, ops.MODE_NVFP4, out=qa, tamax=amax))
+    us8 = med_us(lambda: ops.hadamard_quant(x, b, ops.MODE_INT8, out=qa))
+    for name, us, byt in (("nvfp4_two_pass", us2, nel * 2 + nel // 2 + nel // 16),
+                          ("nvfp4_amax_supplied", us1, nel * 2 + nel // 2 + nel // 16),
+                          ("int8", us8, nel * 3 + m * 4)):
+        gbs = byt / us / 1e3
+        hq[name] = dict(us=round(us, 1), gbs=round(gbs, 1), frac=round(gbs / peaks["hbm"], 4),
+                        algorithmic_bytes=byt)
+    out["hadamard_quant"] = dict(shape=[m, k], had_block=b, peak_gbs=peaks["hbm"],
+                                 peak_source=f"{peaks['src']} copy", **hq)
+    return out
 
 
 def reduce_max(v: float, world: int, device) -> float:
@@ -669,6 +752,10 @@ def run_ours(args):
     e2e_ms = max_over_ranks(statistics.fmean(wl.e2e(args.steps, stream)))
     if wl.launches() is not None:
         launches = wl.launches()
+    parts = None
+    if args.workload.startswith("dit") and not args.no_metric_parts:
+        barrier()
+        parts = metric_parts(torch, ops, dev, _peaks())
 
     if rank == 0:
         peaks = _peaks()
@@ -681,8 +768,11 @@ def run_ours(args):
                              h2d_bytes_per_step=wl.h2d_bytes, d2h_bytes_per_step=wl.d2h_bytes),
                     gpu_launches=launches, roofline=roof, kernels=table, clocks=clk, wall_s=round(wall, 3))
         line.update(wl.extra())
+        if parts is not None:
+            line["metric_parts"] = parts
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+            trace = wl.trace() if hasattr(wl, "trace") else None
+            line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget, trace=trace)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -718,41 +808,128 @@ def _oracle_linear_sample(workload, budget_s):
                        f"GEMMs of all three kinds (weights packed once, untimed), {dt:.1f} s")
 
 
-def _oracle_dit_sample(workload, budget_s):
-    """One INT8 block (both linears, quantizers, statistics) on a token sample, extrapolated to a DiT step."""
+def cpu_model() -> str:
+    """The host CPU's model name (x86 'model name', else lscpu's 'Model name', else the platform)."""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_block_costs(workload, rows, budget_s):
+    """Seconds the oracle takes for one block-step of each kind on `rows` token rows.
+
+    compute kinds (nvfp4, int8, bf16): both quantized linears (or bf16 GEMMs)
+    with GELU and residual, then the block statistics; skip: the TDC skip and
+    its output statistics.  Weights are packed once, untimed.  Each kind is
+    repeated until budget_s / 4 has passed; the mean is returned.
+    """
     import numpy as np
 
     import synthgen
     from oracle import dit as odit
     from oracle import policy, quant, stats
     c = synthgen.DIT_CONFIGS[workload]
-    rows = 64
     x = synthgen.activations(c["seed"], rows, c["hidden"], "laplace", 0.005, 50.0)
     wu = synthgen.weights(c["seed"], c["ffn"], c["hidden"], c["w_std"], stream=100)
     wd = synthgen.weights(c["seed"], c["hidden"], c["ffn"], c["w_std"], stream=101)
     pu, pd = quant.pack_weights(wu, c["had_block"]), quant.pack_weights(wd, c["had_block"])
-    t0 = time.perf_counter()
-    done = 0
-    while True:
-        h = odit.linear(x, pu, policy.INT8, c["had_block"], "gelu")
-        out = odit.linear(h, pd, policy.INT8, c["had_block"], "residual", x)
-        stats.block_stats(x, out, np.zeros_like(x))
-        done += rows
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    sec_per_step = dt / done * c["tokens"] * c["blocks"]
-    return dict(value=round(1.0 / sec_per_step, 8), unit="step/s", cores=os.cpu_count(), kind="oracle",
-                sample=f"{done} token rows of one INT8 block (up GEMM + GELU, down GEMM + residual, both "
-                       f"quantizers, block statistics; weights packed once, untimed) in {dt:.1f} s, "
-                       f"extrapolated to {c['tokens']} tokens x {c['blocks']} blocks per step (all computed)")
+    prev = np.zeros_like(x)
+
+    def compute(mode):
+        h = odit.linear(x, pu, mode, c["had_block"], "gelu")
+        out = odit.linear(h, pd, mode, c["had_block"], "residual", x)
+        stats.block_stats(x, out, prev)
+
+    def skip():
+        stats.tensor_stats(stats.skip_apply(x, prev))
+
+    kinds = {"nvfp4": lambda: compute(policy.NVFP4), "int8": lambda: compute(policy.INT8),
+             "bf16": lambda: compute(policy.BF16), "skip": skip}
+    out = {}
+    for name, fn in kinds.items():
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            fn()
+            n += 1
+            if time.perf_counter() - t0 > budget_s / 4:
+                break
+        out[name] = (time.perf_counter() - t0) / n
+    return out
 
 
-def cpu_baseline(workload: str, budget_s: float = 15.0):
-    """The oracle, as it stands, on a bounded sample of the workload (host cores)."""
-    if workload.startswith("dit"):
-        return _oracle_dit_sample(workload, budget_s)
-    return _oracle_linear_sample(workload, budget_s)
+def _costs_one_core(workload, rows, budget_s):
+    """oracle_block_costs in a fresh process whose numerical libraries use one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1", NUMEXPR_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-costs", "--workload", workload,
+                        "--rows", str(rows), "--cpu-budget", str(budget_s)],
+                       capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return None
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _dit_rate(costs, trace, tokens, rows):
+    """DiT steps/s of the oracle extrapolated over a decision trace (list of per-block mode lists)."""
+    per_step = [sum(costs[mode] for mode in step) * tokens / rows for step in trace]
+    return len(per_step) / sum(per_step)
+
+
+def cpu_baseline(workload: str, budget_s: float = 15.0, trace=None):
+    """The oracle, as it stands, on a bounded sample of the workload (host cores).
+
+    DiT workloads: per-kind block-step times on a token sample, extrapolated
+    over `trace` (the timed window's decisions; every block computing in INT8
+    when no trace is given), on all cores and, in a child process, on one.
+    """
+    if not workload.startswith("dit"):
+        return _oracle_linear_sample(workload, budget_s)
+    import synthgen
+    c = synthgen.DIT_CONFIGS[workload]
+    rows = 32
+    costs = oracle_block_costs(workload, rows, budget_s / 2)
+    costs1 = _costs_one_core(workload, rows, budget_s / 2)
+    if trace is None:
+        trace = [["int8"] * c["blocks"]]
+        how = "every block computing in INT8 (no decision trace)"
+    else:
+        how = f"the decisions of the timed window ({len(trace)} steps x {c['blocks']} blocks)"
+    v = _dit_rate(costs, trace, c["tokens"], rows)
+    out = dict(value=round(v, 10), unit="step/s", cores=os.cpu_count(), kind="oracle",
+               sample=f"oracle block-steps of each kind (NVFP4, INT8, BF16: both linears, GELU, residual, "
+                      f"quantizers, block statistics; SKIP: skip and statistics) on {rows} of {c['tokens']} token "
+                      f"rows, extrapolated to full size over {how}: extrapolated",
+               cpu_model=cpu_model(),
+               block_step_s_per_row={k: round(t / rows, 6) for k, t in costs.items()})
+    if costs1 is not None:
+        out["value_1core"] = round(_dit_rate(costs1, trace, c["tokens"], rows), 10)
+        out["block_step_s_per_row_1core"] = {k: round(t / rows, 6) for k, t in costs1.items()}
+    return out
+
+
+def _reference_dit_step(workload, budget_s):
+    """One reference-arm step: oracle block-steps on a token sample, every block computing in INT8."""
+    import synthgen
+    c = synthgen.DIT_CONFIGS[workload]
+    rows = 32
+    costs = oracle_block_costs(workload, rows, budget_s)
+    v = _dit_rate(costs, [["int8"] * c["blocks"]], c["tokens"], rows)
+    return dict(value=round(v, 10), unit="step/s", cores=os.cpu_count(), kind="oracle", cpu_model=cpu_model(),
+                sample=f"oracle block-steps on {rows} of {c['tokens']} token rows, extrapolated to full size with "
+                       f"every block computing in INT8: extrapolated")
 
 
 def run_reference(args):
@@ -765,7 +942,10 @@ def run_reference(args):
     cb = None
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        cb = cpu_baseline(args.workload, budget_s=per_step if i >= args.warmup else 0.5)
+        if args.workload.startswith("dit"):
+            cb = _reference_dit_step(args.workload, per_step if i >= args.warmup else 0.5)
+        else:
+            cb = cpu_baseline(args.workload, budget_s=per_step if i >= args.warmup else 0.5)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
             vals.append(cb["value"])
@@ -788,12 +968,28 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-metric-parts", action="store_true",
+                    help="DiT workloads: skip the qGEMM / Hadamard-quant kernel figures added to the line")
     ap.add_argument("--dispatch", default="graph", choices=["graph", "host"],
                     help="DiT workloads: 'host' replaces the CUDA graph by host-side dispatch on each block's mode "
                          "word (one sync per block; for profilers that cannot profile conditional graph nodes)")
     ap.add_argument("--blocks", type=int, default=0,
                     help="DiT workloads: use only this many blocks (profiling runs on a smaller device footprint)")
+    ap.add_argument("--oracle-costs", action="store_true", help=argparse.SUPPRESS)  # the 1-core CPU leg's child
+    ap.add_argument("--rows", type=int, default=32, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_costs:
+        print(json.dumps(oracle_block_costs(args.workload, args.rows, args.cpu_budget)), flush=True)
+        return
+    world = os.environ.get("WORLD_SIZE")
+    if world is None and args.gpus > 1:
+        # one process per GPU: relaunch this command under torch.distributed.run
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", os.environ.get("MASTER_PORT", "29511"),
+               os.path.abspath(__file__), *sys.argv[1:]]
+        os.execv(sys.executable, cmd)
+    if world is not None and int(world) != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch one process per GPU")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -73,13 +73,9 @@ enum { SIXBIT_EPI_NONE = 0, SIXBIT_EPI_GELU = 1, SIXBIT_EPI_RESIDUAL = 2 };
  *                unless an amax is supplied)
  *   tensor_scale [1] float: s_t = amax / 2688 (1 when amax == 0)
  * INT8 (technical summary section 2.A):
- *   i8_codes     [M, K] int8, symmetric, per token, in [-127, 127]; optional
- *                when i8_operand is given (the GEMM does not read it)
+ *   i8_codes     [M, K] int8, symmetric, per token, in [-127, 127] (the A
+ *                operand of the W4A8 GEMM)
  *   row_scale    [M] float: s_m = row amax / 127
- *   i8_operand   [M, K] bf16 bit patterns of the same integers (the form the
- *                W4A8 GEMM reads); required by sixbit_qgemm in INT8 mode.
- *                sixbit_hadamard_quant writes whichever of i8_codes and
- *                i8_operand is non-NULL (at least one must be).
  * Debug:
  *   rotated      [M, K] float, the rotated FP32 activations (optional)
  */
@@ -90,7 +86,6 @@ typedef struct {
   float* tensor_scale;
   int8_t* i8_codes;
   float* row_scale;
-  uint16_t* i8_operand;
   float* rotated;
 } sixbit_qact;
 
@@ -102,8 +97,8 @@ typedef struct {
  *   fp4_amax [1], fp4_tensor_scale [1]           -- NVFP4, static tensor scale
  *   i4_codes         [N, K/2] two's-complement nibbles in [-7, 7], even k low
  *   i4_scales        [K/128, N] float (group-major): s[g][n] = amax / 7
- *   i4_operand       [N, K] bf16 bit patterns of the INT4 integers (GEMM operand)
  *   bf16_w           [N, K] bf16(W)
+ * (about 3.1 bytes per weight: 0.5625 NVFP4, 0.53 INT4 with scales, 2 bf16).
  */
 typedef struct {
   uint8_t* fp4_codes;
@@ -112,7 +107,6 @@ typedef struct {
   float* fp4_tensor_scale;
   uint8_t* i4_codes;
   float* i4_scales;
-  uint16_t* i4_operand;
   uint16_t* bf16_w;
 } sixbit_weights;
 
@@ -206,7 +200,8 @@ sixbit_status sixbit_hadamard_quant(const uint16_t* X, int M, int K, int had_blo
  * Quantized GEMM with fused epilogue (technical summary sections 2.A, 2.C, 4):
  *   NVFP4: Y = s_tx * s_tw * sum_k (E2M1*E4M3)_x (E2M1*E4M3)_w   (A = qact, W fp4)
  *   INT8 : Y = s_m * sum_g s_w[g] * acc_g, acc_g exact integer sums over
- *          128-wide K groups (A = qact i8_operand, W i4_operand / i4_scales)
+ *          128-wide K groups (A = qact i8_codes / row_scale, W i4_codes /
+ *          i4_scales)
  *   BF16 : Y = X_bf16 . bf16(W)^T  (A = X_bf16 unrotated, W bf16_w)
  * then epilogue NONE, GELU (exact erf) or RESIDUAL (+ residual [M, N] bf16),
  * rounded to bf16 into Y [M, N] -- or, when Y_f32 is non-NULL, written as
@@ -214,11 +209,19 @@ sixbit_status sixbit_hadamard_quant(const uint16_t* X, int M, int K, int had_blo
  * the tensor cores in FP32 (tcgen05, accumulators in tensor memory).
  * Constraints: K % 128 == 0, N % 16 == 0, M >= 1.  acc_dbg (INT8 only,
  * optional): receives the exact group accumulators as int32 [K/128][M][N].
+ * workspace: device memory of sixbit_qgemm_workspace_bytes(N, K) bytes,
+ * 16-byte aligned, required whenever the INT8 kind may run (mode INT8, or
+ * mode_dev non-NULL), else may be NULL: the INT8 call expands the INT4
+ * weights into it (as fp16) before its GEMM reads them; its contents are
+ * scratch and are not preserved.
  */
 sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W,
                            int M, int N, int K, int mode, const int32_t* mode_dev, int epilogue,
                            const uint16_t* residual, uint16_t* Y, float* Y_f32, int32_t* acc_dbg,
-                           int32_t* err_dev, void* stream);
+                           void* workspace, int32_t* err_dev, void* stream);
+
+/* Bytes of the workspace sixbit_qgemm's INT8 kind needs for an [N, K] weight. */
+size_t sixbit_qgemm_workspace_bytes(int N, int K);
 
 /*
  * The NVFP4 sixbit_qgemm (bf16 output Y) whose epilogue also takes the first

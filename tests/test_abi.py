@@ -63,11 +63,15 @@ def test_argument_errors_return_status_without_launching(lib):
     assert lib.sixbit_hadamard_quant(p, 16, 128, 32, abi.MODE_INT8, None, None, C.byref(qa), None, None) == 2
     # GEMM: missing output, bad epilogue, bad N
     assert lib.sixbit_qgemm(C.byref(qa), None, C.byref(w), 16, 128, 128, 1, None, 0, None, None, None, None,
-                            None, None) == 1
+                            None, None, None) == 1
     assert lib.sixbit_qgemm(C.byref(qa), None, C.byref(w), 16, 120, 128, 1, None, 0, None, p, None, None,
-                            None, None) == 2
+                            None, None, None) == 2
     assert lib.sixbit_qgemm(C.byref(qa), None, C.byref(w), 16, 128, 128, 1, None, 7, None, p, None, None,
-                            None, None) == 1
+                            None, None, None) == 1
+    # INT8 without the weight-expansion workspace
+    assert lib.sixbit_qgemm(C.byref(qa), None, C.byref(w), 16, 128, 128, abi.MODE_INT8, None, 0, None, p, None,
+                            None, None, None, None) == 1
+    assert lib.sixbit_qgemm_workspace_bytes(5760, 1920) == 5760 * 1920 * 2
     # stats: n not a multiple of 8
     assert lib.sixbit_block_stats(p, p, p, 12, None, p, p, None, None) == 2
     assert lib.sixbit_policy_step(None, p, p, p, p, None, None) == 1
@@ -77,6 +81,6 @@ def test_argument_errors_return_status_without_launching(lib):
 
 def test_struct_sizes_match_header():
     from video_dit_mixed_gb300 import abi
-    assert C.sizeof(abi.QAct) == 64 and C.sizeof(abi.Weights) == 64
+    assert C.sizeof(abi.QAct) == 56 and C.sizeof(abi.Weights) == 56
     assert C.sizeof(abi.Stats) == 64 and C.sizeof(abi.PolicyCfg) == 48
     assert C.sizeof(abi.PolicyState) == 80

@@ -58,7 +58,6 @@ def _check_int8(ops, x, b):
     assert np.array_equal(_u32(q.rotated.cpu().numpy()), _u32(ref["y"]))
     np.testing.assert_array_equal(q.i8_codes.cpu().numpy(), ref["q"])
     np.testing.assert_array_equal(_u32(q.row_scale.cpu().numpy()), _u32(ref["s"]))
-    np.testing.assert_array_equal(q.i8_operand.float().cpu().numpy(), ref["q"].astype(np.float32))
 
 
 @pytest.mark.parametrize("m,k,b", CASES)
@@ -99,20 +98,9 @@ def test_int8_extreme_row_magnitudes(ops, k):
     _check_int8(ops, synthgen.bf16_rne(x), 64)
 
 
-def test_int8_operand_without_codes(ops):
-    """i8_codes may be NULL when the bf16 operand is requested: same operand and scales."""
-    x = synthgen.activations(41, 96, 7680, "normal", 0.01, 20.0)
-    q = ops.QActTensors(96, 7680, nvfp4=False, i8_codes=False)
-    assert q.i8_codes is None
-    ops.hadamard_quant(_dev_bf16(x), 64, ops.MODE_INT8, out=q)
-    torch.cuda.synchronize()
-    ref = quant.hadamard_quant(x, 64, "int8")
-    np.testing.assert_array_equal(q.i8_operand.float().cpu().numpy(), ref["q"].astype(np.float32))
-    np.testing.assert_array_equal(_u32(q.row_scale.cpu().numpy()), _u32(ref["s"]))
-
-
-def test_int8_needs_codes_or_operand(ops):
-    q = ops.QActTensors(16, 256, nvfp4=False, i8_codes=False, i8_operand=False)
+def test_int8_needs_codes(ops):
+    q = ops.QActTensors(16, 256, nvfp4=False)
+    q.i8_codes = None
     x = torch.zeros((16, 256), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ops.abi.SixbitError):
         ops.hadamard_quant(x, 64, ops.MODE_INT8, out=q)
@@ -169,7 +157,6 @@ def test_pack_weights_bit_exact(ops, n, k, b):
     assert not sc[n:].any()
     np.testing.assert_array_equal(quant.unpack_nibbles(pw.i4_codes.cpu().numpy(), signed=True), i4["q"])
     np.testing.assert_array_equal(_u32(pw.i4_scales.cpu().numpy().T), _u32(i4["s"]))
-    np.testing.assert_array_equal(pw.i4_operand.float().cpu().numpy(), i4["q"].astype(np.float32))
     np.testing.assert_array_equal(_u32(pw.bf16_w.float().cpu().numpy()), _u32(formats.bf16_round(w)))
 
 

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libsixbit.so")
-SOURCES = ["api.cu", "hadamard_quant.cu", "stats_policy.cu", "qgemm.cu", "noalloc.cu", "graph.cu"]
+SOURCES = ["api.cu", "hadamard_quant.cu", "stats_policy.cu", "qgemm.cu", "qgemm_w4a8.cu", "noalloc.cu", "graph.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-I" + INCLUDE]
 

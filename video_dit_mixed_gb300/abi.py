@@ -16,12 +16,12 @@ MODE_NAMES = {MODE_NVFP4: "NVFP4", MODE_INT8: "INT8", MODE_BF16: "BF16", MODE_SK
 
 class QAct(C.Structure):
     _fields_ = [("fp4_codes", c_p), ("fp4_scales", c_p), ("tensor_amax", c_p), ("tensor_scale", c_p),
-                ("i8_codes", c_p), ("row_scale", c_p), ("i8_operand", c_p), ("rotated", c_p)]
+                ("i8_codes", c_p), ("row_scale", c_p), ("rotated", c_p)]
 
 
 class Weights(C.Structure):
     _fields_ = [("fp4_codes", c_p), ("fp4_scales", c_p), ("fp4_amax", c_p), ("fp4_tensor_scale", c_p),
-                ("i4_codes", c_p), ("i4_scales", c_p), ("i4_operand", c_p), ("bf16_w", c_p)]
+                ("i4_codes", c_p), ("i4_scales", c_p), ("bf16_w", c_p)]
 
 
 class Stats(C.Structure):
@@ -58,7 +58,8 @@ EXPORTS = {
     "sixbit_hadamard_quant": (C.c_int, [c_p, C.c_int, C.c_int, C.c_int, C.c_int, c_p, c_p,
                                         C.POINTER(QAct), c_p, c_p]),
     "sixbit_qgemm": (C.c_int, [C.POINTER(QAct), c_p, C.POINTER(Weights), C.c_int, C.c_int, C.c_int, C.c_int,
-                               c_p, C.c_int, c_p, c_p, c_p, c_p, c_p, c_p]),
+                               c_p, C.c_int, c_p, c_p, c_p, c_p, c_p, c_p, c_p]),
+    "sixbit_qgemm_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int]),
     "sixbit_qgemm_rotamax": (C.c_int, [C.POINTER(QAct), C.POINTER(Weights), C.c_int, C.c_int, C.c_int, c_p, C.c_int,
                                        c_p, c_p, C.c_int, c_p, c_p, c_p]),
     "sixbit_block_stats": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),

@@ -109,6 +109,22 @@ static bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dtype
   return r == CUDA_SUCCESS;
 }
 
+// int8 [rows, cols] for the W4A8 GEMM's activation codes: box 64 bytes of
+// columns x 128 rows, no swizzle (the converter warps read it row-major),
+// out-of-bounds rows read as zero.
+static bool make_map_s8(CUtensorMap* m, const int8_t* base, int rows, int cols) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // bf16 output Y [rows, cols] for the GEMM epilogue's TMA stores: box 32
 // columns (64 bytes) x 32 rows, 64-byte swizzle.
 static bool make_store_map(CUtensorMap* m, const uint16_t* Y, int rows, int cols) {
@@ -141,6 +157,11 @@ size_t sixbit_fp4_scale_offset(int r, int kb, int K) {
 }
 
 size_t sixbit_stats_scratch_bytes(int64_t n) { return stats_scratch_bytes(n); }
+
+size_t sixbit_qgemm_workspace_bytes(int N, int K) {
+  if (N <= 0 || K <= 0) return 0;
+  return w4a8_workspace_bytes(N, K);
+}
 
 uint64_t sixbit_launch_count(void) { return g_launches.load(); }
 
@@ -176,11 +197,10 @@ sixbit_status sixbit_pack_weights(const float* W, int N, int K, int had_block, c
   (void)err_dev;
   if (W == nullptr || out == nullptr || out->fp4_codes == nullptr || out->fp4_scales == nullptr ||
       out->fp4_amax == nullptr || out->fp4_tensor_scale == nullptr || out->i4_codes == nullptr ||
-      out->i4_scales == nullptr || out->i4_operand == nullptr || out->bf16_w == nullptr)
+      out->i4_scales == nullptr || out->bf16_w == nullptr)
     return SIXBIT_EINVAL;
   if (N <= 0 || K <= 0 || K % 128 != 0 || !valid_block(had_block) || K % had_block != 0) return SIXBIT_ESHAPE;
-  if (!aligned16(W) || !aligned16(out->fp4_codes) || !aligned16(out->i4_codes) || !aligned16(out->i4_operand) ||
-      !aligned16(out->bf16_w))
+  if (!aligned16(W) || !aligned16(out->fp4_codes) || !aligned16(out->i4_codes) || !aligned16(out->bf16_w))
     return SIXBIT_EALIGN;
   sixbit_status s = check_device();
   if (s != SIXBIT_OK) return s;
@@ -204,11 +224,9 @@ sixbit_status sixbit_hadamard_quant(const uint16_t* X, int M, int K, int had_blo
   if (want_fp4 && (out->fp4_codes == nullptr || out->fp4_scales == nullptr || out->tensor_scale == nullptr ||
                    (tamax_in == nullptr && out->tensor_amax == nullptr)))
     return SIXBIT_EINVAL;
-  if (want_i8 && (out->row_scale == nullptr || (out->i8_codes == nullptr && out->i8_operand == nullptr)))
-    return SIXBIT_EINVAL;
+  if (want_i8 && (out->row_scale == nullptr || out->i8_codes == nullptr)) return SIXBIT_EINVAL;
   if (want_fp4 && !aligned16(out->fp4_codes)) return SIXBIT_EALIGN;
-  if (want_i8 && ((out->i8_codes && !aligned16(out->i8_codes)) || (out->i8_operand && !aligned16(out->i8_operand))))
-    return SIXBIT_EALIGN;
+  if (want_i8 && !aligned16(out->i8_codes)) return SIXBIT_EALIGN;
   sixbit_status s = check_device();
   if (s != SIXBIT_OK) return s;
   if (want_fp4) {
@@ -231,7 +249,7 @@ sixbit_status sixbit_hadamard_quant(const uint16_t* X, int M, int K, int had_blo
 static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W, int M,
                                 int N, int K, int mode, const int32_t* mode_dev, int epilogue,
                                 const uint16_t* residual, uint16_t* Y, float* Y_f32, int32_t* acc_dbg,
-                                int32_t* err_dev, void* stream, int had_block, float* rot_amax) {
+                                void* workspace, int32_t* err_dev, void* stream, int had_block, float* rot_amax) {
   if (W == nullptr || (Y == nullptr && Y_f32 == nullptr)) return SIXBIT_EINVAL;
   if (epilogue != SIXBIT_EPI_NONE && epilogue != SIXBIT_EPI_GELU && epilogue != SIXBIT_EPI_RESIDUAL)
     return SIXBIT_EINVAL;
@@ -249,13 +267,13 @@ static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, co
   if (run_fp4 && (A->fp4_codes == nullptr || A->fp4_scales == nullptr || A->tensor_scale == nullptr ||
                   W->fp4_codes == nullptr || W->fp4_scales == nullptr || W->fp4_tensor_scale == nullptr))
     return SIXBIT_EINVAL;
-  if (run_i8 && (A->i8_operand == nullptr || A->row_scale == nullptr || W->i4_operand == nullptr ||
-                 W->i4_scales == nullptr))
+  if (run_i8 && (A->i8_codes == nullptr || A->row_scale == nullptr || W->i4_codes == nullptr ||
+                 W->i4_scales == nullptr || workspace == nullptr))
     return SIXBIT_EINVAL;
   if (run_bf && (X_bf16 == nullptr || W->bf16_w == nullptr)) return SIXBIT_EINVAL;
   if ((run_fp4 && (!aligned16(A->fp4_codes) || !aligned16(A->fp4_scales) || !aligned16(W->fp4_codes) ||
                    !aligned16(W->fp4_scales))) ||
-      (run_i8 && (!aligned16(A->i8_operand) || !aligned16(W->i4_operand))) ||
+      (run_i8 && (!aligned16(A->i8_codes) || !aligned16(W->i4_codes) || !aligned16(workspace))) ||
       (run_bf && (!aligned16(X_bf16) || !aligned16(W->bf16_w))))
     return SIXBIT_EALIGN;
   sixbit_status s = check_device();
@@ -299,16 +317,19 @@ static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, co
     if (launch_qgemm_nvf4(ma, mb, q, st) != cudaSuccess) return SIXBIT_ECUDA;
   }
   if (run_i8) {
+    // the INT4 weights, expanded to fp16 once per call into the workspace
+    uint16_t* wexp = static_cast<uint16_t*>(workspace);
     CUtensorMap ma, mb;
-    if (!make_map(&ma, A->i8_operand, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, 128) ||
-        !make_map(&mb, W->i4_operand, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, 256))
+    if (!make_map_s8(&ma, A->i8_codes, M, K) ||
+        !make_map(&mb, wexp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, N, K, 256))
       return SIXBIT_ECUDA;
+    if (launch_w4_expand(W->i4_codes, N, K, wexp, mode_dev, st) != cudaSuccess) return SIXBIT_ECUDA;
     GemmParams q = p;
     q.want_mode = SIXBIT_MODE_INT8;
     q.row_scale = A->row_scale;
     q.grp_scale = W->i4_scales;
     q.acc_dbg = acc_dbg;
-    if (launch_qgemm_int8(ma, mb, my, q, st) != cudaSuccess) return SIXBIT_ECUDA;
+    if (launch_qgemm_w4a8(ma, mb, my, q, st) != cudaSuccess) return SIXBIT_ECUDA;
   }
   if (run_bf) {
     CUtensorMap ma, mb;
@@ -324,9 +345,10 @@ static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, co
 
 sixbit_status sixbit_qgemm(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W, int M, int N,
                            int K, int mode, const int32_t* mode_dev, int epilogue, const uint16_t* residual,
-                           uint16_t* Y, float* Y_f32, int32_t* acc_dbg, int32_t* err_dev, void* stream) {
-  return qgemm_impl(A, X_bf16, W, M, N, K, mode, mode_dev, epilogue, residual, Y, Y_f32, acc_dbg, err_dev, stream,
-                    0, nullptr);
+                           uint16_t* Y, float* Y_f32, int32_t* acc_dbg, void* workspace, int32_t* err_dev,
+                           void* stream) {
+  return qgemm_impl(A, X_bf16, W, M, N, K, mode, mode_dev, epilogue, residual, Y, Y_f32, acc_dbg, workspace, err_dev,
+                    stream, 0, nullptr);
 }
 
 sixbit_status sixbit_qgemm_rotamax(const sixbit_qact* A, const sixbit_weights* W, int M, int N, int K,
@@ -335,7 +357,7 @@ sixbit_status sixbit_qgemm_rotamax(const sixbit_qact* A, const sixbit_weights* W
   if (Y == nullptr || amax_out == nullptr) return SIXBIT_EINVAL;
   if ((had_block != 16 && had_block != 64) || N % 128 != 0) return SIXBIT_ESHAPE;
   return qgemm_impl(A, nullptr, W, M, N, K, SIXBIT_MODE_NVFP4, mode_dev, epilogue, residual, Y, nullptr, nullptr,
-                    err_dev, stream, had_block, amax_out);
+                    nullptr, err_dev, stream, had_block, amax_out);
 }
 
 sixbit_status sixbit_block_stats(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta_cache, int64_t n,

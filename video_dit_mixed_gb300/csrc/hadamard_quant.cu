@@ -258,8 +258,8 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_nvfp4_kernel(const uint16_t*
 // ------------------------------------------------------ INT8 quantization --
 
 // Quantizes and stores one lane's 8 rotated values of row r at column col:
-// q = clamp(RN(y / s), -127, 127); codes (optional), the bf16 operand
-// (optional) and the rotated values (optional).  Rounding to an integer is
+// q = clamp(RN(y / s), -127, 127); the int8 codes and (optional) the rotated
+// values.  Rounding to an integer is
 // done by adding 1.5 * 2^23: for |d| <= 127 the sum lies in [2^23, 2^24),
 // where the float spacing is 1, so the IEEE add rounds d to the nearest
 // integer with ties to even (rint) and the low mantissa bits hold q in two's
@@ -268,24 +268,17 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_nvfp4_kernel(const uint16_t*
 // the reciprocal is taken as 0, which gives q = 0.
 constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
 
-// Writes one lane's 8 results: t = the rounding sums (0x4B400000 + q), o = q
-// as floats; the codes as int8, the operand as bf16 (both optional).
-__device__ __forceinline__ void int8_write8(const uint32_t (&t)[8], const uint32_t (&o)[8], size_t off,
-                                            int8_t* codes, uint16_t* operand) {
-  if (codes != nullptr) {
-    const uint32_t lo = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
-    const uint32_t hi = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
-    *reinterpret_cast<uint2*>(codes + off) = make_uint2(lo, hi);
-  }
-  if (operand != nullptr)
-    *reinterpret_cast<uint4*>(operand + off) =
-        make_uint4(__byte_perm(o[0], o[1], 0x7632), __byte_perm(o[2], o[3], 0x7632), __byte_perm(o[4], o[5], 0x7632),
-                   __byte_perm(o[6], o[7], 0x7632));
+// Writes one lane's 8 codes from t = the rounding sums (0x4B400000 + q): the
+// low byte of each is q in two's complement.
+__device__ __forceinline__ void int8_write8(const uint32_t (&t)[8], size_t off, int8_t* codes) {
+  const uint32_t lo = __byte_perm(__byte_perm(t[0], t[1], 0x0040), __byte_perm(t[2], t[3], 0x0040), 0x5410);
+  const uint32_t hi = __byte_perm(__byte_perm(t[4], t[5], 0x0040), __byte_perm(t[6], t[7], 0x0040), 0x5410);
+  *reinterpret_cast<uint2*>(codes + off) = make_uint2(lo, hi);
 }
 
 __device__ __forceinline__ void int8_chunk_store(const float (&v)[8], int r, int col, int K, float s, bool fast,
-                                                 float rs, int8_t* codes, uint16_t* operand, float* rotated) {
-  uint32_t t[8], o[8];
+                                                 float rs, int8_t* codes, float* rotated) {
+  uint32_t t[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     // With s = RN(amax / 127) normal, |RN(y / s)| <= 127 (1 + 2^-24): the clamp
@@ -293,12 +286,10 @@ __device__ __forceinline__ void int8_chunk_store(const float (&v)[8], int r, int
     // or huge, where s carries less precision).  (A NaN y gives an unspecified
     // code on the fast path.)
     const float d = fast ? div_by_recip(v[i], s, rs) : fminf(fmaxf(__fdiv_rn(v[i], s), -127.f), 127.f);
-    const float ti = __fadd_rn(d, kRound);
-    t[i] = __float_as_uint(ti);                     // 0x4B400000 + q
-    o[i] = __float_as_uint(__fsub_rn(ti, kRound));  // q as float, exact (and exact in bf16)
+    t[i] = __float_as_uint(__fadd_rn(d, kRound));  // 0x4B400000 + q
   }
   const size_t off = static_cast<size_t>(r) * K + col;
-  int8_write8(t, o, off, codes, operand);
+  int8_write8(t, off, codes);
   if (rotated != nullptr) {
     float4* dst = reinterpret_cast<float4*>(rotated + off);
     dst[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -310,8 +301,7 @@ __device__ __forceinline__ void int8_chunk_store(const float (&v)[8], int r, int
 template <int B>
 __global__ void __launch_bounds__(kHqWarps * 32) hq_int8_kernel(const uint16_t* __restrict__ X, int M, int K,
                                                                 const int32_t* mode_dev, int8_t* codes,
-                                                                float* row_scale, uint16_t* operand,
-                                                                float* rotated) {
+                                                                float* row_scale, float* rotated) {
   if (mode_skips(mode_dev, SIXBIT_MODE_INT8)) return;
   const int lane = threadIdx.x & 31;
   const int warp = blockIdx.x * kHqWarps + (threadIdx.x >> 5);
@@ -350,7 +340,7 @@ __global__ void __launch_bounds__(kHqWarps * 32) hq_int8_kernel(const uint16_t* 
         bf16x8_to_f32(raw[u], v);
         fwht8<B>(v, lane);
         const int col = (c0 + u) * 256 + lane * 8;
-        if (col < K) int8_chunk_store(v, r, col, K, s, fast, rs, codes, operand, rotated);
+        if (col < K) int8_chunk_store(v, r, col, K, s, fast, rs, codes, rotated);
       }
     }
   }
@@ -404,7 +394,7 @@ template <int B>
 __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const uint16_t* __restrict__ X, int M,
                                                                         int K, int lr, const int32_t* mode_dev,
                                                                         int8_t* codes, float* row_scale,
-                                                                        uint16_t* operand, float* rotated) {
+                                                                        float* rotated) {
   if (mode_skips(mode_dev, SIXBIT_MODE_INT8)) return;
   constexpr float kScale = B == 16 ? 0.25f : (B == 64 ? 0.125f : 0.0625f);  // 1/sqrt(B), exact
   __shared__ float red[kHqRowWarps];
@@ -453,8 +443,8 @@ __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const
   const uint64_t ns2 = f2_pack(-(s / kScale), -(s / kScale));
 #pragma unroll
   for (int p = 0; p < kHqRowChunks / 2; ++p) {
-    // q as floats (the rounding sums are q + 1.5 * 2^23 again, exactly); the
-    // row-uniform branch keeps the IEEE-division fallback out of the fast loop.
+    // the rounding sums 1.5 * 2^23 + q (low byte: q); the row-uniform branch
+    // keeps the IEEE-division fallback out of the fast loop.
     if (rotated != nullptr) {  // the rotated values y = v / sqrt(B) (FP32, test output)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -475,14 +465,14 @@ __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const
       for (int i = 0; i < 8; ++i) {  // div_by_recip on both lanes
         const uint64_t q = f2_mul(v[p][i], rs2);
         const uint64_t d = f2_fma(f2_fma(ns2, q, v[p][i]), rs2, q);
-        oi[i] = f2_sub(f2_add(d, kr2), kr2);
+        oi[i] = f2_add(d, kr2);
       }
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float dl = fminf(fmaxf(__fdiv_rn(__fmul_rn(f2_lo(v[p][i]), kScale), s), -127.f), 127.f);
         const float dh = fminf(fmaxf(__fdiv_rn(__fmul_rn(f2_hi(v[p][i]), kScale), s), -127.f), 127.f);
-        oi[i] = f2_sub(f2_add(f2_pack(dl, dh), kr2), kr2);
+        oi[i] = f2_add(f2_pack(dl, dh), kr2);
       }
     }
 #pragma unroll
@@ -490,14 +480,10 @@ __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const
       const int c = t + (2 * p + h) * R;
       const int col = c * 256 + lane * 8;
       if (c >= nch || col >= K) continue;
-      uint32_t tt[8], oo[8];
+      uint32_t tt[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) oo[i] = static_cast<uint32_t>(h ? (oi[i] >> 32) : oi[i]);
-      if (codes != nullptr) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) tt[i] = __float_as_uint(__fadd_rn(__uint_as_float(oo[i]), kRound));
-      }
-      int8_write8(tt, oo, static_cast<size_t>(r) * K + col, codes, operand);
+      for (int i = 0; i < 8; ++i) tt[i] = static_cast<uint32_t>(h ? (oi[i] >> 32) : oi[i]);
+      int8_write8(tt, static_cast<size_t>(r) * K + col, codes);
     }
   }
 }
@@ -940,17 +926,13 @@ __global__ void __launch_bounds__(kHqWarps * 32) pack_quant_kernel(const float* 
       const float s = __fdiv_rn(am, 7.0f);
       if (active) {
         uint32_t nib = 0;
-        uint32_t ob[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           float q = 0.f;
           if (s != 0.f) q = fminf(fmaxf(rintf(__fdiv_rn(v[i], s)), -7.f), 7.f);
           nib |= (static_cast<uint32_t>(static_cast<int>(q)) & 0xFu) << (4 * i);
-          ob[i >> 1] |= (__float_as_uint(q) >> 16) << (16 * (i & 1));
         }
         *reinterpret_cast<uint32_t*>(out.i4_codes + static_cast<size_t>(r) * (K >> 1) + (col >> 1)) = nib;
-        *reinterpret_cast<uint4*>(out.i4_operand + static_cast<size_t>(r) * K + col) =
-            make_uint4(ob[0], ob[1], ob[2], ob[3]);
         if ((lane & 15) == 0) out.i4_scales[static_cast<size_t>(col >> 7) * N + r] = s;
       }
     }
@@ -1027,18 +1009,18 @@ cudaError_t launch_hq_int8(const uint16_t* X, int M, int K, int b, const int32_t
     const int grid = (M + rows_per_cta - 1) / rows_per_cta;
     if (b == 16)
       hq_int8_rows_kernel<16><<<grid, kHqRowWarps * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes, o->row_scale,
-                                                                 o->i8_operand, o->rotated);
+                                                                 o->rotated);
     else if (b == 64)
       hq_int8_rows_kernel<64><<<grid, kHqRowWarps * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes, o->row_scale,
-                                                                 o->i8_operand, o->rotated);
+                                                                 o->rotated);
     else
       hq_int8_rows_kernel<256><<<grid, kHqRowWarps * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes, o->row_scale,
-                                                                  o->i8_operand, o->rotated);
+                                                                  o->rotated);
     note_launch();
     return cudaGetLastError();
   }
   const int grid = hq_grid(M);
-  SIXBIT_DISPATCH_B(b, hq_int8_kernel, X, M, K, mode_dev, o->i8_codes, o->row_scale, o->i8_operand, o->rotated);
+  SIXBIT_DISPATCH_B(b, hq_int8_kernel, X, M, K, mode_dev, o->i8_codes, o->row_scale, o->rotated);
   return cudaGetLastError();
 }
 

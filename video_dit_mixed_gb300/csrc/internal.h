@@ -70,7 +70,13 @@ cudaError_t launch_qgemm_nvf4(const CUtensorMap& a, const CUtensorMap& b, const 
 // y: tensor map of the bf16 output (box 32 x 32, 64-byte swizzle), used when p.y_tma.
 cudaError_t launch_qgemm_bf16(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
                               cudaStream_t st);
-cudaError_t launch_qgemm_int8(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
-                              cudaStream_t st);
+// W4A8: INT4 codes [N, K/2] -> fp16 [N, K] into ws (w4a8_workspace_bytes(N, K)),
+// then the GEMM: a_s8 maps the s8 codes [M, K] (box 64 x 128, no swizzle),
+// w_f16 the expanded weights (box 64 x 256, 128-byte swizzle), y the bf16 output.
+size_t w4a8_workspace_bytes(int N, int K);
+cudaError_t launch_w4_expand(const uint8_t* codes, int N, int K, uint16_t* ws, const int32_t* mode_dev,
+                             cudaStream_t st);
+cudaError_t launch_qgemm_w4a8(const CUtensorMap& a_s8, const CUtensorMap& w_f16, const CUtensorMap& y,
+                              const GemmParams& p, cudaStream_t st);
 
 }  // namespace sixbit

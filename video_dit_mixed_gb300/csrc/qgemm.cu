@@ -1,8 +1,10 @@
-// Quantized GEMMs on the fifth-generation tensor cores (tcgen05) of sm_103a.
+// Quantized GEMMs on the fifth-generation tensor cores (tcgen05) of sm_103a:
+// the NVFP4 (W4A4) kind and the BF16 kind.  The W4A8 kind, whose integer
+// operands need their own pipeline, is in qgemm_w4a8.cu.
 //
-// Method: "6Bit-Diffusion" technical summary sections 2.A and 4 (NVFP4 or
-// INT8 activations against 4-bit weights: W4A4 / W4A8) and 2.C (PDR's
-// FP16/BF16 recompute); popular summary section 4 (custom CUDA kernels).
+// Method: "6Bit-Diffusion" technical summary sections 2.A and 4 (NVFP4
+// activations against 4-bit weights: W4A4) and 2.C (PDR's FP16/BF16
+// recompute); popular summary section 4 (custom CUDA kernels).
 //
 // A persistent CTA per SM walks 128 x 256 output tiles with three warp roles:
 //   warp 0      TMA producer: A/B tiles (128-byte swizzle) and, for NVFP4,
@@ -10,10 +12,9 @@
 //               guarded by full/empty mbarriers;
 //   warp 1      allocates tensor memory; one lane issues tcgen05.mma and
 //               tcgen05.commit to release stages and accumulators;
-//   epilogue    16 warps from warp 2 (NVFP4, BF16) or 8 warps from warp 4
-//               (W4A8): tcgen05.ld of the FP32 accumulators (warp w reads
-//               lanes 32*(w%4)..+31 = tile rows, a 64- or 128-column part),
-//               scaling, GELU or residual, bf16 TMA stores (or direct
+//   epilogue    16 warps from warp 2: tcgen05.ld of the FP32 accumulators
+//               (warp w reads lanes 32*(w%4)..+31 = tile rows, a 64-column
+//               part), scaling, GELU or residual, bf16 TMA stores (or direct
 //               stores: NVFP4, FP32 output);
 //   last warp   (NVFP4) tcgen05.cp of each stage's scale factors into its
 //               own tensor-memory slot.
@@ -25,14 +26,8 @@
 //          tensor memory; the epilogue drains the accumulator to registers
 //          and releases it before its stores, so they overlap the next tile.
 //   BF16   kind::f16 with bf16 operands, N = 256 MMAs, 64 K-elements per
-//          stage, two accumulator buffers.  Used for the PDR path and, with
-//          "grouped" accumulation, for W4A8: INT8 activation codes and INT4
-//          weight codes are small integers, exact in bf16, every product and
-//          every 128-term group sum (|.| < 2^17) is an integer exactly
-//          representable in FP32, so each group's FP32 accumulator holds the
-//          exact integer sum.  Groups alternate between the two buffers; the
-//          epilogue folds s_w[g][n] * acc_g into registers while the next
-//          group runs.
+//          stage, two accumulator buffers (the epilogue of tile t overlaps
+//          the MMAs of tile t + 1).
 // Every mbarrier wait is bounded (2 s); on expiry the kernel records
 // SIXBIT_ETIMEOUT in the error word, drains its in-flight copies and tensor
 // core work with bounded waits, frees tensor memory and returns.
@@ -40,53 +35,29 @@
 
 #include "common.cuh"
 #include "ctx_cache.h"
+#include "gemm_common.cuh"
 #include "internal.h"
 
 namespace sixbit {
 
 constexpr int kBM = 128;
-constexpr int kBN = 256;       // output tile columns
-// Epilogue warps: the W4A8 fold keeps 128 running sums per thread, so it uses
-// two warps per tensor-memory lane quarter (128 columns each); the other
-// kinds use four per quarter (64 columns each), which spreads the GELU /
-// residual / store work of a tile over twice the threads (their registers
-// then fit the 96-per-thread budget of 576-608 threads).
-//
-// W4A8 runs 12 warps: warpgroup 0 holds the producer (warp 0), the MMA issuer
-// (warp 1) and two idle warps, and gives registers to the two fold
-// warpgroups (warps 4-11) with setmaxnreg: launched at 168 per thread, it
-// drops to 56 and the fold warps rise to 224 (4 x 56 + 8 x 224 = 12 x 168,
-// and per SM sub-partition 56 + 2 x 224 = 3 x 168), so the fold's 128
-// running sums, its loads and the TMA-store epilogue fit without spills.
-// Each warpgroup executes its setmaxnreg once, all four warps at the same
-// instruction; the host refuses the launch unless the kernel was compiled
-// to the 168 registers the split is sized for (an increase that the
-// released registers could not cover would wait forever).
-template <bool GROUPED>
-struct EpiCfg {
-  static constexpr int kWarps = GROUPED ? 8 : 16;
-  static constexpr int kCols = kBN / (kWarps / 4);  // accumulator columns per thread
-  static constexpr int kWarp0 = GROUPED ? 4 : 2;    // first epilogue warp
-};
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
-constexpr int kGrpRegsLaunch = 168, kGrpRegsLow = 56, kGrpRegsHigh = 224;
-static_assert(4 * kGrpRegsLow + 8 * kGrpRegsHigh <= 12 * kGrpRegsLaunch &&
-                  kGrpRegsLow + 2 * kGrpRegsHigh <= 3 * kGrpRegsLaunch,
-              "the W4A8 register split must fit in what the CTA is launched with");
-constexpr int kGrpCols = EpiCfg<true>::kCols;       // 128
+constexpr int kBN = 256;        // output tile columns
+// 16 epilogue warps, four per tensor-memory lane quarter (64 columns each),
+// spread the GELU / residual / store work of a tile over 512 threads (whose
+// registers fit the 96-per-thread budget of 576-608 threads).
+constexpr int kEpiWarps = 16;
+constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // accumulator columns per thread
+constexpr int kEpiWarp0 = 2;                     // first epilogue warp
 
 enum { KIND_BF16 = 0, KIND_NVF4 = 1 };
 
-// NVFP4 adds a warp that copies the scale factors into tensor memory: every
-// tcgen05 instruction costs its issuing thread tens of cycles, and twelve
-// copies per stage on the MMA thread would pace the main loop.  (Splitting
-// the copies over two warps was slower: the issue cost is shared.)
-template <int KIND, bool GROUPED>
+// NVFP4 adds a warp that copies the scale factors into tensor memory: each
+// tcgen05.cp costs its issuing thread about 64 cycles and an NVFP4 MMA of a
+// stage's K step about 130, so twelve copies per four MMAs on the MMA thread
+// would pace the main loop.  (Splitting the copies over two warps was slower.)
+template <int KIND>
 __host__ __device__ constexpr int gemm_threads() {
-  return GROUPED ? 384 : 64 + EpiCfg<GROUPED>::kWarps * 32 + (KIND == KIND_NVF4 ? 32 : 0);
+  return 64 + kEpiWarps * 32 + (KIND == KIND_NVF4 ? 32 : 0);
 }
 
 template <int KIND>
@@ -119,164 +90,29 @@ template <int KIND>
 __host__ __device__ constexpr int stage_bytes() {
   return kATileBytes + kBTileBytes + GemmCfg<KIND>::kSfaBytes + GemmCfg<KIND>::kSfbBytes;
 }
-// W4A8: each epilogue warp keeps the scales of the next kSwRing groups in a
-// shared-memory ring, fetched kSwRing - 1 groups ahead (an L2 round trip
-// per group would otherwise pace the fold).
-constexpr int kSwRing = 4;
-constexpr int kMaxBufs = 4;  // accumulator buffers the barrier area has room for
 
-// The bf16-operand kinds stage each epilogue warp's 32 x 32 bf16 output chunk
-// in shared memory (64-byte rows, 64-byte TMA swizzle) and write it with one
+// The BF16 kind stages each epilogue warp's 32 x 32 bf16 output chunk in
+// shared memory (64-byte rows, 64-byte TMA swizzle) and writes it with one
 // TMA store: a warp's direct stores would touch 32 rows, 16 bytes each
-// (BF16 310 vs 329 us, W4A8 397 vs 460 us at 17776 x 7680 x 1920).  NVFP4
-// has no shared memory left and stores directly.
-template <int KIND, bool GROUPED>
+// (310 vs 329 us at 17776 x 7680 x 1920).  NVFP4 has no shared memory left
+// and stores directly.
+template <int KIND>
 __host__ __device__ constexpr bool tma_y() {
   return KIND != KIND_NVF4;
 }
 constexpr int kBoxBytes = 32 * 64;
-template <int KIND, bool GROUPED>
+template <int KIND>
 __host__ __device__ constexpr int staging_bytes() {
-  return tma_y<KIND, GROUPED>() ? EpiCfg<GROUPED>::kWarps * kBoxBytes : 0;
+  return tma_y<KIND>() ? kEpiWarps * kBoxBytes : 0;
 }
 
-// Layout: [stages | output staging | barriers (256 B) | W4A8 group-scale rings].
-template <int KIND, bool GROUPED>
+// Layout: [stages | output staging | barriers (256 B)].
+template <int KIND>
 __host__ __device__ constexpr int gemm_smem_bytes() {
-  return GemmCfg<KIND>::kStages * stage_bytes<KIND>() + staging_bytes<KIND, GROUPED>() + 1024 /*align*/ +
-         256 /*barriers*/ + (GROUPED ? kSwRing * EpiCfg<true>::kWarps * kGrpCols * 4 : 0) /*per-warp ring of group scales*/;
+  return GemmCfg<KIND>::kStages * stage_bytes<KIND>() + staging_bytes<KIND>() + 1024 /*align*/ + 256 /*barriers*/;
 }
-static_assert(gemm_smem_bytes<KIND_BF16, true>() <= 227 * 1024 && gemm_smem_bytes<KIND_BF16, false>() <= 227 * 1024 &&
-                  gemm_smem_bytes<KIND_NVF4, false>() <= 227 * 1024,
+static_assert(gemm_smem_bytes<KIND_BF16>() <= 227 * 1024 && gemm_smem_bytes<KIND_NVF4>() <= 227 * 1024,
               "shared memory per CTA");
-
-// GELU(v) = v Phi(v) with Phi(v) = (1 + erf(v / sqrt 2)) / 2.  erfc(z), z = |v| / sqrt 2,
-// is taken as t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2), t = 1 / (1 + p z)
-// (Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26: the
-// erf it gives is within 1.5e-7 of the exact one), then 1 + erf = 2 - erfc for
-// v >= 0 and erfc(|z|) for v < 0, so the negative tail keeps its relative
-// accuracy.  Branch-free; its GELU differs from the exact-erf one by at most
-// a few 1e-7 |v|, inside the FP32 epilogue's error budget.
-__device__ __forceinline__ float gelu_erf(float v) {
-  const float z = fabsf(v) * 0.7071067811865475244f;
-  const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
-  float q = fmaf(t, 1.061405429f, -1.453152027f);
-  q = fmaf(t, q, 1.421413741f);
-  q = fmaf(t, q, -0.284496736f);
-  q = fmaf(t, q, 0.254829592f);
-  const float c = t * q * __expf(-z * z);  // erfc(z)
-  const float w = v >= 0.f ? 2.0f - c : c;  // 1 + erf(v / sqrt 2)
-  return 0.5f * v * w;
-}
-
-// W4A8 group folding: each epilogue thread reads its accumulator columns of
-// one K group from tensor memory in chunks of kFold columns and adds
-// s_w[g][n] * acc_g[n] to its running sums (128 of them: the register budget
-// of 168 per thread leaves no room for a second chunk in flight).
-constexpr int kFold = 16;
-constexpr int kFoldChunks = kGrpCols / kFold;
-
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
-
-__device__ __forceinline__ void fold_chunk(float (&sum)[kGrpCols], int c, const uint32_t (&r)[kFold],
-                                           const float4* sw4) {
-#pragma unroll
-  for (int j4 = 0; j4 < kFold / 4; ++j4) {
-    const float4 s4 = sw4[c * (kFold / 4) + j4];
-    const int j = c * kFold + 4 * j4;
-    sum[j] = fmaf(s4.x, __uint_as_float(r[4 * j4]), sum[j]);
-    sum[j + 1] = fmaf(s4.y, __uint_as_float(r[4 * j4 + 1]), sum[j + 1]);
-    sum[j + 2] = fmaf(s4.z, __uint_as_float(r[4 * j4 + 2]), sum[j + 2]);
-    sum[j + 3] = fmaf(s4.w, __uint_as_float(r[4 * j4 + 3]), sum[j + 3]);
-  }
-}
-
-// 16-byte global -> shared copy without a register round trip (zero-fill when
-// !valid; src must still be a valid address).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-// Waits until at most N of this thread's most recent cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait_newest() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// Hands an accumulator buffer back to the MMA warp: one arrival per warp,
-// after every lane's tensor-memory loads have completed.
-__device__ __forceinline__ void release_acc(uint64_t* bar, int lane) {
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
-}
-
-// Applies the epilogue (GELU, or the residual add) to 32 consecutive columns
-// [n, n+32) of row `row` < M.
-__device__ __forceinline__ void epilogue_apply32(const GemmParams& p, int row, int n, float (&v)[32]) {
-  const size_t base = static_cast<size_t>(row) * p.N + n;
-  if (p.epilogue == SIXBIT_EPI_GELU) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
-  } else if (p.epilogue == SIXBIT_EPI_RESIDUAL) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (n + 8 * q + 8 <= p.N) {
-        const uint4 r = *reinterpret_cast<const uint4*>(p.residual + base + 8 * q);
-        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[8 * q + 2 * i] = __fadd_rn(v[8 * q + 2 * i], __uint_as_float(w[i] << 16));
-          v[8 * q + 2 * i + 1] = __fadd_rn(v[8 * q + 2 * i + 1], __uint_as_float(w[i] & 0xFFFF0000u));
-        }
-      }
-    }
-  }
-}
-
-// Applies the epilogue to 32 consecutive columns [n, n+32) of one row and
-// stores them (bf16 or fp32) directly.
-__device__ __forceinline__ void epilogue_store32(const GemmParams& p, int row, int n, float (&v)[32]) {
-  if (row >= p.M) return;
-  const size_t base = static_cast<size_t>(row) * p.N + n;
-  epilogue_apply32(p, row, n, v);
-  if (p.Yf != nullptr) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (n + 4 * q + 4 <= p.N)
-        *reinterpret_cast<float4*>(p.Yf + base + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-  } else {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
-        w[i] = *reinterpret_cast<const uint32_t*>(&b);
-        v[8 * q + 2 * i] = __uint_as_float(w[i] << 16);            // the stored value (read by rot_amax)
-        v[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-      }
-      if (n + 8 * q + 8 <= p.N) *reinterpret_cast<uint4*>(p.Y + base + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
-}
-
-// Writes row r's 32 values as bf16 (round to nearest even) into a 32-row box
-// of 64-byte rows, 16-byte chunk q of row r at chunk q ^ ((r >> 1) & 3): the
-// TMA 64-byte swizzle (box 512-byte aligned), which also spreads a warp's
-// 16-byte writes over all banks.
-__device__ __forceinline__ void stage_bf16x32(uint8_t* box, int r, const float (&v)[32]) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
-      w[i] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    *reinterpret_cast<uint4*>(box + r * 64 + ((q ^ ((r >> 1) & 3)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
 
 // max |y| over a thread's 64 output columns after the block Hadamard rotation
 // y = x . blockdiag(H_b / sqrt b), b in {16, 64}: the same FP32 butterfly
@@ -315,14 +151,12 @@ __device__ __forceinline__ float rot_amax64(float (&v)[2][32]) {
 
 // Persistent kernel: each CTA walks output tiles t = blockIdx.x, +gridDim.x,
 // ...; p.n_fastest picks whether row or column tiles vary fastest along t.
-template <int KIND, bool GROUPED, bool DBG>
-__global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
+template <int KIND>
+__global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
   using C = GemmCfg<KIND>;
   constexpr int S = C::kStages;
-  constexpr int kEpiWarps = EpiCfg<GROUPED>::kWarps;
-  constexpr int kEpiCols = EpiCfg<GROUPED>::kCols;
   constexpr bool kNvf4 = KIND == KIND_NVF4;
   constexpr uint32_t kCols = 512;
   // NVFP4: the scale factors of stage s live in TMEM columns 256 + 64 s:
@@ -337,19 +171,18 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* tiles = smem;
-  uint8_t* staging = smem + S * stage_bytes<KIND>();  // [kEpiWarps] output boxes (bf16-operand kinds)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + staging_bytes<KIND, GROUPED>());
+  uint8_t* staging = smem + S * stage_bytes<KIND>();  // [kEpiWarps] output boxes (BF16 kind)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + staging_bytes<KIND>());
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* accf = bars + 2 * S;                    // [kBufs] accumulator buffer ready
-  uint64_t* acce = bars + 2 * S + kMaxBufs;         // [kBufs] accumulator buffer drained
-  uint64_t* drain = bars + 2 * S + 2 * kMaxBufs;
+  uint64_t* acce = bars + 2 * S + 2;                // [kBufs] accumulator buffer drained
+  uint64_t* drain = bars + 2 * S + 4;
   uint64_t* sf_full = drain + 1;                    // NVFP4: [S] the stage's scale factors are in tensor memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + S);
-  static_assert((3 * S + 2 * kMaxBufs + 1) * 8 + 8 <= 256, "barrier area");
-  static_assert(kBufs <= kMaxBufs && kBufs * kBN + (kNvf4 ? S * 64 : 0) <= kCols, "tensor memory");
+  static_assert((3 * S + 5) * 8 + 8 <= 256, "barrier area");
+  static_assert(kBufs <= 2 && kBufs * kBN + (kNvf4 ? S * 64 : 0) <= kCols, "tensor memory");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* sw_smem = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);  // GROUPED: per-warp scales
 
   auto A_tile = [&](int s) { return tiles + s * stage_bytes<KIND>(); };
   auto B_tile = [&](int s) { return tiles + s * stage_bytes<KIND>() + kATileBytes; };
@@ -374,7 +207,6 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
   // leaves a half stage at the end (TMA zero-fills its missing columns; only
   // its valid scale chunks are copied and only its valid MMAs issued).
   const int nk = (p.K + C::kKStage - 1) / C::kKStage;
-  const int groups = p.K / 128;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -394,7 +226,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (tma_y<KIND, GROUPED>() && p.y_tma) prefetch_tmap(&tmY);
+    if (tma_y<KIND>() && p.y_tma) prefetch_tmap(&tmY);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kCols);
@@ -405,8 +237,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < EpiCfg<GROUPED>::kWarp0) {
-    if constexpr (GROUPED) setmaxnreg_dec<kGrpRegsLow>();  // the whole warpgroup, one instruction
+  if (warp < kEpiWarp0) {
     if (warp == 0) {
       if (lane == 0) {
         // ------------------------------------------------------ producer --
@@ -446,16 +277,15 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
       if (lane == 0) {
         // ---------------------------------------------------- MMA issuer --
         uint32_t it = 0;  // stage counter
-        uint32_t ac = 0;  // accumulator-buffer use counter (tiles, or K groups when GROUPED)
+        uint32_t ac = 0;  // accumulator-buffer use counter (tiles)
         bool ok = true;
-        constexpr int spg = 128 / C::kKStage > 0 ? 128 / C::kKStage : 1;  // stages per K group (bf16 kinds)
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
           int m_tile, n_tile;
           tile_of(t, m_tile, n_tile);
           (void)m_tile;
           const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;
           for (int kb = 0; kb < nk && ok; ++kb, ++it) {
-            const bool acc_start = GROUPED ? (kb % spg) == 0 : kb == 0;
+            const bool acc_start = kb == 0;
             const uint32_t buf = ac % kBufs;
             // the buffer's previous contents must have been drained by the epilogue
             if (acc_start && ac >= kBufs && !mbar_wait(&acce[buf], ((ac / kBufs) - 1) & 1, abort_flag)) {
@@ -496,9 +326,9 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
                          (acc_start && k == 0) ? 0u : 1u);
             }
             tc_commit(&empty[s]);
-            const bool acc_end = GROUPED ? (kb % spg) == spg - 1 : kb == nk - 1;
+            const bool acc_end = kb == nk - 1;
             if (acc_end) {
-              if constexpr (!GROUPED) tc_commit(&accf[buf]);  // W4A8: the epilogue waits on empty[s]
+              tc_commit(&accf[buf]);
               ++ac;
             }
           }
@@ -510,19 +340,17 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
         tc_commit(drain);  // all tensor-core work issued here completes before exit
         (void)mbar_wait(drain, 0, nullptr);
       }
-    }  // warps 2 and 3 of a W4A8 CTA are idle
-  } else if (warp < EpiCfg<GROUPED>::kWarp0 + kEpiWarps) {
-    if constexpr (GROUPED) setmaxnreg_inc<kGrpRegsHigh>();  // each fold warpgroup, one instruction
+    }
+  } else if (warp < kEpiWarp0 + kEpiWarps) {
     // -------------------------------------------------------- epilogue --
-    const int ew = warp - EpiCfg<GROUPED>::kWarp0;  // 0 .. kEpiWarps-1
+    const int ew = warp - kEpiWarp0;              // 0 .. kEpiWarps-1
     const int q = warp & 3;                       // tensor-memory lane quarter this warp may read
     const int col0 = (ew >> 2) * kEpiCols;        // first accumulator column of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16) + col0;
-    float* my_sw = sw_smem + ew * kSwRing * kEpiCols;  // GROUPED: this warp's ring of group scales
-    uint8_t* my_box = staging + ew * kBoxBytes;         // bf16-operand kinds: this warp's output box
+    uint8_t* my_box = staging + ew * kBoxBytes;   // BF16 kind: this warp's output box
     // Epilogue + store of columns [n, n + 32) of this lane's row (n < N, warp-uniform).
     auto store32 = [&](int row, int n, float (&v)[32]) {
-      if constexpr (tma_y<KIND, GROUPED>()) {
+      if constexpr (tma_y<KIND>()) {
         if (p.y_tma) {
           if (row < p.M) epilogue_apply32(p, row, n, v);
           if (lane == 0) bulk_wait_read0();  // the previous box has been read out
@@ -541,95 +369,19 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
     };
     uint32_t ac = 0;
     bool ok = true;
-    // W4A8: group ac's MMAs are complete when the commit after its last stage
-    // (stage counter 2 ac + 1) arrives on that stage's empty barrier, so no
-    // commit of its own is issued (each tcgen05.commit costs the MMA thread
-    // time per group).  The barrier cannot run a phase past this wait: its
-    // next phase needs the MMAs of group ac + 2, which wait for this group's
-    // buffer to be released.
-    auto grp_done = [&](uint32_t a) { return &empty[(2 * a + 1) % S]; };
-    auto grp_par = [&](uint32_t a) { return ((2 * a + 1) / S) & 1; };
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       int m_tile, n_tile;
       tile_of(t, m_tile, n_tile);
       const int row = m_tile * kBM + 32 * q + lane;
       const int nb = n_tile * kBN + col0;         // first output column of this thread
-      if (nb >= p.N) {                            // nothing of this half exists (ragged N)
-        if constexpr (GROUPED) {
-          for (int g = 0; g < groups && ok; ++g, ++ac) {
-            const uint32_t buf = ac % kBufs;
-            if (!mbar_wait(grp_done(ac), grp_par(ac), abort_flag)) { ok = false; break; }
-            release_acc(&acce[buf], lane);
-          }
-        } else {
-          const uint32_t buf = ac % kBufs;
-          if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) { ok = false; break; }
-          release_acc(&acce[buf], lane);
-          ++ac;
-        }
+      if (nb >= p.N) {                            // nothing of this part exists (ragged N)
+        const uint32_t buf = ac % kBufs;
+        if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) { ok = false; break; }
+        release_acc(&acce[buf], lane);
+        ++ac;
         continue;
       }
-      if constexpr (GROUPED) {
-        float sum[kEpiCols];
-#pragma unroll
-        for (int j = 0; j < kEpiCols; ++j) sum[j] = 0.f;
-        // s_w[g][nb .. nb+128): lane l copies 4 scales; group g goes to slot g % kSwRing.
-        // One cp.async group is committed per fetch (a zero-fill past the last group).
-        auto fetch_sw = [&](int g) {
-          const int n = nb + 4 * lane;
-          const bool v = g < groups && n < p.N;
-          cp_async16(smem_u32(my_sw + (g % kSwRing) * kEpiCols + 4 * lane),
-                     v ? p.grp_scale + static_cast<size_t>(g) * p.N + n : p.grp_scale, v);
-        };
-#pragma unroll
-        for (int g = 0; g < kSwRing - 1; ++g) fetch_sw(g);
-        for (int g = 0; g < groups; ++g, ++ac) {
-          __syncwarp();                            // every lane is done with slot (g - 1) % kSwRing
-          fetch_sw(g + kSwRing - 1);               // ... which now receives group g + kSwRing - 1
-          cp_async_wait_newest<kSwRing - 1>();     // this lane's copy of group g has landed
-          __syncwarp();                            // and every other lane's
-          const uint32_t buf = ac % kBufs;
-          if (!mbar_wait(grp_done(ac), grp_par(ac), abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const float4* sw4 = reinterpret_cast<const float4*>(my_sw + (g % kSwRing) * kEpiCols);
-          const uint32_t acc_addr = lane_addr + buf * kBN;
-          auto dbg = [&](int c, const uint32_t (&r)[kFold]) {
-            if constexpr (DBG) {
-              if (row < p.M) {
-#pragma unroll
-                for (int j = 0; j < kFold; ++j) {
-                  const int n = nb + c * kFold + j;
-                  if (n < p.N)
-                    p.acc_dbg[(static_cast<size_t>(g) * p.M + row) * p.N + n] = __float2int_rn(__uint_as_float(r[j]));
-                }
-              }
-            }
-          };
-#pragma unroll
-          for (int c = 0; c < kFoldChunks; ++c) {
-            uint32_t r[kFold];
-            tmem_ld(acc_addr + c * kFold, r);
-            tmem_ld_wait(r);
-            if (c == kFoldChunks - 1) release_acc(&acce[buf], lane);  // every load of this group has landed
-            dbg(c, r);
-            fold_chunk(sum, c, r, sw4);
-          }
-        }
-        cp_async_wait_all();                       // no scale copy outlives the tile
-        __syncwarp();
-        if (!ok) break;
-        const float sm = (row < p.M) ? p.row_scale[row] : 0.f;
-#pragma unroll
-        for (int c = 0; c < kEpiCols / 32; ++c) {
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(sum[c * 32 + j], sm);
-          if (nb + c * 32 < p.N) store32(row, nb + c * 32, v);
-        }
-      } else {
+      {
         const uint32_t buf = ac % kBufs;
         if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) {
           ok = false;
@@ -685,7 +437,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
       set_error(p.err, SIXBIT_ETIMEOUT);
       *abort_flag = 1;
     }
-    if (tma_y<KIND, GROUPED>() && lane == 0) bulk_wait0();  // every output box has been written
+    if (tma_y<KIND>() && lane == 0) bulk_wait0();  // every output box has been written
     __syncwarp();
     tc_fence_before();
   } else if constexpr (kNvf4) {
@@ -737,28 +489,16 @@ __global__ void __launch_bounds__(gemm_threads<KIND, GROUPED>(), 1)
 
 // ------------------------------------------------------------ host launch --
 
-template <int KIND, bool GROUPED, bool DBG>
+template <int KIND>
 static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
                               cudaStream_t st) {
-  constexpr int smem = gemm_smem_bytes<KIND, GROUPED>();
-  cudaError_t e = set_smem_once<qgemm_kernel<KIND, GROUPED, DBG>>(smem);
+  constexpr int smem = gemm_smem_bytes<KIND>();
+  const cudaError_t e = set_smem_once<qgemm_kernel<KIND>>(smem);
   if (e != cudaSuccess) return e;
-  if constexpr (GROUPED) {
-    static ContextCache<int> regs_cache;
-    int regs = 0;
-    e = regs_cache.get(&regs, [](int* o) {
-      cudaFuncAttributes fa;
-      const cudaError_t r = cudaFuncGetAttributes(&fa, qgemm_kernel<KIND, GROUPED, DBG>);
-      *o = fa.numRegs;
-      return r;
-    });
-    if (e != cudaSuccess) return e;
-    if (regs < kGrpRegsLaunch || 4 * kGrpRegsLow + 8 * kGrpRegsHigh > 12 * regs) return cudaErrorInvalidConfiguration;
-  }
   const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
   const int sms = sm_count();
   const int grid = ntiles < sms ? ntiles : sms;
-  qgemm_kernel<KIND, GROUPED, DBG><<<grid, gemm_threads<KIND, GROUPED>(), smem, st>>>(a, b, y, p);
+  qgemm_kernel<KIND><<<grid, gemm_threads<KIND>(), smem, st>>>(a, b, y, p);
   note_launch();
   return cudaGetLastError();
 }
@@ -766,16 +506,11 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
 cudaError_t launch_qgemm_nvf4(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
   GemmParams q = p;
   q.y_tma = 0;
-  return launch_one<KIND_NVF4, false, false>(a, b, a /*unused*/, q, st);
+  return launch_one<KIND_NVF4>(a, b, a /*unused*/, q, st);
 }
 cudaError_t launch_qgemm_bf16(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
                               cudaStream_t st) {
-  return launch_one<KIND_BF16, false, false>(a, b, y, p, st);
-}
-cudaError_t launch_qgemm_int8(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
-                              cudaStream_t st) {
-  if (p.acc_dbg != nullptr) return launch_one<KIND_BF16, true, true>(a, b, y, p, st);
-  return launch_one<KIND_BF16, true, false>(a, b, y, p, st);
+  return launch_one<KIND_BF16>(a, b, y, p, st);
 }
 
 }  // namespace sixbit

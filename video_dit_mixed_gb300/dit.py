@@ -40,9 +40,10 @@ class DiT:
         self.bufs = [torch.zeros((tokens, hidden), dtype=bf, device=dev) for _ in range(2)]
         self.h = torch.zeros((tokens, ffn), dtype=bf, device=dev)
         self.deltas = torch.zeros((blocks, tokens, hidden), dtype=bf, device=dev)
-        # the W4A8 GEMM reads the bf16 operand form; the int8 codes are not kept
-        self.qa_x = ops.QActTensors(tokens, hidden, dev, i8_codes=False)
-        self.qa_h = ops.QActTensors(tokens, ffn, dev, i8_codes=False)
+        self.qa_x = ops.QActTensors(tokens, hidden, dev)
+        self.qa_h = ops.QActTensors(tokens, ffn, dev)
+        # the W4A8 GEMMs expand their INT4 weights into this (one buffer for both projections)
+        self.ws = torch.empty(ops.qgemm_workspace_bytes(ffn, hidden), dtype=torch.uint8, device=dev)
         self.tstats = torch.zeros(4, dtype=torch.float64, device=dev)
         self.stats = ops.new_stats(dev, blocks)
         self.state = ops.new_policy_state(dev, blocks)
@@ -87,11 +88,12 @@ class DiT:
             up, down = self.packed[l]
             o.hadamard_quant(x, self.b, 0, out=self.qa_x, mode_dev=mode)
             note("hq_x", l)
-            o.qgemm(self.qa_x, x, up, 0, epilogue=o.EPI_GELU, out=self.h, mode_dev=mode)
+            o.qgemm(self.qa_x, x, up, 0, epilogue=o.EPI_GELU, out=self.h, mode_dev=mode, ws=self.ws)
             note("qgemm_up", l)
             o.hadamard_quant(self.h, self.b, 0, out=self.qa_h, mode_dev=mode)
             note("hq_h", l)
-            o.qgemm(self.qa_h, self.h, down, 0, epilogue=o.EPI_RESIDUAL, residual=x, out=out, mode_dev=mode)
+            o.qgemm(self.qa_h, self.h, down, 0, epilogue=o.EPI_RESIDUAL, residual=x, out=out, mode_dev=mode,
+                    ws=self.ws)
             note("qgemm_down", l)
             o.dit_block_end(self.cfg, self.rec, l, self.scratch)
             note("block_stats", l)
@@ -115,13 +117,13 @@ class DiT:
         if fused:
             o.qgemm_rotamax(self.qa_x, up, self.b, self.qa_h.tensor_amax, epilogue=o.EPI_GELU, out=self.h, m=self.T)
         else:
-            o.qgemm(self.qa_x if quant else None, x, up, mode, epilogue=o.EPI_GELU, out=self.h, m=self.T)
+            o.qgemm(self.qa_x if quant else None, x, up, mode, epilogue=o.EPI_GELU, out=self.h, m=self.T, ws=self.ws)
         note("qgemm_up")
         if quant:
             o.hadamard_quant(self.h, self.b, mode, out=self.qa_h, tamax=self.qa_h.tensor_amax if fused else None)
             note("hq_h")
         o.qgemm(self.qa_h if quant else None, self.h, down, mode, epilogue=o.EPI_RESIDUAL, residual=x, out=out,
-                m=self.T)
+                m=self.T, ws=self.ws)
         note("qgemm_down")
         o.dit_block_end(self.cfg, rec, l, self.scratch)
         note("block_stats")

@@ -39,11 +39,29 @@ def launch_count() -> int:
     return int(_lib.sixbit_launch_count())
 
 
+def qgemm_workspace_bytes(n: int, k: int) -> int:
+    return int(_lib.sixbit_qgemm_workspace_bytes(n, k))
+
+
+_workspaces = {}
+
+
+def workspace(n: int, k: int, device) -> torch.Tensor:
+    """A device buffer of at least qgemm_workspace_bytes(n, k) bytes, shared by every call on `device`
+    that passes none of its own (calls that share it must be ordered, e.g. on one stream)."""
+    dev = torch.device(device)
+    need = qgemm_workspace_bytes(n, k)
+    buf = _workspaces.get(dev)
+    if buf is None or buf.numel() < need:
+        buf = torch.empty(need, dtype=torch.uint8, device=dev)
+        _workspaces[dev] = buf
+    return buf
+
+
 class QActTensors:
     """Device buffers of one quantized activation tensor [M, K]."""
 
-    def __init__(self, m: int, k: int, device="cuda", nvfp4=True, int8=True, rotated=False, i8_operand=True,
-                 i8_codes=True):
+    def __init__(self, m: int, k: int, device="cuda", nvfp4=True, int8=True, rotated=False):
         self.m, self.k = m, k
         dev = torch.device(device)
         u8, f32 = torch.uint8, torch.float32
@@ -51,9 +69,8 @@ class QActTensors:
         self.fp4_scales = torch.zeros(fp4_scale_bytes(m, k), dtype=u8, device=dev) if nvfp4 else None
         self.tensor_amax = torch.zeros(1, dtype=f32, device=dev) if nvfp4 else None
         self.tensor_scale = torch.zeros(1, dtype=f32, device=dev) if nvfp4 else None
-        self.i8_codes = torch.empty((m, k), dtype=torch.int8, device=dev) if (int8 and i8_codes) else None
+        self.i8_codes = torch.empty((m, k), dtype=torch.int8, device=dev) if int8 else None
         self.row_scale = torch.empty(m, dtype=f32, device=dev) if int8 else None
-        self.i8_operand = torch.empty((m, k), dtype=torch.bfloat16, device=dev) if (int8 and i8_operand) else None
         self.rotated = torch.empty((m, k), dtype=f32, device=dev) if rotated else None
 
     def c(self) -> QAct:
@@ -72,7 +89,6 @@ class PackedWeights:
         self.fp4_tensor_scale = torch.zeros(1, dtype=torch.float32, device=dev)
         self.i4_codes = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
         self.i4_scales = torch.empty((k // 128, n), dtype=torch.float32, device=dev)
-        self.i4_operand = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
         self.bf16_w = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
 
     def c(self) -> Weights:
@@ -100,8 +116,12 @@ def hadamard_quant(x: torch.Tensor, had_block: int, mode: int, out: QActTensors 
 
 
 def qgemm(a: QActTensors | None, x_bf16, w: PackedWeights, mode: int, epilogue: int = EPI_NONE, residual=None,
-          out=None, out_f32: bool = False, acc_dbg=None, mode_dev=None, err=None, stream=None, m: int | None = None):
+          out=None, out_f32: bool = False, acc_dbg=None, mode_dev=None, err=None, stream=None, m: int | None = None,
+          ws=None):
+    """ws: the INT8 kind's workspace (qgemm_workspace_bytes); by default the device's shared one."""
     n, k = w.n, w.k
+    if ws is None and (mode == MODE_INT8 or mode_dev is not None):
+        ws = workspace(n, k, w.bf16_w.device)
     m = m if m is not None else (a.m if a is not None else x_bf16.shape[0])
     if out is None:
         out = torch.empty((m, n), dtype=torch.float32 if out_f32 else torch.bfloat16, device=w.bf16_w.device)
@@ -110,7 +130,7 @@ def qgemm(a: QActTensors | None, x_bf16, w: PackedWeights, mode: int, epilogue: 
     y = out if out.dtype == torch.bfloat16 else None
     yf = out if out.dtype == torch.float32 else None
     check(_lib.sixbit_qgemm(C.byref(ca) if ca is not None else None, _p(x_bf16), C.byref(cw), m, n, k, mode,
-                            _p(mode_dev), epilogue, _p(residual), _p(y), _p(yf), _p(acc_dbg), _p(err),
+                            _p(mode_dev), epilogue, _p(residual), _p(y), _p(yf), _p(acc_dbg), _p(ws), _p(err),
                             _stream(stream)), "qgemm")
     return out
 
