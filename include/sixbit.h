@@ -416,6 +416,21 @@ sixbit_status sixbit_graph_branch_begin(sixbit_switch* sw, int branch, void** bo
 sixbit_status sixbit_graph_branch_end(sixbit_switch* sw);
 sixbit_status sixbit_graph_switch_end(sixbit_switch* sw);
 
+/*
+ * Test setting for the GEMMs' failure path (every GEMM launched after the
+ * call, process-wide).  Every wait in the GEMM kernels is bounded; this
+ * lets a test make those waits run out on purpose, without faulting anything:
+ * wait_limit_ns replaces the 2 s limit (0 restores it), and with
+ * withhold_first_stage = 1 the producer of every CTA skips the copies of its
+ * first pipeline stage, so the tensor-core thread's wait for it runs out.
+ * The kernel then records SIXBIT_ETIMEOUT in err_dev, stops its other roles,
+ * waits (bounded) for its copies and tensor-core work in flight, frees its
+ * tensor memory and returns, leaving the context usable.  Returns
+ * SIXBIT_EINVAL for withhold_first_stage outside {0, 1}.  Not for production
+ * use: call it with (0, 0) afterwards.
+ */
+sixbit_status sixbit_debug_gemm_timeout(uint64_t wait_limit_ns, int32_t withhold_first_stage);
+
 /* Synchronize `stream` and return the status recorded in err_dev (and clear it). */
 sixbit_status sixbit_check(int32_t* err_dev, void* stream);
 

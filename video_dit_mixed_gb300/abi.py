@@ -77,6 +77,7 @@ EXPORTS = {
     "sixbit_graph_branch_begin": (C.c_int, [c_p, C.c_int, C.POINTER(c_p)]),
     "sixbit_graph_branch_end": (C.c_int, [c_p]),
     "sixbit_graph_switch_end": (C.c_int, [c_p]),
+    "sixbit_debug_gemm_timeout": (C.c_int, [C.c_uint64, C.c_int32]),
     "sixbit_check": (C.c_int, [c_p, c_p]),
     "sixbit_status_str": (C.c_char_p, [C.c_int]),
     "sixbit_launch_count": (C.c_uint64, []),

@@ -52,6 +52,15 @@ int sm_count() {
 static std::atomic<uint64_t> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// sixbit_debug_gemm_timeout's setting (0: the normal 2 s limit, no withheld stage).
+static std::atomic<uint64_t> g_dbg_wait_ns{0};
+static std::atomic<int> g_dbg_withhold{0};
+void gemm_debug_params(GemmParams& p) {
+  const uint64_t w = g_dbg_wait_ns.load();
+  p.wait_ns = w != 0 ? w : kWaitLimitNs;
+  p.withhold_first = g_dbg_withhold.load();
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 static bool valid_block(int b) { return b == 16 || b == 64 || b == 256; }
@@ -179,6 +188,13 @@ const char* sixbit_status_str(sixbit_status s) {
   }
 }
 
+sixbit_status sixbit_debug_gemm_timeout(uint64_t wait_limit_ns, int32_t withhold_first_stage) {
+  if (withhold_first_stage != 0 && withhold_first_stage != 1) return SIXBIT_EINVAL;
+  g_dbg_wait_ns.store(wait_limit_ns);
+  g_dbg_withhold.store(withhold_first_stage);
+  return SIXBIT_OK;
+}
+
 sixbit_status sixbit_check(int32_t* err_dev, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return SIXBIT_ECUDA;
@@ -297,6 +313,7 @@ static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, co
   p.n_fastest = M > N ? 1 : 0;
   p.rot_amax = rot_amax;
   p.had_block = had_block;
+  gemm_debug_params(p);
   // The bf16-operand kinds (BF16, W4A8) write a bf16 Y through TMA stores
   // (Y 16-byte aligned, N % 16 == 0 checked above); an FP32 Y is stored
   // directly.

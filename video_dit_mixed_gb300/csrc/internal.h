@@ -36,7 +36,12 @@ struct GemmParams {
   float* rot_amax;         // NVFP4 epilogue: atomicMax of |bf16(Y) . blockdiag(H_b / sqrt b)| (or NULL)
   int had_block;           // b of rot_amax (16 or 64)
   int y_tma;               // bf16-operand kinds: bf16 Y is written by TMA stores through the Y tensor map
+  uint64_t wait_ns;        // limit of every bounded wait (kWaitLimitNs unless a test shortens it)
+  int withhold_first;      // test of the failure path: each CTA's producer skips its first stage
 };
+
+// Test setting of the GEMMs' failure path (sixbit_debug_gemm_timeout).
+void gemm_debug_params(GemmParams& p);
 
 cudaError_t launch_hq_amax(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, float* amax_out,
                            cudaStream_t st);

@@ -251,12 +251,13 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
           for (int kb = 0; kb < nk; ++kb, ++it) {
             const int s = it % S;
             const uint32_t ph = (it / S) & 1;
-            if (it >= S && !mbar_wait(&empty[s], ph ^ 1, abort_flag)) {
+            if (it >= S && !mbar_wait(&empty[s], ph ^ 1, abort_flag, p.wait_ns)) {
               set_error(p.err, SIXBIT_ETIMEOUT);
               *abort_flag = 1;
               ok = false;
               break;
             }
+            if (p.withhold_first && it == 0) continue;  // failure-path test: stage 0 never lands
             const int kvalid = min(C::kKStage, p.K - kb * C::kKStage);
             const uint32_t sf_bytes = kNvf4 ? static_cast<uint32_t>(kvalid / 64) * 512u : 0u;
             mbar_expect_tx(&full[s], kATileBytes + kBTileBytes + sf_bytes * (1 + (kNvf4 ? nj : 0)));
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
           }
         }
         // every copy this CTA started lands before it can exit
-        for (uint32_t j = (it > S ? it - S : 0); j < it; ++j) (void)mbar_wait(&full[j % S], (j / S) & 1, nullptr);
+        for (uint32_t j = (it > S ? it - S : 0); j < it; ++j) (void)mbar_wait(&full[j % S], (j / S) & 1, nullptr, p.wait_ns);
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -288,12 +289,12 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
             const bool acc_start = kb == 0;
             const uint32_t buf = ac % kBufs;
             // the buffer's previous contents must have been drained by the epilogue
-            if (acc_start && ac >= kBufs && !mbar_wait(&acce[buf], ((ac / kBufs) - 1) & 1, abort_flag)) {
+            if (acc_start && ac >= kBufs && !mbar_wait(&acce[buf], ((ac / kBufs) - 1) & 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
             const int s = it % S;
-            if (!mbar_wait(&full[s], (it / S) & 1, abort_flag)) {
+            if (!mbar_wait(&full[s], (it / S) & 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -305,7 +306,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
               const int nmma = min(C::kKStage, p.K - kb * C::kKStage) / 64;
               const uint32_t sfa_col = tmem + kSfSlot0 + kSfSlotCols * s;
               const uint32_t sfb_col = sfa_col + kSfbOff;
-              if (!mbar_wait(&sf_full[s], (it / S) & 1, abort_flag)) {  // copied by the scale-factor warp
+              if (!mbar_wait(&sf_full[s], (it / S) & 1, abort_flag, p.wait_ns)) {  // copied by the scale-factor warp
                 ok = false;
                 break;
               }
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
           *abort_flag = 1;
         }
         tc_commit(drain);  // all tensor-core work issued here completes before exit
-        (void)mbar_wait(drain, 0, nullptr);
+        (void)mbar_wait(drain, 0, nullptr, p.wait_ns);
       }
     }
   } else if (warp < kEpiWarp0 + kEpiWarps) {
@@ -376,14 +377,14 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
       const int nb = n_tile * kBN + col0;         // first output column of this thread
       if (nb >= p.N) {                            // nothing of this part exists (ragged N)
         const uint32_t buf = ac % kBufs;
-        if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag, p.wait_ns)) { ok = false; break; }
         release_acc(&acce[buf], lane);
         ++ac;
         continue;
       }
       {
         const uint32_t buf = ac % kBufs;
-        if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag)) {
+        if (!mbar_wait(&accf[buf], (ac / kBufs) & 1, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -454,8 +455,8 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
         const int nj = (n_tile * kBN + 128 < p.N) ? 2 : 1;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % S;
-          if ((it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1, abort_flag)) ||
-              !mbar_wait(&full[s], (it / S) & 1, abort_flag)) {
+          if ((it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1, abort_flag, p.wait_ns)) ||
+              !mbar_wait(&full[s], (it / S) & 1, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }

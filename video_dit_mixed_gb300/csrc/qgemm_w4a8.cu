@@ -188,10 +188,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tile_of(t, m_tile, n_tile);
           for (int kb = 0; kb < nk; ++kb, ++it) {
             const int s = it % S;
-            if (it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1, abort_flag)) {
+            if (it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
+            if (p.withhold_first && it == 0) continue;  // failure-path test: stage 0 never lands
             mbar_expect_tx(&full[s], kBTile);
             tma_load_2d(W_op(s), &tmW, &full[s], kb * kKStage, n_tile * kBN);
             mbar_expect_tx(&s8_full[s], kS8Tile);
@@ -204,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // every copy this CTA started lands before it can exit
         for (uint32_t j = (it > S ? it - S : 0); j < it; ++j) {
-          (void)mbar_wait(&full[j % S], (j / S) & 1, nullptr);
-          (void)mbar_wait(&s8_full[j % S], (j / S) & 1, nullptr);
+          (void)mbar_wait(&full[j % S], (j / S) & 1, nullptr, p.wait_ns);
+          (void)mbar_wait(&s8_full[j % S], (j / S) & 1, nullptr, p.wait_ns);
         }
       }
     } else if (warp == 1) {
@@ -217,15 +218,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
           for (int g = 0; g < groups && ok; ++g, ++gi) {
-            if (gi >= 2 && !mbar_wait(&afree[gi & 1], ((gi >> 1) - 1) & 1, abort_flag)) {
+            if (gi >= 2 && !mbar_wait(&afree[gi & 1], ((gi >> 1) - 1) & 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
             const uint32_t d_tmem = tmem + (gi & 1) * kBN;
             for (int ss = 0; ss < 2; ++ss, ++it) {
               const int s = it % S;
-              if (!mbar_wait(&full[s], (it / S) & 1, abort_flag) ||
-                  !mbar_wait(&op_full[s], (it / S) & 1, abort_flag)) {
+              if (!mbar_wait(&full[s], (it / S) & 1, abort_flag, p.wait_ns) ||
+                  !mbar_wait(&op_full[s], (it / S) & 1, abort_flag, p.wait_ns)) {
                 ok = false;
                 break;
               }
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *abort_flag = 1;
         }
         tc_commit(drain);  // all tensor-core work issued here completes before exit
-        (void)mbar_wait(drain, 0, nullptr);
+        (void)mbar_wait(drain, 0, nullptr, p.wait_ns);
       }
     } else {
       // ------------------------------------------------------------ converters --
@@ -262,11 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % S;
-          if (!mbar_wait(&s8_full[s], (it / S) & 1, abort_flag)) {
+          if (!mbar_wait(&s8_full[s], (it / S) & 1, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
-          if (c == 1 && !mbar_wait(&read0[s], (it / S) & 1, abort_flag)) {
+          if (c == 1 && !mbar_wait(&read0[s], (it / S) & 1, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // run a phase past this wait, since its next phase needs group gi + 2,
         // which needs this accumulator back
         const uint32_t last = 2 * gi + 1;
-        if (!mbar_wait(&empty[last % S], (last / S) & 1, abort_flag)) {
+        if (!mbar_wait(&empty[last % S], (last / S) & 1, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
