@@ -16,6 +16,9 @@ random weights, no checkpoints or datasets):
   dit_5b        42 blocks, hidden 3072, FFN 12288.
   qkv_2b        one step = both quantizers and all three GEMM kinds of a
                 17776 x 1920 -> 5760 linear layer.  Metric: TFLOP/s.
+  ffn_2b        one step = the FFN pair 1920 -> 7680 (GELU) -> 1920 (+ residual)
+                in both mode orders (NVFP4 up / INT8 down and the reverse),
+                quantizers included.  Metric: TFLOP/s.
   gemm_sweep_5b one step = quantization + W4A4 and W4A8 GEMM at K = N = 3072
                 for M = 1024 .. 35552.  Metric: TFLOP/s.
 
@@ -213,6 +216,92 @@ class QkvLinear:
         if label == "tensor_stats":
             return ("hbm", mk * 2, False)
         return (None, 0, False)
+
+    def launches(self):
+        return None
+
+    def extra(self):
+        return {}
+
+
+class FfnPair:
+    """The FFN pair of a 2B-shaped block (17776 x 1920 -> 7680 -> 1920, GELU between, residual after),
+    run in both mode orders per step: NVFP4 up / INT8 down, then INT8 up / NVFP4 down."""
+
+    unit = "TFLOP/s"
+
+    def __init__(self, name, torch, ops, device):
+        import synthgen
+        self.name, self.t, self.ops, self.dev = name, torch, ops, device
+        x, wu, c = synthgen.linear_inputs("ffn_2b")
+        wd = synthgen.weights(c["seed"], c["k"], c["n"], stream=3)
+        self.b = c["had_block"]
+        self.m, self.h_dim = x.shape
+        self.f = wu.shape[0]
+        self.x_host = torch.from_numpy(x).to(torch.bfloat16).pin_memory()
+        self.x = self.x_host.to(device)
+        self.pu = ops.pack_weights(torch.from_numpy(wu).to(device), self.b)
+        self.pd = ops.pack_weights(torch.from_numpy(wd).to(device), self.b)
+        self.qx = ops.QActTensors(self.m, self.h_dim, device)
+        self.qh = ops.QActTensors(self.m, self.f, device)
+        self.hid = torch.empty((self.m, self.f), dtype=torch.bfloat16, device=device)
+        self.y = torch.empty((self.m, self.h_dim), dtype=torch.bfloat16, device=device)
+        self.y_host = torch.empty((self.m, self.h_dim), dtype=torch.bfloat16).pin_memory()
+        self.ws = torch.empty(ops.qgemm_workspace_bytes(self.f, self.h_dim), dtype=torch.uint8, device=device)
+        self.flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=device)
+        self.gemm_flops = 2.0 * self.m * self.f * self.h_dim
+        self.h2d_bytes = self.x.numel() * 2
+        self.d2h_bytes = self.y.numel() * 2
+        self.config = dict(workload=name, tokens=self.m, hidden=self.h_dim, ffn=self.f, had_block=self.b,
+                           orders="nvfp4 up + int8 down, int8 up + nvfp4 down", l2="256 MB buffer written between steps")
+
+    def calls(self):
+        o, b = self.ops, self.b
+        out = []
+        for up, down in ((o.MODE_NVFP4, o.MODE_INT8), (o.MODE_INT8, o.MODE_NVFP4)):
+            nu, nd = MODE_NAMES[up], MODE_NAMES[down]
+            out += [
+                (f"hq_x:{nu}", lambda up=up: o.hadamard_quant(self.x, b, up, out=self.qx)),
+                (f"qgemm_up:{nu}", lambda up=up: o.qgemm(self.qx, self.x, self.pu, up, epilogue=o.EPI_GELU,
+                                                         out=self.hid, ws=self.ws)),
+                (f"hq_h:{nd}", lambda down=down: o.hadamard_quant(self.hid, b, down, out=self.qh)),
+                (f"qgemm_down:{nd}", lambda down=down: o.qgemm(self.qh, self.hid, self.pd, down,
+                                                               epilogue=o.EPI_RESIDUAL, residual=self.x, out=self.y,
+                                                               ws=self.ws)),
+            ]
+        return out
+
+    warmup = QkvLinear.warmup
+    timed = QkvLinear.timed
+    profile = QkvLinear.profile
+
+    def e2e(self, k, stream):
+        T = self.t
+        pairs = []
+        for _ in range(k):
+            self.flush.fill_(1.0)
+            a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
+            a.record(stream)
+            self.x.copy_(self.x_host, non_blocking=True)
+            for _, f in self.calls():
+                f()
+            self.y_host.copy_(self.y, non_blocking=True)
+            b.record(stream)
+            pairs.append((a, b))
+        T.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in pairs]
+
+    def value(self, ms):
+        return 4 * self.gemm_flops / (ms / 1e3) / 1e12
+
+    def work(self, label):
+        kind, _, mode = label.partition(":")
+        if kind.startswith("qgemm"):
+            return ("tensor", self.gemm_flops, mode == "nvfp4")
+        n = self.m * (self.h_dim if kind == "hq_x" else self.f)
+        if mode == "nvfp4":
+            return ("hbm", n * 2 + n // 2 + n // 16, False)
+        return ("hbm", n * 3 + self.m * 4, False)
 
     def launches(self):
         return None
@@ -566,7 +655,7 @@ class GemmSweep:
         return {}
 
 
-WORKLOADS = {"qkv_2b": QkvLinear, "dit_2b": DitStep, "dit_2b_gated": DitStep, "dit_5b": DitStep, "gemm_sweep_5b": GemmSweep}
+WORKLOADS = {"qkv_2b": QkvLinear, "ffn_2b": FfnPair, "dit_2b": DitStep, "dit_2b_gated": DitStep, "dit_5b": DitStep, "gemm_sweep_5b": GemmSweep}
 
 
 # --------------------------------------------------------------------- timing --
