@@ -47,8 +47,10 @@
 //
 // Tensor memory holds two 256-column accumulators; K groups alternate between
 // them and the fold warps add s_w[g][n] * acc_g into registers while the next
-// group accumulates.  The MMA thread commits once per stage; a group's
-// completion is the commit after its second stage.
+// group accumulates.  The MMA thread waits on one barrier per stage (the
+// weight tile's copy completes on the barrier the converters arrive on: an
+// mbarrier phase needs its arrivals and its transaction bytes) and commits
+// once per stage; a group's completion is the commit after its second stage.
 // Every mbarrier wait is bounded (2 s); on expiry the kernel records
 // SIXBIT_ETIMEOUT, raises an abort flag for the other roles, waits (bounded)
 // for its copies and tensor-core work in flight, frees tensor memory and
@@ -118,9 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* boxes = smem + S * kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(boxes + kFoldWarps * kBoxBytes);
-  uint64_t* full = bars;            // [S] W tile landed
   uint64_t* s8_full = bars + S;     // [S] s8 A tile landed
-  uint64_t* op_full = bars + 2 * S; // [S] fp16 A operand written (two converter warps)
+  // [S] the stage is ready: the W tile's bytes landed (the producer's
+  // expect-tx arrival) and both converter warps wrote the fp16 A tile
+  uint64_t* op_full = bars + 2 * S;
   uint64_t* empty = bars + 3 * S;   // [S] the stage's MMAs are done
   uint64_t* read0 = bars + 4 * S;   // [S] converter warp 0 holds its s8 codes
   uint64_t* afree = bars + 5 * S;   // [2] accumulator read back (eight fold warps)
@@ -151,9 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
       mbar_init(&s8_full[s], 1);
-      mbar_init(&op_full[s], 2);
+      mbar_init(&op_full[s], 3);
       mbar_init(&empty[s], 1);
       mbar_init(&read0[s], 1);
     }
@@ -193,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             if (p.withhold_first && it == 0) continue;  // failure-path test: stage 0 never lands
-            mbar_expect_tx(&full[s], kBTile);
-            tma_load_2d(W_op(s), &tmW, &full[s], kb * kKStage, n_tile * kBN);
+            mbar_expect_tx(&op_full[s], kBTile);
+            tma_load_2d(W_op(s), &tmW, &op_full[s], kb * kKStage, n_tile * kBN);
             mbar_expect_tx(&s8_full[s], kS8Tile);
             tma_load_2d(A_s8(s), &tmA, &s8_full[s], kb * kKStage, m_tile * kBM);
           }
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // every copy this CTA started lands before it can exit
         for (uint32_t j = (it > S ? it - S : 0); j < it; ++j) {
-          (void)mbar_wait(&full[j % S], (j / S) & 1, nullptr, p.wait_ns);
+          (void)mbar_wait(&op_full[j % S], (j / S) & 1, nullptr, p.wait_ns);
           (void)mbar_wait(&s8_full[j % S], (j / S) & 1, nullptr, p.wait_ns);
         }
       }
@@ -225,8 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t d_tmem = tmem + (gi & 1) * kBN;
             for (int ss = 0; ss < 2; ++ss, ++it) {
               const int s = it % S;
-              if (!mbar_wait(&full[s], (it / S) & 1, abort_flag, p.wait_ns) ||
-                  !mbar_wait(&op_full[s], (it / S) & 1, abort_flag, p.wait_ns)) {
+              if (!mbar_wait(&op_full[s], (it / S) & 1, abort_flag, p.wait_ns)) {
                 ok = false;
                 break;
               }
