@@ -8,6 +8,10 @@ statistics (Gamma, delta cosine, the next block's input outlier ratio) feed
 the next decision.  The GEMM outputs are the float64 references rounded to
 FP32 and then to bf16, as a bf16 activation tensor is stored.
 
+The delta cache is kept in bf16, or (delta_format="mxfp8") in MXFP8: the
+fresh bf16 delta is used as it is by the block statistics and then encoded;
+the previous delta enters the statistics, and a skip, dequantized.
+
 This chains every other oracle module; it is compared with the GPU path on
 small sizes only.
 """
@@ -16,7 +20,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import gemm, policy, quant, stats
-from .formats import bf16_round
+from .formats import bf16_round, mxfp8_decode, mxfp8_encode
 
 
 def _round_bf16(v64):
@@ -41,9 +45,12 @@ def linear(x, pk, mode, b, epilogue, residual=None):
 
 
 class OracleDiT:
-    def __init__(self, weights, had_block, cfg: policy.PolicyConfig | None = None):
+    def __init__(self, weights, had_block, cfg: policy.PolicyConfig | None = None, delta_format: str = "bf16"):
         """weights: list of (W_up [F, H], W_down [H, F]) float32 per block."""
+        if delta_format not in ("bf16", "mxfp8"):
+            raise ValueError(delta_format)
         self.b = had_block
+        self.delta_format = delta_format
         self.cfg = cfg or policy.PolicyConfig()
         self.packs = [(quant.pack_weights(wu, had_block), quant.pack_weights(wd, had_block)) for wu, wd in weights]
         self.L = len(weights)
@@ -60,19 +67,31 @@ class OracleDiT:
             d = policy.decide(st, ratio, self.cfg)
             decisions.append(d)
             if self.deltas[l] is None:
-                self.deltas[l] = np.zeros_like(x)
+                self.store_delta(l, np.zeros_like(x))
             if d.mode == policy.SKIP:
-                out = stats.skip_apply(x, self.deltas[l])
+                out = stats.skip_apply(x, self.cached_delta(l))
                 out_stats = stats.tensor_stats(out)
             else:
                 pu, pd = self.packs[l]
                 h = linear(x, pu, d.mode, self.b, "gelu")
                 out = linear(h, pd, d.mode, self.b, "residual", x)
-                bs = stats.block_stats(x, out, self.deltas[l])
-                self.deltas[l] = bs["delta"]
+                bs = stats.block_stats(x, out, self.cached_delta(l))
+                self.store_delta(l, bs["delta"])
                 policy.fold(st, bs["gamma"], bs["cos"])
                 out_stats = bs["out"]
             ratio = stats.outlier_ratio(out_stats)
             x = out
         self.trace.append(decisions)
         return x
+
+    def store_delta(self, l, d):
+        """Keeps block l's bf16 delta in the cache's format."""
+        d = np.asarray(d, np.float32)
+        self.deltas[l] = (d.copy(), None) if self.delta_format == "bf16" else (d.shape, mxfp8_encode(d))
+
+    def cached_delta(self, l):
+        """Block l's cached delta as float32 values (dequantized for MXFP8; exact in float32)."""
+        a, enc = self.deltas[l]
+        if enc is None:
+            return a
+        return mxfp8_decode(*enc).astype(np.float32).reshape(a)

@@ -12,6 +12,16 @@ not define the formats; the definitions below are the public ones:
   no infinities, exponent-15/mantissa-7 is NaN, largest finite 448,
   smallest subnormal 2**-9.
 * bfloat16: the top 16 bits of an IEEE binary32.
+* MXFP8 (OCP Microscaling Formats v1.0, E4M3 elements): blocks of 32
+  consecutive elements share one E8M0 scale 2**X (an 8-bit biased exponent,
+  bias 127, code 255 = NaN, no sign and no mantissa).  X is the exponent of
+  the block's largest magnitude minus that of E4M3's largest normal (8),
+  floor(log2 amax) - 8, clamped to E8M0's range [-127, 127]; an all-zero
+  block takes the smallest scale.  Each element is E4M3(v / 2**X) with the
+  rounding below.  Magnitudes in [448, 512) * 2**X saturate to 448 * 2**X.
+  The method only says that the temporal delta cache can be kept in a low
+  precision ("6Bit-Diffusion" popular summary, section 7); MXFP8 is the
+  reading taken for it.
 
 Rounding is round-to-nearest, ties-to-even on the mantissa LSB, and
 "satfinite": magnitudes beyond the largest finite value become that value.
@@ -134,3 +144,45 @@ def bf16_bits(x) -> np.ndarray:
 def bf16_from_bits(b) -> np.ndarray:
     b = np.ascontiguousarray(b, dtype=np.uint16)
     return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------------ MXFP8 --
+
+MX_BLOCK = 32
+E8M0_BIAS = 127
+
+
+def e8m0_decode(code) -> np.ndarray:
+    """2**(code - 127) as float64; code 255 is NaN."""
+    c = np.asarray(code).astype(np.int64)
+    return np.where(c == 255, np.nan, np.ldexp(1.0, c - E8M0_BIAS))
+
+
+def mx_shared_exponent(amax) -> np.ndarray:
+    """X = floor(log2 amax) - 8, clamped to [-127, 127]; amax == 0 gives -127."""
+    a = np.asarray(amax, dtype=np.float64)
+    _, ex = np.frexp(a)                   # a = f * 2**ex, f in [0.5, 1): floor(log2 a) = ex - 1
+    x = np.where(a > 0, ex - 1 - 8, -E8M0_BIAS)
+    return np.clip(x, -E8M0_BIAS, E8M0_BIAS).astype(np.int64)
+
+
+def mxfp8_encode(v, block: int = MX_BLOCK):
+    """MXFP8 (E4M3 elements) of a flat array whose length is a multiple of `block`.
+
+    Returns (codes uint8 [n], scales uint8 [n / block]) with scales the E8M0
+    codes X + 127.
+    """
+    v = np.asarray(v, dtype=np.float64).reshape(-1)
+    if v.size % block:
+        raise ValueError("length must be a multiple of the block")
+    blocks = v.reshape(-1, block)
+    x = mx_shared_exponent(np.abs(blocks).max(axis=1) if blocks.size else np.zeros(0))
+    scaled = blocks / np.ldexp(1.0, x)[:, None]          # exact: a power of two
+    codes = encode(scaled, E4M3).reshape(-1)
+    return codes, (x + E8M0_BIAS).astype(np.uint8)
+
+
+def mxfp8_decode(codes, scales, block: int = MX_BLOCK) -> np.ndarray:
+    """float64 values of MXFP8 codes (flat) with one E8M0 scale per `block` codes."""
+    c = np.asarray(codes).reshape(-1, block)
+    return (decode(c, E4M3) * e8m0_decode(scales)[:, None]).reshape(-1)

@@ -165,3 +165,31 @@ def test_quantized_linear_mutations_are_caught(monkeypatch):
     monkeypatch.undo()
     monkeypatch.setattr(gemm, "gelu", lambda v: 0.5 * np.asarray(v, np.float64) * (1 + np.tanh(np.asarray(v))))
     assert _fails(tc.test_linear_with_the_hadamard_weight_closed_form, policy.BF16)    # a different activation
+
+
+def test_mxfp8_mutations_are_caught(monkeypatch):
+    import tests.test_oracle_mxfp8 as tm
+    orig_x = formats.mx_shared_exponent
+    monkeypatch.setattr(formats, "mx_shared_exponent", lambda a: orig_x(a) + 1)        # exponent one too high
+    assert _fails(tm.test_hand_worked_blocks, *tm.HAND[1])
+    assert _fails(tm.test_brute_force_nearest_on_random_blocks)
+    monkeypatch.setattr(formats, "mx_shared_exponent", lambda a: orig_x(a) - 1)        # one too low: saturates
+    assert _fails(tm.test_hand_worked_blocks, *tm.HAND[0])
+
+    def unclamped(a):
+        a = np.asarray(a, np.float64)
+        _, ex = np.frexp(a)
+        return np.where(a > 0, ex - 9, -127).astype(np.int64)
+    monkeypatch.setattr(formats, "mx_shared_exponent", unclamped)                      # no E8M0 range clamp
+    assert _fails(tm.test_hand_worked_blocks, *tm.HAND[3])
+    monkeypatch.undo()
+    orig_dec = formats.mxfp8_decode
+    monkeypatch.setattr(formats, "mxfp8_decode",
+                        lambda c, s, block=32: formats.decode(np.asarray(c), formats.E4M3))  # scale dropped
+    assert _fails(tm.test_decode_is_code_value_times_scale)
+    monkeypatch.undo()
+    monkeypatch.setattr(dit.OracleDiT, "store_delta",
+                        lambda self, l, d: self.deltas.__setitem__(l, (np.asarray(d, np.float32).copy(), None)))
+    assert _fails(tm.test_dit_mxfp8_cache_cosine_and_skip_closed_forms)                # cache kept in bf16
+    monkeypatch.undo()
+    assert orig_dec is formats.mxfp8_decode
