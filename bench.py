@@ -334,7 +334,9 @@ class DitStep:
             wd = torch.randn((H, F), generator=gen, device=device, dtype=torch.float32) * (c["w_std"] * gates[l])
             packed.append((ops.pack_weights(wu, b), ops.pack_weights(wd, b)))
             del wu, wd
-        self.model = dit.DiT(T, H, F, L, b, packed, device=device)
+        self.model = dit.DiT(T, H, F, L, b, packed, device=device, delta_format=self.delta_format)
+        # bytes per element of one block's Delta cache (MXFP8: one code byte, one scale byte per 32)
+        self.delta_bytes = 2.0 if self.delta_format == "bf16" else 1.0 + 1.0 / 32
         # input trajectory, resident in HBM before timing
         x0 = synthgen.activations(c["seed"], T, H, "laplace", c.get("outlier_frac", 0.005),
                                   c.get("outlier_scale", 50.0))
@@ -351,7 +353,8 @@ class DitStep:
         self.d2h_bytes = T * H * 2
         self.config = dict(workload=name, tokens=T, hidden=H, ffn=F, blocks=L, steps_per_run=c["steps"],
                            had_block=b, gate=c["gate"], policy="gamma 0.1, cos 0.99, err_cap 0.05, pdr 30",
-                           l2="working set > 10 GB, no flush needed", cuda_graph=not self.host_dispatch)
+                           l2="working set > 10 GB, no flush needed", cuda_graph=not self.host_dispatch,
+                           delta_cache=self.delta_format)
         self.mode_log = []
         self.timed_steps = []
         self.skip_run_bytes = 0
@@ -365,6 +368,7 @@ class DitStep:
         return x
 
     host_dispatch = False   # --dispatch host: no graph, the host launches each block's chosen kernels
+    delta_format = "bf16"   # --delta-format mxfp8: the Delta cache in MXFP8
 
     def _step(self, x):
         if self.host_dispatch:
@@ -490,7 +494,7 @@ class DitStep:
             kk = 1
             while l + kk < self.L and low[j, l + kk] == 4:
                 kk += 1
-            sizes.append((4 + 2 * kk) * self.T * self.H)
+            sizes.append((4 + self.delta_bytes * kk) * self.T * self.H)
         self.skip_run_bytes = (sum(sizes) / len(sizes)) if sizes else 0
         self.mode_log = mh
         m.reset()
@@ -549,8 +553,8 @@ class DitStep:
             if mode == "int8":   # read, int8 codes, row scales
                 return ("hbm", n * 3 + T * 4, False)
             return (None, 0, False)
-        if label == "block_stats":
-            return ("hbm", 8 * T * H, False)
+        if label == "block_stats":   # x_in, x_out read; Delta read and written
+            return ("hbm", (4 + 2 * self.delta_bytes) * T * H, False)
         if label == "tensor_stats":
             return ("hbm", 2 * T * H, False)
         return (None, 0, False)
@@ -808,6 +812,8 @@ def run_ours(args):
         cls = type(cls.__name__, (cls,), dict(blocks_override=args.blocks))
     if args.dispatch == "host":
         cls = type(cls.__name__, (cls,), dict(host_dispatch=True))
+    if args.delta_format != "bf16":
+        cls = type(cls.__name__, (cls,), dict(delta_format=args.delta_format))
     wl = cls(args.workload, torch, ops, dev)
     stream = torch.cuda.current_stream()
 
@@ -1062,6 +1068,8 @@ def main():
     ap.add_argument("--dispatch", default="graph", choices=["graph", "host"],
                     help="DiT workloads: 'host' replaces the CUDA graph by host-side dispatch on each block's mode "
                          "word (one sync per block; for profilers that cannot profile conditional graph nodes)")
+    ap.add_argument("--delta-format", default="bf16", choices=["bf16", "mxfp8"],
+                    help="storage of the DiT's Delta cache (MXFP8: E4M3 codes, one E8M0 scale per 32)")
     ap.add_argument("--blocks", type=int, default=0,
                     help="DiT workloads: use only this many blocks (profiling runs on a smaller device footprint)")
     ap.add_argument("--oracle-costs", action="store_true", help=argparse.SUPPRESS)  # the 1-core CPU leg's child

@@ -276,10 +276,15 @@ sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_sta
  *               it zero between steps)
  *   in_stats0   [4] float64, written by sixbit_dit_begin: {max |x0|,
  *               sum |x0|, count, sum x0^2}
- *   x0 [n], buf[0], buf[1] [n] bf16; deltas [L][n] bf16, the Delta cache
+ *   x0 [n], buf[0], buf[1] [n] bf16
+ *   deltas      the Delta cache, one slice of n elements per block, in
+ *               delta_format: SIXBIT_DELTA_BF16, [L][n] bf16; or
+ *               SIXBIT_DELTA_MXFP8, [L][n] E4M3 codes with delta_scales
+ *               [L][n / 32] E8M0 codes (see sixbit_block_stats_mxfp8)
+ *   delta_scales NULL for a bf16 cache
  *   conds       NULL, or [L] conditional handles (sixbit_graph_cond_create)
  *               of the per-block switches of a captured graph
- * n % 8 == 0; 16-byte aligned tensors.
+ * n % 8 == 0 (n % 32 == 0 for MXFP8); 16-byte aligned tensors.
  */
 typedef struct {
   sixbit_policy_state* states;
@@ -288,12 +293,13 @@ typedef struct {
   double* in_stats0;
   const uint16_t* x0;
   uint16_t* buf[2];
-  uint16_t* deltas;
+  void* deltas;
+  uint8_t* delta_scales;
   uint32_t* run_len;
   const uint64_t* conds;
   int64_t n;
   int32_t L;
-  int32_t reserved;
+  int32_t delta_format;
 } sixbit_dit_blocks;
 
 /*
@@ -333,6 +339,35 @@ sixbit_status sixbit_dit_block_end(const sixbit_policy_cfg* cfg, const sixbit_di
                                    void* scratch, int32_t* err_dev, void* stream);
 sixbit_status sixbit_dit_skip_run(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
                                   void* scratch, int32_t* err_dev, void* stream);
+
+/*
+ * Storage format of the Delta cache.  The method only says the cache may be
+ * kept in a low precision to save memory (popular summary, section 7);
+ * MXFP8 is the OCP Microscaling format with E4M3 elements: blocks of 32
+ * consecutive elements share an E8M0 scale 2^X, X = floor(log2 max|Delta|)
+ * - 8 clamped to [-127, 127] (-127 for an all-zero block), stored as the byte
+ * X + 127; element k is E4M3(Delta_k / 2^X), round to nearest even,
+ * saturating at 448, stored in byte k.  About 1.03 bytes per element instead
+ * of 2.
+ */
+enum { SIXBIT_DELTA_BF16 = 0, SIXBIT_DELTA_MXFP8 = 1 };
+
+/*
+ * sixbit_block_stats with the Delta cache in MXFP8: the fresh
+ * Delta = bf16(f32(x_out) - f32(x_in)) enters the sums as it is; the
+ * previous one, read from (delta_codes [n], delta_scales [n / 32]),
+ * dequantized (exact in FP32); then the fresh Delta is encoded over it.  A
+ * zeroed cache holds Delta = 0.  n % 32 == 0; delta_codes 16-byte aligned.
+ */
+sixbit_status sixbit_block_stats_mxfp8(const uint16_t* x_in, const uint16_t* x_out, uint8_t* delta_codes,
+                                       uint8_t* delta_scales, int64_t n, const int32_t* mode_dev,
+                                       sixbit_stats* stats_dev, void* scratch, int32_t* err_dev, void* stream);
+
+/* sixbit_skip_apply with an MXFP8 Delta cache: x_out = bf16(f32(x_in) +
+ * dequantized Delta).  n % 32 == 0; delta_codes 16-byte aligned. */
+sixbit_status sixbit_skip_apply_mxfp8(const uint16_t* x_in, const uint8_t* delta_codes, const uint8_t* delta_scales,
+                                      uint16_t* x_out, int64_t n, const int32_t* mode_dev, sixbit_stats* stats_dev,
+                                      void* scratch, int32_t* err_dev, void* stream);
 
 /* ---- companions of the hot path ---------------------------------------- */
 

@@ -11,6 +11,8 @@ every step independently (the oracle never sees a GPU tensor).  Bar:
 - the run takes every branch: BF16 (PDR), NVFP4, INT8, SKIP and a refresh;
 - the CUDA-graph replay of a step, and host-side dispatch on the mode word,
   give bit-identical results to eager launches.
+Both Delta-cache formats (bf16 and MXFP8) are run, each against the oracle
+keeping its cache in the same format.
 """
 import numpy as np
 import pytest
@@ -35,11 +37,12 @@ def _margin(st, ratio, cfg):
     return min(m)
 
 
-def _run_gpu(name, graph, switched=True, host_dispatch=False):
+def _run_gpu(name, graph, switched=True, host_dispatch=False, delta_format="bf16"):
     from video_dit_mixed_gb300 import dit, ops
     c = synthgen.DIT_CONFIGS[name]
     packed = dit.pack_block_weights(synthgen.dit_weights(name), c["had_block"])
-    model = dit.DiT(c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"], packed)
+    model = dit.DiT(c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"], packed,
+                    delta_format=delta_format)
     xs = [torch.from_numpy(x).to(torch.bfloat16).cuda() for x in synthgen.dit_trajectory(name)]
     outs, words = [], []
     for s, x in enumerate(xs):
@@ -52,12 +55,13 @@ def _run_gpu(name, graph, switched=True, host_dispatch=False):
     return outs, words, model
 
 
-def test_tiny_dit_against_oracle_chain():
+@pytest.mark.parametrize("delta_format", ["bf16", "mxfp8"])
+def test_tiny_dit_against_oracle_chain(delta_format):
     name = "dit_tiny"
     c = synthgen.DIT_CONFIGS[name]
-    outs, words, _ = _run_gpu(name, graph=False)
+    outs, words, _ = _run_gpu(name, graph=False, delta_format=delta_format)
     cfg = policy.PolicyConfig()
-    ref = OracleDiT(synthgen.dit_weights(name), c["had_block"], cfg)
+    ref = OracleDiT(synthgen.dit_weights(name), c["had_block"], cfg, delta_format=delta_format)
     # record the oracle's distance to its thresholds at every decision
     margins = []
     orig = policy.decide
@@ -93,10 +97,10 @@ def test_tiny_dit_against_oracle_chain():
         odit.policy.decide = orig
 
 
-@pytest.mark.parametrize("switched", [False, True])
-def test_graph_replay_matches_eager(switched):
-    o_eager, w_eager, _ = _run_gpu("dit_tiny", graph=False)
-    o_graph, w_graph, m = _run_gpu("dit_tiny", graph=True, switched=switched)
+@pytest.mark.parametrize("switched,delta_format", [(False, "bf16"), (True, "bf16"), (True, "mxfp8")])
+def test_graph_replay_matches_eager(switched, delta_format):
+    o_eager, w_eager, _ = _run_gpu("dit_tiny", graph=False, delta_format=delta_format)
+    o_graph, w_graph, m = _run_gpu("dit_tiny", graph=True, switched=switched, delta_format=delta_format)
     assert m.graph is not None
     for a, b in zip(w_eager, w_graph):
         np.testing.assert_array_equal(a, b)

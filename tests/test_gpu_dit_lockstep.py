@@ -19,14 +19,17 @@ GPU's own tensors, the way the DiT chains them.
   slope and the epilogue's 4e-7 |g| on the up projection).
 The weights and the trajectory noise are drawn on the device from a seeded
 generator (as the benchmark does); the oracle reads exactly the tensors it
-checks.
+checks.  With the MXFP8 delta cache, the codes and scales the GPU writes are
+checked bit for bit on seeded rows against the oracle's encoding of
+bf16(x_out - x_in), and the oracle's view of the cache is the GPU's cache
+decoded through the oracle's own code and scale tables.
 """
 import numpy as np
 import pytest
 import torch
 
 import synthgen
-from oracle import gemm, hadamard, policy, quant, stats
+from oracle import formats, gemm, hadamard, policy, quant, stats
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-5
@@ -46,7 +49,7 @@ def _half_ulp_bf16(v):
 class Run:
     """The product DiT on device-seeded weights and trajectory, driven one block at a time."""
 
-    def __init__(self, name, blocks=None):
+    def __init__(self, name, blocks=None, delta_format="bf16"):
         from video_dit_mixed_gb300 import dit, ops
         self.ops = ops
         c = dict(synthgen.DIT_CONFIGS[name])
@@ -61,7 +64,7 @@ class Run:
             wd = torch.randn((self.H, self.F), generator=gen, device="cuda") * (c["w_std"] * float(gates[l]))
             packed.append((ops.pack_weights(wu, self.b), ops.pack_weights(wd, self.b)))
             self.w.append((wu, wd))
-        self.model = dit.DiT(self.T, self.H, self.F, L, self.b, packed)
+        self.model = dit.DiT(self.T, self.H, self.F, L, self.b, packed, delta_format=delta_format)
         x0 = synthgen.activations(c["seed"], self.T, self.H, "laplace", c.get("outlier_frac", 0.005),
                                   c.get("outlier_scale", 50.0))
         self.x = torch.from_numpy(x0).to(torch.bfloat16).cuda()
@@ -141,8 +144,25 @@ def _deep_check(run, l, mode, x_np, h_dev, out_np, rows):
     assert np.all(err <= tol), f"down rows of block {l}: {int((err > tol).sum())} outside"
 
 
-def _lockstep(name, steps, blocks=None, deep_every=5, nrows=32):
-    run = Run(name, blocks)
+_E4M3 = formats.decode(np.arange(256), formats.E4M3)       # value of every code (NaN for 0x7F / 0xFF)
+_E8M0 = formats.e8m0_decode(np.arange(256))
+
+
+def _mx_cache_check(run, l, delta, rng):
+    """GPU MXFP8 cache of block l vs the oracle's encoding of `delta` on seeded rows; returns the
+    GPU cache decoded (float32 [T, H])."""
+    m = run.model
+    codes = m.deltas[l].cpu().numpy().reshape(run.T, run.H)
+    scales = m.delta_scales[l].cpu().numpy().reshape(run.T, run.H // 32)
+    rows = np.unique(np.append(rng.choice(run.T, 255, replace=False), run.T - 1))
+    wc, ws = formats.mxfp8_encode(delta[rows].reshape(-1))
+    assert np.array_equal(codes[rows].reshape(-1), wc) and np.array_equal(scales[rows].reshape(-1), ws)
+    vals = _E4M3[codes].reshape(run.T, run.H // 32, 32) * _E8M0[scales][:, :, None]
+    return vals.reshape(run.T, run.H).astype(np.float32)
+
+
+def _lockstep(name, steps, blocks=None, deep_every=5, nrows=32, delta_format="bf16"):
+    run = Run(name, blocks, delta_format)
     o, m = run.ops, run.model
     cfg = policy.PolicyConfig()
     st = [policy.PolicyState() for _ in range(run.L)]
@@ -210,7 +230,12 @@ def _lockstep(name, steps, blocks=None, deep_every=5, nrows=32):
             torch.cuda.synchronize()
             out_np = _np(out)
             bs = stats.block_stats(x_np, out_np, prev[l])
-            assert np.array_equal(_np(m.deltas[l]).view(np.uint32), bs["delta"].view(np.uint32)), f"delta {s}, {l}"
+            if delta_format == "bf16":
+                assert np.array_equal(_np(m.deltas[l]).view(np.uint32), bs["delta"].view(np.uint32)), \
+                    f"delta {s}, {l}"
+                new_prev = bs["delta"]
+            else:
+                new_prev = _mx_cache_check(run, l, bs["delta"], rng)
             if l >= deep_from:
                 rows = np.sort(rng.choice(run.T, nrows - 1, replace=False))
                 rows = np.unique(np.append(rows, run.T - 1))     # the ragged last tile
@@ -218,7 +243,7 @@ def _lockstep(name, steps, blocks=None, deep_every=5, nrows=32):
                 checked += 1
                 deep_from = run.L
             policy.fold(st[l], bs["gamma"], bs["cos"])
-            prev[l] = bs["delta"]
+            prev[l] = new_prev
             x_np, xd = out_np, out
             ratio = stats.outlier_ratio(bs["out"])
             l += 1
@@ -241,3 +266,9 @@ def test_dit_5b_lockstep_first_steps():
     r = _lockstep("dit_5b", steps=3, deep_every=1, nrows=16)
     assert r["checked"] >= 2, r
     print(f"dit_5b: {r}")
+
+
+def test_dit_2b_lockstep_mxfp8_cache():
+    r = _lockstep("dit_2b", steps=20, deep_every=10, delta_format="mxfp8")
+    assert {policy.INT8, policy.BF16, policy.SKIP} <= r["seen"], r
+    print(f"dit_2b mxfp8: {r}")

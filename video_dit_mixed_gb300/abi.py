@@ -45,9 +45,8 @@ class PolicyState(C.Structure):
 
 class DitBlocks(C.Structure):
     _fields_ = [("states", c_p), ("stats", c_p), ("modes", c_p), ("in_stats0", c_p),
-                ("x0", c_p), ("buf", c_p * 2), ("deltas", c_p), ("run_len", c_p), ("conds", c_p),
-                ("n", C.c_int64), ("L", C.c_int32),
-                ("reserved", C.c_int32)]
+                ("x0", c_p), ("buf", c_p * 2), ("deltas", c_p), ("delta_scales", c_p), ("run_len", c_p),
+                ("conds", c_p), ("n", C.c_int64), ("L", C.c_int32), ("delta_format", C.c_int32)]
 
 
 EXPORTS = {
@@ -66,6 +65,8 @@ EXPORTS = {
     "sixbit_policy_step": (C.c_int, [C.POINTER(PolicyCfg), c_p, c_p, c_p, c_p, c_p, c_p]),
     "sixbit_tensor_stats": (C.c_int, [c_p, C.c_int64, c_p, c_p, c_p, c_p]),
     "sixbit_skip_apply": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),
+    "sixbit_block_stats_mxfp8": (C.c_int, [c_p, c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),
+    "sixbit_skip_apply_mxfp8": (C.c_int, [c_p, c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),
     "sixbit_block_stats_noalloc": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p]),
     "sixbit_block_stats_noalloc_max_elems": (C.c_int64, []),
     "sixbit_dit_begin": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), c_p, c_p, c_p]),

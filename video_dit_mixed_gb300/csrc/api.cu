@@ -416,6 +416,36 @@ sixbit_status sixbit_skip_apply(const uint16_t* x_in, const uint16_t* delta_cach
       launch_skip_apply(x_in, delta_cache, x_out, n, mode_dev, stats_dev, scratch, static_cast<cudaStream_t>(stream)));
 }
 
+sixbit_status sixbit_block_stats_mxfp8(const uint16_t* x_in, const uint16_t* x_out, uint8_t* delta_codes,
+                                       uint8_t* delta_scales, int64_t n, const int32_t* mode_dev,
+                                       sixbit_stats* stats_dev, void* scratch, int32_t* err_dev, void* stream) {
+  (void)err_dev;
+  if (x_in == nullptr || x_out == nullptr || delta_codes == nullptr || delta_scales == nullptr ||
+      stats_dev == nullptr || scratch == nullptr)
+    return SIXBIT_EINVAL;
+  if (n <= 0 || n % 32 != 0) return SIXBIT_ESHAPE;
+  if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(delta_codes) || !aligned16(scratch)) return SIXBIT_EALIGN;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+  return cuda_status(launch_block_stats_mx(x_in, x_out, delta_codes, delta_scales, n, mode_dev, stats_dev, scratch,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+sixbit_status sixbit_skip_apply_mxfp8(const uint16_t* x_in, const uint8_t* delta_codes, const uint8_t* delta_scales,
+                                      uint16_t* x_out, int64_t n, const int32_t* mode_dev, sixbit_stats* stats_dev,
+                                      void* scratch, int32_t* err_dev, void* stream) {
+  (void)err_dev;
+  if (x_in == nullptr || delta_codes == nullptr || delta_scales == nullptr || x_out == nullptr ||
+      stats_dev == nullptr || scratch == nullptr)
+    return SIXBIT_EINVAL;
+  if (n <= 0 || n % 32 != 0) return SIXBIT_ESHAPE;
+  if (!aligned16(x_in) || !aligned16(x_out) || !aligned16(delta_codes) || !aligned16(scratch)) return SIXBIT_EALIGN;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+  return cuda_status(launch_skip_apply_mx(x_in, delta_codes, delta_scales, x_out, n, mode_dev, stats_dev, scratch,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_state* state_dev,
                                  const sixbit_stats* last_stats_dev, const double* in_stats_dev, int32_t* mode_dev,
                                  int32_t* err_dev, void* stream) {
@@ -437,7 +467,10 @@ static sixbit_status check_blocks(const sixbit_policy_cfg* cfg, const sixbit_dit
       B.in_stats0 == nullptr || B.x0 == nullptr || B.buf[0] == nullptr || B.buf[1] == nullptr ||
       B.deltas == nullptr)
     return SIXBIT_EINVAL;
+  if (B.delta_format != SIXBIT_DELTA_BF16 && B.delta_format != SIXBIT_DELTA_MXFP8) return SIXBIT_EINVAL;
+  if (B.delta_format == SIXBIT_DELTA_MXFP8 && B.delta_scales == nullptr) return SIXBIT_EINVAL;
   if (B.L <= 0 || l < 0 || l >= B.L || B.n <= 0 || B.n % 8 != 0) return SIXBIT_ESHAPE;
+  if (B.delta_format == SIXBIT_DELTA_MXFP8 && B.n % 32 != 0) return SIXBIT_ESHAPE;
   if (!aligned16(B.x0) || !aligned16(B.buf[0]) || !aligned16(B.buf[1]) || !aligned16(B.deltas) ||
       !aligned16(scratch))
     return SIXBIT_EALIGN;

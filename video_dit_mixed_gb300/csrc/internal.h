@@ -62,6 +62,12 @@ cudaError_t launch_block_stats_fixed_grid(const uint16_t* x_in, const uint16_t* 
                                           cudaStream_t st);
 cudaError_t launch_skip_apply(const uint16_t* x_in, const uint16_t* delta, uint16_t* x_out, int64_t n,
                               const int32_t* mode_dev, sixbit_stats* stats, void* scratch, cudaStream_t st);
+cudaError_t launch_block_stats_mx(const uint16_t* x_in, const uint16_t* x_out, uint8_t* codes, uint8_t* scales,
+                                  int64_t n, const int32_t* mode_dev, sixbit_stats* stats, void* scratch,
+                                  cudaStream_t st);
+cudaError_t launch_skip_apply_mx(const uint16_t* x_in, const uint8_t* codes, const uint8_t* scales, uint16_t* x_out,
+                                 int64_t n, const int32_t* mode_dev, sixbit_stats* stats, void* scratch,
+                                 cudaStream_t st);
 cudaError_t launch_dit_begin(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, void* scratch, int32_t* err,
                              cudaStream_t st);
 cudaError_t launch_dit_block_end(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, void* scratch,

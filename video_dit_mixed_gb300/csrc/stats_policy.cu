@@ -389,6 +389,212 @@ __global__ void __launch_bounds__(kStThreads) skip_apply_kernel(const uint16_t* 
   }
 }
 
+// ------------------------------------------------- MXFP8 Delta cache --
+//
+// The cache can hold each Delta in MXFP8 (OCP Microscaling, E4M3 elements):
+// blocks of 32 consecutive elements share an E8M0 scale 2^X with
+// X = floor(log2 amax) - 8 (clamped to >= -127; a zero block takes -127), and
+// element k is E4M3(Delta_k / 2^X), round to nearest even, saturating at 448.
+// Codes: [n] bytes, element k in byte k; scales: [n / 32] E8M0 bytes (X + 127).
+// The fresh bf16 Delta feeds the statistics as it is and is then encoded; the
+// previous Delta enters the statistics (and a skip) dequantized, which is
+// exact in FP32 (4 significant bits times 2^X, X >= -127).
+//
+// In the grid-stride loops a thread's vector index i has i % 4 == lane % 4
+// (the CTA size and the stride are multiples of 4), so lanes 4g .. 4g+3 hold
+// one 32-element block: its maximum is two xor-shuffles among those lanes,
+// and with n % 32 == 0 every branch is uniform over the four.
+
+// 2^(c - 127) for an E8M0 code (c = 0: 2^-127, a subnormal; c = 255: NaN)
+__device__ __forceinline__ float e8m0_value(uint32_t c) {
+  return __uint_as_float(c == 0 ? 0x00400000u : (c == 255 ? 0x7FC00000u : c << 23));
+}
+
+// E8M0 code of a block whose largest magnitude is amax >= 0: the biased FP32
+// exponent of amax minus 8, or 0 (X = -127) for amax below 2^-118.
+__device__ __forceinline__ uint32_t mx_scale_code(float amax) {
+  const int e = static_cast<int>(__float_as_uint(amax) >> 23);
+  return static_cast<uint32_t>(e > 8 ? e - 8 : 0);
+}
+
+__device__ __forceinline__ float f16_bits_to_f32(uint32_t h) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(static_cast<uint16_t>(h)));
+  return f;
+}
+
+// eight E4M3 codes (element k in byte k) times 2^X -> four FP32 pairs (exact)
+__device__ __forceinline__ void mx_unpack8(const uint2& c, float scale, uint64_t (&p)[4]) {
+  const uint64_t s2 = f2_pack(scale, scale);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w = j < 2 ? c.x : c.y;
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(w >> (16 * (j & 1)))));
+    p[j] = f2_mul(f2_pack(f16_bits_to_f32(h2 & 0xFFFFu), f16_bits_to_f32(h2 >> 16)), s2);
+  }
+}
+
+// four FP32 pairs times 2^-X -> eight E4M3 codes (RN, satfinite)
+__device__ __forceinline__ uint2 mx_pack8(const uint64_t (&d)[4], uint32_t code) {
+  const float inv = __uint_as_float((254u - code) << 23);  // 2^-X, X in [-127, 119]: a normal float
+  const uint64_t i2 = f2_pack(inv, inv);
+  uint32_t h[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t q = f2_mul(d[j], i2);  // exact unless it underflows, which rounds to zero in E4M3 anyway
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(f2_hi(q)), "f"(f2_lo(q)));
+    h[j] = r;
+  }
+  return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
+__device__ __forceinline__ uint2 ld8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld8_nc(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_u8_nc(const uint8_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// One vector of the MXFP8 block-statistics pass (vector i of the caller's
+// loop, whose four-lane group is `gmask`): statistics as block_stats_vec with
+// the previous Delta (codes pc; scale byte ps, read by the group leader)
+// dequantized, then the new Delta encoded over it.  The leader read the old
+// scale before it writes the new one, so read and write are one thread's.
+__device__ __forceinline__ void block_stats_mx_vec(const uint4& ra, const uint4& rb, const uint2& pc, uint32_t ps,
+                                                   uint8_t* codes, uint8_t* scales, int64_t i, unsigned gmask,
+                                                   int leader, TwoF2& d2, Kahan2& xi2, TwoF2& ddp, TwoF2& dp2,
+                                                   float& mx, Kahan2& sa) {
+  ps = __shfl_sync(gmask, ps, leader);
+  uint64_t a[4], b[4], p[4], d[4];
+  unpack4x2(ra, a);
+  unpack4x2(rb, b);
+  mx_unpack8(pc, e8m0_value(ps), p);
+  float dmax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    d[j] = f2_from_bf16x2(f2_to_bf16x2(f2_sub(b[j], a[j])));  // Delta = bf16(x_out - x_in)
+    two_add2(d2, f2_mul(d[j], d[j]));
+    two_add2(ddp, f2_mul(d[j], p[j]));
+    two_add2(dp2, f2_mul(p[j], p[j]));
+    kahan_add2(xi2, f2_mul(a[j], a[j]));
+    mx = f2_max_abs(b[j], mx);
+    kahan_add2(sa, f2_abs(b[j]));
+    dmax = f2_max_abs(d[j], dmax);
+  }
+  dmax = fmaxf(dmax, __shfl_xor_sync(gmask, dmax, 1));
+  dmax = fmaxf(dmax, __shfl_xor_sync(gmask, dmax, 2));
+  const uint32_t code = mx_scale_code(dmax);
+  *reinterpret_cast<uint2*>(codes + 8 * i) = mx_pack8(d, code);
+  if ((threadIdx.x & 3) == 0) scales[i >> 2] = static_cast<uint8_t>(code);
+}
+
+__device__ __forceinline__ uint32_t ld_u8(const uint8_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// block_stats_body with the Delta cache in MXFP8 (n % 32 == 0).  Both
+// vectors' loads (activations, codes, the leader's scale bytes) are issued
+// before either is used.
+template <bool W0 = false>
+__device__ bool block_stats_mx_body(const uint16_t* __restrict__ x_in, const uint16_t* __restrict__ x_out,
+                                    uint8_t* codes, uint8_t* scales, int64_t n, void* scratch, double (&tot)[6]) {
+  const int64_t n8 = n >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
+  const int lane = threadIdx.x & 31, leader = lane & ~3;
+  const unsigned gmask = 0xFu << leader;
+  const bool lead = (lane & 3) == 0;
+  float mx = 0.f;
+  TwoF2 d2{0, 0}, ddp{0, 0}, dp2{0, 0};
+  Kahan2 xi2{0, 0}, sa{0, 0};
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8; i += 2 * stride) {
+    const int64_t i1 = i + stride;
+    const bool two = i1 < n8;  // uniform over the four lanes of a block
+    const uint4 a0 = ld16(x_in + 8 * i), b0 = ld16(x_out + 8 * i);
+    const uint2 c0 = ld8(codes + 8 * i);
+    const uint32_t s0 = lead ? ld_u8(scales + (i >> 2)) : 0u;
+    uint4 a1 = make_uint4(0, 0, 0, 0), b1 = a1;
+    uint2 c1 = make_uint2(0, 0);
+    uint32_t s1 = 0;
+    if (two) {
+      a1 = ld16(x_in + 8 * i1);
+      b1 = ld16(x_out + 8 * i1);
+      c1 = ld8(codes + 8 * i1);
+      if (lead) s1 = ld_u8(scales + (i1 >> 2));
+    }
+    block_stats_mx_vec(a0, b0, c0, s0, codes, scales, i, gmask, leader, d2, xi2, ddp, dp2, mx, sa);
+    if (two) block_stats_mx_vec(a1, b1, c1, s1, codes, scales, i1, gmask, leader, d2, xi2, ddp, dp2, mx, sa);
+  }
+  FF v[6] = {to_ff(d2), to_ff(xi2), to_ff(ddp), to_ff(dp2), FF{mx, 0.f}, to_ff(sa)};
+  const bool is_max[6] = {false, false, false, false, true, false};
+  return grid_reduce<6, W0>(v, is_max, scratch_view(scratch), tot);
+}
+
+__global__ void __launch_bounds__(kStThreads) block_stats_mx_kernel(const uint16_t* __restrict__ x_in,
+                                                                    const uint16_t* __restrict__ x_out,
+                                                                    uint8_t* codes, uint8_t* scales, int64_t n,
+                                                                    const int32_t* mode_dev, sixbit_stats* stats,
+                                                                    void* scratch) {
+  if (mode_is(mode_dev, SIXBIT_MODE_SKIP)) return;
+  double tot[6];
+  if (block_stats_mx_body(x_in, x_out, codes, scales, n, scratch, tot)) write_block_stats(stats, tot, n);
+}
+
+// v += dequantized Delta (vector i of a cache with `codes` / `scales`), rounded to bf16 per element
+__device__ __forceinline__ void mx_skip_add(uint64_t (&v)[4], const uint2& c, uint32_t sc) {
+  uint64_t d[4];
+  mx_unpack8(c, e8m0_value(sc), d);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
+}
+
+__global__ void __launch_bounds__(kStThreads) skip_apply_mx_kernel(const uint16_t* __restrict__ x_in,
+                                                                   const uint8_t* __restrict__ codes,
+                                                                   const uint8_t* __restrict__ scales,
+                                                                   uint16_t* x_out, int64_t n, const int32_t* mode_dev,
+                                                                   sixbit_stats* stats, void* scratch) {
+  if (mode_is_not(mode_dev, SIXBIT_MODE_SKIP)) return;
+  const int64_t n8 = n >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
+  float mx = 0.f;
+  Kahan2 sa{0, 0};
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8; i += stride) {
+    uint64_t v[4];
+    unpack4x2(ld16(x_in + 8 * i), v);
+    mx_skip_add(v, ld8_nc(codes + 8 * i), ld_u8_nc(scales + (i >> 2)));
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      w[q] = f2_to_bf16x2(v[q]);  // exact: v holds bf16 values
+      mx = f2_max_abs(v[q], mx);
+      kahan_add2(sa, f2_abs(v[q]));
+    }
+    *reinterpret_cast<uint4*>(x_out + 8 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  FF v[2] = {FF{mx, 0.f}, to_ff(sa)};
+  const bool is_max[2] = {true, false};
+  double tot[2];
+  if (grid_reduce<2>(v, is_max, scratch_view(scratch), tot)) {
+    stats->max_abs_out = tot[0];
+    stats->sum_abs_out = tot[1];
+    stats->count = static_cast<double>(n);
+  }
+}
+
 // ------------------------------------------------------------------ policy --
 
 __device__ __forceinline__ bool near_thr(double v, double thr, double rel) { return fabs(v - thr) <= rel * fabs(thr); }
@@ -505,8 +711,10 @@ __global__ void policy_kernel(sixbit_policy_cfg cfg, sixbit_policy_state* st, co
 // with its {max, sum |x|, count} into stats[l+k-1].  Each decision also sets
 // the block's graph condition when a handle array is given: a compute mode
 // to its body (0, 1, 2), a run start to 3, a block inside a run to none (4).
-// The protocol's kernels cap registers at 64 (launch bounds): the decisions
-// run in one warp at the tail and may spill; the streaming body may not.
+// The protocol's kernels cap registers at 64 (launch bounds; 80 for the
+// MXFP8-cache block end, which keeps both vectors' loads in flight): the
+// decisions run in one warp at the tail and may spill; the streaming body
+// may not.
 __device__ __forceinline__ const double* block_in_stats(const sixbit_dit_blocks& B, int l) {
   return l == 0 ? B.in_stats0 : &B.stats[l - 1].max_abs_out;  // {max, sum |x|, count}
 }
@@ -590,25 +798,104 @@ __global__ void __launch_bounds__(kStThreads, 4) dit_begin_kernel(sixbit_policy_
   }
 }
 
-__global__ void __launch_bounds__(kStThreads, 4) dit_block_end_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l,
+template <bool MX>
+__global__ void __launch_bounds__(kStThreads, MX ? 3 : 4) dit_block_end_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l,
                                                                    void* scratch, int32_t* err) {
   if (SIXBIT_MODE_OF(B.modes[l]) == SIXBIT_MODE_SKIP) return;  // uniform: a skipped block has no end
   double tot[6];
-  if (block_stats_body<true>(block_input(B, l), block_output(B, l), B.deltas + static_cast<size_t>(l) * B.n, B.n,
-                             scratch, tot)) {  // warp 0 of the last CTA
+  bool last;
+  if constexpr (MX)
+    last = block_stats_mx_body<true>(block_input(B, l), block_output(B, l),
+                                     static_cast<uint8_t*>(B.deltas) + static_cast<size_t>(l) * B.n,
+                                     B.delta_scales + static_cast<size_t>(l) * (B.n >> 5), B.n, scratch, tot);
+  else
+    last = block_stats_body<true>(block_input(B, l), block_output(B, l),
+                                  static_cast<uint16_t*>(B.deltas) + static_cast<size_t>(l) * B.n, B.n, scratch, tot);
+  if (last) {  // warp 0 of the last CTA
     if (threadIdx.x == 0) write_block_stats(&B.stats[l], tot, B.n);
     __syncwarp();
     if (l + 1 < B.L) decide_block(cfg, B, l + 1);
   }
 }
 
+// v = bf16(v + Delta_j) for the k cached deltas of a run, in order (bf16 cache:
+// vector i of each [n] slice; eight / four / one loads in flight)
+__device__ __forceinline__ void skip_run_bf16(uint64_t (&v)[4], const uint16_t* dp, int64_t n, int k) {
+  int j = 0;
+  for (; j + 8 <= k; j += 8) {
+    uint4 r[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) r[u] = ld16(dp + static_cast<size_t>(j + u) * n);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint64_t d[4];
+      unpack4x2(r[u], d);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
+    }
+  }
+  if (j + 4 <= k) {
+    uint4 r[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) r[u] = ld16(dp + static_cast<size_t>(j + u) * n);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      uint64_t d[4];
+      unpack4x2(r[u], d);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
+    }
+    j += 4;
+  }
+  for (; j < k; ++j) {
+    uint64_t d[4];
+    unpack4x2(ld16(dp + static_cast<size_t>(j) * n), d);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
+  }
+}
+
+// The same with an MXFP8 cache: cp = codes of vector i in block l's slice
+// (slices n bytes apart), sp = its scale byte (slices n / 32 bytes apart);
+// eight / four / one deltas in flight
+__device__ __forceinline__ void skip_run_mx(uint64_t (&v)[4], const uint8_t* cp, const uint8_t* sp, int64_t n,
+                                            int k) {
+  const int64_t ns = n >> 5;
+  int j = 0;
+  for (; j + 8 <= k; j += 8) {
+    uint2 c[8];
+    uint32_t sc[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      c[u] = ld8_nc(cp + static_cast<size_t>(j + u) * n);
+      sc[u] = ld_u8_nc(sp + static_cast<size_t>(j + u) * ns);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mx_skip_add(v, c[u], sc[u]);
+  }
+  if (j + 4 <= k) {
+    uint2 c[4];
+    uint32_t sc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      c[u] = ld8_nc(cp + static_cast<size_t>(j + u) * n);
+      sc[u] = ld_u8_nc(sp + static_cast<size_t>(j + u) * ns);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) mx_skip_add(v, c[u], sc[u]);
+    j += 4;
+  }
+  for (; j < k; ++j)
+    mx_skip_add(v, ld8_nc(cp + static_cast<size_t>(j) * n), ld_u8_nc(sp + static_cast<size_t>(j) * ns));
+}
+
+template <bool MX>
 __global__ void __launch_bounds__(kStThreads, 4) dit_skip_run_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B, int l,
                                                                   void* scratch, int32_t* err) {
   const int k = static_cast<int>(B.run_len[l]);
   if (k == 0) return;  // uniform across the grid: block l starts no run
   const uint16_t* __restrict__ x_in = block_input(B, l);
   uint16_t* x_out = block_output(B, l + k - 1);
-  const uint16_t* __restrict__ d0 = B.deltas + static_cast<size_t>(l) * B.n;
   const int64_t n8 = B.n >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
   float mx = 0.f;
@@ -616,39 +903,11 @@ __global__ void __launch_bounds__(kStThreads, 4) dit_skip_run_kernel(sixbit_poli
   for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8; i += stride) {
     uint64_t v[4];
     unpack4x2(ld16(x_in + 8 * i), v);
-    const uint16_t* dp = d0 + 8 * i;
-    int j = 0;
-    for (; j + 8 <= k; j += 8) {  // eight Delta loads in flight, applied in order
-      uint4 r[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) r[u] = ld16(dp + static_cast<size_t>(j + u) * B.n);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        uint64_t d[4];
-        unpack4x2(r[u], d);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
-      }
-    }
-    if (j + 4 <= k) {
-      uint4 r[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) r[u] = ld16(dp + static_cast<size_t>(j + u) * B.n);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint64_t d[4];
-        unpack4x2(r[u], d);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
-      }
-      j += 4;
-    }
-    for (; j < k; ++j) {
-      uint64_t d[4];
-      unpack4x2(ld16(dp + static_cast<size_t>(j) * B.n), d);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) v[q] = f2_from_bf16x2(f2_to_bf16x2(f2_add(v[q], d[q])));
-    }
+    if constexpr (MX)
+      skip_run_mx(v, static_cast<const uint8_t*>(B.deltas) + static_cast<size_t>(l) * B.n + 8 * i,
+                  B.delta_scales + static_cast<size_t>(l) * (B.n >> 5) + (i >> 2), B.n, k);
+    else
+      skip_run_bf16(v, static_cast<const uint16_t*>(B.deltas) + static_cast<size_t>(l) * B.n + 8 * i, B.n, k);
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -742,14 +1001,42 @@ cudaError_t launch_dit_begin(const sixbit_policy_cfg& cfg, const sixbit_dit_bloc
 
 cudaError_t launch_dit_block_end(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, void* scratch,
                                  int32_t* err, cudaStream_t st) {
-  dit_block_end_kernel<<<stats_grid<dit_block_end_kernel>(B.n), kStThreads, 0, st>>>(cfg, B, l, scratch, err);
+  if (B.delta_format == SIXBIT_DELTA_MXFP8)
+    dit_block_end_kernel<true><<<stats_grid<dit_block_end_kernel<true>>(B.n), kStThreads, 0, st>>>(cfg, B, l, scratch,
+                                                                                                  err);
+  else
+    dit_block_end_kernel<false><<<stats_grid<dit_block_end_kernel<false>>(B.n), kStThreads, 0, st>>>(cfg, B, l,
+                                                                                                    scratch, err);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_dit_skip_run(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l, void* scratch,
                                 int32_t* err, cudaStream_t st) {
-  dit_skip_run_kernel<<<stats_grid<dit_skip_run_kernel>(B.n), kStThreads, 0, st>>>(cfg, B, l, scratch, err);
+  if (B.delta_format == SIXBIT_DELTA_MXFP8)
+    dit_skip_run_kernel<true><<<stats_grid<dit_skip_run_kernel<true>>(B.n), kStThreads, 0, st>>>(cfg, B, l, scratch,
+                                                                                                err);
+  else
+    dit_skip_run_kernel<false><<<stats_grid<dit_skip_run_kernel<false>>(B.n), kStThreads, 0, st>>>(cfg, B, l, scratch,
+                                                                                                  err);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_stats_mx(const uint16_t* x_in, const uint16_t* x_out, uint8_t* codes, uint8_t* scales,
+                                  int64_t n, const int32_t* mode_dev, sixbit_stats* stats, void* scratch,
+                                  cudaStream_t st) {
+  block_stats_mx_kernel<<<stats_grid<block_stats_mx_kernel>(n), kStThreads, 0, st>>>(x_in, x_out, codes, scales, n,
+                                                                                      mode_dev, stats, scratch);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_skip_apply_mx(const uint16_t* x_in, const uint8_t* codes, const uint8_t* scales, uint16_t* x_out,
+                                 int64_t n, const int32_t* mode_dev, sixbit_stats* stats, void* scratch,
+                                 cudaStream_t st) {
+  skip_apply_mx_kernel<<<stats_grid<skip_apply_mx_kernel>(n), kStThreads, 0, st>>>(x_in, codes, scales, x_out, n,
+                                                                                    mode_dev, stats, scratch);
   note_launch();
   return cudaGetLastError();
 }

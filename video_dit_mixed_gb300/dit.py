@@ -28,9 +28,11 @@ from . import ops
 
 class DiT:
     def __init__(self, tokens: int, hidden: int, ffn: int, blocks: int, had_block: int, packed, cfg=None,
-                 device="cuda"):
-        """packed: list of (PackedWeights up [ffn, hidden], PackedWeights down [hidden, ffn])."""
+                 device="cuda", delta_format: str = "bf16"):
+        """packed: list of (PackedWeights up [ffn, hidden], PackedWeights down [hidden, ffn]);
+        delta_format: the Delta cache's storage, "bf16" or "mxfp8" (about half the bytes)."""
         assert len(packed) == blocks
+        assert delta_format in ("bf16", "mxfp8")
         dev = torch.device(device)
         self.T, self.H, self.F, self.L, self.b = tokens, hidden, ffn, blocks, had_block
         self.packed = packed
@@ -39,7 +41,12 @@ class DiT:
         self.x_in = torch.zeros((tokens, hidden), dtype=bf, device=dev)
         self.bufs = [torch.zeros((tokens, hidden), dtype=bf, device=dev) for _ in range(2)]
         self.h = torch.zeros((tokens, ffn), dtype=bf, device=dev)
-        self.deltas = torch.zeros((blocks, tokens, hidden), dtype=bf, device=dev)
+        self.delta_format = delta_format
+        if delta_format == "bf16":
+            self.deltas = torch.zeros((blocks, tokens, hidden), dtype=bf, device=dev)
+            self.delta_scales = None
+        else:
+            self.deltas, self.delta_scales = ops.mxfp8_cache(tokens * hidden, dev, blocks)
         self.qa_x = ops.QActTensors(tokens, hidden, dev)
         self.qa_h = ops.QActTensors(tokens, ffn, dev)
         # the W4A8 GEMMs expand their INT4 weights into this (one buffer for both projections)
@@ -57,11 +64,13 @@ class DiT:
 
     def _record(self, conds):
         return ops.dit_blocks(self.state, self.stats, self.modes, self.run_len, self.tstats, self.x_in,
-                              self.bufs[0], self.bufs[1], self.deltas, conds)
+                              self.bufs[0], self.bufs[1], self.deltas, conds, self.delta_scales)
 
     def reset(self):
         """Back to the state before the first denoising step."""
         self.deltas.zero_()
+        if self.delta_scales is not None:
+            self.delta_scales.zero_()
         self.stats.zero_()
         self.state.zero_()
         self.modes.zero_()

@@ -176,6 +176,37 @@ def skip_apply(x_in, delta_cache, x_out, stats: torch.Tensor, scratch: torch.Ten
     return x_out
 
 
+DELTA_BF16, DELTA_MXFP8 = 0, 1
+MX_BLOCK = 32
+
+
+def mxfp8_cache(n: int, device, blocks: int | None = None):
+    """A zeroed MXFP8 Delta cache of n elements (per block when `blocks` is given): (codes, scales) uint8."""
+    assert n % MX_BLOCK == 0
+    lead = () if blocks is None else (blocks,)
+    return (torch.zeros(lead + (n,), dtype=torch.uint8, device=device),
+            torch.zeros(lead + (n // MX_BLOCK,), dtype=torch.uint8, device=device))
+
+
+def block_stats_mxfp8(x_in, x_out, codes, scales, stats: torch.Tensor, scratch: torch.Tensor, mode_dev=None,
+                      stream=None):
+    """sixbit_block_stats_mxfp8: the Delta cache in MXFP8 (codes [n] uint8, scales [n / 32] uint8)."""
+    n = x_in.numel()
+    assert codes.dtype == torch.uint8 and codes.numel() == n and scales.numel() == n // MX_BLOCK
+    check(_lib.sixbit_block_stats_mxfp8(_p(x_in), _p(x_out), _p(codes), _p(scales), n, _p(mode_dev), _p(stats),
+                                        _p(scratch), None, _stream(stream)), "block_stats_mxfp8")
+    return stats
+
+
+def skip_apply_mxfp8(x_in, codes, scales, x_out, stats: torch.Tensor, scratch: torch.Tensor, mode_dev=None,
+                     stream=None):
+    n = x_in.numel()
+    assert codes.dtype == torch.uint8 and codes.numel() == n and scales.numel() == n // MX_BLOCK
+    check(_lib.sixbit_skip_apply_mxfp8(_p(x_in), _p(codes), _p(scales), _p(x_out), n, _p(mode_dev), _p(stats),
+                                       _p(scratch), None, _stream(stream)), "skip_apply_mxfp8")
+    return x_out
+
+
 def policy_cfg(gamma_thr=0.1, cos_thr=0.99, err_cap=0.05, pdr_ratio=30.0, near_rel=1e-6, refresh_bf16=False):
     return PolicyCfg(gamma_thr, cos_thr, err_cap, pdr_ratio, near_rel, int(refresh_bf16), 0)
 
@@ -187,17 +218,28 @@ def policy_step(cfg: PolicyCfg, state: torch.Tensor, last_stats: torch.Tensor, i
     return mode_word
 
 
-def dit_blocks(states, stats, modes, run_len, in_stats0, x0, buf0, buf1, deltas, conds=None) -> DitBlocks:
+def dit_blocks(states, stats, modes, run_len, in_stats0, x0, buf0, buf1, deltas, conds=None,
+               delta_scales=None) -> DitBlocks:
     """The sixbit_dit_blocks record of a stack of residual blocks (device tensors; deltas [L, ...];
-    run_len: int32 [L], zeroed; conds: int64 [L] graph condition handles, or None)."""
+    run_len: int32 [L], zeroed; conds: int64 [L] graph condition handles, or None).  The Delta
+    cache is bf16 (deltas bf16 [L, n]) or, with delta_scales, MXFP8 (deltas uint8 [L, n] E4M3
+    codes, delta_scales uint8 [L, n / 32] E8M0 codes)."""
     L = states.shape[0]
     n = x0.numel()
     assert stats.shape[0] == L and modes.numel() == L and run_len.numel() == L and deltas.shape[0] == L
     assert run_len.dtype == torch.int32 and run_len.is_contiguous() and deltas.numel() == L * n
     assert in_stats0.dtype == torch.float64 and in_stats0.numel() >= 4
     assert conds is None or (conds.dtype == torch.int64 and conds.numel() == L)
+    if delta_scales is None:
+        assert deltas.dtype == torch.bfloat16
+        fmt = DELTA_BF16
+    else:
+        assert deltas.dtype == torch.uint8 and delta_scales.dtype == torch.uint8
+        assert delta_scales.is_contiguous() and delta_scales.numel() == L * (n // MX_BLOCK)
+        fmt = DELTA_MXFP8
     return DitBlocks(_p(states), _p(stats), _p(modes), _p(in_stats0), _p(x0),
-                     (C.c_void_p * 2)(buf0.data_ptr(), buf1.data_ptr()), _p(deltas), _p(run_len), _p(conds), n, L, 0)
+                     (C.c_void_p * 2)(buf0.data_ptr(), buf1.data_ptr()), _p(deltas), _p(delta_scales), _p(run_len),
+                     _p(conds), n, L, fmt)
 
 
 def dit_begin(cfg: PolicyCfg, blocks: DitBlocks, scratch: torch.Tensor, err=None, stream=None):
