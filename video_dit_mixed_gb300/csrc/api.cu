@@ -118,18 +118,19 @@ static bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dtype
   return r == CUDA_SUCCESS;
 }
 
-// int8 [rows, cols] for the W4A8 GEMM's activation codes: box 64 bytes of
-// columns x 128 rows, no swizzle (the converter warps read it row-major),
-// out-of-bounds rows read as zero.
+// int8 [rows, cols] for the W4A8 GEMM's activation codes: box 128 bytes of
+// columns x 128 rows, 128-byte swizzle (16-byte chunk c of row r lands at
+// chunk c ^ (r & 7), so each converter thread's reads of its own row are
+// conflict-free), out-of-bounds rows read as zero.
 static bool make_map_s8(CUtensorMap* m, const int8_t* base, int rows, int cols) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {128, 128};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(base), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -338,7 +339,7 @@ static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, co
     uint16_t* wexp = static_cast<uint16_t*>(workspace);
     CUtensorMap ma, mb;
     if (!make_map_s8(&ma, A->i8_codes, M, K) ||
-        !make_map(&mb, wexp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, N, K, 256))
+        !make_map(&mb, wexp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, N, K, 192))
       return SIXBIT_ECUDA;
     if (launch_w4_expand(W->i4_codes, N, K, wexp, mode_dev, st) != cudaSuccess) return SIXBIT_ECUDA;
     GemmParams q = p;

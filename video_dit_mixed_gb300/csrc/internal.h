@@ -82,8 +82,9 @@ cudaError_t launch_qgemm_nvf4(const CUtensorMap& a, const CUtensorMap& b, const 
 cudaError_t launch_qgemm_bf16(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
                               cudaStream_t st);
 // W4A8: INT4 codes [N, K/2] -> fp16 [N, K] into ws (w4a8_workspace_bytes(N, K)),
-// then the GEMM: a_s8 maps the s8 codes [M, K] (box 64 x 128, no swizzle),
-// w_f16 the expanded weights (box 64 x 256, 128-byte swizzle), y the bf16 output.
+// then the GEMM: a_s8 maps the s8 codes [M, K] (box 128 x 128, 128-byte
+// swizzle), w_f16 the expanded weights (box 64 x 192, 128-byte swizzle), y the
+// bf16 output.
 size_t w4a8_workspace_bytes(int N, int K);
 cudaError_t launch_w4_expand(const uint8_t* codes, int N, int K, uint16_t* ws, const int32_t* mode_dev,
                              cudaStream_t st);

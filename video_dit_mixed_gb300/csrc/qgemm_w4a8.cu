@@ -17,41 +17,52 @@
 // accumulator of a group holds the exact integer sum, and the group's scale is
 // applied afterwards.
 //
-// Operand expansion.  The weights are expanded once per call (w4_expand_kernel:
-// INT4 -> fp16 into a caller-provided workspace of N*K*2 bytes, which stays in
-// L2 for the GEMM that follows).  The activation codes are read by the GEMM
-// itself (TMA, one byte per element) and expanded on chip by two converter
-// warps: with u = q ^ 0x80, the fp16 bit pattern 0x64:u is 1024 + u =
-// 1152 + q, and one fp16 subtraction of 1152 leaves q exactly.  (Expanding the
-// 256-row weight tile on chip as well would repeat that work for every one of
-// the ceil(M/128) output-row tiles and needs about 2.5 bytes of load/store
-// traffic per element, beyond what the SM's shared-memory port has left next
-// to the tensor core's own operand traffic.)
+// Operands.  The weights are expanded once per call (w4_expand_kernel: INT4
+// -> fp16 into a caller-provided workspace of N*K*2 bytes, which stays in L2
+// for the GEMM that follows) and reach the tensor core from shared memory
+// (TMA, 128-byte swizzle).  The activation codes are read by the GEMM itself,
+// one byte per element, and the A operand is held in tensor memory: four
+// converter warps, one per 32-lane quarter, turn each thread's row of a
+// stage's codes into 64 fp16 values (with u = q ^ 0x80, the fp16 bit pattern
+// 0x64:u is 1152 + q, and one fp16 subtraction of 1152 leaves q exactly) and
+// store them into the row's tensor-memory lane (column j holds k = 2j, 2j+1),
+// from where the MMA reads A.  So shared memory carries only the weight tiles
+// (their copies in, the tensor core's reads out), the codes (8 KB a stage)
+// and the group scales; with the A operand in shared memory its writes and
+// the tensor core's reads of it made the shared-memory port, not the tensor
+// core, the limit.
 //
-// A persistent CTA per SM walks 128 x 256 output tiles through a ring of four
-// 64-K stages (fp16 A tile 16 KB, fp16 W tile 32 KB).  The s8 codes of a
-// stage land in the upper half of its A tile; each converter warp reads its
-// rows' codes into registers before it writes their fp16 rows over the region
-// (warp 1, whose rows overwrite every row's codes, starts after warp 0 holds
-// its own).
+// A persistent CTA per SM walks 128 x 192 output tiles in 64-K stages through
+// three rings: fp16 W tiles (six slots of 24 KB in shared memory, TMA), s8
+// codes (six slots of 8 KB in shared memory, TMA with the 64-byte swizzle:
+// chunk c of row r at chunk c ^ ((r >> 1) & 3), so a thread's reads of its own
+// row are conflict-free) and fp16 A tiles (four slots of 32 columns in tensor
+// memory).  The codes run up to six stages ahead of their conversion, so
+// their copies' latency (~2500-3600 cycles under load, measured; they queue
+// behind the weight tiles in the SM's copy engine) is off the refill path.  A
+// stage's MMAs wait for its W slot (bytes landed) and its A slot (four
+// converter warps done) and free both with one commit each.  (Copying the
+// codes per lane with cp.async instead cost the converter warps ~300 cycles a
+// stage in issue stalls, measured.)
 // Warps:
-//   0       TMA producer: the s8 A tile and the fp16 W tile of each stage
+//   0       TMA producer: the fp16 W tile of each stage
 //   1       allocates tensor memory; one lane issues tcgen05.mma and commits
-//   2, 3    converters: s8 -> fp16 A operand, rows 64 c .. 64 c + 63 of a stage
-//   4 - 11  fold + epilogue
-// Warpgroup 0 lowers itself to 72 registers with setmaxnreg and the fold
-// warpgroups raise themselves to 216 (4 x 72 + 8 x 216 = 12 x 168, and per SM
-// sub-partition 72 + 2 x 216 = 3 x 168): a converter's 8 chunks of codes, and
-// a fold thread's 128 running sums with a 32-column accumulator load, fit
-// without spills.
+//   2       TMA producer: the s8 code tile of each stage
+//   3       idle
+//   4 - 7   converters: warp 4 + q copies and converts rows 32 q .. 32 q + 31
+//   8 - 15  fold + epilogue: warp 8 + e reads lanes 32 (e & 3) .. + 31 and
+//           columns 96 (e >> 2) .. + 95 of each accumulator
+// The CTA launches with 128 registers a thread; setmaxnreg gives warpgroup 0
+// 56, the converters 88 and the fold warpgroups 184 (4 x 56 + 4 x 88 + 8 x 184
+// = 16 x 126, and per SM sub-partition 56 + 88 + 2 x 184 = 4 x 128): a fold
+// thread's 96 running sums with a 32-column accumulator load fit.
 //
-// Tensor memory holds two 256-column accumulators; K groups alternate between
-// them and the fold warps add s_w[g][n] * acc_g into registers while the next
-// group accumulates.  The MMA thread waits on one barrier per stage (the
-// weight tile's copy completes on the barrier the converters arrive on: an
-// mbarrier phase needs its arrivals and its transaction bytes) and commits
-// once per stage; a group's completion is the commit after its second stage.
-// Every mbarrier wait is bounded (2 s); on expiry the kernel records
+// Tensor memory: two 192-column accumulators (columns 0 .. 191 and
+// 256 .. 447; K groups alternate between them and the fold warps add
+// s_w[g][n] * acc_g into registers while the next group accumulates) and the
+// four 32-column A slots beside them (192, 224, 448, 480).  A group's
+// completion is the W-slot commit after its second stage.  Every mbarrier
+// wait is bounded (2 s); on expiry the kernel records
 // SIXBIT_ETIMEOUT, raises an abort flag for the other roles, waits (bounded)
 // for its copies and tensor-core work in flight, frees tensor memory and
 // returns.
@@ -65,29 +76,66 @@
 namespace sixbit {
 namespace w4a8 {
 
-constexpr int kBM = 128, kBN = 256, kHalf = 128;
-constexpr int kStages = 4;
-constexpr int kKStage = 64;                          // K elements per stage
-constexpr int kATile = kBM * kKStage * 2;            // fp16 A operand, 16 KB (128-byte swizzle)
-constexpr int kBTile = kBN * kKStage * 2;            // fp16 W operand, 32 KB
-constexpr int kS8Tile = kBM * kKStage;               // s8 A codes, 8 KB (row-major, 64-byte rows)
-constexpr int kS8Off = kATile - kS8Tile;             // ... landing in the A tile's upper half
-constexpr int kStageBytes = kATile + kBTile;
-constexpr int kFoldWarps = 8, kWarp0 = 4, kThreads = 384;
-constexpr int kCols = 64;                            // columns of each half a fold thread folds
-constexpr int kSums = 2 * kCols;                     // running sums per fold thread
+constexpr int kBM = 128, kBN = 192;
+constexpr int kKStage = 128;                         // K elements per stage: one scale group
+constexpr int kStages = 3;                           // W ring (shared memory)
+constexpr int kS8Stages = 3;                         // code ring (shared memory)
+constexpr int kAStages = 2;                          // A ring (tensor memory)
+constexpr int kBHalf = kBN * 64 * 2;                 // fp16 W tile of 64 K (128-byte rows, 128-byte swizzle), 24 KB
+constexpr int kBTile = 2 * kBHalf;                   // a stage's two halves, 48 KB
+constexpr int kS8Slot = kBM * kKStage;               // s8 codes of a stage, 16 KB (128-byte rows, 128-byte swizzle)
+constexpr int kAccStride = 256;                      // tensor-memory columns between the two accumulators
+constexpr int kAColsPerStage = kKStage / 2;          // fp16 pairs of a row's stage
+// A slot a: the 64 columns after accumulator a (192 .. 255 and 448 .. 511)
+__host__ __device__ constexpr int a_slot_col(int a) { return a * kAccStride + kBN; }
+static_assert(kAStages == 2 && kBN + kAColsPerStage <= kAccStride && a_slot_col(1) + kAColsPerStage <= 512,
+              "tensor memory columns");
+constexpr int kConvWarp0 = 4, kFoldWarp0 = 8, kFoldWarps = 8, kThreads = 512;
+constexpr int kCols = kBN / 2;                       // columns (and running sums) per fold thread
 constexpr int kSwRing = 4;                           // groups of scales in flight per fold warp
+constexpr int kSwLanes = kCols / 4;                  // lanes copying a group's scales (16 bytes each)
 constexpr int kBoxBytes = 32 * 64;                   // one 32 x 32 bf16 output box
-constexpr int kRegsLaunch = 168, kRegsLow = 72, kRegsHigh = 216;
-static_assert(4 * kRegsLow + 8 * kRegsHigh <= 12 * kRegsLaunch && kRegsLow + 2 * kRegsHigh <= 3 * kRegsLaunch,
+constexpr int kWarpArea = 2048;                      // a fold warp's scale ring, or its output box
+static_assert(kSwRing * kCols * 4 <= kWarpArea && kBoxBytes <= kWarpArea, "fold warp area");
+constexpr int kRegsLaunch = 128, kRegsLow = 56, kRegsConv = 88, kRegsHigh = 184;
+static_assert(4 * kRegsLow + 4 * kRegsConv + 8 * kRegsHigh <= 16 * kRegsLaunch &&
+                  kRegsLow + kRegsConv + 2 * kRegsHigh <= 4 * kRegsLaunch,
               "the register split must fit in what the CTA is launched with");
 constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>(kBM >> 4) << 24);  // f16 x f16 -> f32, M 128, N 256, K-major
+                            (static_cast<uint32_t>(kBM >> 4) << 24);  // f16 x f16 -> f32, M 128, N 192, K-major
 
-// [stages | output boxes | barriers (256 B) | per-warp rings of group scales]
-constexpr int kSmemBytes = kStages * kStageBytes + kFoldWarps * kBoxBytes + 1024 + 256 +
-                           kSwRing * kFoldWarps * kSums * 4;
+// [W ring | code ring | fold warp areas | barriers].  A fold warp's
+// output box is its scale ring: the ring is idle from the end of a tile's
+// last group until the next tile's first scale copies, which wait for the
+// box's last store to have been read out.
+constexpr int kBarBytes = 512;
+constexpr int kSmemBytes = kStages * kBTile + kS8Stages * kS8Slot + kFoldWarps * kWarpArea + 1024 + kBarBytes;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, fp16 inputs, fp32 accumulate (kind::f16).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Each thread of the warp writes 32 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // fp16 pair (1152 + a, 1152 + b) -> (a, b): exact (both sides integers below 2048)
 __device__ __forceinline__ uint32_t hsub1152(uint32_t x) {
@@ -96,17 +144,14 @@ __device__ __forceinline__ uint32_t hsub1152(uint32_t x) {
   return d;
 }
 
-// 16 s8 codes -> 16 fp16 values (two 16-byte chunks, element order kept).
-__device__ __forceinline__ void s8x16_to_f16(const uint4& in, uint4& lo, uint4& hi) {
+// 16 s8 codes -> 8 fp16 pairs (element order kept: pair i holds codes 2i, 2i + 1).
+__device__ __forceinline__ void s8x16_to_f16x8(const uint4& in, uint32_t* o) {
   const uint32_t w[4] = {in.x ^ 0x80808080u, in.y ^ 0x80808080u, in.z ^ 0x80808080u, in.w ^ 0x80808080u};
-  uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     o[2 * i] = hsub1152(__byte_perm(w[i], 0x64646464u, 0x4140));      // bytes 0, 1 -> 0x64:b0, 0x64:b1
     o[2 * i + 1] = hsub1152(__byte_perm(w[i], 0x64646464u, 0x4342));  // bytes 2, 3
   }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 template <bool DBG>
@@ -118,24 +163,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint8_t* boxes = smem + S * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(boxes + kFoldWarps * kBoxBytes);
-  uint64_t* s8_full = bars + S;     // [S] s8 A tile landed
-  // [S] the stage is ready: the W tile's bytes landed (the producer's
-  // expect-tx arrival) and both converter warps wrote the fp16 A tile
-  uint64_t* op_full = bars + 2 * S;
-  uint64_t* empty = bars + 3 * S;   // [S] the stage's MMAs are done
-  uint64_t* read0 = bars + 4 * S;   // [S] converter warp 0 holds its s8 codes
-  uint64_t* afree = bars + 5 * S;   // [2] accumulator read back (eight fold warps)
+  uint8_t* s8_ring = smem + S * kBTile;
+  uint8_t* fold_area = s8_ring + kS8Stages * kS8Slot;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(fold_area + kFoldWarps * kWarpArea);
+  uint64_t* w_full = bars;                    // [S] W tile landed (the producer's expect-tx arrival + bytes)
+  uint64_t* w_empty = bars + S;               // [S] the stage's MMAs are done with the W slot
+  uint64_t* a_full = bars + 2 * S;            // [kAStages] the four converter warps stored the A tile
+  uint64_t* a_empty = a_full + kAStages;      // [kAStages] the stage's MMAs are done with the A slot
+  uint64_t* c_full = a_empty + kAStages;      // [kS8Stages] code tile landed
+  uint64_t* c_empty = c_full + kS8Stages;     // [kS8Stages] the four converter warps read the code tile
+  uint64_t* afree = c_empty + kS8Stages;      // [2] accumulator read back (eight fold warps)
   uint64_t* drain = afree + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  static_assert((5 * kStages + 3) * 8 + 8 <= 256, "barrier area");
-  float* sw_smem = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);
+  static_assert((2 * kStages + 2 * kAStages + 2 * kS8Stages + 3) * 8 + 8 <= kBarBytes, "barrier area");
 
-  auto A_op = [&](int s) { return smem + s * kStageBytes; };
-  auto W_op = [&](int s) { return smem + s * kStageBytes + kATile; };
-  auto A_s8 = [&](int s) { return smem + s * kStageBytes + kS8Off; };
+  auto W_op = [&](int s) { return smem + s * kBTile; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_m = (p.M + kBM - 1) / kBM, tiles_n = (p.N + kBN - 1) / kBN;
@@ -154,10 +197,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&s8_full[s], 1);
-      mbar_init(&op_full[s], 3);
-      mbar_init(&empty[s], 1);
-      mbar_init(&read0[s], 1);
+      mbar_init(&w_full[s], 1);
+      mbar_init(&w_empty[s], 1);
+    }
+    for (int a = 0; a < kAStages; ++a) {
+      mbar_init(&a_full[a], 4);
+      mbar_init(&a_empty[a], 1);
+    }
+    for (int c = 0; c < kS8Stages; ++c) {
+      mbar_init(&c_full[c], 1);
+      mbar_init(&c_empty[c], 4);
     }
     for (int b = 0; b < 2; ++b) mbar_init(&afree[b], kFoldWarps);
     mbar_init(drain, 1);
@@ -178,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < kWarp0) {
+  if (warp < kConvWarp0) {
     setmaxnreg_dec<kRegsLow>();  // the whole warpgroup, one instruction
     if (warp == 0) {
       if (lane == 0) {
@@ -190,55 +239,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           tile_of(t, m_tile, n_tile);
           for (int kb = 0; kb < nk; ++kb, ++it) {
             const int s = it % S;
-            if (it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1, abort_flag, p.wait_ns)) {
+            if (it >= S && !mbar_wait(&w_empty[s], ((it / S) - 1) & 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
             if (p.withhold_first && it == 0) continue;  // failure-path test: stage 0 never lands
-            mbar_expect_tx(&op_full[s], kBTile);
-            tma_load_2d(W_op(s), &tmW, &op_full[s], kb * kKStage, n_tile * kBN);
-            mbar_expect_tx(&s8_full[s], kS8Tile);
-            tma_load_2d(A_s8(s), &tmA, &s8_full[s], kb * kKStage, m_tile * kBM);
+            mbar_expect_tx(&w_full[s], kBTile);
+            tma_load_2d(W_op(s), &tmW, &w_full[s], kb * kKStage, n_tile * kBN);
+            tma_load_2d(W_op(s) + kBHalf, &tmW, &w_full[s], kb * kKStage + 64, n_tile * kBN);
           }
         }
         if (!ok) {
           set_error(p.err, SIXBIT_ETIMEOUT);
           *abort_flag = 1;
         }
-        // every copy this CTA started lands before it can exit
-        for (uint32_t j = (it > S ? it - S : 0); j < it; ++j) {
-          (void)mbar_wait(&op_full[j % S], (j / S) & 1, nullptr, p.wait_ns);
-          (void)mbar_wait(&s8_full[j % S], (j / S) & 1, nullptr, p.wait_ns);
-        }
+        // every copy this warp started lands before it can exit
+        for (uint32_t j = (it > S ? it - S : 0); j < it; ++j)
+          (void)mbar_wait(&w_full[j % S], (j / S) & 1, nullptr, p.wait_ns);
       }
     } else if (warp == 1) {
       if (lane == 0) {
         // -------------------------------------------------------- MMA issuer --
-        // Stage counter it and K-group counter gi run across tiles; group gi
-        // is stages 2 gi and 2 gi + 1 and accumulates into buffer gi & 1.
-        uint32_t it = 0, gi = 0;
+        // Stage (= K group) counter gi runs across tiles; group gi
+        // accumulates into buffer gi & 1 and uses A slot gi & 1.
+        uint32_t gi = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-          for (int g = 0; g < groups && ok; ++g, ++gi) {
-            if (gi >= 2 && !mbar_wait(&afree[gi & 1], ((gi >> 1) - 1) & 1, abort_flag, p.wait_ns)) {
+          for (int g = 0; g < groups; ++g, ++gi) {
+            const int s = gi % S, a = gi % kAStages;
+            if ((gi >= 2 && !mbar_wait(&afree[gi & 1], ((gi >> 1) - 1) & 1, abort_flag, p.wait_ns)) ||
+                !mbar_wait(&w_full[s], (gi / S) & 1, abort_flag, p.wait_ns) ||
+                !mbar_wait(&a_full[a], (gi / kAStages) & 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
-            const uint32_t d_tmem = tmem + (gi & 1) * kBN;
-            for (int ss = 0; ss < 2; ++ss, ++it) {
-              const int s = it % S;
-              if (!mbar_wait(&op_full[s], (it / S) & 1, abort_flag, p.wait_ns)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t a_base = smem_u32(A_op(s)), b_base = smem_u32(W_op(s));
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + (gi & 1) * kAccStride;
+            const uint32_t a_tmem = tmem + a_slot_col(a), b_base = smem_u32(W_op(s));
 #pragma unroll
-              for (int k = 0; k < kKStage / 16; ++k)
-                mma_bf16(d_tmem, sdesc_sw128(a_base + 32 * k), sdesc_sw128(b_base + 32 * k), kIdesc,
-                         (ss == 0 && k == 0) ? 0u : 1u);
-              tc_commit(&empty[s]);  // frees the stage; after a group's second stage, also its completion
-            }
+            for (int k = 0; k < kKStage / 16; ++k)  // k < 4 from the first 64-K half of the W tile, then the second
+              mma_f16_tmem_a(d_tmem, a_tmem + 8 * k, sdesc_sw128(b_base + (k >> 2) * kBHalf + 32 * (k & 3)), kIdesc,
+                             k == 0 ? 0u : 1u);
+            tc_commit(&a_empty[a]);
+            tc_commit(&w_empty[s]);  // frees the W slot; also the group's completion
           }
         }
         if (!ok) {
@@ -248,83 +291,126 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(drain);  // all tensor-core work issued here completes before exit
         (void)mbar_wait(drain, 0, nullptr, p.wait_ns);
       }
-    } else {
-      // ------------------------------------------------------------ converters --
-      // Warp c converts rows 64 c .. 64 c + 63.  Each lane first loads its 8
-      // chunks (rows 64 c + 8 i + lane / 4, 16 bytes at column 16 (lane % 4):
-      // every load of the warp reads 512 contiguous bytes); then each chunk
-      // becomes two fp16 chunks of the 128-byte-swizzled operand (16-byte
-      // chunk j of row r at j ^ (r & 7)).  The fp16 rows 0 .. 63 lie below the
-      // s8 codes, but rows 64 .. 127 overwrite the codes of every row, so warp
-      // 1 starts only once warp 0 holds its codes (read0, a bounded wait);
-      // nothing but warp 1 itself overwrites warp 1's codes.
-      const int c = warp - 2;
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % S;
-          if (!mbar_wait(&s8_full[s], (it / S) & 1, abort_flag, p.wait_ns)) {
-            ok = false;
-            break;
+    } else if (warp == 2) {
+      if (lane == 0) {
+        // ----------------------------------------------------- code producer --
+        uint32_t j = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+          int m_tile, n_tile;
+          tile_of(t, m_tile, n_tile);
+          for (int kb = 0; kb < nk; ++kb, ++j) {
+            const int c = j % kS8Stages;
+            if (j >= kS8Stages && !mbar_wait(&c_empty[c], ((j / kS8Stages) - 1) & 1, abort_flag, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&c_full[c], kS8Slot);
+            tma_load_2d(s8_ring + c * kS8Slot, &tmA, &c_full[c], kb * kKStage, m_tile * kBM);
           }
-          if (c == 1 && !mbar_wait(&read0[s], (it / S) & 1, abort_flag, p.wait_ns)) {
-            ok = false;
-            break;
-          }
-          const uint8_t* src = A_s8(s);
-          uint8_t* dst = A_op(s);
-          const int j = lane & 3;
-          uint4 in[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) in[i] = *reinterpret_cast<const uint4*>(src + (64 * c + 8 * i + (lane >> 2)) * 64 + j * 16);
-          __syncwarp();
-          if (c == 0 && lane == 0) mbar_arrive(&read0[s]);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = 64 * c + 8 * i + (lane >> 2);
-            uint4 lo, hi;
-            s8x16_to_f16(in[i], lo, hi);
-            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * j) ^ (r & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
-          }
-          fence_proxy_async_smem();  // the tensor core reads these through the async proxy
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&op_full[s]);
         }
+        if (!ok) {
+          set_error(p.err, SIXBIT_ETIMEOUT);
+          *abort_flag = 1;
+        }
+        // every copy this warp started lands before it can exit
+        for (uint32_t jj = (j > kS8Stages ? j - kS8Stages : 0); jj < j; ++jj)
+          (void)mbar_wait(&c_full[jj % kS8Stages], (jj / kS8Stages) & 1, nullptr, p.wait_ns);
       }
-      if (!ok && lane == 0) {
-        set_error(p.err, SIXBIT_ETIMEOUT);
-        *abort_flag = 1;
+    }
+  } else if (warp < kFoldWarp0) {
+    setmaxnreg_dec<kRegsConv>();
+    // ------------------------------------------------------------ converters --
+    // Warp 4 + q converts rows 32 q .. 32 q + 31 of every stage; thread
+    // `lane` converts row 32 q + lane, the row of its tensor-memory lane.
+    // Per stage: wait for the code tile, read the row's eight chunks, release
+    // the slot, wait for the A slot, convert and store 64 columns (two halves
+    // of 32, through one set of registers), arrive.  The
+    // release comes after every lane's reads have returned (each lane's value
+    // of `zero` needs them) and each lane's proxy fence: the refill is an
+    // async-proxy write after these generic-proxy reads, and without the
+    // fence such refills overwrote codes still being read (measured: wrong
+    // group sums in every stage whose slot was refilled).
+    const int q = warp & 3;
+    const int myrow = 32 * q + lane;
+    const uint32_t rd_off = static_cast<uint32_t>(myrow * 128);
+    const int swz = myrow & 7;  // 128-byte swizzle: chunk c of row r at chunk c ^ (r & 7)
+    uint32_t it = 0;
+    int r_slot = 0;  // code ring slot of stage it
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int a = it % kAStages;
+        if (!mbar_wait(&c_full[r_slot], (it / kS8Stages) & 1, abort_flag, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* row = s8_ring + r_slot * kS8Slot + rd_off;
+        uint4 in[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) in[c] = *reinterpret_cast<const uint4*>(row + ((c ^ swz) << 4));
+        uint32_t zero;
+        asm volatile("and.b32 %0, %1, 0;"
+                     : "=r"(zero)
+                     : "r"(in[0].x ^ in[1].x ^ in[2].x ^ in[3].x ^ in[4].x ^ in[5].x ^ in[6].x ^ in[7].x));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c_empty[r_slot]);
+        r_slot = r_slot + 1 == kS8Stages ? 0 : r_slot + 1;
+        if (it >= kAStages && !mbar_wait(&a_empty[a], ((it / kAStages) - 1) & 1, abort_flag, p.wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acol = tmem + (static_cast<uint32_t>(32 * q) << 16) + a_slot_col(a);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) s8x16_to_f16x8(in[4 * h + c], v + 8 * c);
+          tmem_st32(acol + 32 * h, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[a]);
       }
+    }
+    if (!ok && lane == 0) {
+      set_error(p.err, SIXBIT_ETIMEOUT);
+      *abort_flag = 1;
     }
   } else {
     setmaxnreg_inc<kRegsHigh>();  // each fold warpgroup, one instruction
     // -------------------------------------------------------- fold + epilogue --
-    const int ew = warp - kWarp0;          // 0 .. 7
+    const int ew = warp - kFoldWarp0;      // 0 .. 7
     const int q = warp & 3;                // tensor-memory lane quarter this warp may read
-    const int cs = (ew >> 2) * kCols;      // first column of this thread within each half
+    const int cs = (ew >> 2) * kCols;      // first column of this thread within the tile
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16) + cs;
-    float* my_sw = sw_smem + ew * kSwRing * kSums;  // [slot][half][64]
-    uint8_t* my_box = boxes + ew * kBoxBytes;
+    float* my_sw = reinterpret_cast<float*>(fold_area + ew * kWarpArea);  // [slot][96]
+    uint8_t* my_box = fold_area + ew * kWarpArea;                          // the same bytes
     uint32_t gi = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       int m_tile, n_tile;
       tile_of(t, m_tile, n_tile);
       const int row = m_tile * kBM + 32 * q + lane;
-      const int n0 = n_tile * kBN + cs;    // output column of sum[0]; sum[64 + j] is column n0 + 128 + j
-      float sum[kSums];
+      const int n0 = n_tile * kBN + cs;    // output column of sum[0]
+      float sum[kCols];
 #pragma unroll
-      for (int j = 0; j < kSums; ++j) sum[j] = 0.f;
-      // s_w[g][n0 .. n0 + 64) and s_w[g][n0 + 128 .. + 64): lanes 0-15 copy the
-      // first, 16-31 the second, 16 bytes each; group g goes to slot g % kSwRing.
+      for (int j = 0; j < kCols; ++j) sum[j] = 0.f;
+      // s_w[g][n0 .. n0 + 96): lanes 0 .. 23 copy 16 bytes each; group g goes
+      // to slot g % kSwRing.
       auto fetch_sw = [&](int g) {
-        const int n = n0 + (lane >> 4) * kHalf + 4 * (lane & 15);
-        const bool v = g < groups && n < p.N;
-        cp_async16(smem_u32(my_sw + (g % kSwRing) * kSums + 4 * lane),
-                   v ? p.grp_scale + static_cast<size_t>(g) * p.N + n : p.grp_scale, v);
+        if (lane < kSwLanes) {
+          const int n = n0 + 4 * lane;
+          const bool v = g < groups && n < p.N;
+          cp_async16(smem_u32(my_sw + (g % kSwRing) * kCols + 4 * lane),
+                     v ? p.grp_scale + static_cast<size_t>(g) * p.N + n : p.grp_scale, v);
+        }
       };
+      if (lane == 0) bulk_wait_read0();  // the ring doubled as the last tile's output box
+      __syncwarp();
 #pragma unroll
       for (int g = 0; g < kSwRing - 1; ++g) fetch_sw(g);
       for (int g = 0; g < groups; ++g, ++gi) {
@@ -332,35 +418,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         fetch_sw(g + kSwRing - 1);             // ... which now receives group g + kSwRing - 1
         cp_async_wait_newest<kSwRing - 1>();   // this lane's copy of group g has landed
         __syncwarp();                          // and every other lane's
-        const float4* sw4 = reinterpret_cast<const float4*>(my_sw + (g % kSwRing) * kSums);
-        // group gi is complete when the commit after its second stage (stage
-        // counter 2 gi + 1) arrives on that stage's barrier; that barrier cannot
-        // run a phase past this wait, since its next phase needs group gi + 2,
-        // which needs this accumulator back
-        const uint32_t last = 2 * gi + 1;
-        if (!mbar_wait(&empty[last % S], (last / S) & 1, abort_flag, p.wait_ns)) {
+        const float4* sw4 = reinterpret_cast<const float4*>(my_sw + (g % kSwRing) * kCols);
+        // group gi is complete when its commit arrives on its stage's W-slot
+        // barrier; that barrier cannot run a phase past this wait, since its
+        // next phase is group gi + 3, which needs buffer (gi + 1) & 1 back
+        if (!mbar_wait(&w_empty[gi % S], (gi / S) & 1, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t acc_addr = lane_addr + (gi & 1) * kBN;
+        const uint32_t acc_addr = lane_addr + (gi & 1) * kAccStride;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {            // 32-column loads: columns cs + 32 (c & 1) of half c >> 1
-          const int h = c >> 1, hc = c & 1;
+        for (int c = 0; c < kCols / 32; ++c) {
           uint32_t r[32];
-          tmem_ld32(acc_addr + h * kHalf + 32 * hc, r);
+          tmem_ld32(acc_addr + 32 * c, r);
           tmem_ld_wait(r);
-          if (c == 3) release_acc(&afree[gi & 1], lane);  // the accumulator is free once read back
+          if (c == kCols / 32 - 1) release_acc(&afree[gi & 1], lane);  // free once read back
           if (DBG && row < p.M) {
             for (int j = 0; j < 32; ++j) {
-              const int n = n0 + h * kHalf + 32 * hc + j;
+              const int n = n0 + 32 * c + j;
               if (n < p.N) p.acc_dbg[(static_cast<size_t>(g) * p.M + row) * p.N + n] = __float2int_rn(__uint_as_float(r[j]));
             }
           }
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 s4 = sw4[h * (kCols / 4) + hc * 8 + j4];
-            float* sm = sum + h * kCols + 32 * hc + 4 * j4;
+            const float4 s4 = sw4[c * 8 + j4];
+            float* sm = sum + 32 * c + 4 * j4;
             sm[0] = fmaf(s4.x, __uint_as_float(r[4 * j4]), sm[0]);
             sm[1] = fmaf(s4.y, __uint_as_float(r[4 * j4 + 1]), sm[1]);
             sm[2] = fmaf(s4.z, __uint_as_float(r[4 * j4 + 2]), sm[2]);
@@ -374,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const float sm = (row < p.M) ? p.row_scale[row] : 0.f;
 #pragma unroll
-      for (int c = 0; c < kSums / 32; ++c) {
-        const int n = n0 + (c >> 1) * kHalf + (c & 1) * 32;  // warp-uniform
+      for (int c = 0; c < kCols / 32; ++c) {
+        const int n = n0 + 32 * c;  // warp-uniform
         if (n >= p.N) continue;
         float v[32];
 #pragma unroll
@@ -472,7 +555,7 @@ static cudaError_t launch_w4a8(const CUtensorMap& a_s8, const CUtensorMap& w_f16
   if (e != cudaSuccess) return e;
   // setmaxnreg.inc waits until the block's own registers cover the increase:
   // launch only with the register count the split was sized for.
-  if (regs < kRegsLaunch || 4 * kRegsLow + 8 * kRegsHigh > 12 * regs) return cudaErrorInvalidConfiguration;
+  if (regs < kRegsLaunch || 4 * (kRegsLow + kRegsConv) + 8 * kRegsHigh > 16 * regs) return cudaErrorInvalidConfiguration;
   const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
   const int sms = sm_count();
   const int grid = ntiles < sms ? ntiles : sms;
