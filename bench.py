@@ -718,7 +718,8 @@ def metric_parts(torch, ops, dev, peaks):
     stream = torch.cuda.current_stream()
 
     def laplace(m, k):
-        u = torch.rand((m, k), generator=gen, device=dev) - 0.5
+        # u strictly inside (-1/2, 1/2): rand can return 0, and u = -1/2 would give log1p(-1) = -inf
+        u = (torch.rand((m, k), generator=gen, device=dev) - 0.5).clamp(-0.5 + 2.0 ** -24, 0.5 - 2.0 ** -24)
         x = -torch.sign(u) * torch.log1p(-2 * u.abs())
         idx = torch.randperm(k, generator=gen, device=dev)[: max(1, round(0.005 * k))]
         x[:, idx] *= 50.0
