@@ -8,6 +8,11 @@ statistics (Gamma, delta cosine, the next block's input outlier ratio) feed
 the next decision.  The GEMM outputs are the float64 references rounded to
 FP32 and then to bf16, as a bf16 activation tensor is stored.
 
+Per-depth thresholds: `cfg` may be one PolicyConfig for every block or a
+list with one per block (the finding that blocks at different depths differ
+in temporal stability, popular summary section 5, read as: each block may
+carry its own thresholds under the same rules).
+
 The delta cache is kept in bf16, or (delta_format="mxfp8") in MXFP8: the
 fresh bf16 delta is used as it is by the block statistics and then encoded;
 the previous delta enters the statistics, and a skip, dequantized.
@@ -51,9 +56,13 @@ class OracleDiT:
             raise ValueError(delta_format)
         self.b = had_block
         self.delta_format = delta_format
-        self.cfg = cfg or policy.PolicyConfig()
-        self.packs = [(quant.pack_weights(wu, had_block), quant.pack_weights(wd, had_block)) for wu, wd in weights]
         self.L = len(weights)
+        cfg = cfg or policy.PolicyConfig()
+        self.cfgs = list(cfg) if isinstance(cfg, (list, tuple)) else [cfg] * self.L
+        if len(self.cfgs) != self.L:
+            raise ValueError("one policy configuration per block")
+        self.cfg = self.cfgs[0]
+        self.packs = [(quant.pack_weights(wu, had_block), quant.pack_weights(wd, had_block)) for wu, wd in weights]
         self.states = [policy.PolicyState() for _ in range(self.L)]
         self.deltas = [None] * self.L
         self.trace = []          # per step: list of Decision per block
@@ -64,7 +73,7 @@ class OracleDiT:
         decisions = []
         for l in range(self.L):
             st = self.states[l]
-            d = policy.decide(st, ratio, self.cfg)
+            d = policy.decide(st, ratio, self.cfgs[l])
             decisions.append(d)
             if self.deltas[l] is None:
                 self.store_delta(l, np.zeros_like(x))

@@ -69,3 +69,37 @@ def test_gelu_sits_between_the_projections():
     x = np.where((np.arange(m * h).reshape(m, h) % 3) == 0, -2.0, 2.0).astype(np.float32)
     y = OracleDiT([(4.0 * eye, -0.5 * eye)], 64, cfg).step(x)
     np.testing.assert_array_equal(y, np.full_like(x, -2.0))
+
+
+def test_per_depth_thresholds_closed_form():
+    """Per-block thresholds (one PolicyConfig per block).  Zero weights keep
+    every Delta zero, so Gamma = 0 and cos = 1 at every block: a block whose
+    gamma_thr is 0 computes INT8 (Gamma >= 0) where the others take NVFP4,
+    and a block whose cos_thr is above 1 never skips."""
+    m, h, f, L = 8, 128, 256, 3
+    w = [(np.zeros((f, h), np.float32), np.zeros((h, f), np.float32)) for _ in range(L)]
+    base = policy.PolicyConfig()
+    cfgs = [base, policy.PolicyConfig(cos_thr=1.5), policy.PolicyConfig(gamma_thr=0.0)]
+    dit = OracleDiT(w, 64, cfgs)
+    x = _x(m, h)
+    for _ in range(5):
+        y = dit.step(x)
+        assert np.array_equal(y.view(np.uint32), x.view(np.uint32))
+    modes = [[d.mode for d in step] for step in dit.trace]
+    assert modes[0] == [policy.INT8] * L
+    assert modes[1] == [policy.NVFP4, policy.NVFP4, policy.INT8]
+    for s in modes[2:]:
+        assert s == [policy.SKIP, policy.NVFP4, policy.SKIP]
+
+
+def test_per_depth_list_of_equal_configs_equals_one_config():
+    rng = np.random.default_rng(4)
+    m, h, f, L = 4, 128, 256, 3
+    w = [((rng.normal(size=(f, h)) * 0.02).astype(np.float32), (rng.normal(size=(h, f)) * 0.02).astype(np.float32))
+         for _ in range(L)]
+    cfg = policy.PolicyConfig(pdr_ratio=1e9)
+    a, b = OracleDiT(w, 64, cfg), OracleDiT(w, 64, [cfg] * L)
+    x = _x(m, h, seed=9)
+    for _ in range(4):
+        np.testing.assert_array_equal(a.step(x), b.step(x))
+    assert [[d.mode for d in s] for s in a.trace] == [[d.mode for d in s] for s in b.trace]

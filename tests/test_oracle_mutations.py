@@ -193,3 +193,13 @@ def test_mxfp8_mutations_are_caught(monkeypatch):
     assert _fails(tm.test_dit_mxfp8_cache_cosine_and_skip_closed_forms)                # cache kept in bf16
     monkeypatch.undo()
     assert orig_dec is formats.mxfp8_decode
+
+
+def test_per_depth_threshold_mutation_is_caught(monkeypatch):
+    orig = dit.OracleDiT.__init__
+
+    def first_config_everywhere(self, weights, had_block, cfg=None, delta_format="bf16"):
+        orig(self, weights, had_block, cfg, delta_format)
+        self.cfgs = [self.cfgs[0]] * self.L      # per-block thresholds ignored
+    monkeypatch.setattr(dit.OracleDiT, "__init__", first_config_everywhere)
+    assert _fails(td.test_per_depth_thresholds_closed_form)
