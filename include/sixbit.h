@@ -284,6 +284,11 @@ sixbit_status sixbit_policy_step(const sixbit_policy_cfg* cfg, sixbit_policy_sta
  *   delta_scales NULL for a bf16 cache
  *   conds       NULL, or [L] conditional handles (sixbit_graph_cond_create)
  *               of the per-block switches of a captured graph
+ *   block_cfg   NULL, or [L] per-block thresholds (DEVICE memory): block l
+ *               decides with block_cfg[l] instead of the call's cfg.  The
+ *               popular summary (section 5) finds that blocks at different
+ *               depths differ in temporal stability; per-depth thresholds
+ *               are the configuration that finding calls for.
  * n % 8 == 0 (n % 32 == 0 for MXFP8); 16-byte aligned tensors.
  */
 typedef struct {
@@ -297,6 +302,7 @@ typedef struct {
   uint8_t* delta_scales;
   uint32_t* run_len;
   const uint64_t* conds;
+  const sixbit_policy_cfg* block_cfg;
   int64_t n;
   int32_t L;
   int32_t delta_format;

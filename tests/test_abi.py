@@ -101,7 +101,7 @@ def test_struct_sizes_match_header():
     from video_dit_mixed_gb300 import abi
     assert C.sizeof(abi.QAct) == 56 and C.sizeof(abi.Weights) == 56
     assert C.sizeof(abi.Stats) == 64 and C.sizeof(abi.PolicyCfg) == 48
-    assert C.sizeof(abi.PolicyState) == 80 and C.sizeof(abi.DitBlocks) == 104
+    assert C.sizeof(abi.PolicyState) == 80 and C.sizeof(abi.DitBlocks) == 112
 
 
 def test_struct_layouts_match_the_c_compiler(tmp_path):

@@ -37,11 +37,14 @@ def _margin(st, ratio, cfg):
     return min(m)
 
 
-def _run_gpu(name, graph, switched=True, host_dispatch=False, delta_format="bf16"):
+def _run_gpu(name, graph, switched=True, host_dispatch=False, delta_format="bf16", cfgs=None):
     from video_dit_mixed_gb300 import dit, ops
     c = synthgen.DIT_CONFIGS[name]
     packed = dit.pack_block_weights(synthgen.dit_weights(name), c["had_block"])
-    model = dit.DiT(c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"], packed,
+    gpu_cfg = None if cfgs is None else [ops.policy_cfg(gamma_thr=k.gamma_thr, cos_thr=k.cos_thr, err_cap=k.err_cap,
+                                                        pdr_ratio=k.pdr_ratio, refresh_bf16=k.refresh_bf16)
+                                         for k in cfgs]
+    model = dit.DiT(c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"], packed, cfg=gpu_cfg,
                     delta_format=delta_format)
     xs = [torch.from_numpy(x).to(torch.bfloat16).cuda() for x in synthgen.dit_trajectory(name)]
     outs, words = [], []
@@ -55,13 +58,19 @@ def _run_gpu(name, graph, switched=True, host_dispatch=False, delta_format="bf16
     return outs, words, model
 
 
-@pytest.mark.parametrize("delta_format", ["bf16", "mxfp8"])
-def test_tiny_dit_against_oracle_chain(delta_format):
+# per-depth thresholds: every block its own (the run must still take every branch)
+DEPTH_CFGS = [policy.PolicyConfig(), policy.PolicyConfig(cos_thr=0.995, gamma_thr=0.08),
+              policy.PolicyConfig(err_cap=0.03, gamma_thr=0.12), policy.PolicyConfig(cos_thr=0.985, pdr_ratio=28.0)]
+
+
+@pytest.mark.parametrize("delta_format,depth", [("bf16", False), ("mxfp8", False), ("bf16", True)])
+def test_tiny_dit_against_oracle_chain(delta_format, depth):
     name = "dit_tiny"
     c = synthgen.DIT_CONFIGS[name]
-    outs, words, _ = _run_gpu(name, graph=False, delta_format=delta_format)
+    cfgs = DEPTH_CFGS if depth else None
+    outs, words, _ = _run_gpu(name, graph=False, delta_format=delta_format, cfgs=cfgs)
     cfg = policy.PolicyConfig()
-    ref = OracleDiT(synthgen.dit_weights(name), c["had_block"], cfg, delta_format=delta_format)
+    ref = OracleDiT(synthgen.dit_weights(name), c["had_block"], cfgs or cfg, delta_format=delta_format)
     # record the oracle's distance to its thresholds at every decision
     margins = []
     orig = policy.decide
@@ -97,10 +106,12 @@ def test_tiny_dit_against_oracle_chain(delta_format):
         odit.policy.decide = orig
 
 
-@pytest.mark.parametrize("switched,delta_format", [(False, "bf16"), (True, "bf16"), (True, "mxfp8")])
-def test_graph_replay_matches_eager(switched, delta_format):
-    o_eager, w_eager, _ = _run_gpu("dit_tiny", graph=False, delta_format=delta_format)
-    o_graph, w_graph, m = _run_gpu("dit_tiny", graph=True, switched=switched, delta_format=delta_format)
+@pytest.mark.parametrize("switched,delta_format,depth", [(False, "bf16", False), (True, "bf16", False),
+                                                          (True, "mxfp8", False), (True, "bf16", True)])
+def test_graph_replay_matches_eager(switched, delta_format, depth):
+    cfgs = DEPTH_CFGS if depth else None
+    o_eager, w_eager, _ = _run_gpu("dit_tiny", graph=False, delta_format=delta_format, cfgs=cfgs)
+    o_graph, w_graph, m = _run_gpu("dit_tiny", graph=True, switched=switched, delta_format=delta_format, cfgs=cfgs)
     assert m.graph is not None
     for a, b in zip(w_eager, w_graph):
         np.testing.assert_array_equal(a, b)

@@ -46,7 +46,7 @@ class PolicyState(C.Structure):
 class DitBlocks(C.Structure):
     _fields_ = [("states", c_p), ("stats", c_p), ("modes", c_p), ("in_stats0", c_p),
                 ("x0", c_p), ("buf", c_p * 2), ("deltas", c_p), ("delta_scales", c_p), ("run_len", c_p),
-                ("conds", c_p), ("n", C.c_int64), ("L", C.c_int32), ("delta_format", C.c_int32)]
+                ("conds", c_p), ("block_cfg", c_p), ("n", C.c_int64), ("L", C.c_int32), ("delta_format", C.c_int32)]
 
 
 EXPORTS = {

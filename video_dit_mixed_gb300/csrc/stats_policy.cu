@@ -735,12 +735,17 @@ __device__ __forceinline__ void set_branch(const sixbit_dit_blocks& B, int l, in
 // (__ballot_sync): only those blocks are recorded (state, mode word, no
 // body), exactly the ones a walk that stops at the first non-skip records;
 // the first non-skip is decided later, from the run's output statistics.
+// Block l's thresholds: its own entry of B.block_cfg (per-depth thresholds), or the step's cfg.
+__device__ __forceinline__ sixbit_policy_cfg cfg_of(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l) {
+  return B.block_cfg != nullptr ? B.block_cfg[l] : cfg;
+}
+
 __device__ void decide_block(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l) {
   const int lane = threadIdx.x & 31;
   int word = 0;
   if (lane == 0) {
     sixbit_policy_state s = B.states[l];
-    word = policy_decide(cfg, s, &B.stats[l], block_in_stats(B, l));
+    word = policy_decide(cfg_of(cfg, B, l), s, &B.stats[l], block_in_stats(B, l));
     B.states[l] = s;
     B.modes[l] = word;
     if (SIXBIT_MODE_OF(word) != SIXBIT_MODE_SKIP) set_branch(B, l, SIXBIT_MODE_OF(word) - SIXBIT_MODE_NVFP4);
@@ -756,7 +761,7 @@ __device__ void decide_block(const sixbit_policy_cfg& cfg, const sixbit_dit_bloc
     if (j < B.L) {
       sj = B.states[j];
       const sixbit_stats tj = B.stats[j];
-      wj = policy_decide(cfg, sj, &tj, &B.stats[j - 1].max_abs_out);  // input stats: block j-1's output
+      wj = policy_decide(cfg_of(cfg, B, j), sj, &tj, &B.stats[j - 1].max_abs_out);  // input: block j-1's output
       skip = SIXBIT_MODE_OF(wj) == SIXBIT_MODE_SKIP;
     }
     const unsigned sk = __ballot_sync(0xffffffffu, skip);

@@ -30,13 +30,21 @@ class DiT:
     def __init__(self, tokens: int, hidden: int, ffn: int, blocks: int, had_block: int, packed, cfg=None,
                  device="cuda", delta_format: str = "bf16"):
         """packed: list of (PackedWeights up [ffn, hidden], PackedWeights down [hidden, ffn]);
+        cfg: one policy_cfg for every block, or a list of one per block (per-depth thresholds);
         delta_format: the Delta cache's storage, "bf16" or "mxfp8" (about half the bytes)."""
         assert len(packed) == blocks
         assert delta_format in ("bf16", "mxfp8")
         dev = torch.device(device)
         self.T, self.H, self.F, self.L, self.b = tokens, hidden, ffn, blocks, had_block
         self.packed = packed
-        self.cfg = cfg or ops.policy_cfg()
+        cfg = cfg or ops.policy_cfg()
+        if isinstance(cfg, (list, tuple)):
+            assert len(cfg) == blocks
+            self.cfg = cfg[0]          # passed to the calls; each block decides with its own entry
+            self.block_cfg = ops.policy_cfgs_tensor(cfg, dev)
+        else:
+            self.cfg = cfg
+            self.block_cfg = None
         bf = torch.bfloat16
         self.x_in = torch.zeros((tokens, hidden), dtype=bf, device=dev)
         self.bufs = [torch.zeros((tokens, hidden), dtype=bf, device=dev) for _ in range(2)]
@@ -64,7 +72,7 @@ class DiT:
 
     def _record(self, conds):
         return ops.dit_blocks(self.state, self.stats, self.modes, self.run_len, self.tstats, self.x_in,
-                              self.bufs[0], self.bufs[1], self.deltas, conds, self.delta_scales)
+                              self.bufs[0], self.bufs[1], self.deltas, conds, self.delta_scales, self.block_cfg)
 
     def reset(self):
         """Back to the state before the first denoising step."""

@@ -218,12 +218,19 @@ def policy_step(cfg: PolicyCfg, state: torch.Tensor, last_stats: torch.Tensor, i
     return mode_word
 
 
+def policy_cfgs_tensor(cfgs, device="cuda") -> torch.Tensor:
+    """Per-block thresholds as the device array sixbit_dit_blocks.block_cfg points to."""
+    raw = b"".join(bytes(c) for c in cfgs)
+    return torch.frombuffer(bytearray(raw), dtype=torch.uint8).to(device)
+
+
 def dit_blocks(states, stats, modes, run_len, in_stats0, x0, buf0, buf1, deltas, conds=None,
-               delta_scales=None) -> DitBlocks:
+               delta_scales=None, block_cfg=None) -> DitBlocks:
     """The sixbit_dit_blocks record of a stack of residual blocks (device tensors; deltas [L, ...];
     run_len: int32 [L], zeroed; conds: int64 [L] graph condition handles, or None).  The Delta
     cache is bf16 (deltas bf16 [L, n]) or, with delta_scales, MXFP8 (deltas uint8 [L, n] E4M3
-    codes, delta_scales uint8 [L, n / 32] E8M0 codes)."""
+    codes, delta_scales uint8 [L, n / 32] E8M0 codes).  block_cfg: the policy_cfgs_tensor of L
+    per-block thresholds, or None."""
     L = states.shape[0]
     n = x0.numel()
     assert stats.shape[0] == L and modes.numel() == L and run_len.numel() == L and deltas.shape[0] == L
@@ -237,9 +244,10 @@ def dit_blocks(states, stats, modes, run_len, in_stats0, x0, buf0, buf1, deltas,
         assert deltas.dtype == torch.uint8 and delta_scales.dtype == torch.uint8
         assert delta_scales.is_contiguous() and delta_scales.numel() == L * (n // MX_BLOCK)
         fmt = DELTA_MXFP8
+    assert block_cfg is None or (block_cfg.dtype == torch.uint8 and block_cfg.numel() == L * C.sizeof(PolicyCfg))
     return DitBlocks(_p(states), _p(stats), _p(modes), _p(in_stats0), _p(x0),
                      (C.c_void_p * 2)(buf0.data_ptr(), buf1.data_ptr()), _p(deltas), _p(delta_scales), _p(run_len),
-                     _p(conds), n, L, fmt)
+                     _p(conds), _p(block_cfg), n, L, fmt)
 
 
 def dit_begin(cfg: PolicyCfg, blocks: DitBlocks, scratch: torch.Tensor, err=None, stream=None):
