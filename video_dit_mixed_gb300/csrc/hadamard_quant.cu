@@ -488,6 +488,128 @@ __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const
   }
 }
 
+// b = 64 with 32 consecutive elements per lane (half a Hadamard block, the
+// other half in the neighbouring lane): a warp covers 1024 consecutive
+// elements of its row, a team of R = 2^lr warps the row (K <= 16384).  The
+// lane's elements i and i + 16 share an f32x2 register, so the stages of
+// stride 1, 2, 4, 8 are one f32x2 instruction for two butterflies, stride 16
+// pairs the two lanes of a register, and only stride 32 crosses lanes (one
+// 64-bit shuffle per pair: a third of the cross-lane traffic of the
+// 8-elements-per-lane form above, whose stages 8, 16, 32 all cross lanes).
+// Same stage order, same roundings, same division: bit-identical results.
+// CTAs of W warps (W * 1024 >= K; smaller CTAs let more of them overlap
+// their load, reduction and store phases on an SM).
+template <int W>
+__global__ void __launch_bounds__(W * 32, 32 / W) hq_int8_half_kernel(const uint16_t* __restrict__ X, int M, int K,
+                                                                    int lr, const int32_t* mode_dev, int8_t* codes,
+                                                                    float* row_scale, float* rotated) {
+  if (mode_skips(mode_dev, SIXBIT_MODE_INT8)) return;
+  constexpr float kScale = 0.125f;  // 1/sqrt(64), exact
+  __shared__ float red[W];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int R = 1 << lr;
+  const int team = warp >> lr, t = warp & (R - 1);
+  const int r = blockIdx.x * (W >> lr) + team;
+  const bool row_ok = r < M;
+  const int col = t * 1024 + lane * 32;  // K % 64 == 0: a block's two halves are both in range or both out
+  const bool have = row_ok && col < K;
+  const uint16_t* src = X + static_cast<size_t>(row_ok ? r : 0) * K + (have ? col : 0);
+  uint4 raw[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) raw[c] = have ? ld_nc_16(src + 8 * c) : make_uint4(0, 0, 0, 0);
+  uint64_t P[16];  // P[i] = (element i, element i + 16) of the lane's 32
+  {
+    float e0[8], e1[8], e2[8], e3[8];
+    bf16x8_to_f32(raw[0], e0);
+    bf16x8_to_f32(raw[1], e1);
+    bf16x8_to_f32(raw[2], e2);
+    bf16x8_to_f32(raw[3], e3);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      P[i] = f2_pack(e0[i], e2[i]);
+      P[8 + i] = f2_pack(e1[i], e3[i]);
+    }
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & h) == 0) {
+        const uint64_t a = P[i], c = P[i + h];
+        P[i] = f2_add(a, c);
+        P[i + h] = f2_sub(a, c);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {  // stride 16: the two lanes of each register
+    const float a = f2_lo(P[i]), c = f2_hi(P[i]);
+    P[i] = f2_pack(__fadd_rn(a, c), __fsub_rn(a, c));
+  }
+  {  // stride 32: the neighbouring lane holds the block's other half
+    const float sgn = (lane & 1) ? -1.0f : 1.0f;  // lower half: v + o; upper half: o - v (one rounding)
+    const uint64_t sg2 = f2_pack(sgn, sgn);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, static_cast<unsigned long long>(P[i]), 1);
+      P[i] = f2_fma(sg2, P[i], o);
+    }
+  }
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fabsf(f2_lo(P[i])), fabsf(f2_hi(P[i]))));
+  m = warp_max(m);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  m = red[team << lr];
+  for (int i = 1; i < R; ++i) m = fmaxf(m, red[(team << lr) + i]);
+  if (!have) return;
+  const float s = __fdiv_rn(__fmul_rn(m, kScale), 127.0f);
+  const bool fast = recip_ok(s) || s == 0.f;
+  const float rs = s != 0.f ? __frcp_rn(s) : 0.f;
+  if (t == 0 && lane == 0) row_scale[r] = s;
+  const size_t off = static_cast<size_t>(r) * K + col;
+  if (rotated != nullptr) {  // the rotated values y = v / 8 (FP32, test output)
+    float4* dst = reinterpret_cast<float4*>(rotated + off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      dst[i] = make_float4(__fmul_rn(f2_lo(P[4 * i]), kScale), __fmul_rn(f2_lo(P[4 * i + 1]), kScale),
+                           __fmul_rn(f2_lo(P[4 * i + 2]), kScale), __fmul_rn(f2_lo(P[4 * i + 3]), kScale));
+      dst[4 + i] = make_float4(__fmul_rn(f2_hi(P[4 * i]), kScale), __fmul_rn(f2_hi(P[4 * i + 1]), kScale),
+                               __fmul_rn(f2_hi(P[4 * i + 2]), kScale), __fmul_rn(f2_hi(P[4 * i + 3]), kScale));
+    }
+  }
+  const uint64_t kr2 = f2_pack(kRound, kRound);
+  uint64_t oi[16];
+  if (fast) {
+    const uint64_t rs2 = f2_pack(rs * kScale, rs * kScale);  // RN(1 / (8 s)), exact
+    const uint64_t ns2 = f2_pack(-(s / kScale), -(s / kScale));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {  // div_by_recip on both lanes
+      const uint64_t q = f2_mul(P[i], rs2);
+      const uint64_t d = f2_fma(f2_fma(ns2, q, P[i]), rs2, q);
+      oi[i] = f2_add(d, kr2);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float dl = fminf(fmaxf(__fdiv_rn(__fmul_rn(f2_lo(P[i]), kScale), s), -127.f), 127.f);
+      const float dh = fminf(fmaxf(__fdiv_rn(__fmul_rn(f2_hi(P[i]), kScale), s), -127.f), 127.f);
+      oi[i] = f2_add(f2_pack(dl, dh), kr2);
+    }
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {  // elements 0..15 from the low lanes, 16..31 from the high lanes
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      uint32_t tt[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) tt[i] = static_cast<uint32_t>(hh ? (oi[8 * g + i] >> 32) : oi[8 * g + i]);
+      int8_write8(tt, off + 16 * hh + 8 * g, codes);
+    }
+  }
+}
+
 // ----------------------------------- thread-per-block NVFP4 forms (b = 16) --
 //
 // For b <= 64 one thread holds a whole Hadamard block (b contiguous elements
@@ -1001,6 +1123,22 @@ cudaError_t launch_hq_nvfp4(const uint16_t* X, int M, int K, int b, const int32_
 
 cudaError_t launch_hq_int8(const uint16_t* X, int M, int K, int b, const int32_t* mode_dev, const sixbit_qact* o,
                            cudaStream_t st) {
+  if (b == 64 && K <= kHqRowWarps * 1024) {  // half a block per lane: one warp per 1024 elements of a row
+    int lr = 0;
+    while ((1024 << lr) < K) ++lr;
+    if (lr <= 3) {  // rows up to 8192 elements: 8-warp CTAs
+      const int rows_per_cta = 8 >> lr;
+      const int grid = (M + rows_per_cta - 1) / rows_per_cta;
+      hq_int8_half_kernel<8><<<grid, 8 * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes, o->row_scale, o->rotated);
+    } else {
+      const int rows_per_cta = kHqRowWarps >> lr;
+      const int grid = (M + rows_per_cta - 1) / rows_per_cta;
+      hq_int8_half_kernel<kHqRowWarps><<<grid, kHqRowWarps * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes,
+                                                                        o->row_scale, o->rotated);
+    }
+    note_launch();
+    return cudaGetLastError();
+  }
   const int nch = (K + 255) / 256;
   int lr = 0;
   while ((kHqRowChunks << lr) < nch && lr < 5) ++lr;
