@@ -48,14 +48,19 @@
 //   0       TMA producer: the fp16 W tile of each stage
 //   1       allocates tensor memory; one lane issues tcgen05.mma and commits
 //   2       TMA producer: the s8 code tile of each stage
-//   3       idle
+//   3       gate: one lane waits for a group's W slot, A slot and (group
+//           g >= 2) accumulator, then arrives on the group's go barrier, the
+//           only barrier the MMA thread waits on (tcgen05.mma issue blocks
+//           at the tensor core's rate, so each wait on the MMA thread adds
+//           ~100-280 cycles of idle tensor core per group, measured)
 //   4 - 7   converters: warp 4 + q copies and converts rows 32 q .. 32 q + 31
 //   8 - 15  fold + epilogue: warp 8 + e reads lanes 32 (e & 3) .. + 31 and
 //           columns 96 (e >> 2) .. + 95 of each accumulator
 // The CTA launches with 128 registers a thread; setmaxnreg gives warpgroup 0
-// 56, the converters 88 and the fold warpgroups 184 (4 x 56 + 4 x 88 + 8 x 184
-// = 16 x 126, and per SM sub-partition 56 + 88 + 2 x 184 = 4 x 128): a fold
-// thread's 96 running sums with a 32-column accumulator load fit.
+// 40, the converters 80 and the fold warpgroups 192 (4 x 40 + 4 x 80 + 8 x 192
+// = 2016 <= 16 x 128, and per SM sub-partition 40 + 80 + 2 x 192 = 504 <= 512):
+// a fold thread's 96 running sums with three 16-column accumulator loads in
+// flight fit.
 //
 // Tensor memory: two 192-column accumulators (columns 0 .. 191 and
 // 256 .. 447; K groups alternate between them and the fold warps add
@@ -97,7 +102,7 @@ constexpr int kSwLanes = kCols / 4;                  // lanes copying a group's 
 constexpr int kBoxBytes = 32 * 64;                   // one 32 x 32 bf16 output box
 constexpr int kWarpArea = 2048;                      // a fold warp's scale ring, or its output box
 static_assert(kSwRing * kCols * 4 <= kWarpArea && kBoxBytes <= kWarpArea, "fold warp area");
-constexpr int kRegsLaunch = 128, kRegsLow = 56, kRegsConv = 88, kRegsHigh = 184;
+constexpr int kRegsLaunch = 128, kRegsLow = 40, kRegsConv = 80, kRegsHigh = 192;
 static_assert(4 * kRegsLow + 4 * kRegsConv + 8 * kRegsHigh <= 16 * kRegsLaunch &&
                   kRegsLow + kRegsConv + 2 * kRegsHigh <= 4 * kRegsLaunch,
               "the register split must fit in what the CTA is launched with");
@@ -173,10 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* c_full = a_empty + kAStages;      // [kS8Stages] code tile landed
   uint64_t* c_empty = c_full + kS8Stages;     // [kS8Stages] the four converter warps read the code tile
   uint64_t* afree = c_empty + kS8Stages;      // [2] accumulator read back (eight fold warps)
-  uint64_t* drain = afree + 2;
+  uint64_t* go = afree + 2;                   // [2] group g's operands and accumulator are ready (gate)
+  uint64_t* drain = go + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  static_assert((2 * kStages + 2 * kAStages + 2 * kS8Stages + 3) * 8 + 8 <= kBarBytes, "barrier area");
+  static_assert((2 * kStages + 2 * kAStages + 2 * kS8Stages + 5) * 8 + 8 <= kBarBytes, "barrier area");
 
   auto W_op = [&](int s) { return smem + s * kBTile; };
 
@@ -209,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c_empty[c], 4);
     }
     for (int b = 0; b < 2; ++b) mbar_init(&afree[b], kFoldWarps);
+    for (int b = 0; b < 2; ++b) mbar_init(&go[b], 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -261,15 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // -------------------------------------------------------- MMA issuer --
         // Stage (= K group) counter gi runs across tiles; group gi
-        // accumulates into buffer gi & 1 and uses A slot gi & 1.
+        // accumulates into buffer gi & 1 and uses A slot gi & 1.  The gate
+        // (warp 3) has waited for its operands and accumulator.
         uint32_t gi = 0;
+        int s = 0;  // W slot of group gi
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
           for (int g = 0; g < groups; ++g, ++gi) {
-            const int s = gi % S, a = gi % kAStages;
-            if ((gi >= 2 && !mbar_wait(&afree[gi & 1], ((gi >> 1) - 1) & 1, abort_flag, p.wait_ns)) ||
-                !mbar_wait(&w_full[s], (gi / S) & 1, abort_flag, p.wait_ns) ||
-                !mbar_wait(&a_full[a], (gi / kAStages) & 1, abort_flag, p.wait_ns)) {
+            const int a = static_cast<int>(gi & 1);
+            if (!mbar_wait(&go[a], (gi >> 1) & 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -282,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              k == 0 ? 0u : 1u);
             tc_commit(&a_empty[a]);
             tc_commit(&w_empty[s]);  // frees the W slot; also the group's completion
+            s = s + 1 == S ? 0 : s + 1;
           }
         }
         if (!ok) {
@@ -290,6 +298,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(drain);  // all tensor-core work issued here completes before exit
         (void)mbar_wait(drain, 0, nullptr, p.wait_ns);
+      }
+    } else if (warp == 3) {
+      if (lane == 0) {
+        // -------------------------------------------------------------- gate --
+        uint32_t gi = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+          for (int g = 0; g < groups; ++g, ++gi) {
+            const int a = static_cast<int>(gi & 1), s = static_cast<int>(gi % S);
+            if ((gi >= 2 && !mbar_wait(&afree[a], ((gi >> 1) - 1) & 1, abort_flag, p.wait_ns)) ||
+                !mbar_wait(&w_full[s], (gi / S) & 1, abort_flag, p.wait_ns) ||
+                !mbar_wait(&a_full[a], (gi >> 1) & 1, abort_flag, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+            // go[a] cannot run a phase ahead of the MMA thread: group gi + 2's
+            // gate needs buffer a back, which needs group gi's MMAs
+            mbar_arrive(&go[a]);
+          }
+        }
+        if (!ok) {
+          set_error(p.err, SIXBIT_ETIMEOUT);
+          *abort_flag = 1;
+        }
       }
     } else if (warp == 2) {
       if (lane == 0) {
@@ -428,28 +460,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t acc_addr = lane_addr + (gi & 1) * kAccStride;
-#pragma unroll
-        for (int c = 0; c < kCols / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(acc_addr + 32 * c, r);
-          tmem_ld_wait(r);
-          if (c == kCols / 32 - 1) release_acc(&afree[gi & 1], lane);  // free once read back
+        // Six 16-column chunks, three loads in flight: chunks 0-2 are loaded
+        // together, and chunk c + 3 is loaded as soon as chunk c is folded,
+        // so the buffer goes back to the MMA thread two load latencies after
+        // the group completes (the MMA of group gi + 2 waits for it) instead
+        // of one per chunk.
+        auto fold16 = [&](int c, const uint32_t (&r)[16]) {
           if (DBG && row < p.M) {
-            for (int j = 0; j < 32; ++j) {
-              const int n = n0 + 32 * c + j;
+            for (int j = 0; j < 16; ++j) {
+              const int n = n0 + 16 * c + j;
               if (n < p.N) p.acc_dbg[(static_cast<size_t>(g) * p.M + row) * p.N + n] = __float2int_rn(__uint_as_float(r[j]));
             }
           }
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 s4 = sw4[c * 8 + j4];
-            float* sm = sum + 32 * c + 4 * j4;
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const float4 s4 = sw4[c * 4 + j4];
+            float* sm = sum + 16 * c + 4 * j4;
             sm[0] = fmaf(s4.x, __uint_as_float(r[4 * j4]), sm[0]);
             sm[1] = fmaf(s4.y, __uint_as_float(r[4 * j4 + 1]), sm[1]);
             sm[2] = fmaf(s4.z, __uint_as_float(r[4 * j4 + 2]), sm[2]);
             sm[3] = fmaf(s4.w, __uint_as_float(r[4 * j4 + 3]), sm[3]);
           }
-        }
+        };
+        static_assert(kCols == 96, "six 16-column chunks");
+        uint32_t r0[16], r1[16], r2[16];
+        tmem_ld16(acc_addr, r0);
+        tmem_ld16(acc_addr + 16, r1);
+        tmem_ld16(acc_addr + 32, r2);
+        tmem_ld_wait(r0);
+        tmem_ld_wait(r1);   // (no load outstanding: ties the registers to the wait)
+        tmem_ld_wait(r2);
+        fold16(0, r0);
+        tmem_ld16(acc_addr + 48, r0);
+        fold16(1, r1);
+        tmem_ld16(acc_addr + 64, r1);
+        fold16(2, r2);
+        tmem_ld16(acc_addr + 80, r2);
+        tmem_ld_wait(r0);
+        tmem_ld_wait(r1);
+        tmem_ld_wait(r2);
+        release_acc(&afree[gi & 1], lane);  // the accumulator is free once read back
+        fold16(3, r0);
+        fold16(4, r1);
+        fold16(5, r2);
         if (!ok) break;
       }
       cp_async_wait_all();  // no scale copy outlives the tile
