@@ -23,37 +23,37 @@
 // (TMA, 128-byte swizzle).  The activation codes are read by the GEMM itself,
 // one byte per element, and the A operand is held in tensor memory: four
 // converter warps, one per 32-lane quarter, turn each thread's row of a
-// stage's codes into 64 fp16 values (with u = q ^ 0x80, the fp16 bit pattern
+// stage's codes into 128 fp16 values (with u = q ^ 0x80, the fp16 bit pattern
 // 0x64:u is 1152 + q, and one fp16 subtraction of 1152 leaves q exactly) and
 // store them into the row's tensor-memory lane (column j holds k = 2j, 2j+1),
 // from where the MMA reads A.  So shared memory carries only the weight tiles
-// (their copies in, the tensor core's reads out), the codes (8 KB a stage)
+// (their copies in, the tensor core's reads out), the codes (16 KB a stage)
 // and the group scales; with the A operand in shared memory its writes and
 // the tensor core's reads of it made the shared-memory port, not the tensor
 // core, the limit.
 //
-// A persistent CTA per SM walks 128 x 192 output tiles in 64-K stages through
-// three rings: fp16 W tiles (six slots of 24 KB in shared memory, TMA), s8
-// codes (six slots of 8 KB in shared memory, TMA with the 64-byte swizzle:
-// chunk c of row r at chunk c ^ ((r >> 1) & 3), so a thread's reads of its own
-// row are conflict-free) and fp16 A tiles (four slots of 32 columns in tensor
-// memory).  The codes run up to six stages ahead of their conversion, so
-// their copies' latency (~2500-3600 cycles under load, measured; they queue
-// behind the weight tiles in the SM's copy engine) is off the refill path.  A
-// stage's MMAs wait for its W slot (bytes landed) and its A slot (four
-// converter warps done) and free both with one commit each.  (Copying the
-// codes per lane with cp.async instead cost the converter warps ~300 cycles a
-// stage in issue stalls, measured.)
+// A persistent CTA per SM walks 128 x 192 output tiles in 128-K stages (one
+// scale group each) through three rings: fp16 W tiles (three slots of 48 KB in
+// shared memory, TMA, two 64-K halves a stage), s8 codes (three slots of
+// 16 KB in shared memory, TMA with the 128-byte swizzle: chunk c of row r at
+// chunk c ^ (r & 7), so a thread's reads of its own row are conflict-free)
+// and fp16 A tiles (two slots of 64 columns in tensor memory).  A group's
+// MMAs wait for its W slot (bytes landed), its A slot (four converter warps
+// done) and its accumulator (eight fold warps done with group g - 2), and
+// free the A slot and the W slot with one commit each; the W-slot commit is
+// also the group's completion for the fold warps.  (Copying the codes per
+// lane with cp.async instead cost the converter warps ~300 cycles a stage in
+// issue stalls, measured.)
 // Warps:
 //   0       TMA producer: the fp16 W tile of each stage
-//   1       allocates tensor memory; one lane issues tcgen05.mma and commits
+//   1, 3    MMA issuers: one lane of warp 1 issues the even groups, one lane
+//           of warp 3 the odd ones (tcgen05.mma issue blocks at the tensor
+//           core's rate, so a single issuer's barrier waits and commits left
+//           the tensor core idle ~45% of each group, measured with a clock64
+//           trace; with two, each one's waits overlap the other's MMAs).
+//           Warp 1 also allocates tensor memory.
 //   2       TMA producer: the s8 code tile of each stage
-//   3       gate: one lane waits for a group's W slot, A slot and (group
-//           g >= 2) accumulator, then arrives on the group's go barrier, the
-//           only barrier the MMA thread waits on (tcgen05.mma issue blocks
-//           at the tensor core's rate, so each wait on the MMA thread adds
-//           ~100-280 cycles of idle tensor core per group, measured)
-//   4 - 7   converters: warp 4 + q copies and converts rows 32 q .. 32 q + 31
+//   4 - 7   converters: warp 4 + q converts rows 32 q .. 32 q + 31
 //   8 - 15  fold + epilogue: warp 8 + e reads lanes 32 (e & 3) .. + 31 and
 //           columns 96 (e >> 2) .. + 95 of each accumulator
 // The CTA launches with 128 registers a thread; setmaxnreg gives warpgroup 0
@@ -65,12 +65,10 @@
 // Tensor memory: two 192-column accumulators (columns 0 .. 191 and
 // 256 .. 447; K groups alternate between them and the fold warps add
 // s_w[g][n] * acc_g into registers while the next group accumulates) and the
-// four 32-column A slots beside them (192, 224, 448, 480).  A group's
-// completion is the W-slot commit after its second stage.  Every mbarrier
-// wait is bounded (2 s); on expiry the kernel records
-// SIXBIT_ETIMEOUT, raises an abort flag for the other roles, waits (bounded)
-// for its copies and tensor-core work in flight, frees tensor memory and
-// returns.
+// two 64-column A slots beside them (192 and 448).  Every mbarrier wait is
+// bounded (2 s); on expiry the kernel records SIXBIT_ETIMEOUT, raises an abort
+// flag for the other roles, waits (bounded) for its copies and tensor-core
+// work in flight, frees tensor memory and returns.
 #include <cstdint>
 
 #include "common.cuh"
@@ -178,11 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* c_full = a_empty + kAStages;      // [kS8Stages] code tile landed
   uint64_t* c_empty = c_full + kS8Stages;     // [kS8Stages] the four converter warps read the code tile
   uint64_t* afree = c_empty + kS8Stages;      // [2] accumulator read back (eight fold warps)
-  uint64_t* go = afree + 2;                   // [2] group g's operands and accumulator are ready (gate)
-  uint64_t* drain = go + 2;
+  uint64_t* drain = afree + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  static_assert((2 * kStages + 2 * kAStages + 2 * kS8Stages + 5) * 8 + 8 <= kBarBytes, "barrier area");
+  static_assert((2 * kStages + 2 * kAStages + 2 * kS8Stages + 3) * 8 + 8 <= kBarBytes, "barrier area");
 
   auto W_op = [&](int s) { return smem + s * kBTile; };
 
@@ -215,8 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&c_empty[c], 4);
     }
     for (int b = 0; b < 2; ++b) mbar_init(&afree[b], kFoldWarps);
-    for (int b = 0; b < 2; ++b) mbar_init(&go[b], 1);
-    mbar_init(drain, 1);
+    mbar_init(drain, 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -264,24 +260,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t j = (it > S ? it - S : 0); j < it; ++j)
           (void)mbar_wait(&w_full[j % S], (j / S) & 1, nullptr, p.wait_ns);
       }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 3) {
       if (lane == 0) {
-        // -------------------------------------------------------- MMA issuer --
-        // Stage (= K group) counter gi runs across tiles; group gi
-        // accumulates into buffer gi & 1 and uses A slot gi & 1.  The gate
-        // (warp 3) has waited for its operands and accumulator.
+        // ------------------------------------------------------- MMA issuers --
+        // Group counter gi runs across tiles; group gi accumulates into
+        // buffer gi & 1, reads A slot gi & 1 and W slot gi % S.  Warp 1's
+        // lane issues the even groups, warp 3's the odd ones, each waiting
+        // for its own group's operands and accumulator: tcgen05.mma issue
+        // blocks at the tensor core's rate, so one issuer's waits and
+        // commits leave the tensor core idle, while with two each one's
+        // waits overlap the other's MMAs.  A commit tracks only its own
+        // thread's MMAs, which is the group's.
+        const uint32_t par = warp == 1 ? 0u : 1u;
         uint32_t gi = 0;
-        int s = 0;  // W slot of group gi
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
           for (int g = 0; g < groups; ++g, ++gi) {
-            const int a = static_cast<int>(gi & 1);
-            if (!mbar_wait(&go[a], (gi >> 1) & 1, abort_flag, p.wait_ns)) {
+            if ((gi & 1) != par) continue;
+            const int a = static_cast<int>(par), s = static_cast<int>(gi % S);
+            if ((gi >= 2 && !mbar_wait(&afree[a], ((gi >> 1) - 1) & 1, abort_flag, p.wait_ns)) ||
+                !mbar_wait(&w_full[s], (gi / S) & 1, abort_flag, p.wait_ns) ||
+                !mbar_wait(&a_full[a], (gi >> 1) & 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t d_tmem = tmem + (gi & 1) * kAccStride;
+            const uint32_t d_tmem = tmem + par * kAccStride;
             const uint32_t a_tmem = tmem + a_slot_col(a), b_base = smem_u32(W_op(s));
 #pragma unroll
             for (int k = 0; k < kKStage / 16; ++k)  // k < 4 from the first 64-K half of the W tile, then the second
@@ -289,39 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                              k == 0 ? 0u : 1u);
             tc_commit(&a_empty[a]);
             tc_commit(&w_empty[s]);  // frees the W slot; also the group's completion
-            s = s + 1 == S ? 0 : s + 1;
           }
         }
         if (!ok) {
           set_error(p.err, SIXBIT_ETIMEOUT);
           *abort_flag = 1;
         }
-        tc_commit(drain);  // all tensor-core work issued here completes before exit
+        tc_commit(drain);  // all tensor-core work issued here completes before exit (count 2: both issuers)
         (void)mbar_wait(drain, 0, nullptr, p.wait_ns);
-      }
-    } else if (warp == 3) {
-      if (lane == 0) {
-        // -------------------------------------------------------------- gate --
-        uint32_t gi = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-          for (int g = 0; g < groups; ++g, ++gi) {
-            const int a = static_cast<int>(gi & 1), s = static_cast<int>(gi % S);
-            if ((gi >= 2 && !mbar_wait(&afree[a], ((gi >> 1) - 1) & 1, abort_flag, p.wait_ns)) ||
-                !mbar_wait(&w_full[s], (gi / S) & 1, abort_flag, p.wait_ns) ||
-                !mbar_wait(&a_full[a], (gi >> 1) & 1, abort_flag, p.wait_ns)) {
-              ok = false;
-              break;
-            }
-            // go[a] cannot run a phase ahead of the MMA thread: group gi + 2's
-            // gate needs buffer a back, which needs group gi's MMAs
-            mbar_arrive(&go[a]);
-          }
-        }
-        if (!ok) {
-          set_error(p.err, SIXBIT_ETIMEOUT);
-          *abort_flag = 1;
-        }
       }
     } else if (warp == 2) {
       if (lane == 0) {
