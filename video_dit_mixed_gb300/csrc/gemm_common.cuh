@@ -1,5 +1,5 @@
 // Device helpers shared by the GEMM kernels: register reallocation, the
-// exact-erf GELU of the up projection, cp.async, accumulator hand-back, and
+// erf GELU of the up projection, cp.async, accumulator hand-back, and
 // the bf16 epilogue (GELU or residual, direct or TMA-staged stores).
 #pragma once
 
@@ -14,23 +14,53 @@ template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
-// GELU(v) = v Phi(v) with Phi(v) = (1 + erf(v / sqrt 2)) / 2.  erfc(z), z = |v| / sqrt 2,
-// is taken as t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2), t = 1 / (1 + p z)
-// (Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26: the
-// erf it gives is within 1.5e-7 of the exact one), then 1 + erf = 2 - erfc for
-// v >= 0 and erfc(|z|) for v < 0, so the negative tail keeps its relative
-// accuracy.  Branch-free; its GELU differs from the exact-erf one by at most
-// a few 1e-7 |v|, inside the FP32 epilogue's error budget.
-__device__ __forceinline__ float gelu_erf(float v) {
-  const float z = fabsf(v) * 0.7071067811865475244f;
-  const float t = __fdividef(1.0f, fmaf(0.3275911f, z, 1.0f));
-  float q = fmaf(t, 1.061405429f, -1.453152027f);
-  q = fmaf(t, q, 1.421413741f);
-  q = fmaf(t, q, -0.284496736f);
-  q = fmaf(t, q, 0.254829592f);
-  const float c = t * q * __expf(-z * z);  // erfc(z)
-  const float w = v >= 0.f ? 2.0f - c : c;  // 1 + erf(v / sqrt 2)
-  return 0.5f * v * w;
+// GELU(v) = v Phi(v) = 0.5 v (1 + erf(x)), x = v / sqrt 2, for two elements at
+// once (packed f32x2 arithmetic).  erf(x) = x Q(s) on |x| <= 3.9, where
+// Q(s) ~ erf(x) / x is the degree-15 Chebyshev interpolant of that even
+// function in s = 2 x^2 / 3.9^2 - 1, written as monomial coefficients in s
+// (all below 1 in magnitude) and evaluated by Horner in s; x is first clamped
+// to +-3.9 (erf(3.9) = 1 - 3.5e-8), in one instruction (min.xorsign.abs keeps
+// x's sign).  In FP32 with FMAs the erf is within 1.9e-7 of the exact one for
+// every x and the GELU within 1.3e-7 |v|.  No reciprocal or exponential: the
+// special-function unit, a quarter-rate pipe, paced the epilogue with the
+// two an element of Abramowitz & Stegun's formula 7.1.26.  The coefficients
+// are printed by gelu_coeffs.py (beside this file).
+__host__ __device__ constexpr float gelu_q(int i) {  // coefficient c_i of Q
+  constexpr float c[16] = {
+      0x1.7349360000000p-2f,  // c_0
+      -0x1.72b5ec0000000p-3f,  // c_1
+      0x1.13d9060000000p-3f,  // c_2
+      -0x1.c0a6ce0000000p-4f,  // c_3
+      0x1.735e940000000p-4f,  // c_4
+      -0x1.2e36520000000p-4f,  // c_5
+      0x1.da8d980000000p-5f,  // c_6
+      -0x1.5f5f0c0000000p-5f,  // c_7
+      0x1.dc399a0000000p-6f,  // c_8
+      -0x1.3b50de0000000p-6f,  // c_9
+      0x1.c06c100000000p-7f,  // c_10
+      -0x1.eeb2900000000p-8f,  // c_11
+      0x1.df33080000000p-10f,  // c_12
+      -0x1.2e7bc00000000p-10f,  // c_13
+      0x1.fdde5c0000000p-10f,  // c_14
+      -0x1.ac851a0000000p-11f,  // c_15
+  };
+  return c[i];
+}
+constexpr float kGeluS = 0x1.0d4be80000000p-3f;  // 2 / 3.9^2, rounded
+__device__ __forceinline__ float clamp_erf_arg(float x) {  // sign(x) min(|x|, 3.9)
+  float d;
+  asm("min.xorsign.abs.f32 %0, %1, %2;" : "=f"(d) : "f"(x), "f"(3.9f));
+  return d;
+}
+__device__ __forceinline__ uint64_t gelu_pair(uint64_t v) {
+  const uint64_t x = f2_mul(v, f2_pack(0.7071067811865475244f, 0.7071067811865475244f));
+  const uint64_t xc = f2_pack(clamp_erf_arg(f2_lo(x)), clamp_erf_arg(f2_hi(x)));
+  const uint64_t s = f2_fma(f2_mul(xc, xc), f2_pack(kGeluS, kGeluS), f2_pack(-1.0f, -1.0f));
+  uint64_t q = f2_pack(gelu_q(15), gelu_q(15));
+#pragma unroll
+  for (int i = 14; i >= 0; --i) q = f2_fma(q, s, f2_pack(gelu_q(i), gelu_q(i)));
+  const uint64_t h = f2_mul(v, f2_pack(0.5f, 0.5f));
+  return f2_fma(h, f2_mul(xc, q), h);  // h (1 + erf)
 }
 
 // 16-byte global -> shared copy without a register round trip (zero-fill when
@@ -58,7 +88,11 @@ __device__ __forceinline__ void epilogue_apply32(const GemmParams& p, int row, i
   const size_t base = static_cast<size_t>(row) * p.N + n;
   if (p.epilogue == SIXBIT_EPI_GELU) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+    for (int j = 0; j < 32; j += 2) {
+      const uint64_t g = gelu_pair(f2_pack(v[j], v[j + 1]));
+      v[j] = f2_lo(g);
+      v[j + 1] = f2_hi(g);
+    }
   } else if (p.epilogue == SIXBIT_EPI_RESIDUAL) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
