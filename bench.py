@@ -338,7 +338,8 @@ class DitStep:
             wd = torch.randn((H, F), generator=gen, device=device, dtype=torch.float32) * (c["w_std"] * gates[l])
             packed.append((ops.pack_weights(wu, b), ops.pack_weights(wd, b)))
             del wu, wd
-        self.model = dit.DiT(T, H, F, L, b, packed, device=device, delta_format=self.delta_format)
+        self.model = dit.DiT(T, H, F, L, b, packed, device=device, delta_format=self.delta_format,
+                             fused_stats=self.fused_stats)
         # bytes per element of one block's Delta cache (MXFP8: one code byte, one scale byte per 32)
         self.delta_bytes = 2.0 if self.delta_format == "bf16" else 1.0 + 1.0 / 32
         # input trajectory, resident in HBM before timing
@@ -358,7 +359,9 @@ class DitStep:
         self.config = dict(workload=name, tokens=T, hidden=H, ffn=F, blocks=L, steps_per_run=c["steps"],
                            had_block=b, gate=c["gate"], policy="gamma 0.1, cos 0.99, err_cap 0.05, pdr 30",
                            l2="working set > 10 GB, no flush needed", cuda_graph=not self.host_dispatch,
-                           delta_cache=self.delta_format)
+                           delta_cache=self.delta_format,
+                           block_stats=("BF16 blocks: down-projection epilogue; others: separate pass"
+                                        if self.model.fused_stats else "separate pass"))
         self.mode_log = []
         self.timed_steps = []
         self.skip_run_bytes = 0
@@ -373,6 +376,7 @@ class DitStep:
 
     host_dispatch = False   # --dispatch host: no graph, the host launches each block's chosen kernels
     delta_format = "bf16"   # --delta-format mxfp8: the Delta cache in MXFP8
+    fused_stats = True      # --unfused-stats: the block statistics as a separate pass
 
     def _step(self, x):
         if self.host_dispatch:
@@ -558,6 +562,8 @@ class DitStep:
                 return ("hbm", n * 3 + T * 4, False)
             return (None, 0, False)
         if label == "block_stats":   # x_in, x_out read; Delta read and written
+            if mode == "bf16" and self.model.fused_stats:   # only the fold of the down projection's partial rows
+                return (None, 0, False)
             return ("hbm", (4 + 2 * self.delta_bytes) * T * H, False)
         if label == "tensor_stats":
             return ("hbm", 2 * T * H, False)
@@ -819,6 +825,8 @@ def run_ours(args):
         cls = type(cls.__name__, (cls,), dict(host_dispatch=True))
     if args.delta_format != "bf16":
         cls = type(cls.__name__, (cls,), dict(delta_format=args.delta_format))
+    if args.unfused_stats:
+        cls = type(cls.__name__, (cls,), dict(fused_stats=False))
     wl = cls(args.workload, torch, ops, dev)
     stream = torch.cuda.current_stream()
 
@@ -1075,6 +1083,9 @@ def main():
                          "word (one sync per block; for profilers that cannot profile conditional graph nodes)")
     ap.add_argument("--delta-format", default="bf16", choices=["bf16", "mxfp8"],
                     help="storage of the DiT's Delta cache (MXFP8: E4M3 codes, one E8M0 scale per 32)")
+    ap.add_argument("--unfused-stats", action="store_true",
+                    help="DiT workloads: a computed block's statistics and Delta update as a separate pass "
+                         "instead of in its down projection's epilogue")
     ap.add_argument("--blocks", type=int, default=0,
                     help="DiT workloads: use only this many blocks (profiling runs on a smaller device footprint)")
     ap.add_argument("--oracle-costs", action="store_true", help=argparse.SUPPRESS)  # the 1-core CPU leg's child

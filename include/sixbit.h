@@ -238,6 +238,39 @@ sixbit_status sixbit_qgemm_rotamax(const sixbit_qact* A, const sixbit_weights* W
                                    int had_block, float* amax_out, int32_t* err_dev, void* stream);
 
 /*
+ * sixbit_qgemm with the RESIDUAL epilogue (Y = bf16(A.W^T + residual), bf16
+ * Y required) whose epilogue also does the block statistics pass of
+ * sixbit_block_stats for x_in = residual and x_out = Y (technical summary
+ * sections 2.A-2.B; popular summary sections 3-4: the statistics fused into
+ * the kernel that produces the block output): delta_cache [M*N] bf16 holds
+ * Delta_prev on entry and Delta = bf16(f32(x_out) - f32(x_in)) on return,
+ * exactly as sixbit_block_stats writes it, and the sums go as partial rows
+ * to parts (device memory of sixbit_blockstats_parts_bytes() bytes, 16-byte
+ * aligned; written whole by the call, no initial contents needed), to be
+ * folded by sixbit_block_stats_parts or sixbit_dit_block_end_parts.  The
+ * partial rows are a fixed function of the launch, so the folded sums are
+ * run-to-run deterministic; they equal sixbit_block_stats's up to the order
+ * of the float-float additions (about 1e-7 relative, Kahan sums; 1e-12,
+ * TwoSum sums), while Delta and Y are bit-identical.  Other arguments,
+ * constraints and mode gating as for sixbit_qgemm.
+ */
+sixbit_status sixbit_qgemm_blockstats(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W, int M,
+                                      int N, int K, int mode, const int32_t* mode_dev, const uint16_t* residual,
+                                      uint16_t* Y, uint16_t* delta_cache, void* parts, void* workspace,
+                                      int32_t* err_dev, void* stream);
+
+/* Bytes of sixbit_qgemm_blockstats's parts buffer on the current device (0 on error). */
+size_t sixbit_blockstats_parts_bytes(void);
+
+/*
+ * Folds the partial rows of a sixbit_qgemm_blockstats call into stats_dev
+ * (the sums of sixbit_stats, count = n = M*N).  One CTA on `stream`, which
+ * must order it after the GEMM.
+ */
+sixbit_status sixbit_block_stats_parts(const void* parts, int64_t n, sixbit_stats* stats_dev, int32_t* err_dev,
+                                       void* stream);
+
+/*
  * Block statistics and delta cache update for a computed block step
  * (technical summary sections 2.A-2.C; popular summary sections 1-3):
  * Delta = bf16(f32(x_out) - f32(x_in)) overwrites delta_cache (which holds
@@ -345,6 +378,16 @@ sixbit_status sixbit_dit_block_end(const sixbit_policy_cfg* cfg, const sixbit_di
                                    void* scratch, int32_t* err_dev, void* stream);
 sixbit_status sixbit_dit_skip_run(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
                                   void* scratch, int32_t* err_dev, void* stream);
+
+/*
+ * sixbit_dit_block_end for a block l whose down projection ran as
+ * sixbit_qgemm_blockstats (residual = x_{l-1}, Y = x_l, delta_cache =
+ * Delta_l's slot of blocks->deltas) with these parts: folds them into
+ * stats[l], then block l+1's decision; nothing for a skipped block.  Bf16
+ * Delta cache only (delta_format SIXBIT_DELTA_BF16).
+ */
+sixbit_status sixbit_dit_block_end_parts(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
+                                         const void* parts, int32_t* err_dev, void* stream);
 
 /*
  * Storage format of the Delta cache.  The method only says the cache may be

@@ -92,6 +92,16 @@ def test_argument_errors_return_status_without_launching(lib):
     blocks.delta_scales = p.value
     blocks.n = 40                                              # MXFP8 needs n % 32 == 0
     assert lib.sixbit_dit_skip_run(C.byref(cfg), C.byref(blocks), 0, p, None, None) == 2
+    # the down projection with the block statistics: residual, Y, Delta cache and parts required;
+    # their fold: parts given, n > 0; the DiT's fold: a bf16 Delta cache only
+    assert lib.sixbit_qgemm_blockstats(C.byref(qa), None, C.byref(w), 16, 128, 128, 1, None, None, p, p, p, None,
+                                       None, None) == 1
+    assert lib.sixbit_qgemm_blockstats(C.byref(qa), None, C.byref(w), 16, 128, 128, 1, None, p, p, p, None, None,
+                                       None, None) == 1
+    assert lib.sixbit_block_stats_parts(None, 64, p, None, None) == 1
+    assert lib.sixbit_block_stats_parts(p, 0, p, None, None) == 2
+    blocks.n, blocks.delta_format = 64, 1
+    assert lib.sixbit_dit_block_end_parts(C.byref(cfg), C.byref(blocks), 0, p, None, None) == 1
     assert lib.sixbit_policy_step(None, p, p, p, p, None, None) == 1
     assert lib.sixbit_launch_count() == before
     assert lib.sixbit_status_str(6) == b"device-side wait timed out"

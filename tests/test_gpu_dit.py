@@ -37,7 +37,7 @@ def _margin(st, ratio, cfg):
     return min(m)
 
 
-def _run_gpu(name, graph, switched=True, host_dispatch=False, delta_format="bf16", cfgs=None):
+def _run_gpu(name, graph, switched=True, host_dispatch=False, delta_format="bf16", cfgs=None, fused_stats=True):
     from video_dit_mixed_gb300 import dit, ops
     c = synthgen.DIT_CONFIGS[name]
     packed = dit.pack_block_weights(synthgen.dit_weights(name), c["had_block"])
@@ -45,7 +45,7 @@ def _run_gpu(name, graph, switched=True, host_dispatch=False, delta_format="bf16
                                                         pdr_ratio=k.pdr_ratio, refresh_bf16=k.refresh_bf16)
                                          for k in cfgs]
     model = dit.DiT(c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"], packed, cfg=gpu_cfg,
-                    delta_format=delta_format)
+                    delta_format=delta_format, fused_stats=fused_stats)
     xs = [torch.from_numpy(x).to(torch.bfloat16).cuda() for x in synthgen.dit_trajectory(name)]
     outs, words = [], []
     for s, x in enumerate(xs):
@@ -63,12 +63,17 @@ DEPTH_CFGS = [policy.PolicyConfig(), policy.PolicyConfig(cos_thr=0.995, gamma_th
               policy.PolicyConfig(err_cap=0.03, gamma_thr=0.12), policy.PolicyConfig(cos_thr=0.985, pdr_ratio=28.0)]
 
 
-@pytest.mark.parametrize("delta_format,depth", [("bf16", False), ("mxfp8", False), ("bf16", True)])
-def test_tiny_dit_against_oracle_chain(delta_format, depth):
+# fused: BF16 blocks take their statistics from their down projection's epilogue (bf16
+# cache), in the host-dispatched (and graph) steps; the eager mode-gated step and the MXFP8
+# cache take the separate statistics pass
+@pytest.mark.parametrize("delta_format,depth,fused", [("bf16", False, True), ("mxfp8", False, False),
+                                                      ("bf16", True, True), ("bf16", False, False)])
+def test_tiny_dit_against_oracle_chain(delta_format, depth, fused):
     name = "dit_tiny"
     c = synthgen.DIT_CONFIGS[name]
     cfgs = DEPTH_CFGS if depth else None
-    outs, words, _ = _run_gpu(name, graph=False, delta_format=delta_format, cfgs=cfgs)
+    outs, words, _ = _run_gpu(name, graph=False, delta_format=delta_format, cfgs=cfgs, fused_stats=fused,
+                              host_dispatch=fused)
     cfg = policy.PolicyConfig()
     ref = OracleDiT(synthgen.dit_weights(name), c["had_block"], cfgs or cfg, delta_format=delta_format)
     # record the oracle's distance to its thresholds at every decision

@@ -62,6 +62,10 @@ EXPORTS = {
     "sixbit_qgemm_rotamax": (C.c_int, [C.POINTER(QAct), C.POINTER(Weights), C.c_int, C.c_int, C.c_int, c_p, C.c_int,
                                        c_p, c_p, C.c_int, c_p, c_p, c_p]),
     "sixbit_block_stats": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),
+    "sixbit_qgemm_blockstats": (C.c_int, [C.POINTER(QAct), c_p, C.POINTER(Weights), C.c_int, C.c_int, C.c_int,
+                                          C.c_int, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p]),
+    "sixbit_blockstats_parts_bytes": (C.c_size_t, []),
+    "sixbit_block_stats_parts": (C.c_int, [c_p, C.c_int64, c_p, c_p, c_p]),
     "sixbit_policy_step": (C.c_int, [C.POINTER(PolicyCfg), c_p, c_p, c_p, c_p, c_p, c_p]),
     "sixbit_tensor_stats": (C.c_int, [c_p, C.c_int64, c_p, c_p, c_p, c_p]),
     "sixbit_skip_apply": (C.c_int, [c_p, c_p, c_p, C.c_int64, c_p, c_p, c_p, c_p, c_p]),
@@ -71,6 +75,7 @@ EXPORTS = {
     "sixbit_block_stats_noalloc_max_elems": (C.c_int64, []),
     "sixbit_dit_begin": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), c_p, c_p, c_p]),
     "sixbit_dit_block_end": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), C.c_int, c_p, c_p, c_p]),
+    "sixbit_dit_block_end_parts": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), C.c_int, c_p, c_p, c_p]),
     "sixbit_dit_skip_run": (C.c_int, [C.POINTER(PolicyCfg), C.POINTER(DitBlocks), C.c_int, c_p, c_p, c_p]),
     "sixbit_graph_switch_begin": (C.c_int, [c_p, c_p, c_p, C.c_int, C.c_int, C.POINTER(c_p)]),
     "sixbit_graph_cond_create": (C.c_int, [c_p, C.c_int, C.POINTER(C.c_uint64)]),

@@ -266,7 +266,8 @@ sixbit_status sixbit_hadamard_quant(const uint16_t* X, int M, int K, int had_blo
 static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W, int M,
                                 int N, int K, int mode, const int32_t* mode_dev, int epilogue,
                                 const uint16_t* residual, uint16_t* Y, float* Y_f32, int32_t* acc_dbg,
-                                void* workspace, int32_t* err_dev, void* stream, int had_block, float* rot_amax) {
+                                void* workspace, int32_t* err_dev, void* stream, int had_block, float* rot_amax,
+                                uint16_t* bs_delta = nullptr, void* bs_parts = nullptr) {
   if (W == nullptr || (Y == nullptr && Y_f32 == nullptr)) return SIXBIT_EINVAL;
   if (epilogue != SIXBIT_EPI_NONE && epilogue != SIXBIT_EPI_GELU && epilogue != SIXBIT_EPI_RESIDUAL)
     return SIXBIT_EINVAL;
@@ -314,6 +315,8 @@ static sixbit_status qgemm_impl(const sixbit_qact* A, const uint16_t* X_bf16, co
   p.n_fastest = M > N ? 1 : 0;
   p.rot_amax = rot_amax;
   p.had_block = had_block;
+  p.bs_delta = bs_delta;
+  p.bs_parts = bs_parts;
   gemm_debug_params(p);
   // The bf16-operand kinds (BF16, W4A8) write a bf16 Y through TMA stores
   // (Y 16-byte aligned, N % 16 == 0 checked above); an FP32 Y is stored
@@ -376,6 +379,32 @@ sixbit_status sixbit_qgemm_rotamax(const sixbit_qact* A, const sixbit_weights* W
   if ((had_block != 16 && had_block != 64) || N % 128 != 0) return SIXBIT_ESHAPE;
   return qgemm_impl(A, nullptr, W, M, N, K, SIXBIT_MODE_NVFP4, mode_dev, epilogue, residual, Y, nullptr, nullptr,
                     nullptr, err_dev, stream, had_block, amax_out);
+}
+
+sixbit_status sixbit_qgemm_blockstats(const sixbit_qact* A, const uint16_t* X_bf16, const sixbit_weights* W, int M,
+                                      int N, int K, int mode, const int32_t* mode_dev, const uint16_t* residual,
+                                      uint16_t* Y, uint16_t* delta_cache, void* parts, void* workspace,
+                                      int32_t* err_dev, void* stream) {
+  if (residual == nullptr || Y == nullptr || delta_cache == nullptr || parts == nullptr) return SIXBIT_EINVAL;
+  if (!aligned16(delta_cache) || !aligned16(parts)) return SIXBIT_EALIGN;
+  return qgemm_impl(A, X_bf16, W, M, N, K, mode, mode_dev, SIXBIT_EPI_RESIDUAL, residual, Y, nullptr, nullptr,
+                    workspace, err_dev, stream, 0, nullptr, delta_cache, parts);
+}
+
+size_t sixbit_blockstats_parts_bytes(void) {
+  if (check_device() != SIXBIT_OK) return 0;
+  return bs_parts_bytes();
+}
+
+sixbit_status sixbit_block_stats_parts(const void* parts, int64_t n, sixbit_stats* stats_dev, int32_t* err_dev,
+                                       void* stream) {
+  (void)err_dev;
+  if (parts == nullptr || stats_dev == nullptr) return SIXBIT_EINVAL;
+  if (n <= 0) return SIXBIT_ESHAPE;
+  if (!aligned16(parts)) return SIXBIT_EALIGN;
+  sixbit_status s = check_device();
+  if (s != SIXBIT_OK) return s;
+  return cuda_status(launch_block_stats_parts(parts, n, stats_dev, static_cast<cudaStream_t>(stream)));
 }
 
 sixbit_status sixbit_block_stats(const uint16_t* x_in, const uint16_t* x_out, uint16_t* delta_cache, int64_t n,
@@ -490,6 +519,16 @@ sixbit_status sixbit_dit_block_end(const sixbit_policy_cfg* cfg, const sixbit_di
   const sixbit_status s = check_blocks(cfg, blocks, l, scratch);
   if (s != SIXBIT_OK) return s;
   return cuda_status(launch_dit_block_end(*cfg, *blocks, l, scratch, err_dev, static_cast<cudaStream_t>(stream)));
+}
+
+sixbit_status sixbit_dit_block_end_parts(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,
+                                         const void* parts, int32_t* err_dev, void* stream) {
+  (void)err_dev;
+  if (parts == nullptr || (blocks != nullptr && blocks->delta_format != SIXBIT_DELTA_BF16)) return SIXBIT_EINVAL;
+  if (!aligned16(parts)) return SIXBIT_EALIGN;
+  const sixbit_status s = check_blocks(cfg, blocks, l, const_cast<void*>(parts));
+  if (s != SIXBIT_OK) return s;
+  return cuda_status(launch_dit_block_end_parts(*cfg, *blocks, l, parts, static_cast<cudaStream_t>(stream)));
 }
 
 sixbit_status sixbit_dit_skip_run(const sixbit_policy_cfg* cfg, const sixbit_dit_blocks* blocks, int l,

@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "stats_common.cuh"
 
 namespace sixbit {
 
@@ -150,6 +151,108 @@ __device__ __forceinline__ void stage_bf16x32(uint8_t* box, int r, const float (
       w[i] = *reinterpret_cast<const uint32_t*>(&b);
     }
     *reinterpret_cast<uint4*>(box + r * 64 + ((q ^ ((r >> 1) & 3)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// ------------------------------------ block statistics from the epilogue --
+// With p.bs_delta set, the residual epilogue of a block's down projection also
+// does that block's statistics pass (technical summary sections 2.A-2.B,
+// popular summary section 3; the separate pass is block_stats_body in
+// stats_policy.cu): per 8 output elements x_out = bf16(Y) as stored, x_in =
+// the residual, Delta_prev read from bs_delta and Delta = bf16(x_out - x_in)
+// written over it, and the six sums accumulated per thread by the same
+// block_stats_vec.  When a thread is done, each epilogue warp reduces its
+// sums (shuffle tree) into one partial row at a fixed index; the row count
+// goes to the first word.  A separate kernel folds the rows in a fixed
+// order, so the totals are run-to-run deterministic.
+struct BsAcc {
+  TwoF2 d2, ddp, dp2;
+  Kahan2 xi2, sa;
+  float mx;
+};
+__device__ __forceinline__ BsAcc bs_zero() { return BsAcc{{0, 0}, {0, 0}, {0, 0}, {0, 0}, {0, 0}, 0.f}; }
+
+// Columns [n, n + 32) of row `row` < M; v holds their fp32 outputs (residual
+// added); the bf16 rounding of Y is redone here (round to nearest even).
+__device__ __forceinline__ void bs_chunk32(const GemmParams& p, int row, int n, const float (&v)[32], BsAcc& a) {
+  const size_t base = static_cast<size_t>(row) * p.N + n;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (n + 8 * q + 8 <= p.N) {
+      const uint4 ra = *reinterpret_cast<const uint4*>(p.residual + base + 8 * q);
+      const uint4 rp = *reinterpret_cast<const uint4*>(p.bs_delta + base + 8 * q);
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+        w[i] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      *reinterpret_cast<uint4*>(p.bs_delta + base + 8 * q) =
+          block_stats_vec(ra, make_uint4(w[0], w[1], w[2], w[3]), rp, a.d2, a.xi2, a.ddp, a.dp2, a.mx, a.sa);
+    }
+  }
+}
+
+// The RESIDUAL epilogue and bs_chunk32 in one: per half of the chunk, the
+// residual and Delta_prev vectors are loaded together (one memory round trip
+// for both), the residual added to v (as epilogue_apply32 does), and the
+// statistics taken.
+__device__ __forceinline__ void residual_bs_chunk32(const GemmParams& p, int row, int n, float (&v)[32], BsAcc& a) {
+  const size_t base = static_cast<size_t>(row) * p.N + n;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint4 ra[2], rp[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int q = 2 * h + u;
+      if (n + 8 * q + 8 <= p.N) {
+        ra[u] = *reinterpret_cast<const uint4*>(p.residual + base + 8 * q);
+        rp[u] = *reinterpret_cast<const uint4*>(p.bs_delta + base + 8 * q);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int q = 2 * h + u;
+      if (n + 8 * q + 8 <= p.N) {
+        const uint32_t x[4] = {ra[u].x, ra[u].y, ra[u].z, ra[u].w};
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[8 * q + 2 * i] = __fadd_rn(v[8 * q + 2 * i], __uint_as_float(x[i] << 16));
+          v[8 * q + 2 * i + 1] = __fadd_rn(v[8 * q + 2 * i + 1], __uint_as_float(x[i] & 0xFFFF0000u));
+          const __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+          w[i] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        *reinterpret_cast<uint4*>(p.bs_delta + base + 8 * q) =
+            block_stats_vec(ra[u], make_uint4(w[0], w[1], w[2], w[3]), rp[u], a.d2, a.xi2, a.ddp, a.dp2, a.mx, a.sa);
+      }
+    }
+  }
+}
+
+// L2 prefetch of the residual and Delta_prev of columns [n, n + ncols) of
+// row `row` (ncols * 2 bytes, one line per 128 bytes and the last one);
+// ncols >= 1.
+__device__ __forceinline__ void bs_prefetch(const GemmParams& p, int row, int n, int ncols) {
+  const size_t base = static_cast<size_t>(row) * p.N + n;
+  for (int c = 0; c < ncols; c += 64) {
+    prefetch_l2(p.residual + base + c);
+    prefetch_l2(p.bs_delta + base + c);
+  }
+  prefetch_l2(p.residual + base + ncols - 1);
+  prefetch_l2(p.bs_delta + base + ncols - 1);
+}
+
+// Warp `slot` of the grid (nslots rows in all) writes its partial row.
+__device__ __forceinline__ void bs_flush(const GemmParams& p, const BsAcc& a, int slot, int nslots, int lane) {
+  FF v[kBsSums] = {to_ff(a.d2), to_ff(a.xi2), to_ff(a.ddp), to_ff(a.dp2), FF{a.mx, 0.f}, to_ff(a.sa)};
+  const bool is_max[kBsSums] = {false, false, false, false, true, false};
+  warp_reduce<kBsSums>(v, is_max);
+  if (lane == 0) {
+    FF* row = reinterpret_cast<FF*>(static_cast<char*>(p.bs_parts) + 16) + static_cast<size_t>(slot) * kBsSums;
+#pragma unroll
+    for (int k = 0; k < kBsSums; ++k) row[k] = v[k];
+    if (slot == 0) *static_cast<uint32_t*>(p.bs_parts) = static_cast<uint32_t>(nslots);
   }
 }
 

@@ -38,7 +38,20 @@ struct GemmParams {
   int y_tma;               // bf16-operand kinds: bf16 Y is written by TMA stores through the Y tensor map
   uint64_t wait_ns;        // limit of every bounded wait (kWaitLimitNs unless a test shortens it)
   int withhold_first;      // test of the failure path: each CTA's producer skips its first stage
+  uint16_t* bs_delta;      // residual epilogue: the block's Delta cache (Delta_prev in, Delta out), or NULL
+  void* bs_parts;          // ... and its statistics, one partial row per epilogue warp (see gemm_common.cuh)
 };
+
+// Partial rows of a GEMM epilogue's block statistics: a uint32 row count at
+// byte 0, then rows of kBsSums float-float values {hi, lo} from byte 16, in
+// the order sum Delta^2, sum x_in^2, sum Delta Delta_prev, sum Delta_prev^2,
+// max |x_out| (lo = 0), sum |x_out|.  At most sm_count * kBsMaxWarps rows.
+constexpr int kBsSums = 6;
+constexpr int kBsMaxWarps = 16;
+size_t bs_parts_bytes();
+cudaError_t launch_block_stats_parts(const void* parts, int64_t n, sixbit_stats* stats, cudaStream_t st);
+cudaError_t launch_dit_block_end_parts(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l,
+                                       const void* parts, cudaStream_t st);
 
 // Test setting of the GEMMs' failure path (sixbit_debug_gemm_timeout).
 void gemm_debug_params(GemmParams& p);

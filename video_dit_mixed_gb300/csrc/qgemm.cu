@@ -151,7 +151,9 @@ __device__ __forceinline__ float rot_amax64(float (&v)[2][32]) {
 
 // Persistent kernel: each CTA walks output tiles t = blockIdx.x, +gridDim.x,
 // ...; p.n_fastest picks whether row or column tiles vary fastest along t.
-template <int KIND>
+// BS: the residual epilogue also produces the block's statistics and Delta
+// (p.bs_delta, p.bs_parts; gemm_common.cuh).
+template <int KIND, bool BS>
 __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
@@ -349,11 +351,17 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
     const int col0 = (ew >> 2) * kEpiCols;        // first accumulator column of this thread
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16) + col0;
     uint8_t* my_box = staging + ew * kBoxBytes;   // BF16 kind: this warp's output box
+    BsAcc bs = bs_zero();
     // Epilogue + store of columns [n, n + 32) of this lane's row (n < N, warp-uniform).
     auto store32 = [&](int row, int n, float (&v)[32]) {
       if constexpr (tma_y<KIND>()) {
         if (p.y_tma) {
-          if (row < p.M) epilogue_apply32(p, row, n, v);
+          if (row < p.M) {
+            if constexpr (BS)
+              residual_bs_chunk32(p, row, n, v, bs);
+            else
+              epilogue_apply32(p, row, n, v);
+          }
           if (lane == 0) bulk_wait_read0();  // the previous box has been read out
           __syncwarp();
           stage_bf16x32(my_box, lane, v);
@@ -366,7 +374,9 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
           return;
         }
       }
-      epilogue_store32(p, row, n, v);
+      epilogue_store32(p, row, n, v);  // leaves the stored bf16 values in v
+      if constexpr (BS)
+        if (row < p.M) bs_chunk32(p, row, n, v, bs);
     };
     uint32_t ac = 0;
     bool ok = true;
@@ -391,7 +401,24 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
         tc_fence_after();
         float alpha = 1.0f;
         if constexpr (kNvf4) alpha = __fmul_rn(*p.s_a, *p.s_b);
-        if constexpr (kNvf4) {
+        if constexpr (kNvf4 && BS) {
+          // the block statistics need the registers: one 32-column chunk at a
+          // time, the accumulator released after the last load
+#pragma unroll 1
+          for (int c = 0; c < kEpiCols / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(lane_addr + c * 32, r);
+            tmem_ld_wait(r);
+            if (c == kEpiCols / 32 - 1) release_acc(&acce[buf], lane);
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), alpha);
+            if (nb + c * 32 < p.N) {
+              epilogue_store32(p, row, nb + c * 32, v);  // leaves the stored bf16 values in v
+              if (row < p.M) bs_chunk32(p, row, nb + c * 32, v, bs);
+            }
+          }
+        } else if constexpr (kNvf4) {
           // single accumulator: drain all of this thread's columns, release, then store
           uint32_t r[kEpiCols / 32][32];
 #pragma unroll
@@ -406,7 +433,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
             for (int j = 0; j < 32; ++j) v[c][j] = __fmul_rn(__uint_as_float(r[c][j]), alpha);
             if (nb + c * 32 < p.N) epilogue_store32(p, row, nb + c * 32, v[c]);
           }
-          if constexpr (kEpiCols == 64) {
+          if constexpr (kEpiCols == 64 && !BS) {  // (an up projection's epilogue; BS is a down projection's)
             if (p.rot_amax != nullptr) {  // the next quantizer's amax pass, on the stored values
               float m = 0.f;
               if (row < p.M && nb < p.N) m = p.had_block == 16 ? rot_amax64<16>(v) : rot_amax64<64>(v);
@@ -434,6 +461,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
         ++ac;
       }
     }
+    if constexpr (BS) bs_flush(p, bs, blockIdx.x * kEpiWarps + ew, gridDim.x * kEpiWarps, lane);
     if (!ok) {
       set_error(p.err, SIXBIT_ETIMEOUT);
       *abort_flag = 1;
@@ -490,16 +518,16 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
 
 // ------------------------------------------------------------ host launch --
 
-template <int KIND>
+template <int KIND, bool BS>
 static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
                               cudaStream_t st) {
   constexpr int smem = gemm_smem_bytes<KIND>();
-  const cudaError_t e = set_smem_once<qgemm_kernel<KIND>>(smem);
+  const cudaError_t e = set_smem_once<qgemm_kernel<KIND, BS>>(smem);
   if (e != cudaSuccess) return e;
   const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
   const int sms = sm_count();
   const int grid = ntiles < sms ? ntiles : sms;
-  qgemm_kernel<KIND><<<grid, gemm_threads<KIND>(), smem, st>>>(a, b, y, p);
+  qgemm_kernel<KIND, BS><<<grid, gemm_threads<KIND>(), smem, st>>>(a, b, y, p);
   note_launch();
   return cudaGetLastError();
 }
@@ -507,11 +535,13 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
 cudaError_t launch_qgemm_nvf4(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t st) {
   GemmParams q = p;
   q.y_tma = 0;
-  return launch_one<KIND_NVF4>(a, b, a /*unused*/, q, st);
+  return q.bs_delta != nullptr ? launch_one<KIND_NVF4, true>(a, b, a /*unused*/, q, st)
+                                : launch_one<KIND_NVF4, false>(a, b, a /*unused*/, q, st);
 }
 cudaError_t launch_qgemm_bf16(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const GemmParams& p,
                               cudaStream_t st) {
-  return launch_one<KIND_BF16>(a, b, y, p, st);
+  return p.bs_delta != nullptr ? launch_one<KIND_BF16, true>(a, b, y, p, st)
+                                : launch_one<KIND_BF16, false>(a, b, y, p, st);
 }
 
 }  // namespace sixbit

@@ -157,7 +157,9 @@ __device__ __forceinline__ void s8x16_to_f16x8(const uint4& in, uint32_t* o) {
   }
 }
 
-template <bool DBG>
+// DBG: write the exact group sums to p.acc_dbg.  BS: the residual epilogue
+// also produces the block's statistics and Delta (p.bs_delta, p.bs_parts).
+template <bool DBG, bool BS>
 __global__ void __launch_bounds__(kThreads, 1)
     w4a8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                 const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
@@ -402,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* my_box = fold_area + ew * kWarpArea;                          // the same bytes
     uint32_t gi = 0;
     bool ok = true;
+    BsAcc bs = bs_zero();
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
       int m_tile, n_tile;
       tile_of(t, m_tile, n_tile);
@@ -430,6 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         cp_async_wait_newest<kSwRing - 1>();   // this lane's copy of group g has landed
         __syncwarp();                          // and every other lane's
         const float4* sw4 = reinterpret_cast<const float4*>(my_sw + (g % kSwRing) * kCols);
+        if constexpr (BS)  // the epilogue's residual and Delta_prev, to L2 a few groups ahead
+          if (g == (groups > 4 ? groups - 4 : 0) && row < p.M && n0 < p.N) bs_prefetch(p, row, n0, min(kCols, p.N - n0));
         // group gi is complete when its commit arrives on its stage's W-slot
         // barrier; that barrier cannot run a phase past this wait, since its
         // next phase is group gi + 3, which needs buffer (gi + 1) & 1 back
@@ -499,7 +504,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           epilogue_store32(p, row, n, v);
           continue;
         }
-        if (row < p.M) epilogue_apply32(p, row, n, v);
+        if (row < p.M) {
+          if constexpr (BS)
+            residual_bs_chunk32(p, row, n, v, bs);
+          else
+            epilogue_apply32(p, row, n, v);
+        }
         if (lane == 0) bulk_wait_read0();  // the previous box has been read out
         __syncwarp();
         stage_bf16x32(my_box, lane, v);
@@ -511,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if constexpr (BS) bs_flush(p, bs, blockIdx.x * kFoldWarps + ew, gridDim.x * kFoldWarps, lane);
     if (!ok) {
       set_error(p.err, SIXBIT_ETIMEOUT);
       *abort_flag = 1;
@@ -570,17 +581,17 @@ cudaError_t launch_w4_expand(const uint8_t* codes, int N, int K, uint16_t* ws, c
   return cudaGetLastError();
 }
 
-template <bool DBG>
+template <bool DBG, bool BS>
 static cudaError_t launch_w4a8(const CUtensorMap& a_s8, const CUtensorMap& w_f16, const CUtensorMap& y,
                                const GemmParams& p, cudaStream_t st) {
   using namespace w4a8;
-  cudaError_t e = set_smem_once<w4a8_kernel<DBG>>(kSmemBytes);
+  cudaError_t e = set_smem_once<w4a8_kernel<DBG, BS>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   static ContextCache<int> regs_cache;
   int regs = 0;
   e = regs_cache.get(&regs, [](int* o) {
     cudaFuncAttributes fa;
-    const cudaError_t r = cudaFuncGetAttributes(&fa, w4a8_kernel<DBG>);
+    const cudaError_t r = cudaFuncGetAttributes(&fa, w4a8_kernel<DBG, BS>);
     *o = fa.numRegs;
     return r;
   });
@@ -591,14 +602,16 @@ static cudaError_t launch_w4a8(const CUtensorMap& a_s8, const CUtensorMap& w_f16
   const int ntiles = ((p.M + kBM - 1) / kBM) * ((p.N + kBN - 1) / kBN);
   const int sms = sm_count();
   const int grid = ntiles < sms ? ntiles : sms;
-  w4a8_kernel<DBG><<<grid, kThreads, kSmemBytes, st>>>(a_s8, w_f16, y, p);
+  w4a8_kernel<DBG, BS><<<grid, kThreads, kSmemBytes, st>>>(a_s8, w_f16, y, p);
   note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_qgemm_w4a8(const CUtensorMap& a_s8, const CUtensorMap& w_f16, const CUtensorMap& y,
                               const GemmParams& p, cudaStream_t st) {
-  return p.acc_dbg != nullptr ? launch_w4a8<true>(a_s8, w_f16, y, p, st) : launch_w4a8<false>(a_s8, w_f16, y, p, st);
+  if (p.acc_dbg != nullptr) return launch_w4a8<true, false>(a_s8, w_f16, y, p, st);
+  return p.bs_delta != nullptr ? launch_w4a8<false, true>(a_s8, w_f16, y, p, st)
+                               : launch_w4a8<false, false>(a_s8, w_f16, y, p, st);
 }
 
 }  // namespace sixbit

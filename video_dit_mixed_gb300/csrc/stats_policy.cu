@@ -21,6 +21,7 @@
 #include "common.cuh"
 #include "ctx_cache.h"
 #include "internal.h"
+#include "stats_common.cuh"
 
 namespace sixbit {
 
@@ -28,69 +29,6 @@ constexpr int kStThreads = 256;
 constexpr int kStMaxBlocks = 1216;  // 152 SMs x 8
 constexpr int kNumSums = 8;
 
-// Per-thread accumulators on packed FP32 pairs (two independent lanes per
-// instruction, lane-wise identical rounding); a thread accumulates even and
-// odd elements in the two lanes.  TwoF2 keeps an unevaluated sum s + c with
-// Knuth's TwoSum (about 48 bits); Kahan2 keeps s - c with Kahan compensation
-// (error about 2u|S| for a thread's partial, enough for the outlier ratio and
-// Gamma, whose bands are relative 1e-6).
-struct TwoF2 {
-  uint64_t s, c;
-};
-
-__device__ __forceinline__ void two_add2(TwoF2& a, uint64_t x) {
-  const uint64_t s = f2_add(a.s, x);
-  const uint64_t bp = f2_sub(s, a.s);
-  const uint64_t err = f2_add(f2_sub(a.s, f2_sub(s, bp)), f2_sub(x, bp));
-  a.s = s;
-  a.c = f2_add(a.c, err);
-}
-
-struct Kahan2 {
-  uint64_t s, c;
-};
-
-__device__ __forceinline__ void kahan_add2(Kahan2& k, uint64_t x) {
-  const uint64_t y = f2_sub(x, k.c);
-  const uint64_t t = f2_add(k.s, y);
-  k.c = f2_sub(f2_sub(t, k.s), y);
-  k.s = t;
-}
-
-// Float-float value hi + lo (|lo| <= ulp(hi)/2 after ff_add).  ff_add is the
-// double-float addition of Dekker / Bailey: TwoSum of the high parts, then the
-// low parts folded in and renormalised; its error is a few 2^-44 of |a| + |b|.
-// Combining partials this way keeps GB300's slow FP64 pipe off the reduction.
-struct FF {
-  float hi, lo;
-};
-
-__device__ __forceinline__ FF ff_add(FF a, FF b) {
-  const float s = __fadd_rn(a.hi, b.hi);
-  const float bp = __fsub_rn(s, a.hi);
-  const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bp)), __fsub_rn(b.hi, bp));
-  const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), e);
-  const float hi = __fadd_rn(s, lo);
-  return FF{hi, __fsub_rn(lo, __fsub_rn(hi, s))};
-}
-
-__device__ __forceinline__ FF ff_max(FF a, FF b) { return FF{fmaxf(a.hi, b.hi), 0.f}; }
-
-__device__ __forceinline__ FF to_ff(const TwoF2& a) {
-  return ff_add(FF{f2_lo(a.s), f2_lo(a.c)}, FF{f2_hi(a.s), f2_hi(a.c)});
-}
-
-__device__ __forceinline__ FF to_ff(const Kahan2& k) {
-  return ff_add(FF{f2_lo(k.s), -f2_lo(k.c)}, FF{f2_hi(k.s), -f2_hi(k.c)});
-}
-
-__device__ __forceinline__ FF ff_shfl_xor(FF a, int o) {
-  return FF{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
-}
-
-__device__ __forceinline__ float f2_max_abs(uint64_t v, float m) {
-  return fmaxf(m, fmaxf(fabsf(f2_lo(v)), fabsf(f2_hi(v))));
-}
 
 __device__ __forceinline__ uint4 ld16(const void* p) {
   uint4 v;
@@ -124,19 +62,6 @@ __device__ __forceinline__ Scratch scratch_view(void* p) {
   return s;
 }
 
-// Combines v[k] over a warp (xor-shuffle tree; sums with ff_add, maxima with
-// ff_max), leaving the result in every lane.
-template <int NS, int W = 32>
-__device__ __forceinline__ void warp_reduce(FF (&v)[NS], const bool (&is_max)[NS]) {
-#pragma unroll
-  for (int o = W / 2; o > 0; o >>= 1) {
-#pragma unroll
-    for (int k = 0; k < NS; ++k) {
-      const FF y = ff_shfl_xor(v[k], o);
-      v[k] = is_max[k] ? ff_max(v[k], y) : ff_add(v[k], y);
-    }
-  }
-}
 
 // Combines the warps' values through shared memory; the CTA's result ends up
 // in warp 0.
@@ -220,12 +145,6 @@ __device__ __forceinline__ bool mode_is(const int32_t* mode_dev, int want) {
 // Each thread walks vectors of 8 elements (four packed pairs) with a grid
 // stride, two vectors per iteration (both loads issued before either is used).
 
-__device__ __forceinline__ void unpack4x2(const uint4& r, uint64_t (&v)[4]) {
-  v[0] = f2_from_bf16x2(r.x);
-  v[1] = f2_from_bf16x2(r.y);
-  v[2] = f2_from_bf16x2(r.z);
-  v[3] = f2_from_bf16x2(r.w);
-}
 
 __device__ __forceinline__ void tensor_stats_vec(const uint4& r, float& mx, Kahan2& sa, Kahan2& sq) {
   uint64_t v[4];
@@ -270,26 +189,6 @@ __global__ void __launch_bounds__(kStThreads) tensor_stats_kernel(const uint16_t
   }
 }
 
-__device__ __forceinline__ uint4 block_stats_vec(const uint4& ra, const uint4& rb, const uint4& rp, TwoF2& d2,
-                                                 Kahan2& xi2, TwoF2& ddp, TwoF2& dp2, float& mx, Kahan2& sa) {
-  uint64_t a[4], b[4], p[4];
-  unpack4x2(ra, a);
-  unpack4x2(rb, b);
-  unpack4x2(rp, p);
-  uint32_t w[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    w[j] = f2_to_bf16x2(f2_sub(b[j], a[j]));      // Delta = bf16(x_out - x_in)
-    const uint64_t d = f2_from_bf16x2(w[j]);
-    two_add2(d2, f2_mul(d, d));
-    two_add2(ddp, f2_mul(d, p[j]));
-    two_add2(dp2, f2_mul(p[j], p[j]));
-    kahan_add2(xi2, f2_mul(a[j], a[j]));
-    mx = f2_max_abs(b[j], mx);
-    kahan_add2(sa, f2_abs(b[j]));
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
 
 // One pass over x_in, x_out, Delta_prev: writes Delta_new over Delta_prev and
 // reduces {sum Delta^2, sum x_in^2, sum Delta*Delta_prev, sum Delta_prev^2,
@@ -823,6 +722,65 @@ __global__ void __launch_bounds__(kStThreads, MX ? 3 : 4) dit_block_end_kernel(s
   }
 }
 
+// Folds the partial rows a GEMM epilogue wrote for a block's statistics
+// (count, then rows of kBsSums float-float values; internal.h) in a fixed
+// order: thread t takes rows t, t + 256, ..., then the CTA tree.  One CTA;
+// true in warp 0, with the totals in tot.
+__device__ bool fold_bs_parts(const void* parts, double (&tot)[kBsSums]) {
+  __shared__ FF red[kStThreads / 32][kBsSums];
+  const bool is_max[kBsSums] = {false, false, false, false, true, false};
+  FF v[kBsSums];
+#pragma unroll
+  for (int k = 0; k < kBsSums; ++k) v[k] = FF{0.f, 0.f};
+  const uint32_t rows = *static_cast<const uint32_t*>(parts);
+  const FF* base = reinterpret_cast<const FF*>(static_cast<const char*>(parts) + 16);
+  uint32_t r = threadIdx.x;
+  for (; r + 3 * kStThreads < rows; r += 4 * kStThreads) {  // four rows' loads in flight
+    FF y[4][kBsSums];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int k = 0; k < kBsSums; ++k) y[u][k] = base[static_cast<size_t>(r + u * kStThreads) * kBsSums + k];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int k = 0; k < kBsSums; ++k) v[k] = is_max[k] ? ff_max(v[k], y[u][k]) : ff_add(v[k], y[u][k]);
+  }
+  for (; r < rows; r += kStThreads) {
+#pragma unroll
+    for (int k = 0; k < kBsSums; ++k) {
+      const FF y = base[static_cast<size_t>(r) * kBsSums + k];
+      v[k] = is_max[k] ? ff_max(v[k], y) : ff_add(v[k], y);
+    }
+  }
+  cta_reduce<kBsSums>(v, is_max, red);
+  if (threadIdx.x >= 32) return false;
+#pragma unroll
+  for (int k = 0; k < kBsSums; ++k)
+    tot[k] = static_cast<double>(__shfl_sync(0xffffffffu, v[k].hi, 0)) +
+             static_cast<double>(__shfl_sync(0xffffffffu, v[k].lo, 0));
+  return true;
+}
+
+__global__ void __launch_bounds__(kStThreads) block_stats_parts_kernel(const void* parts, int64_t n,
+                                                                       sixbit_stats* stats) {
+  double tot[kBsSums];
+  if (fold_bs_parts(parts, tot) && threadIdx.x == 0) write_block_stats(stats, tot, n);
+}
+
+// dit_block_end_kernel for a block whose down projection produced the
+// statistics and Delta in its epilogue: the fold, stats[l], block l+1's
+// decision.
+__global__ void __launch_bounds__(kStThreads) dit_block_end_parts_kernel(sixbit_policy_cfg cfg, sixbit_dit_blocks B,
+                                                                         int l, const void* parts) {
+  if (SIXBIT_MODE_OF(B.modes[l]) == SIXBIT_MODE_SKIP) return;  // uniform: a skipped block has no end
+  double tot[kBsSums];
+  if (!fold_bs_parts(parts, tot)) return;  // warp 0 continues
+  if (threadIdx.x == 0) write_block_stats(&B.stats[l], tot, B.n);
+  __syncwarp();
+  if (l + 1 < B.L) decide_block(cfg, B, l + 1);
+}
+
 // v = bf16(v + Delta_j) for the k cached deltas of a run, in order (bf16 cache:
 // vector i of each [n] slice; eight / four / one loads in flight)
 __device__ __forceinline__ void skip_run_bf16(uint64_t (&v)[4], const uint16_t* dp, int64_t n, int k) {
@@ -963,6 +921,20 @@ static int stats_grid(int64_t n) {
 }
 
 size_t stats_scratch_bytes(int64_t) { return 16 + static_cast<size_t>(kStMaxBlocks) * kNumSums * sizeof(FF); }
+size_t bs_parts_bytes() { return 16 + static_cast<size_t>(sm_count()) * kBsMaxWarps * kBsSums * sizeof(FF); }
+
+cudaError_t launch_block_stats_parts(const void* parts, int64_t n, sixbit_stats* stats, cudaStream_t st) {
+  block_stats_parts_kernel<<<1, kStThreads, 0, st>>>(parts, n, stats);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dit_block_end_parts(const sixbit_policy_cfg& cfg, const sixbit_dit_blocks& B, int l,
+                                       const void* parts, cudaStream_t st) {
+  dit_block_end_parts_kernel<<<1, kStThreads, 0, st>>>(cfg, B, l, parts);
+  note_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_tensor_stats(const uint16_t* x, int64_t n, double* out, void* scratch, cudaStream_t st) {
   tensor_stats_kernel<<<stats_grid<tensor_stats_kernel>(n), kStThreads, 0, st>>>(x, n, out, scratch);

@@ -28,10 +28,17 @@ from . import ops
 
 class DiT:
     def __init__(self, tokens: int, hidden: int, ffn: int, blocks: int, had_block: int, packed, cfg=None,
-                 device="cuda", delta_format: str = "bf16"):
+                 device="cuda", delta_format: str = "bf16", fused_stats: bool = True):
         """packed: list of (PackedWeights up [ffn, hidden], PackedWeights down [hidden, ffn]);
         cfg: one policy_cfg for every block, or a list of one per block (per-depth thresholds);
-        delta_format: the Delta cache's storage, "bf16" or "mxfp8" (about half the bytes)."""
+        delta_format: the Delta cache's storage, "bf16" or "mxfp8" (about half the bytes);
+        fused_stats (bf16 cache): a block computed in BF16 takes its statistics and Delta from its
+        down projection's epilogue (qgemm_blockstats + dit_block_end_parts) instead of a separate
+        pass, in the graph and host-dispatched steps (the mode-gated eager step keeps the pass).
+        Measured at dit_2b's down projection, the epilogue adds 31 us to the BF16 GEMM against the
+        pass's 63 us, but 131 us to the W4A8 and 130 us to the NVFP4 one (their epilogue runs on
+        the warps that also feed the tensor core, or holds its single accumulator), so those keep
+        the pass."""
         assert len(packed) == blocks
         assert delta_format in ("bf16", "mxfp8")
         dev = torch.device(device)
@@ -65,6 +72,9 @@ class DiT:
         self.modes = torch.zeros(blocks, dtype=torch.int32, device=dev)
         self.run_len = torch.zeros(blocks, dtype=torch.int32, device=dev)   # per run start, within a step
         self.scratch = ops.new_scratch(tokens * ffn, dev)
+        self.fused_stats = fused_stats and delta_format == "bf16"
+        self.fused_modes = (ops.MODE_BF16,) if self.fused_stats else ()
+        self.parts = ops.new_blockstats_parts(dev) if self.fused_stats else None
         self.conds = torch.zeros(blocks, dtype=torch.int64, device=dev)  # graph condition handles
         self.rec = self._record(None)
         self.graph = None
@@ -121,7 +131,7 @@ class DiT:
 
     def _compute_body(self, x, out, l, mode, rec=None, note=None):
         """The kernels of one computed block in a fixed mode (no mode word), ending with
-        dit_block_end; note(label) is called on the host after each call when given."""
+        dit_block_end (or dit_block_end_parts); note(label) is called on the host after each call when given."""
         o = ops
         rec = rec or self.rec
         note = note or (lambda label: None)
@@ -139,10 +149,16 @@ class DiT:
         if quant:
             o.hadamard_quant(self.h, self.b, mode, out=self.qa_h, tamax=self.qa_h.tensor_amax if fused else None)
             note("hq_h")
-        o.qgemm(self.qa_h if quant else None, self.h, down, mode, epilogue=o.EPI_RESIDUAL, residual=x, out=out,
-                m=self.T, ws=self.ws)
-        note("qgemm_down")
-        o.dit_block_end(self.cfg, rec, l, self.scratch)
+        if mode in self.fused_modes:
+            o.qgemm_blockstats(self.qa_h if quant else None, self.h, down, mode, residual=x, out=out,
+                               delta_cache=self.deltas[l], parts=self.parts, m=self.T, ws=self.ws)
+            note("qgemm_down")
+            o.dit_block_end_parts(self.cfg, rec, l, self.parts)
+        else:
+            o.qgemm(self.qa_h if quant else None, self.h, down, mode, epilogue=o.EPI_RESIDUAL, residual=x, out=out,
+                    m=self.T, ws=self.ws)
+            note("qgemm_down")
+            o.dit_block_end(self.cfg, rec, l, self.scratch)
         note("block_stats")
 
     def enqueue_step_switched(self, body_stream):

@@ -148,6 +148,36 @@ def qgemm_rotamax(a: QActTensors, w: PackedWeights, had_block: int, amax_out: to
     return out
 
 
+def qgemm_blockstats(a: QActTensors | None, x_bf16, w: PackedWeights, mode: int, residual, out, delta_cache,
+                     parts, mode_dev=None, err=None, stream=None, m: int | None = None, ws=None):
+    """qgemm with the RESIDUAL epilogue that also updates delta_cache (Delta_prev -> Delta) and writes
+    the block statistics' partial rows to parts (blockstats_parts_bytes(); fold with block_stats_parts
+    or dit_block_end_parts)."""
+    n, k = w.n, w.k
+    if ws is None and (mode == MODE_INT8 or mode_dev is not None):
+        ws = workspace(n, k, w.bf16_w.device)
+    m = m if m is not None else (a.m if a is not None else x_bf16.shape[0])
+    ca = a.c() if a is not None else None
+    cw = w.c()
+    check(_lib.sixbit_qgemm_blockstats(C.byref(ca) if ca is not None else None, _p(x_bf16), C.byref(cw), m, n, k,
+                                       mode, _p(mode_dev), _p(residual), _p(out), _p(delta_cache), _p(parts), _p(ws),
+                                       _p(err), _stream(stream)), "qgemm_blockstats")
+    return out
+
+
+def blockstats_parts_bytes() -> int:
+    return int(_lib.sixbit_blockstats_parts_bytes())
+
+
+def new_blockstats_parts(device="cuda") -> torch.Tensor:
+    return torch.zeros(blockstats_parts_bytes(), dtype=torch.uint8, device=device)
+
+
+def block_stats_parts(parts: torch.Tensor, n: int, stats: torch.Tensor, stream=None):
+    check(_lib.sixbit_block_stats_parts(_p(parts), n, _p(stats), None, _stream(stream)), "block_stats_parts")
+    return stats
+
+
 def tensor_stats(x: torch.Tensor, out: torch.Tensor, scratch: torch.Tensor, stream=None) -> torch.Tensor:
     check(_lib.sixbit_tensor_stats(_p(x), x.numel(), _p(out), _p(scratch), None, _stream(stream)), "tensor_stats")
     return out
@@ -253,6 +283,13 @@ def dit_blocks(states, stats, modes, run_len, in_stats0, x0, buf0, buf1, deltas,
 def dit_begin(cfg: PolicyCfg, blocks: DitBlocks, scratch: torch.Tensor, err=None, stream=None):
     """sixbit_dit_begin: statistics of the step input, then block 0's decision."""
     check(_lib.sixbit_dit_begin(C.byref(cfg), C.byref(blocks), _p(scratch), _p(err), _stream(stream)), "dit_begin")
+
+
+def dit_block_end_parts(cfg: PolicyCfg, blocks: DitBlocks, l: int, parts: torch.Tensor, err=None, stream=None):
+    """sixbit_dit_block_end_parts: fold the statistics block l's down projection wrote to parts, then
+    block l+1's decision (nothing when block l skipped)."""
+    check(_lib.sixbit_dit_block_end_parts(C.byref(cfg), C.byref(blocks), l, _p(parts), _p(err), _stream(stream)),
+          "dit_block_end_parts")
 
 
 def dit_block_end(cfg: PolicyCfg, blocks: DitBlocks, l: int, scratch: torch.Tensor, err=None, stream=None):
