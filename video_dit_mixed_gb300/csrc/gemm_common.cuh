@@ -243,16 +243,30 @@ __device__ __forceinline__ void bs_prefetch(const GemmParams& p, int row, int n,
   prefetch_l2(p.bs_delta + base + ncols - 1);
 }
 
-// Warp `slot` of the grid (nslots rows in all) writes its partial row.
-__device__ __forceinline__ void bs_flush(const GemmParams& p, const BsAcc& a, int slot, int nslots, int lane) {
+// The epilogue's nw warps (warp index ew, all lanes) end the statistics:
+// each reduces its threads' sums (shuffle tree), the CTA's rows meet in
+// shared memory behind a named barrier over those warps only (id 1), and
+// warp 0 folds them in a fixed order into the CTA's partial row (row
+// blockIdx.x); CTA 0 also writes the row count.
+__device__ __forceinline__ void bs_flush(const GemmParams& p, const BsAcc& a, int ew, int nw, int lane) {
+  __shared__ FF bs_red[kBsMaxWarps][kBsSums];
   FF v[kBsSums] = {to_ff(a.d2), to_ff(a.xi2), to_ff(a.ddp), to_ff(a.dp2), FF{a.mx, 0.f}, to_ff(a.sa)};
   const bool is_max[kBsSums] = {false, false, false, false, true, false};
   warp_reduce<kBsSums>(v, is_max);
   if (lane == 0) {
-    FF* row = reinterpret_cast<FF*>(static_cast<char*>(p.bs_parts) + 16) + static_cast<size_t>(slot) * kBsSums;
+#pragma unroll
+    for (int k = 0; k < kBsSums; ++k) bs_red[ew][k] = v[k];
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(nw * 32) : "memory");
+  if (ew != 0) return;
+#pragma unroll
+  for (int k = 0; k < kBsSums; ++k) v[k] = lane < nw ? bs_red[lane][k] : FF{0.f, 0.f};
+  warp_reduce<kBsSums, kBsMaxWarps>(v, is_max);
+  if (lane == 0) {
+    FF* row = reinterpret_cast<FF*>(static_cast<char*>(p.bs_parts) + 16) + static_cast<size_t>(blockIdx.x) * kBsSums;
 #pragma unroll
     for (int k = 0; k < kBsSums; ++k) row[k] = v[k];
-    if (slot == 0) *static_cast<uint32_t*>(p.bs_parts) = static_cast<uint32_t>(nslots);
+    if (blockIdx.x == 0) *static_cast<uint32_t*>(p.bs_parts) = gridDim.x;
   }
 }
 

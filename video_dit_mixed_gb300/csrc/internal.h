@@ -43,9 +43,10 @@ struct GemmParams {
 };
 
 // Partial rows of a GEMM epilogue's block statistics: a uint32 row count at
-// byte 0, then rows of kBsSums float-float values {hi, lo} from byte 16, in
-// the order sum Delta^2, sum x_in^2, sum Delta Delta_prev, sum Delta_prev^2,
-// max |x_out| (lo = 0), sum |x_out|.  At most sm_count * kBsMaxWarps rows.
+// byte 0, then one row per CTA of kBsSums float-float values {hi, lo} from
+// byte 16, in the order sum Delta^2, sum x_in^2, sum Delta Delta_prev,
+// sum Delta_prev^2, max |x_out| (lo = 0), sum |x_out|.  At most sm_count
+// rows; a CTA has at most kBsMaxWarps epilogue warps.
 constexpr int kBsSums = 6;
 constexpr int kBsMaxWarps = 16;
 size_t bs_parts_bytes();

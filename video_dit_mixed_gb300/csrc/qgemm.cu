@@ -48,6 +48,7 @@ constexpr int kBN = 256;        // output tile columns
 constexpr int kEpiWarps = 16;
 constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // accumulator columns per thread
 constexpr int kEpiWarp0 = 2;                     // first epilogue warp
+static_assert(kEpiWarps <= kBsMaxWarps, "block statistics: one partial per epilogue warp");
 
 enum { KIND_BF16 = 0, KIND_NVF4 = 1 };
 
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(gemm_threads<KIND>(), 1)
         ++ac;
       }
     }
-    if constexpr (BS) bs_flush(p, bs, blockIdx.x * kEpiWarps + ew, gridDim.x * kEpiWarps, lane);
+    if constexpr (BS) bs_flush(p, bs, ew, kEpiWarps, lane);
     if (!ok) {
       set_error(p.err, SIXBIT_ETIMEOUT);
       *abort_flag = 1;

@@ -100,6 +100,7 @@ constexpr int kSwLanes = kCols / 4;                  // lanes copying a group's 
 constexpr int kBoxBytes = 32 * 64;                   // one 32 x 32 bf16 output box
 constexpr int kWarpArea = 2048;                      // a fold warp's scale ring, or its output box
 static_assert(kSwRing * kCols * 4 <= kWarpArea && kBoxBytes <= kWarpArea, "fold warp area");
+static_assert(kFoldWarps <= kBsMaxWarps, "block statistics: one partial per fold warp");
 constexpr int kRegsLaunch = 128, kRegsLow = 40, kRegsConv = 80, kRegsHigh = 192;
 static_assert(4 * kRegsLow + 4 * kRegsConv + 8 * kRegsHigh <= 16 * kRegsLaunch &&
                   kRegsLow + kRegsConv + 2 * kRegsHigh <= 4 * kRegsLaunch,
@@ -521,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if constexpr (BS) bs_flush(p, bs, blockIdx.x * kFoldWarps + ew, gridDim.x * kFoldWarps, lane);
+    if constexpr (BS) bs_flush(p, bs, ew, kFoldWarps, lane);
     if (!ok) {
       set_error(p.err, SIXBIT_ETIMEOUT);
       *abort_flag = 1;

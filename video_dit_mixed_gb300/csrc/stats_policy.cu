@@ -921,7 +921,7 @@ static int stats_grid(int64_t n) {
 }
 
 size_t stats_scratch_bytes(int64_t) { return 16 + static_cast<size_t>(kStMaxBlocks) * kNumSums * sizeof(FF); }
-size_t bs_parts_bytes() { return 16 + static_cast<size_t>(sm_count()) * kBsMaxWarps * kBsSums * sizeof(FF); }
+size_t bs_parts_bytes() { return 16 + static_cast<size_t>(sm_count()) * kBsSums * sizeof(FF); }
 
 cudaError_t launch_block_stats_parts(const void* parts, int64_t n, sixbit_stats* stats, cudaStream_t st) {
   block_stats_parts_kernel<<<1, kStThreads, 0, st>>>(parts, n, stats);
