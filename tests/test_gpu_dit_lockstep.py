@@ -1,4 +1,5 @@
-"""Full-size DiT runs checked in lockstep against the oracle (C3 dit_2b, its gated variant, C4 dit_5b).
+"""DiT runs checked in lockstep against the oracle (C3 dit_2b, its gated variant, C4 dit_5b, and the
+small dit_tiny with every step deep-checked).
 
 At these sizes the oracle cannot run the chain itself (a float64 block-step
 is ~1 TFLOP), so the comparison is staged: every block-step is checked on the
@@ -248,6 +249,14 @@ def _lockstep(name, steps, blocks=None, deep_every=5, nrows=32, delta_format="bf
             ratio = stats.outlier_ratio(bs["out"])
             l += 1
     return dict(near=near, seen=seen, checked=checked)
+
+
+def test_dit_tiny_lockstep_every_step():
+    """The small DiT (256 tokens, 4 blocks) in lockstep, one block-step deep-checked every step:
+    the element-wise counterpart of the independent-chain comparison in test_gpu_dit.py."""
+    r = _lockstep("dit_tiny", steps=20, deep_every=1, nrows=32)
+    assert r["checked"] >= 15 and {policy.NVFP4, policy.INT8, policy.BF16, policy.SKIP} <= r["seen"], r
+    print(f"dit_tiny: {r}")
 
 
 def test_dit_2b_lockstep():
