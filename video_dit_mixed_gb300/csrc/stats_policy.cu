@@ -143,7 +143,8 @@ __device__ __forceinline__ bool mode_is(const int32_t* mode_dev, int want) {
 }
 
 // Each thread walks vectors of 8 elements (four packed pairs) with a grid
-// stride, two vectors per iteration (both loads issued before either is used).
+// stride, several vectors per iteration (their loads issued before any is
+// used).
 
 
 __device__ __forceinline__ void tensor_stats_vec(const uint4& r, float& mx, Kahan2& sa, Kahan2& sq) {
@@ -165,12 +166,14 @@ __device__ bool tensor_stats_body(const uint16_t* __restrict__ x, int64_t n, voi
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kStThreads;
   float mx = 0.f;
   Kahan2 sa{0, 0}, sq{0, 0};
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8; i += 2 * stride) {
-    const bool two = i + stride < n8;
-    const uint4 r0 = ld16(x + 8 * i);
-    const uint4 r1 = two ? ld16(x + 8 * (i + stride)) : make_uint4(0, 0, 0, 0);
-    tensor_stats_vec(r0, mx, sa, sq);
-    tensor_stats_vec(r1, mx, sa, sq);   // zeros add nothing
+  // four vectors a thread per iteration, all four loads issued before any is
+  // used (few registers are live here, so more bytes can be in flight)
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kStThreads) + threadIdx.x; i < n8; i += 4 * stride) {
+    uint4 r[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) r[u] = i + u * stride < n8 ? ld16(x + 8 * (i + u * stride)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) tensor_stats_vec(r[u], mx, sa, sq);   // zeros add nothing
   }
   FF v[3] = {FF{mx, 0.f}, to_ff(sa), to_ff(sq)};
   const bool is_max[3] = {true, false, false};
