@@ -538,32 +538,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// INT4 codes [N, K/2] -> fp16 [N, K] (exact); one thread per 16 code bytes.
+// INT4 codes [N, K/2] -> fp16 [N, K] (exact).  A warp converts 512 code
+// bytes an iteration: lane t takes the 4-byte words t, t + 32, t + 64 and
+// t + 96 of the chunk (each load instruction reads 128 contiguous bytes) and
+// writes each word's 8 fp16 values as one 16-byte store (each store
+// instruction writes 512 contiguous bytes); nbytes % 4 == 0.
+__device__ __forceinline__ uint4 w4_word_to_f16x8(uint32_t w) {
+  uint32_t o[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t byte = (w >> (8 * b)) & 0xFFu;
+    // nibble x -> fp16 0x64:(x ^ 8) = 1024 + (v + 8), v the signed value; minus 1032 -> v
+    const uint32_t pair = (((byte & 0xFu) ^ 8u) | ((((byte >> 4) & 0xFu) ^ 8u) << 16)) | 0x64006400u;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[b]) : "r"(pair), "r"(0x64086408u));
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __global__ void __launch_bounds__(256) w4_expand_kernel(const uint8_t* __restrict__ codes, int64_t nbytes,
                                                         uint16_t* __restrict__ out, const int32_t* mode_dev) {
   if (mode_dev != nullptr && SIXBIT_MODE_OF(*mode_dev) != SIXBIT_MODE_INT8) return;
-  const int64_t n16 = nbytes >> 4;
-  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n16; i += static_cast<int64_t>(gridDim.x) * 256) {
-    const uint4 in = *reinterpret_cast<const uint4*>(codes + 16 * i);
-    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-    uint32_t o[16];
+  const int64_t nwords = nbytes >> 2;
+  const uint32_t* in = reinterpret_cast<const uint32_t*>(codes);
+  uint4* dst = reinterpret_cast<uint4*>(out);
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t c = (blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5)) * 128; c < nwords;
+       c += warps * 128) {
+    uint32_t w[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t byte = (w[j] >> (8 * b)) & 0xFFu;
-        // nibble x -> fp16 0x64:(x ^ 8) = 1024 + (v + 8), v the signed value; minus 1032 -> v
-        const uint32_t pair = (((byte & 0xFu) ^ 8u) | ((((byte >> 4) & 0xFu) ^ 8u) << 16)) | 0x64006400u;
-        uint32_t d;
-        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(pair), "r"(0x64086408u));
-        o[4 * j + b] = d;
-      }
+    for (int u = 0; u < 4; ++u) {
+      const int64_t k = c + 32 * u + lane;
+      w[u] = k < nwords ? __ldg(in + k) : 0u;
     }
-    uint4* dst = reinterpret_cast<uint4*>(out + 32 * i);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-    dst[2] = make_uint4(o[8], o[9], o[10], o[11]);
-    dst[3] = make_uint4(o[12], o[13], o[14], o[15]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t k = c + 32 * u + lane;
+      if (k < nwords) dst[k] = w4_word_to_f16x8(w[u]);
+    }
   }
 }
 
@@ -573,8 +585,8 @@ size_t w4a8_workspace_bytes(int N, int K) { return static_cast<size_t>(N) * stat
 
 cudaError_t launch_w4_expand(const uint8_t* codes, int N, int K, uint16_t* ws, const int32_t* mode_dev,
                              cudaStream_t st) {
-  const int64_t nbytes = static_cast<int64_t>(N) * (K / 2);
-  const int64_t want = ((nbytes >> 4) + 255) / 256;
+  const int64_t nbytes = static_cast<int64_t>(N) * (K / 2);  // K % 128 == 0: a multiple of 64
+  const int64_t want = ((nbytes >> 2) + 1023) / 1024;       // 8 warps x 128 words a CTA iteration
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
   w4a8::w4_expand_kernel<<<grid, 256, 0, st>>>(codes, nbytes, ws, mode_dev);
