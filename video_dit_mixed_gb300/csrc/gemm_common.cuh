@@ -243,6 +243,13 @@ __device__ __forceinline__ void bs_prefetch(const GemmParams& p, int row, int n,
   prefetch_l2(p.bs_delta + base + ncols - 1);
 }
 
+// The same for the residual alone (the plain RESIDUAL epilogue).
+__device__ __forceinline__ void residual_prefetch(const GemmParams& p, int row, int n, int ncols) {
+  const size_t base = static_cast<size_t>(row) * p.N + n;
+  for (int c = 0; c < ncols; c += 64) prefetch_l2(p.residual + base + c);
+  prefetch_l2(p.residual + base + ncols - 1);
+}
+
 // The epilogue's nw warps (warp index ew, all lanes) end the statistics:
 // each reduces its threads' sums (shuffle tree), the CTA's rows meet in
 // shared memory behind a named barrier over those warps only (id 1), and

@@ -411,6 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_of(t, m_tile, n_tile);
       const int row = m_tile * kBM + 32 * q + lane;
       const int n0 = n_tile * kBN + cs;    // output column of sum[0]
+      // The epilogue's residual rows to L2 while the tile's groups run: from
+      // HBM its loads kept the epilogue waiting ~1.5 us a 32-column chunk
+      // (clock64 trace: ~9600 cycles for a tile's residual epilogue, against
+      // the ~2700 the MMAs can run ahead), 465 -> 458 us at 17776 x 1920 x
+      // 7680.  (The same prefetch issued inside the group loop cost more
+      // than it saved.)
+      if constexpr (!BS)
+        if (p.epilogue == SIXBIT_EPI_RESIDUAL && row < p.M && n0 < p.N)
+          residual_prefetch(p, row, n0, min(kCols, p.N - n0));
       float sum[kCols];
 #pragma unroll
       for (int j = 0; j < kCols; ++j) sum[j] = 0.f;
