@@ -15,7 +15,7 @@ erf(X) = 1 - 3.5e-8: the clamped value is erf to within that.
 Run this script to print the constants; it needs numpy and scipy (erf in
 float64 as the definition).  Rounded to FP32 and evaluated with FP32 FMAs,
 the result is within ~2e-7 of erf(x) for every x (checked by
-``tests/test_kernel_identities.py``), the same budget as the Abramowitz and
+``tests/test_numerics_cpu.py``), the same budget as the Abramowitz and
 Stegun 7.1.26 rational form it replaces, without its reciprocal and
 exponential (two special-function-unit operations an element).
 """
