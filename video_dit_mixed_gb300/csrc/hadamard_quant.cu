@@ -497,115 +497,137 @@ __global__ void __launch_bounds__(kHqRowWarps * 32, 2) hq_int8_rows_kernel(const
 // 64-bit shuffle per pair: a third of the cross-lane traffic of the
 // 8-elements-per-lane form above, whose stages 8, 16, 32 all cross lanes).
 // Same stage order, same roundings, same division: bit-identical results.
-// CTAs of W warps (W * 1024 >= K; smaller CTAs let more of them overlap
-// their load, reduction and store phases on an SM).
-template <int W>
-__global__ void __launch_bounds__(W * 32, 32 / W) hq_int8_half_kernel(const uint16_t* __restrict__ X, int M, int K,
-                                                                    int lr, const int32_t* mode_dev, int8_t* codes,
-                                                                    float* row_scale, float* rotated) {
+// Persistent CTAs of W warps (W * 1024 >= K), MINB per SM, each walking
+// groups of W / R rows; every thread loads its part of the next group
+// before it works on the current one, so an SM keeps the loads of a whole
+// group per thread in flight while it computes.  (With one load phase per
+// row, HBM idled while the row was computed: long-scoreboard stalls led and
+// DRAM was ~49% busy at 17776 x 7680; prefetched, 101.0 -> 94.9 us there and
+// 31.4 -> 29.3 us at 17776 x 1920, four CTAs an SM; three, 96.9 us.)
+template <int W, int MINB>
+__global__ void __launch_bounds__(W * 32, MINB) hq_int8_half_kernel(const uint16_t* __restrict__ X, int M, int K,
+                                                                  int lr, const int32_t* mode_dev, int8_t* codes,
+                                                                  float* row_scale, float* rotated) {
   if (mode_skips(mode_dev, SIXBIT_MODE_INT8)) return;
   constexpr float kScale = 0.125f;  // 1/sqrt(64), exact
-  __shared__ float red[W];
+  __shared__ float red[2][W];       // the team's warp maxima, two groups apart
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int R = 1 << lr;
   const int team = warp >> lr, t = warp & (R - 1);
-  const int r = blockIdx.x * (W >> lr) + team;
-  const bool row_ok = r < M;
+  const int rows_per_cta = W >> lr;
+  const int ngroups = (M + rows_per_cta - 1) / rows_per_cta;
   const int col = t * 1024 + lane * 32;  // K % 64 == 0: a block's two halves are both in range or both out
-  const bool have = row_ok && col < K;
-  const uint16_t* src = X + static_cast<size_t>(row_ok ? r : 0) * K + (have ? col : 0);
+  auto load = [&](int g, uint4 (&raw)[4]) {
+    const int r = g * rows_per_cta + team;
+    const bool have = g < ngroups && r < M && col < K;
+    const uint16_t* src = X + static_cast<size_t>(have ? r : 0) * K + (have ? col : 0);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) raw[c] = have ? ld_nc_16(src + 8 * c) : make_uint4(0, 0, 0, 0);
+  };
   uint4 raw[4];
+  load(blockIdx.x, raw);
+  int par = 0;
+  for (int g = blockIdx.x; g < ngroups; g += gridDim.x, par ^= 1) {
+    uint4 nxt[4];
+    load(g + gridDim.x, nxt);  // in flight while this group is computed
+    const int r = g * rows_per_cta + team;
+    const bool have = r < M && col < K;
+    uint64_t P[16];  // P[i] = (element i, element i + 16) of the lane's 32
+    {
+      float e0[8], e1[8], e2[8], e3[8];
+      bf16x8_to_f32(raw[0], e0);
+      bf16x8_to_f32(raw[1], e1);
+      bf16x8_to_f32(raw[2], e2);
+      bf16x8_to_f32(raw[3], e3);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) raw[c] = have ? ld_nc_16(src + 8 * c) : make_uint4(0, 0, 0, 0);
-  uint64_t P[16];  // P[i] = (element i, element i + 16) of the lane's 32
-  {
-    float e0[8], e1[8], e2[8], e3[8];
-    bf16x8_to_f32(raw[0], e0);
-    bf16x8_to_f32(raw[1], e1);
-    bf16x8_to_f32(raw[2], e2);
-    bf16x8_to_f32(raw[3], e3);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      P[i] = f2_pack(e0[i], e2[i]);
-      P[8 + i] = f2_pack(e1[i], e3[i]);
-    }
-  }
-#pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if ((i & h) == 0) {
-        const uint64_t a = P[i], c = P[i + h];
-        P[i] = f2_add(a, c);
-        P[i + h] = f2_sub(a, c);
+      for (int i = 0; i < 8; ++i) {
+        P[i] = f2_pack(e0[i], e2[i]);
+        P[8 + i] = f2_pack(e1[i], e3[i]);
       }
     }
-  }
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {  // stride 16: the two lanes of each register
-    const float a = f2_lo(P[i]), c = f2_hi(P[i]);
-    P[i] = f2_pack(__fadd_rn(a, c), __fsub_rn(a, c));
-  }
-  {  // stride 32: the neighbouring lane holds the block's other half
-    const float sgn = (lane & 1) ? -1.0f : 1.0f;  // lower half: v + o; upper half: o - v (one rounding)
-    const uint64_t sg2 = f2_pack(sgn, sgn);
+    for (int c = 0; c < 4; ++c) raw[c] = nxt[c];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, static_cast<unsigned long long>(P[i]), 1);
-      P[i] = f2_fma(sg2, P[i], o);
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if ((i & h) == 0) {
+          const uint64_t a = P[i], c = P[i + h];
+          P[i] = f2_add(a, c);
+          P[i + h] = f2_sub(a, c);
+        }
+      }
     }
-  }
-  float m = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fabsf(f2_lo(P[i])), fabsf(f2_hi(P[i]))));
-  m = warp_max(m);
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  m = red[team << lr];
-  for (int i = 1; i < R; ++i) m = fmaxf(m, red[(team << lr) + i]);
-  if (!have) return;
-  const float s = __fdiv_rn(__fmul_rn(m, kScale), 127.0f);
-  const bool fast = recip_ok(s) || s == 0.f;
-  const float rs = s != 0.f ? __frcp_rn(s) : 0.f;
-  if (t == 0 && lane == 0) row_scale[r] = s;
-  const size_t off = static_cast<size_t>(r) * K + col;
-  if (rotated != nullptr) {  // the rotated values y = v / 8 (FP32, test output)
-    float4* dst = reinterpret_cast<float4*>(rotated + off);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      dst[i] = make_float4(__fmul_rn(f2_lo(P[4 * i]), kScale), __fmul_rn(f2_lo(P[4 * i + 1]), kScale),
-                           __fmul_rn(f2_lo(P[4 * i + 2]), kScale), __fmul_rn(f2_lo(P[4 * i + 3]), kScale));
-      dst[4 + i] = make_float4(__fmul_rn(f2_hi(P[4 * i]), kScale), __fmul_rn(f2_hi(P[4 * i + 1]), kScale),
-                               __fmul_rn(f2_hi(P[4 * i + 2]), kScale), __fmul_rn(f2_hi(P[4 * i + 3]), kScale));
+    for (int i = 0; i < 16; ++i) {  // stride 16: the two lanes of each register
+      const float a = f2_lo(P[i]), c = f2_hi(P[i]);
+      P[i] = f2_pack(__fadd_rn(a, c), __fsub_rn(a, c));
     }
-  }
-  const uint64_t kr2 = f2_pack(kRound, kRound);
-  uint64_t oi[16];
-  if (fast) {
-    const uint64_t rs2 = f2_pack(rs * kScale, rs * kScale);  // RN(1 / (8 s)), exact
-    const uint64_t ns2 = f2_pack(-(s / kScale), -(s / kScale));
+    {  // stride 32: the neighbouring lane holds the block's other half
+      const float sgn = (lane & 1) ? -1.0f : 1.0f;  // lower half: v + o; upper half: o - v (one rounding)
+      const uint64_t sg2 = f2_pack(sgn, sgn);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {  // div_by_recip on both lanes
-      const uint64_t q = f2_mul(P[i], rs2);
-      const uint64_t d = f2_fma(f2_fma(ns2, q, P[i]), rs2, q);
-      oi[i] = f2_add(d, kr2);
+      for (int i = 0; i < 16; ++i) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, static_cast<unsigned long long>(P[i]), 1);
+        P[i] = f2_fma(sg2, P[i], o);
+      }
     }
-  } else {
+    float m = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float dl = fminf(fmaxf(__fdiv_rn(__fmul_rn(f2_lo(P[i]), kScale), s), -127.f), 127.f);
-      const float dh = fminf(fmaxf(__fdiv_rn(__fmul_rn(f2_hi(P[i]), kScale), s), -127.f), 127.f);
-      oi[i] = f2_add(f2_pack(dl, dh), kr2);
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fmaxf(fabsf(f2_lo(P[i])), fabsf(f2_hi(P[i]))));
+    m = warp_max(m);
+    // one barrier a group: red[par] is rewritten two groups later, after
+    // every warp has passed the next group's barrier (and so read it)
+    if (lane == 0) red[par][warp] = m;
+    __syncthreads();
+    m = red[par][team << lr];
+    for (int i = 1; i < R; ++i) m = fmaxf(m, red[par][(team << lr) + i]);
+    if (!have) continue;
+    const float s = __fdiv_rn(__fmul_rn(m, kScale), 127.0f);
+    const bool fast = recip_ok(s) || s == 0.f;
+    const float rs = s != 0.f ? __frcp_rn(s) : 0.f;
+    if (t == 0 && lane == 0) row_scale[r] = s;
+    const size_t off = static_cast<size_t>(r) * K + col;
+    if (rotated != nullptr) {  // the rotated values y = v / 8 (FP32, test output)
+      float4* dst = reinterpret_cast<float4*>(rotated + off);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        dst[i] = make_float4(__fmul_rn(f2_lo(P[4 * i]), kScale), __fmul_rn(f2_lo(P[4 * i + 1]), kScale),
+                             __fmul_rn(f2_lo(P[4 * i + 2]), kScale), __fmul_rn(f2_lo(P[4 * i + 3]), kScale));
+        dst[4 + i] = make_float4(__fmul_rn(f2_hi(P[4 * i]), kScale), __fmul_rn(f2_hi(P[4 * i + 1]), kScale),
+                                 __fmul_rn(f2_hi(P[4 * i + 2]), kScale), __fmul_rn(f2_hi(P[4 * i + 3]), kScale));
+      }
     }
-  }
+    const uint64_t kr2 = f2_pack(kRound, kRound);
+    uint64_t oi[16];
+    if (fast) {
+      const uint64_t rs2 = f2_pack(rs * kScale, rs * kScale);  // RN(1 / (8 s)), exact
+      const uint64_t ns2 = f2_pack(-(s / kScale), -(s / kScale));
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {  // elements 0..15 from the low lanes, 16..31 from the high lanes
+      for (int i = 0; i < 16; ++i) {  // div_by_recip on both lanes
+        const uint64_t q = f2_mul(P[i], rs2);
+        const uint64_t d = f2_fma(f2_fma(ns2, q, P[i]), rs2, q);
+        oi[i] = f2_add(d, kr2);
+      }
+    } else {
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      uint32_t tt[8];
+      for (int i = 0; i < 16; ++i) {
+        const float dl = fminf(fmaxf(__fdiv_rn(__fmul_rn(f2_lo(P[i]), kScale), s), -127.f), 127.f);
+        const float dh = fminf(fmaxf(__fdiv_rn(__fmul_rn(f2_hi(P[i]), kScale), s), -127.f), 127.f);
+        oi[i] = f2_add(f2_pack(dl, dh), kr2);
+      }
+    }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) tt[i] = static_cast<uint32_t>(hh ? (oi[8 * g + i] >> 32) : oi[8 * g + i]);
-      int8_write8(tt, off + 16 * hh + 8 * g, codes);
+    for (int hh = 0; hh < 2; ++hh) {  // elements 0..15 from the low lanes, 16..31 from the high lanes
+      uint32_t w[4];                  // one 16-byte store each
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t tt[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tt[i] = static_cast<uint32_t>(hh ? (oi[4 * j + i] >> 32) : oi[4 * j + i]);
+        w[j] = __byte_perm(__byte_perm(tt[0], tt[1], 0x0040), __byte_perm(tt[2], tt[3], 0x0040), 0x5410);
+      }
+      *reinterpret_cast<uint4*>(codes + off + 16 * hh) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
@@ -1126,15 +1148,17 @@ cudaError_t launch_hq_int8(const uint16_t* X, int M, int K, int b, const int32_t
   if (b == 64 && K <= kHqRowWarps * 1024) {  // half a block per lane: one warp per 1024 elements of a row
     int lr = 0;
     while ((1024 << lr) < K) ++lr;
-    if (lr <= 3) {  // rows up to 8192 elements: 8-warp CTAs
-      const int rows_per_cta = 8 >> lr;
-      const int grid = (M + rows_per_cta - 1) / rows_per_cta;
-      hq_int8_half_kernel<8><<<grid, 8 * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes, o->row_scale, o->rotated);
+    const int sms = sm_count();
+    if (lr <= 3) {  // rows up to 8192 elements: 8-warp CTAs, four per SM (62 registers a thread)
+      const int groups = (M + (8 >> lr) - 1) / (8 >> lr);
+      const int grid = groups < 4 * sms ? groups : 4 * sms;
+      hq_int8_half_kernel<8, 4><<<grid, 8 * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes, o->row_scale,
+                                                         o->rotated);
     } else {
-      const int rows_per_cta = kHqRowWarps >> lr;
-      const int grid = (M + rows_per_cta - 1) / rows_per_cta;
-      hq_int8_half_kernel<kHqRowWarps><<<grid, kHqRowWarps * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes,
-                                                                        o->row_scale, o->rotated);
+      const int groups = (M + (kHqRowWarps >> lr) - 1) / (kHqRowWarps >> lr);
+      const int grid = groups < sms ? groups : sms;
+      hq_int8_half_kernel<kHqRowWarps, 1><<<grid, kHqRowWarps * 32, 0, st>>>(X, M, K, lr, mode_dev, o->i8_codes,
+                                                                           o->row_scale, o->rotated);
     }
     note_launch();
     return cudaGetLastError();
