@@ -132,10 +132,10 @@ typedef struct {
 
 /* Policy thresholds (technical summary sections 2.A-2.C; popular summary sections 1-3). */
 typedef struct {
-  double gamma_thr;   /* Gamma >= gamma_thr -> INT8, else NVFP4 */
+  double gamma_thr;   /* Gamma >= gamma_thr (or NaN) -> INT8, else NVFP4 */
   double cos_thr;     /* cos(Delta_{t-1}, Delta_{t-2}) >= cos_thr may skip */
   double err_cap;     /* accumulated 1 - cos above err_cap forces a refresh */
-  double pdr_ratio;   /* input max/mean above pdr_ratio forces BF16 */
+  double pdr_ratio;   /* input max/mean above pdr_ratio (or NaN) forces BF16 */
   double near_rel;    /* relative band around thresholds reported as "near" */
   int32_t refresh_bf16; /* 1: every forced refresh runs BF16 */
   int32_t reserved;
@@ -152,7 +152,10 @@ typedef struct {
   double acc;
   int32_t last_word;
   int32_t steps;
-  int32_t n_skip, n_refresh, n_pdr, n_near, n_nvfp4, n_int8, n_bf16, reserved;
+  int32_t n_skip, n_refresh, n_pdr, n_near, n_nvfp4, n_int8, n_bf16;
+  int32_t n_nonfinite;  /* decisions taken on a statistic that was not a number
+                           (a NaN cosine never skips, a NaN Gamma picks INT8,
+                           a NaN input ratio picks BF16) */
 } sixbit_policy_state;
 
 /* ---- sizes and layouts ------------------------------------------------- */

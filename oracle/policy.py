@@ -21,16 +21,19 @@ Readings where the pages are silent (listed with the code that takes them):
         refresh BF16 (the popular summary's "full precision" refresh);
   (iv)  the PDR test runs before computing, on the block input;
   (v)   one decision per block covers all its linear layers;
-  (vi)  the first two computed steps never skip (no cosine yet).
+  (vi)  the first two computed steps never skip (no cosine yet);
+  (vii) a statistic that is not a number (a corrupted or overflowed sum)
+        fails its threshold test toward the safer path: a NaN cosine never
+        skips, a NaN Gamma picks INT8 and a NaN input ratio picks BF16.
 
 Decision of step s, then the fold of its statistics (if it computed):
 
     if n_computed >= 2 and cos >= cos_thr:
         if acc + (1 - cos) <= err_cap: SKIP; acc += 1 - cos; skipped_last = True
         else: REFRESH (a compute, flagged)
-    compute: BF16 if ratio > pdr_ratio (or refresh and refresh_bf16)
+    compute: BF16 if ratio > pdr_ratio or NaN (or refresh and refresh_bf16)
              else INT8 if skipped_last or no Gamma yet
-             else INT8 if Gamma >= gamma_thr else NVFP4
+             else NVFP4 if Gamma < gamma_thr else INT8 (so a NaN Gamma: INT8)
     after a compute: Gamma <- new Gamma; cos <- cos(Delta_new, Delta_prev) if a
         previous delta existed; n_computed += 1; acc = 0; skipped_last = False
 """
@@ -92,13 +95,14 @@ def decide(st: PolicyState, ratio: float, cfg: PolicyConfig) -> Decision:
                 return d
             refresh = True
     near |= _near(ratio, cfg.pdr_ratio, cfg.near_rel)
-    if ratio > cfg.pdr_ratio or (refresh and cfg.refresh_bf16):
-        d = Decision(BF16, refresh=refresh, pdr=ratio > cfg.pdr_ratio, near=near)
+    pdr = not (ratio <= cfg.pdr_ratio)   # above the threshold, or not a number
+    if pdr or (refresh and cfg.refresh_bf16):
+        d = Decision(BF16, refresh=refresh, pdr=pdr, near=near)
     elif st.skipped_last or not st.have_gamma:
         d = Decision(INT8, refresh=refresh, post_skip=st.skipped_last, near=near)
     else:
         near |= _near(st.gamma, cfg.gamma_thr, cfg.near_rel)
-        d = Decision(INT8 if st.gamma >= cfg.gamma_thr else NVFP4, refresh=refresh, near=near)
+        d = Decision(NVFP4 if st.gamma < cfg.gamma_thr else INT8, refresh=refresh, near=near)   # NaN: INT8
     st.history.append(d)
     return d
 

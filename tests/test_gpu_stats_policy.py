@@ -144,8 +144,8 @@ def _traces():
     return out
 
 
-def _run_device_trace(ops, cfg, steps):
-    state = ops.new_policy_state()
+def _run_device_trace(ops, cfg, steps, state=None):
+    state = ops.new_policy_state() if state is None else state
     last = ops.new_stats()
     ins = torch.zeros(3, dtype=torch.float64, device="cuda")
     word = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -194,3 +194,25 @@ def test_device_policy_matches_oracle_on_random_statistics(ops):
             and not r.near]
     assert not mism, mism[:5]
     assert {r.mode for r in ref} == {"NVFP4", "INT8", "BF16", "SKIP"}
+
+
+def test_device_policy_nan_statistics(ops):
+    """A statistic that is not a number fails its threshold test toward the safer path, as in the oracle: a NaN
+    cosine never skips, a NaN Gamma picks INT8 (not NVFP4), a NaN input ratio picks BF16 with the PDR flag; the
+    state counts the decisions taken on a NaN statistic (n_nonfinite)."""
+    nan = float("nan")
+    steps = [dict(ratio=12.0, gamma=0.04, cos=None),    # INT8 (first step)
+             dict(ratio=12.0, gamma=nan, cos=nan),      # NVFP4 (Gamma 0.04); its own statistics are NaN
+             dict(ratio=12.0, gamma=0.04, cos=0.98),    # NaN cosine and Gamma: INT8, counted
+             dict(ratio=nan, gamma=0.04, cos=0.995),    # NaN ratio: BF16 + PDR, counted
+             dict(ratio=12.0, gamma=None, cos=None),    # SKIP
+             dict(ratio=12.0, gamma=None, cos=None)]    # SKIP
+    ref = policy.run_trace([dict(s) for s in steps], policy.PolicyConfig())
+    state = ops.new_policy_state()
+    got = _run_device_trace(ops, ops.policy_cfg(), [dict(s) for s in steps], state=state)
+    names = {1: "NVFP4", 2: "INT8", 3: "BF16", 4: "SKIP"}
+    assert [names[w & 0xFF] for w in got] == [r.mode for r in ref] == ["INT8", "NVFP4", "INT8", "BF16", "SKIP",
+                                                                       "SKIP"]
+    assert [bool(w & ops.abi.FLAG_PDR) for w in got] == [r.pdr for r in ref]
+    st = ops.decode_state(state[0])
+    assert st.n_nonfinite == 2 and st.n_pdr == 1 and st.n_skip == 2

@@ -99,3 +99,35 @@ def test_policy_near_threshold_flag():
     assert got[0].mode == "BF16" and got[0].near
     got = policy.run_trace([dict(ratio=29.0, gamma=0.2)], cfg)
     assert not got[0].near
+
+
+# A statistic that is not a number fails its threshold test toward the safer path.
+NAN = float("nan")
+NAN_TRACE = [   # (ratio, gamma, cos of the step's own compute), expected mode, pdr
+    (12.0, 0.04, None, "INT8", False),   # first step
+    (12.0, NAN, NAN, "NVFP4", False),    # decided on Gamma 0.04; this compute's statistics are NaN
+    (12.0, 0.04, 0.98, "INT8", False),   # NaN cosine: no skip; NaN Gamma: INT8, not NVFP4
+    (NAN, 0.04, 0.995, "BF16", True),    # NaN input ratio: BF16 with the PDR flag
+    (12.0, None, None, "SKIP", False),   # cos 0.995, acc 0.005 <= 0.05
+    (12.0, None, None, "SKIP", False),   # acc 0.010 <= 0.05
+]
+
+
+def test_policy_nan_statistics_take_the_safer_path():
+    steps = [dict(ratio=r, gamma=g, cos=c) for r, g, c, _, _ in NAN_TRACE]
+    got = policy.run_trace(steps, policy.PolicyConfig())
+    assert [d.mode for d in got] == [m for *_, m, _ in NAN_TRACE]
+    assert [d.pdr for d in got] == [p for *_, p in NAN_TRACE]
+
+
+def test_policy_nan_statistics_single_steps():
+    cfg = policy.PolicyConfig()
+    st = policy.PolicyState(n_computed=2, have_gamma=True, gamma=NAN, cos=0.5)
+    assert policy.decide(st, 12.0, cfg).mode == "INT8"       # volatile without a usable Gamma
+    st = policy.PolicyState(n_computed=2, have_gamma=True, gamma=0.01, cos=NAN)
+    assert policy.decide(st, 12.0, cfg).mode == "NVFP4"      # no skip on a NaN cosine; Gamma decides
+    st = policy.PolicyState(n_computed=2, have_gamma=True, gamma=0.01, cos=0.5)
+    d = policy.decide(st, NAN, cfg)
+    assert d.mode == "BF16" and d.pdr
+    st = policy.PolicyState(n_computed=2, have_gamma=True, gamma=0.01, cos=0.5)
+    assert policy.decide(st, 30.0, cfg).mode == "NVFP4"      # finite values: unchanged (ratio 30 is not > 30)

@@ -40,7 +40,7 @@ class PolicyState(C.Structure):
                 ("pending", C.c_int32), ("gamma", C.c_double), ("cos", C.c_double), ("acc", C.c_double),
                 ("last_word", C.c_int32), ("steps", C.c_int32)] + \
                [(n, C.c_int32) for n in ("n_skip", "n_refresh", "n_pdr", "n_near", "n_nvfp4", "n_int8",
-                                         "n_bf16", "reserved")]
+                                         "n_bf16", "n_nonfinite")]
 
 
 class DitBlocks(C.Structure):

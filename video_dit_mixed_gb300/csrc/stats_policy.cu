@@ -525,10 +525,15 @@ __device__ int policy_decide(const sixbit_policy_cfg& cfg, sixbit_policy_state& 
     s.skipped_last = 0;
     s.pending = 0;
   }
+  // A statistic that is not a number (a corrupted or overflowed sum) fails
+  // its threshold test toward the safer path: a NaN cosine never skips, a
+  // NaN Gamma picks INT8, a NaN input ratio picks BF16; each such decision
+  // is counted (n_nonfinite).
   int word = 0;
-  bool near = false, refresh = false;
+  bool near = false, refresh = false, nonfinite = false;
   bool decided = false;
   if (s.n_computed >= 2) {
+    nonfinite |= isnan(s.cos);
     near |= near_thr(s.cos, cfg.cos_thr, cfg.near_rel);
     if (s.cos >= cfg.cos_thr) {
       const double pred = s.acc + (1.0 - s.cos);
@@ -549,17 +554,20 @@ __device__ int policy_decide(const sixbit_policy_cfg& cfg, sixbit_policy_state& 
     // float64 divisions, slow on this GPU, are not spent on a skip)
     const double mx = in_stats[0], sabs = in_stats[1], cnt = in_stats[2];
     const double ratio = (sabs == 0.0) ? 0.0 : mx / (sabs / cnt);
+    const bool pdr = !(ratio <= cfg.pdr_ratio);  // ratio > pdr_ratio, or not a number
+    nonfinite |= isnan(ratio);
     near |= near_thr(ratio, cfg.pdr_ratio, cfg.near_rel);
-    if (ratio > cfg.pdr_ratio || (refresh && cfg.refresh_bf16)) {
-      word = SIXBIT_MODE_BF16 | (ratio > cfg.pdr_ratio ? SIXBIT_FLAG_PDR : 0);
-      if (ratio > cfg.pdr_ratio) s.n_pdr += 1;
+    if (pdr || (refresh && cfg.refresh_bf16)) {
+      word = SIXBIT_MODE_BF16 | (pdr ? SIXBIT_FLAG_PDR : 0);
+      if (pdr) s.n_pdr += 1;
       s.n_bf16 += 1;
     } else if (s.skipped_last || !s.have_gamma) {
       word = SIXBIT_MODE_INT8 | (s.skipped_last ? SIXBIT_FLAG_POSTSKIP : 0);
       s.n_int8 += 1;
     } else {
       near |= near_thr(s.gamma, cfg.gamma_thr, cfg.near_rel);
-      if (s.gamma >= cfg.gamma_thr) {
+      nonfinite |= isnan(s.gamma);
+      if (!(s.gamma < cfg.gamma_thr)) {  // Gamma >= gamma_thr, or not a number
         word = SIXBIT_MODE_INT8;
         s.n_int8 += 1;
       } else {
@@ -573,6 +581,7 @@ __device__ int policy_decide(const sixbit_policy_cfg& cfg, sixbit_policy_state& 
     }
     s.pending = 1;
   }
+  if (nonfinite) s.n_nonfinite += 1;
   if (near) {
     word |= SIXBIT_FLAG_NEAR;
     s.n_near += 1;
