@@ -157,3 +157,40 @@ def test_pipelined_host_io_matches_eager():
     torch.cuda.synchronize()
     for a, b in zip(o_eager, outs):
         np.testing.assert_array_equal(a.view(np.uint32), b.float().numpy().view(np.uint32))
+
+
+@pytest.mark.parametrize("delta_format", ["bf16", "mxfp8"])
+def test_checkpoint_resume_is_bit_identical(delta_format):
+    """state_dict() half-way through a trajectory, through torch.save, into a fresh model: the rest of the
+    trajectory gives the same outputs and mode words, bit for bit, as the uninterrupted run."""
+    import io
+    from video_dit_mixed_gb300 import dit
+    name = "dit_tiny"
+    c = synthgen.DIT_CONFIGS[name]
+    packed = dit.pack_block_weights(synthgen.dit_weights(name), c["had_block"])
+    xs = [torch.from_numpy(x).to(torch.bfloat16).cuda() for x in synthgen.dit_trajectory(name)]
+    k = len(xs) // 2
+
+    def model():
+        return dit.DiT(c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"], packed,
+                       delta_format=delta_format)
+
+    a = model()
+    outs, words, buf = [], [], None
+    for s, x in enumerate(xs):
+        outs.append(a.step(x).clone())
+        words.append(a.modes.clone())
+        if s == k - 1:
+            buf = io.BytesIO()
+            torch.save(a.state_dict(), buf)
+    b = model()
+    buf.seek(0)
+    b.load_state_dict(torch.load(buf))
+    for s in range(k, len(xs)):
+        y = b.step(xs[s])
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), outs[s].view(torch.int16)), s
+        assert torch.equal(b.modes, words[s]), s
+    with pytest.raises(ValueError):
+        dit.DiT(c["tokens"], c["hidden"], c["ffn"], c["blocks"], c["had_block"], packed,
+                delta_format="mxfp8" if delta_format == "bf16" else "bf16").load_state_dict(a.state_dict())

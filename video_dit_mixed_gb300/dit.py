@@ -94,6 +94,31 @@ class DiT:
         self.modes.zero_()
         self.run_len.zero_()
 
+    # the trajectory state carried from one denoising step to the next (what reset() clears)
+    STATE = ("deltas", "delta_scales", "stats", "state", "modes", "run_len")
+
+    def state_dict(self) -> dict:
+        """Checkpoint: host copies of the trajectory state between two steps (delta caches, statistics,
+        policy states, mode words), after the steps already enqueued on the current stream have run.
+        load_state_dict() on a model of the same shape and delta format resumes the trajectory with
+        bit-identical outputs and decisions.  The result can be saved with torch.save."""
+        torch.cuda.current_stream().synchronize()
+        sd = {k: getattr(self, k).to("cpu", copy=True) for k in self.STATE if getattr(self, k) is not None}
+        sd["shape"] = (self.T, self.H, self.F, self.L, self.b)
+        sd["delta_format"] = self.delta_format
+        return sd
+
+    def load_state_dict(self, sd: dict) -> None:
+        """Resume from state_dict(): the buffers are overwritten in place, so a captured graph keeps
+        working; raises ValueError on a checkpoint of another shape or delta format."""
+        if tuple(sd["shape"]) != (self.T, self.H, self.F, self.L, self.b) or sd["delta_format"] != self.delta_format:
+            raise ValueError(f"checkpoint of {sd['shape']} / {sd['delta_format']}, model "
+                             f"{(self.T, self.H, self.F, self.L, self.b)} / {self.delta_format}")
+        for k in self.STATE:
+            t = getattr(self, k)
+            if t is not None:
+                t.copy_(sd[k].to(device=t.device, dtype=t.dtype), non_blocking=False)
+
     CALLS = ("hq_x", "qgemm_up", "hq_h", "qgemm_down", "block_stats", "skip_run")
 
     def enqueue_step(self, after_call=None):
