@@ -377,6 +377,7 @@ class DitStep:
     host_dispatch = False   # --dispatch host: no graph, the host launches each block's chosen kernels
     delta_format = "bf16"   # --delta-format mxfp8: the Delta cache in MXFP8
     fused_stats = True      # --unfused-stats: the block statistics as a separate pass
+    log_decisions = False   # --log-jsonl: keep every block's decision record of the replayed window
 
     def _step(self, x):
         if self.host_dispatch:
@@ -451,6 +452,7 @@ class DitStep:
         recs = []                 # (key, start event, end event)
         run_bytes = []
         mh = np.zeros((len(steps), self.L), dtype=np.int64)
+        dlog = []
 
         def timed(key, fn):
             a, b = T.cuda.Event(enable_timing=True), T.cuda.Event(enable_timing=True)
@@ -491,7 +493,10 @@ class DitStep:
                     last[0] = b2
                     m._compute_body(x, out, l, mode, note=note)
                 x = out
+            if self.log_decisions:   # one read of the mode words and policy states after the step
+                dlog.extend(dict(step=int(s), **r) for r in m.decision_records())
         T.cuda.synchronize()
+        self.decision_log = dlog
         low = mh & 0xFF
         per = {}
         for key, a, b in recs:
@@ -827,6 +832,8 @@ def run_ours(args):
         cls = type(cls.__name__, (cls,), dict(delta_format=args.delta_format))
     if args.unfused_stats:
         cls = type(cls.__name__, (cls,), dict(fused_stats=False))
+    if args.log_jsonl:
+        cls = type(cls.__name__, (cls,), dict(log_decisions=True))
     wl = cls(args.workload, torch, ops, dev)
     stream = torch.cuda.current_stream()
 
@@ -856,6 +863,10 @@ def run_ours(args):
 
     if per is None:
         per = wl.profile(args.steps, stream)
+    if args.log_jsonl and rank == 0:
+        with open(args.log_jsonl, "w") as f:
+            for r in getattr(wl, "decision_log", []):
+                f.write(json.dumps(r) + "\n")
     barrier()
     e2e_ms = max_over_ranks(statistics.fmean(wl.e2e(args.steps, stream)))
     if wl.launches() is not None:
@@ -1088,9 +1099,14 @@ def main():
                          "instead of in its down projection's epilogue")
     ap.add_argument("--blocks", type=int, default=0,
                     help="DiT workloads: use only this many blocks (profiling runs on a smaller device footprint)")
+    ap.add_argument("--log-jsonl", default=None, metavar="PATH",
+                    help="DiT workloads: write one JSON record per timed step and block (mode, flags, Gamma, cosine, "
+                         "accumulated skip error) to PATH, read in the replay pass after the timed region")
     ap.add_argument("--oracle-costs", action="store_true", help=argparse.SUPPRESS)  # the 1-core CPU leg's child
     ap.add_argument("--rows", type=int, default=32, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.log_jsonl and not args.workload.startswith("dit"):
+        ap.error("--log-jsonl records DiT decisions: use a dit_* workload")
     if args.oracle_costs:
         print(json.dumps(oracle_block_costs(args.workload, args.rows, args.cpu_budget)), flush=True)
         return

@@ -21,6 +21,8 @@ Per block l (reads bufs[(l-1) % 2], x_in for l = 0; writes bufs[l % 2]):
 """
 from __future__ import annotations
 
+import math
+
 import torch
 
 from . import ops
@@ -312,6 +314,13 @@ class DiT:
         P["k"] += 1
         return P["out_free"][i]
 
+    def decision_records(self) -> list:
+        """Per block, the decision of the last step and the policy values it was taken on (one read of
+        the mode words and policy states, after the work already enqueued on the current stream):
+        see decode_decisions."""
+        torch.cuda.current_stream().synchronize()
+        return decode_decisions(self.modes.cpu().numpy(), self.state.cpu().numpy())
+
     def decision_counts(self):
         """Per block: (n_nvfp4, n_int8, n_bf16, n_skip, n_refresh, n_pdr, n_near) from the device state."""
         out = []
@@ -319,6 +328,30 @@ class DiT:
             s = ops.decode_state(self.state[l])
             out.append((s.n_nvfp4, s.n_int8, s.n_bf16, s.n_skip, s.n_refresh, s.n_pdr, s.n_near))
         return out
+
+
+def _num(v: float):
+    """A float for a JSON record: non-finite values as the strings "nan", "inf", "-inf"."""
+    return v if math.isfinite(v) else ("nan" if math.isnan(v) else ("inf" if v > 0 else "-inf"))
+
+
+def decode_decisions(modes, states) -> list:
+    """Decision records of one step from host copies of the mode words [L] and policy states [L, 80]:
+    per block its mode, flags (refresh, pdr, post_skip, near), and the Gamma, cosine, accumulated
+    skip error and computed-step count the policy state holds after the decision (Gamma and the
+    cosine as used for it; acc including a skip's own 1 - cos).  Gamma is absent before the first
+    computed step, the cosine before the second."""
+    out = []
+    for l, w in enumerate(modes):
+        w = int(w)
+        st = ops.decode_state(torch.as_tensor(states[l]))
+        out.append(dict(block=l, mode=ops.abi.MODE_NAMES.get(w & 0xFF, "?"),
+                        refresh=bool(w & ops.abi.FLAG_REFRESH), pdr=bool(w & ops.abi.FLAG_PDR),
+                        post_skip=bool(w & ops.abi.FLAG_POSTSKIP), near=bool(w & ops.abi.FLAG_NEAR),
+                        gamma=_num(st.gamma) if st.have_gamma else None,
+                        cos=_num(st.cos) if st.n_computed >= 2 else None,
+                        acc=_num(st.acc), n_computed=int(st.n_computed)))
+    return out
 
 
 def pack_block_weights(weights, had_block, device="cuda"):
