@@ -13,6 +13,8 @@ A roofline fraction is only as good as its numerator.
 - The table and the dominant kernel's roofline divide that work by the
   measured per-call time and by the measured peak of the kernel's own
   dtype (the FP4 one at 6 x bf16).
+- The CPU baseline scales the oracle's per-kind block-step time on a token
+  sample to the full token count, over the window's actual decisions.
 
 The workload objects are built without a GPU (no __init__): only the
 attributes the accounting reads are set.
@@ -94,3 +96,17 @@ def test_roofline_divides_work_by_time_and_the_dtype_peak(bench):
     assert q["frac"] == pytest.approx(q["gbs"] / 8000.0, abs=1e-4)
     assert "frac" not in table["block_stats:bf16"] and table["block_stats:bf16"]["calls"] == 1
     assert bench.FP4_OVER_BF16 == pytest.approx(13.5 / 2.25)
+
+
+def test_cpu_baseline_extrapolates_over_the_decision_trace(bench):
+    """The oracle's rate is its per-kind block-step time on a token sample, scaled to the full token
+    count and summed over each step's actual decisions: here steps of 2.5 s and 1 s on 32 rows, run
+    on 64 tokens (x 2), give 2 steps / 7 s."""
+    costs = {"int8": 2.0, "nvfp4": 1.5, "bf16": 3.0, "skip": 0.5}
+    trace = [["int8", "skip"], ["skip", "skip"]]
+    assert bench._dit_rate(costs, trace, tokens=64, rows=32) == pytest.approx(2 / 7, rel=1e-15)
+    # every block computing in INT8 (the reference arm's extrapolation)
+    assert bench._dit_rate(costs, [["int8"] * 30], tokens=17776, rows=32) == pytest.approx(
+        1 / (30 * 2.0 * 17776 / 32), rel=1e-15)
+    # the bench's mode names are the cost table's keys
+    assert {bench.MODE_NAMES[k] for k in (1, 2, 3, 4)} == set(costs)
