@@ -18,12 +18,14 @@ float32, which is IEEE-754 round-to-nearest-even for every single
 operation.  Reference GEMM values and statistics are computed in float64.
 
 Module map:
-  formats   small-float encoders/decoders (E2M1, E4M3, bf16)
+  formats   small-float encoders/decoders (E2M1, E4M3, bf16, MXFP8 blocks)
   hadamard  block Fast Walsh-Hadamard transform and the dense Sylvester matrix
   quant     NVFP4 / INT8 activation quantizers, 4-bit weight packing
   gemm      reference quantized GEMMs, GELU, residual, tolerance bounds
   stats     block statistics (Gamma, cosine, max/mean outlier ratio)
   policy    per-block DMPQ / TDC / PDR decision state machine
+  dit       the residual-MLP DiT chain (x + W_d GELU(W_u x) per block) under
+            the policy, with a bf16 or MXFP8 delta cache
 
 Parity status: every function here is pinned by tests in
 tests/test_oracle_*.py except the policy thresholds themselves, whose
