@@ -203,3 +203,25 @@ def test_per_depth_threshold_mutation_is_caught(monkeypatch):
         self.cfgs = [self.cfgs[0]] * self.L      # per-block thresholds ignored
     monkeypatch.setattr(dit.OracleDiT, "__init__", first_config_everywhere)
     assert _fails(td.test_per_depth_thresholds_closed_form)
+
+
+def test_nan_statistic_reading_mutations_are_caught(monkeypatch):
+    """Reading a NaN Gamma as stable (NVFP4), or a NaN input ratio as no outlier (no PDR), fails the
+    NaN pins."""
+    import math
+    orig = policy.decide
+
+    def nan_gamma_stable(st, ratio, cfg):
+        if math.isnan(st.gamma):
+            st.gamma = 0.0
+        return orig(st, ratio, cfg)
+
+    def nan_ratio_no_pdr(st, ratio, cfg):
+        return orig(st, 0.0 if math.isnan(ratio) else ratio, cfg)
+
+    for mutant in (nan_gamma_stable, nan_ratio_no_pdr):
+        monkeypatch.setattr(policy, "decide", mutant)
+        assert _fails(ts.test_policy_nan_statistics_take_the_safer_path), mutant.__name__
+        assert _fails(ts.test_policy_nan_statistics_single_steps), mutant.__name__
+    monkeypatch.setattr(policy, "decide", orig)
+    ts.test_policy_nan_statistics_take_the_safer_path()
